@@ -1,0 +1,423 @@
+/*
+ * gdn_oracle.c -- plain, slow, fp64 CPU oracle of the chunkwise gated-delta
+ * prefill core (dense and event-sparse forms).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: it is used by the tests, by the smoke check and by the
+ * benchmark's CPU-baseline leg.  It shares no code with the CUDA library.
+ *
+ * Source of every formula: "SparseGDN: Chunk Sparse in Linear Attention",
+ * Chinese reading notes (cc.laoqi.cc), which paraphrase the paper section by
+ * section.  Section / equation numbers below are the paper's, as those notes
+ * quote them.
+ *
+ * Notation (one value head h, its query/key head p = h/2, chunk c of L = 64
+ * tokens, local token index i):
+ *   g_{c,i}   within-chunk inclusive cumulative log2 retention   (Sec. 2.1)
+ *   gamma_c   g at the chunk's last token                         (Sec. 2.1)
+ *   A_Delta[t,s] = beta_t <k_t,k_s> 2^(g_t-g_s) [s<t],  M = I + A_Delta  (Sec. 2.3, Eqs. 5-6)
+ *   U = M^-1 diag(beta) V,  W = M^-1 diag(beta 2^g) K                     (Eqs. 6, 8, 15)
+ *   selected chunk:   U' = U - W S,  S+ = 2^gamma S + K^T (U' * 2^(gamma-g))  (Eqs. 1-2)
+ *   unselected chunk: U' = U,        S+ = 2^gamma S                           (Eqs. 17-18)
+ *   group (c, c+1) = (2r, 2r+1), entry state S_c:                             (Eqs. 22-24)
+ *     O_c   = [2^g_c * (Q_c S_c) + A_cc U'_c] / sqrt(d)
+ *     O_c+1 = [2^(g_c+1 + gamma_c) * (Q_c+1 S_c) + A_c+1,c U'_c + A_c+1,c+1 U'_c+1] / sqrt(d)
+ *     A_cc[i,j] = <q_i,k_j> 2^(g_i - g_j) [j<=i];  A_c+1,c[i,j] = <q_i,k_j> 2^(g_c+1,i + gamma_c - g_c,j)
+ *   chunk form (Eqs. 3-4): O_c = [2^g_c * (Q_c S_c) + A_cc U'_c] / sqrt(d) for every c.
+ *   block-adjacent solver (Eq. 7): C_ii = M_ii^-1, C_i,i-1 = -C_ii M_i,i-1 C_i-1,i-1,
+ *     every other 16x16 block zero; exact ("Full64") solver: C = M^-1.
+ *   tail score (Eq. 9): s_c = ||U[48:64, :]||_F.
+ *
+ * Readings where the pages leave a step open (each is also listed in the
+ * design notes):
+ *   - g is inclusive of token i's own gate (only then does Eq. 4's diagonal
+ *     term carry weight 2^0 and Eqs. 5-6 match the token recurrence);
+ *   - beta and g are per value head; q, k are per query/key head p = h/2;
+ *   - 1/sqrt(d) scales both output terms; no other query scaling;
+ *   - a partial last chunk of n < 64 tokens uses gamma = g at its last token
+ *     and the tail window of its last min(16, n) tokens; the 16-token blocks
+ *     of the solver are cut at n;
+ *   - the state entering a group is the directly propagated state (the
+ *     prefix-gap recovery of Eq. 21 is not used here, so it can be tested).
+ *
+ * Exported entry points: gdn_oracle_prefill(), gdn_oracle_events().
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define LCH 64   /* chunk length L */
+#define BLK 16   /* solver block size */
+
+enum { SOLVER_EXACT = 0, SOLVER_BLOCK_ADJ = 1 };
+
+typedef struct {
+    int B, T, Nq, Nv, d, dv, solver;
+    const double *q, *k, *v, *beta, *g, *h0;
+    const unsigned char *mask; /* [B, Nv/2, C]; NULL = every chunk selected */
+    double *o, *s_final;       /* required outputs */
+    /* optional diagnostics (NULL to skip) */
+    double *o_chunk, *u, *u_prime, *w, *s_in, *score, *cinv;
+    int nthreads;
+} job_t;
+
+/* ---- small dense helpers (row-major, explicit sizes) --------------------- */
+
+static double dot(const double *a, const double *b, int n)
+{
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += a[i] * b[i];
+    return s;
+}
+
+/* X = M^-1 for the n x n unit lower-triangular M, by forward substitution,
+ * one column of the identity at a time. */
+static void inverse_unit_lower(const double *M, int n, double *X)
+{
+    memset(X, 0, sizeof(double) * LCH * LCH);
+    for (int j = 0; j < n; ++j) {
+        for (int i = 0; i < n; ++i) {
+            if (i < j) { X[i * LCH + j] = 0.0; continue; }
+            if (i == j) { X[i * LCH + j] = 1.0; continue; }
+            double acc = 0.0;
+            for (int s = j; s < i; ++s) acc += M[i * LCH + s] * X[s * LCH + j];
+            X[i * LCH + j] = -acc;
+        }
+    }
+}
+
+/* Block-adjacent approximation of M^-1 (Sec. 2.3, Eq. 7). */
+static void inverse_block_adjacent(const double *M, int n, double *X)
+{
+    memset(X, 0, sizeof(double) * LCH * LCH);
+    int nb = (n + BLK - 1) / BLK;
+    /* diagonal blocks: C_ii = M_ii^-1 (forward substitution inside the block) */
+    for (int bi = 0; bi < nb; ++bi) {
+        int r0 = bi * BLK, r1 = r0 + BLK < n ? r0 + BLK : n;
+        for (int j = r0; j < r1; ++j) {
+            for (int i = j; i < r1; ++i) {
+                if (i == j) { X[i * LCH + j] = 1.0; continue; }
+                double acc = 0.0;
+                for (int s = j; s < i; ++s) acc += M[i * LCH + s] * X[s * LCH + j];
+                X[i * LCH + j] = -acc;
+            }
+        }
+    }
+    /* sub-diagonal blocks: C_i,i-1 = -C_ii M_i,i-1 C_i-1,i-1 */
+    for (int bi = 1; bi < nb; ++bi) {
+        int r0 = bi * BLK, r1 = r0 + BLK < n ? r0 + BLK : n;
+        int c0 = (bi - 1) * BLK, c1 = c0 + BLK;
+        double T1[BLK * BLK]; /* T1 = M_i,i-1 C_i-1,i-1 */
+        for (int i = r0; i < r1; ++i)
+            for (int j = c0; j < c1; ++j) {
+                double acc = 0.0;
+                for (int m = c0; m < c1; ++m) acc += M[i * LCH + m] * X[m * LCH + j];
+                T1[(i - r0) * BLK + (j - c0)] = acc;
+            }
+        for (int i = r0; i < r1; ++i)
+            for (int j = c0; j < c1; ++j) {
+                double acc = 0.0;
+                for (int m = r0; m < r1; ++m) acc += X[i * LCH + m] * T1[(m - r0) * BLK + (j - c0)];
+                X[i * LCH + j] = -acc;
+            }
+    }
+}
+
+/* ---- one (b, value head) unit ------------------------------------------- */
+
+typedef struct {
+    /* per-chunk local copies */
+    double *Qc, *Kc, *Vc, *bet, *gg;
+    /* intra results */
+    double *M, *Cm, *U, *W, *Up;
+    /* previous chunk of the current group (for the odd chunk's cross term) */
+    double *Qp, *Kp, *Up_prev, *gp;
+    double *S, *Sgrp, *Sent; /* running state, group entry state, chunk entry state */
+    double *tmp;
+} scratch_t;
+
+static void load_chunk(const job_t *J, int b, int h, int c, int n,
+                       double *Qc, double *Kc, double *Vc, double *bet, double *gg)
+{
+    int p = h / 2, d = J->d, dv = J->dv;
+    for (int i = 0; i < n; ++i) {
+        size_t t = (size_t)c * LCH + i;
+        size_t qk = (((size_t)b * J->T + t) * J->Nq + p) * d;
+        size_t vv = (((size_t)b * J->T + t) * J->Nv + h) * dv;
+        size_t sc = ((size_t)b * J->T + t) * J->Nv + h;
+        memcpy(Qc + (size_t)i * d, J->q + qk, sizeof(double) * d);
+        memcpy(Kc + (size_t)i * d, J->k + qk, sizeof(double) * d);
+        memcpy(Vc + (size_t)i * dv, J->v + vv, sizeof(double) * dv);
+        bet[i] = J->beta[sc];
+        gg[i] = J->g[sc];
+    }
+}
+
+/* Intra-chunk step (Sec. 2.3): M, the solver's C, U = C diag(beta) V,
+ * W = C diag(beta 2^g) K. */
+static void intra(const job_t *J, int n, scratch_t *X)
+{
+    int d = J->d, dv = J->dv;
+    for (int t = 0; t < LCH; ++t)
+        for (int s = 0; s < LCH; ++s) X->M[t * LCH + s] = 0.0;
+    for (int t = 0; t < n; ++t) {
+        X->M[t * LCH + t] = 1.0;
+        for (int s = 0; s < t; ++s)
+            X->M[t * LCH + s] = X->bet[t] * dot(X->Kc + (size_t)t * d, X->Kc + (size_t)s * d, d)
+                                * exp2(X->gg[t] - X->gg[s]);
+    }
+    if (J->solver == SOLVER_EXACT) inverse_unit_lower(X->M, n, X->Cm);
+    else inverse_block_adjacent(X->M, n, X->Cm);
+    for (int t = 0; t < n; ++t) {
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int s = 0; s <= t; ++s) acc += X->Cm[t * LCH + s] * X->bet[s] * X->Vc[(size_t)s * dv + j];
+            X->U[(size_t)t * dv + j] = acc;
+        }
+        for (int j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int s = 0; s <= t; ++s)
+                acc += X->Cm[t * LCH + s] * X->bet[s] * exp2(X->gg[s]) * X->Kc[(size_t)s * d + j];
+            X->W[(size_t)t * d + j] = acc;
+        }
+    }
+}
+
+/* State read/write of one chunk (Eqs. 1-2 when selected, 17-18 otherwise). */
+static void propagate(const job_t *J, int n, int selected, scratch_t *X)
+{
+    int d = J->d, dv = J->dv;
+    double gam = X->gg[n - 1];
+    if (selected) {
+        for (int t = 0; t < n; ++t)
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int m = 0; m < d; ++m) acc += X->W[(size_t)t * d + m] * X->S[(size_t)m * dv + j];
+                X->Up[(size_t)t * dv + j] = X->U[(size_t)t * dv + j] - acc;
+            }
+        for (int m = 0; m < d; ++m)
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int t = 0; t < n; ++t)
+                    acc += X->Kc[(size_t)t * d + m] * X->Up[(size_t)t * dv + j] * exp2(gam - X->gg[t]);
+                X->S[(size_t)m * dv + j] = exp2(gam) * X->S[(size_t)m * dv + j] + acc;
+            }
+    } else {
+        memcpy(X->Up, X->U, sizeof(double) * (size_t)n * dv);
+        for (size_t e = 0; e < (size_t)d * dv; ++e) X->S[e] = exp2(gam) * X->S[e];
+    }
+}
+
+/* O rows for the tokens of one chunk given an entry state Sx and an extra
+ * exponent `shift` on the state read (gamma_c for the odd chunk of a group).
+ * Adds the local term A_cc U'_c.  out has stride dv, rows n. */
+static void output_local(const job_t *J, int n, const double *Qc, const double *Kc, const double *Up,
+                         const double *gg, const double *Sx, double shift, double *out)
+{
+    int d = J->d, dv = J->dv;
+    double scale = 1.0 / sqrt((double)d);
+    for (int i = 0; i < n; ++i) {
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int m = 0; m < d; ++m) acc += Qc[(size_t)i * d + m] * Sx[(size_t)m * dv + j];
+            out[(size_t)i * dv + j] = exp2(gg[i] + shift) * acc;
+        }
+        for (int s = 0; s <= i; ++s) {
+            double a = dot(Qc + (size_t)i * d, Kc + (size_t)s * d, d) * exp2(gg[i] - gg[s]);
+            for (int j = 0; j < dv; ++j) out[(size_t)i * dv + j] += a * Up[(size_t)s * dv + j];
+        }
+        for (int j = 0; j < dv; ++j) out[(size_t)i * dv + j] *= scale;
+    }
+}
+
+static void store_rows(const job_t *J, double *dst, int b, int h, int c, int n, const double *src, int width)
+{
+    if (!dst) return;
+    for (int i = 0; i < n; ++i) {
+        size_t t = (size_t)c * LCH + i;
+        memcpy(dst + (((size_t)b * J->T + t) * J->Nv + h) * width, src + (size_t)i * width, sizeof(double) * width);
+    }
+}
+
+static void run_unit(const job_t *J, int b, int h, scratch_t *X)
+{
+    int d = J->d, dv = J->dv, T = J->T, P = J->Nv / 2, p = h / 2;
+    int C = (T + LCH - 1) / LCH;
+    size_t SS = (size_t)d * dv;
+    double scale = 1.0 / sqrt((double)d);
+
+    if (J->h0) memcpy(X->S, J->h0 + ((size_t)b * J->Nv + h) * SS, sizeof(double) * SS);
+    else memset(X->S, 0, sizeof(double) * SS);
+
+    double *orow = X->tmp; /* LCH x dv output rows */
+    for (int c = 0; c < C; ++c) {
+        int n = (c + 1) * LCH <= T ? LCH : T - c * LCH;
+        int odd = c & 1;
+        int sel = J->mask ? J->mask[((size_t)b * P + p) * C + c] != 0 : 1;
+        if (!odd) memcpy(X->Sgrp, X->S, sizeof(double) * SS); /* group entry state S_c */
+        if (J->s_in) memcpy(J->s_in + (((size_t)b * J->Nv + h) * C + c) * SS, X->S, sizeof(double) * SS);
+
+        load_chunk(J, b, h, c, n, X->Qc, X->Kc, X->Vc, X->bet, X->gg);
+        intra(J, n, X);
+        if (J->score) {
+            double acc = 0.0;
+            int t0 = n > BLK ? n - BLK : 0;
+            for (int t = t0; t < n; ++t)
+                for (int j = 0; j < dv; ++j) acc += X->U[(size_t)t * dv + j] * X->U[(size_t)t * dv + j];
+            J->score[((size_t)b * J->Nv + h) * C + c] = sqrt(acc);
+        }
+        if (J->cinv) memcpy(J->cinv + (((size_t)b * J->Nv + h) * C + c) * LCH * LCH, X->Cm, sizeof(double) * LCH * LCH);
+        store_rows(J, J->u, b, h, c, n, X->U, dv);
+        store_rows(J, J->w, b, h, c, n, X->W, d);
+
+        /* the chunk form (Eqs. 3-4) reads the state entering this chunk */
+        if (J->o_chunk) memcpy(X->Sent, X->S, sizeof(double) * SS);
+        propagate(J, n, sel, X);
+        store_rows(J, J->u_prime, b, h, c, n, X->Up, dv);
+        if (J->o_chunk) {
+            output_local(J, n, X->Qc, X->Kc, X->Up, X->gg, X->Sent, 0.0, orow);
+            store_rows(J, J->o_chunk, b, h, c, n, orow, dv);
+        }
+
+        /* group-wise output (Eqs. 22-24) */
+        if (!odd) {
+            output_local(J, n, X->Qc, X->Kc, X->Up, X->gg, X->Sgrp, 0.0, orow);
+            store_rows(J, J->o, b, h, c, n, orow, dv);
+            /* remember chunk c for the odd chunk's cross term */
+            memcpy(X->Qp, X->Qc, sizeof(double) * LCH * d);
+            memcpy(X->Kp, X->Kc, sizeof(double) * LCH * d);
+            memcpy(X->Up_prev, X->Up, sizeof(double) * LCH * dv);
+            memcpy(X->gp, X->gg, sizeof(double) * LCH);
+        } else {
+            double gam_prev = X->gp[LCH - 1]; /* chunk c-1 is full whenever c is odd */
+            output_local(J, n, X->Qc, X->Kc, X->Up, X->gg, X->Sgrp, gam_prev, orow);
+            for (int i = 0; i < n; ++i)
+                for (int s = 0; s < LCH; ++s) {
+                    double a = dot(X->Qc + (size_t)i * d, X->Kp + (size_t)s * d, d)
+                               * exp2(X->gg[i] + gam_prev - X->gp[s]) * scale;
+                    for (int j = 0; j < dv; ++j) orow[(size_t)i * dv + j] += a * X->Up_prev[(size_t)s * dv + j];
+                }
+            store_rows(J, J->o, b, h, c, n, orow, dv);
+        }
+    }
+    memcpy(J->s_final + ((size_t)b * J->Nv + h) * SS, X->S, sizeof(double) * SS);
+}
+
+typedef struct { const job_t *J; int tid; } worker_arg_t;
+
+static void *worker(void *arg)
+{
+    const worker_arg_t *a = (const worker_arg_t *)arg;
+    const job_t *J = a->J;
+    int d = J->d, dv = J->dv;
+    scratch_t X;
+    size_t sz[] = {LCH * (size_t)d, LCH * (size_t)d, LCH * (size_t)dv, LCH, LCH,
+                   LCH * LCH, LCH * LCH, LCH * (size_t)dv, LCH * (size_t)d, LCH * (size_t)dv,
+                   LCH * (size_t)d, LCH * (size_t)d, LCH * (size_t)dv, LCH,
+                   (size_t)d * dv, (size_t)d * dv, (size_t)d * dv, LCH * (size_t)dv};
+    double **ptr[] = {&X.Qc, &X.Kc, &X.Vc, &X.bet, &X.gg, &X.M, &X.Cm, &X.U, &X.W, &X.Up,
+                      &X.Qp, &X.Kp, &X.Up_prev, &X.gp, &X.S, &X.Sgrp, &X.Sent, &X.tmp};
+    int nbuf = (int)(sizeof(sz) / sizeof(sz[0]));
+    for (int i = 0; i < nbuf; ++i) *ptr[i] = (double *)calloc(sz[i], sizeof(double));
+    int units = J->B * J->Nv;
+    for (int u = a->tid; u < units; u += J->nthreads) run_unit(J, u / J->Nv, u % J->Nv, &X);
+    for (int i = 0; i < nbuf; ++i) free(*ptr[i]);
+    return NULL;
+}
+
+/* Full prefill.  All arrays are dense row-major fp64 (mask: uint8).
+ *   q, k [B,T,Nq,d]; v [B,T,Nv,dv]; beta, g [B,T,Nv]; h0 [B,Nv,d,dv] or NULL;
+ *   mask [B,Nv/2,ceil(T/64)] or NULL (= dense path, every chunk selected);
+ *   o [B,T,Nv,dv]; s_final [B,Nv,d,dv].
+ * Optional diagnostics (NULL to skip): o_chunk [B,T,Nv,dv] (chunk-form
+ * output with the same states), u, u_prime [B,T,Nv,dv], w [B,T,Nv,d],
+ * s_in [B,Nv,C,d,dv] (state entering each chunk), score [B,Nv,C],
+ * cinv [B,Nv,C,64,64] (the solver's C).
+ * Returns 0, or -1 on a bad argument. */
+int gdn_oracle_prefill(int B, int T, int Nq, int Nv, int d, int dv,
+                       const double *q, const double *k, const double *v,
+                       const double *beta, const double *g, const double *h0,
+                       const unsigned char *mask, int solver, int nthreads,
+                       double *o, double *s_final,
+                       double *o_chunk, double *u, double *u_prime, double *w,
+                       double *s_in, double *score, double *cinv)
+{
+    if (B < 0 || T < 0 || Nq <= 0 || Nv != 2 * Nq || d <= 0 || dv <= 0) return -1;
+    if (solver != SOLVER_EXACT && solver != SOLVER_BLOCK_ADJ) return -1;
+    if (!s_final || (T > 0 && (!q || !k || !v || !beta || !g || !o))) return -1;
+    job_t J = {B, T, Nq, Nv, d, dv, solver, q, k, v, beta, g, h0, mask, o, s_final,
+               o_chunk, u, u_prime, w, s_in, score, cinv, nthreads < 1 ? 1 : nthreads};
+    int units = B * Nv;
+    if (J.nthreads > units) J.nthreads = units > 0 ? units : 1;
+    pthread_t th[1024];
+    worker_arg_t args[1024];
+    if (J.nthreads > 1024) J.nthreads = 1024;
+    for (int t = 0; t < J.nthreads; ++t) {
+        args[t].J = &J; args[t].tid = t;
+        pthread_create(&th[t], NULL, worker, &args[t]);
+    }
+    for (int t = 0; t < J.nthreads; ++t) pthread_join(th[t], NULL);
+    return 0;
+}
+
+/* ---- event compaction (Sec. 2.5 CSR layout) ------------------------------
+ * Rows: one per (sequence b, head pair p), physical id i = b*P + p, ordered by
+ * event count descending, ties by physical id ascending (a caller mask has no
+ * tiers; "long chains first").  Events inside a row ascend in chunk index.
+ *   row_pair[j]      physical id of row j                           [B*P]
+ *   row_ptr[j]       offset of row j's first event; row_ptr[B*P] = E [B*P+1]
+ *   ev_chunk[e]      chunk index of event e                         [E]
+ *   grp_pred[i*G+r]  global index of the last event of pair i with chunk < 2r,
+ *                    or -1 (G = ceil(C/2))                          [B*P*G]
+ *   snap_slot[e]     dense number, in global event order, of the events that
+ *                    are some group's predecessor; -1 otherwise     [E]
+ * Returns 0, 1 when E exceeds `capacity` (outputs beyond row_ptr untouched),
+ * -1 on a bad argument. */
+int gdn_oracle_events(int B, int P, int C, const unsigned char *mask, int capacity,
+                      int *row_pair, int *row_ptr, int *ev_chunk, int *grp_pred,
+                      int *snap_slot, int *n_events, int *n_snap)
+{
+    if (B < 0 || P <= 0 || C < 0) return -1;
+    int R = B * P, G = (C + 1) / 2;
+    int *cnt = (int *)calloc(R > 0 ? R : 1, sizeof(int));
+    for (int i = 0; i < R; ++i)
+        for (int c = 0; c < C; ++c) cnt[i] += mask[(size_t)i * C + c] != 0;
+    /* insertion sort: count descending, id ascending */
+    for (int i = 0; i < R; ++i) row_pair[i] = i;
+    for (int i = 1; i < R; ++i) {
+        int x = row_pair[i], j = i - 1;
+        while (j >= 0 && (cnt[row_pair[j]] < cnt[x] || (cnt[row_pair[j]] == cnt[x] && row_pair[j] > x))) {
+            row_pair[j + 1] = row_pair[j];
+            --j;
+        }
+        row_pair[j + 1] = x;
+    }
+    row_ptr[0] = 0;
+    for (int j = 0; j < R; ++j) row_ptr[j + 1] = row_ptr[j] + cnt[row_pair[j]];
+    int E = row_ptr[R];
+    *n_events = E;
+    if (E > capacity) { free(cnt); *n_snap = 0; return 1; }
+    for (int j = 0; j < R; ++j) {
+        int i = row_pair[j], e = row_ptr[j];
+        for (int c = 0; c < C; ++c)
+            if (mask[(size_t)i * C + c]) ev_chunk[e++] = c;
+    }
+    for (int e = 0; e < E; ++e) snap_slot[e] = -1;
+    for (int j = 0; j < R; ++j) {
+        int i = row_pair[j];
+        for (int r = 0; r < G; ++r) {
+            int pred = -1;
+            for (int e = row_ptr[j]; e < row_ptr[j + 1]; ++e)
+                if (ev_chunk[e] < 2 * r) pred = e;
+            grp_pred[(size_t)i * G + r] = pred;
+            if (pred >= 0) snap_slot[pred] = -2; /* mark: referenced by a group */
+        }
+    }
+    int ns = 0;
+    for (int e = 0; e < E; ++e)
+        if (snap_slot[e] == -2) snap_slot[e] = ns++;
+    *n_snap = ns;
+    free(cnt);
+    return 0;
+}
