@@ -1,0 +1,24 @@
+"""GB300-native chunkwise Gated Delta Network prefill core (dense and event-sparse).
+
+The compute path is libgdn.so (hand-written CUDA for sm_103a behind the C ABI
+in include/gdn.h); this package is its thin ctypes binding.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    GdnError,
+    GdnEvents,
+    GdnShape,
+    STAGES,
+    Workspace,
+    gdn_events_status,
+    gdn_prefill_dense,
+    gdn_prefill_sparse,
+    gdn_profile_enable,
+    gdn_profile_read,
+    gdn_select_events,
+    gdn_version,
+    gdn_workspace_bytes,
+    gdn_workspace_status,
+    load,
+    shape_of,
+)

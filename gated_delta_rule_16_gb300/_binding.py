@@ -1,0 +1,253 @@
+"""ctypes binding of libgdn's C ABI (include/gdn.h), with the same entry-point names.
+
+Argument marshalling only: every step of the prefill runs in libgdn's CUDA
+kernels.  PyTorch supplies device memory (inputs, outputs, workspace) and the
+stream.  If libgdn.so is missing or cannot be loaded, every call raises: there
+is no CPU or library fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgdn.so")
+
+GDN_BF16, GDN_F32 = 0, 1
+SOLVERS = {"exact": 0, "block_adj": 1}
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
+          5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_UNSUPPORTED", 7: "GDN_ERR_CUDA", 8: "GDN_ERR_DEVICE",
+          9: "GDN_ERR_CAPACITY"}
+EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn_prefill_dense",
+           "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
+           "gdn_profile_enable", "gdn_profile_read")
+STAGES = ("select", "prefix", "intra", "wbuild", "scan", "output")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({msg})")
+        self.status = status
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Nq", ctypes.c_int32), ("Nv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("dv", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class GdnEvents(ctypes.Structure):
+    _fields_ = [("row_pair", ctypes.c_void_p), ("row_ptr", ctypes.c_void_p), ("ev_chunk", ctypes.c_void_p),
+                ("grp_pred", ctypes.c_void_p), ("snap_slot", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("capacity", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None):
+    """Load libgdn.so (raises if it is absent: build it with gated_delta_rule_16_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libgdn.so not found at {p}; run `python -m gated_delta_rule_16_gb300.build`")
+            lib = ctypes.CDLL(p)
+            vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+            shp = ctypes.POINTER(GdnShape)
+            evp = ctypes.POINTER(GdnEvents)
+            lib.gdn_workspace_bytes.argtypes = [shp, i32, i32]
+            lib.gdn_workspace_bytes.restype = sz
+            lib.gdn_select_events.argtypes = [shp, vp, evp, vp]
+            lib.gdn_select_events.restype = i32
+            lib.gdn_events_status.argtypes = [evp, vp]
+            lib.gdn_events_status.restype = i32
+            lib.gdn_prefill_dense.argtypes = [shp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+            lib.gdn_prefill_dense.restype = i32
+            lib.gdn_prefill_sparse.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+            lib.gdn_prefill_sparse.restype = i32
+            lib.gdn_workspace_status.argtypes = [vp, vp]
+            lib.gdn_workspace_status.restype = i32
+            lib.gdn_status_string.argtypes = [i32]
+            lib.gdn_status_string.restype = ctypes.c_char_p
+            lib.gdn_version.argtypes = []
+            lib.gdn_version.restype = ctypes.c_int32
+            lib.gdn_profile_enable.argtypes = [i32]
+            lib.gdn_profile_enable.restype = i32
+            lib.gdn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int32,
+                                             ctypes.POINTER(ctypes.c_int32)]
+            lib.gdn_profile_read.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise GdnError(fn, status, load().gdn_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def shape_of(q: torch.Tensor, v: torch.Tensor) -> GdnShape:
+    B, T, Nq, d = q.shape
+    return GdnShape(B, T, Nq, v.shape[2], d, v.shape[3], _dtype_code(q))
+
+
+def _need(t, name, dtype=None, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def gdn_workspace_bytes(shape: GdnShape, solver: str = "block_adj", sparse: bool = True) -> int:
+    return int(load().gdn_workspace_bytes(ctypes.byref(shape), SOLVERS[solver], int(sparse)))
+
+
+class Workspace:
+    """A reusable device workspace (a torch uint8 buffer) sized by gdn_workspace_bytes."""
+
+    def __init__(self):
+        self.buf = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != torch.device(device):
+            self.buf = None
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace(ws, nbytes, device):
+    if ws is None:
+        key = torch.device(device)
+        ws = _default_ws.setdefault(key, Workspace())
+    if isinstance(ws, Workspace):
+        return ws.get(nbytes, device)
+    return ws
+
+
+def _prefill(fn, q, k, v, beta, g, mask, h0, solver, o, s_final, score, workspace, stream):
+    B, T, Nq, d = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    C = (T + 63) // 64
+    _need(q, "q", shape=(B, T, Nq, d))
+    _need(k, "k", dtype=q.dtype, shape=(B, T, Nq, d))
+    _need(v, "v", dtype=q.dtype, shape=(B, T, Nv, dv))
+    _need(beta, "beta", torch.float32, (B, T, Nv))
+    _need(g, "g", torch.float32, (B, T, Nv))
+    _need(h0, "h0", torch.float32, (B, Nv, d, dv))
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, (B, Nv // 2, C))
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, T, Nv, dv), dtype=q.dtype, device=dev)
+    if s_final is None:
+        s_final = torch.empty((B, Nv, d, dv), dtype=torch.float32, device=dev)
+    _need(o, "o", q.dtype, (B, T, Nv, dv))
+    _need(s_final, "s_final", torch.float32, (B, Nv, d, dv))
+    _need(score, "score", torch.float32, (B, Nv, C))
+    shape = shape_of(q, v)
+    nbytes = gdn_workspace_bytes(shape, solver, mask is not None)
+    ws = _workspace(workspace, nbytes, dev)
+    lib = load()
+    args = [ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0)]
+    if fn == "gdn_prefill_sparse":
+        args.append(_ptr(mask))
+    args += [SOLVERS[solver], _ptr(o), _ptr(s_final), _ptr(score), _ptr(ws), ws.numel(), _stream(stream)]
+    with torch.cuda.device(dev):
+        _check(fn, getattr(lib, fn)(*args))
+    return o, s_final
+
+
+def gdn_prefill_dense(q, k, v, beta, g, *, h0=None, solver="exact", o=None, s_final=None, score=None,
+                      workspace=None, stream=None):
+    """Dense prefill through the C ABI; returns (o, s_final)."""
+    return _prefill("gdn_prefill_dense", q, k, v, beta, g, None, h0, solver, o, s_final, score, workspace, stream)
+
+
+def gdn_prefill_sparse(q, k, v, beta, g, mask, *, h0=None, solver="block_adj", o=None, s_final=None,
+                       score=None, workspace=None, stream=None):
+    """Event-sparse prefill through the C ABI; returns (o, s_final)."""
+    if mask is None:
+        raise ValueError("gdn_prefill_sparse needs an event mask")
+    return _prefill("gdn_prefill_sparse", q, k, v, beta, g, mask, h0, solver, o, s_final, score, workspace,
+                    stream)
+
+
+def gdn_select_events(mask: torch.Tensor, Nq: int | None = None, capacity: int | None = None, stream=None):
+    """Mask [B,P,C] uint8 -> CSR event lists on the device (dict of int32 tensors)."""
+    _need(mask, "mask", torch.uint8)
+    B, P, C = mask.shape
+    G = (C + 1) // 2
+    cap = B * P * C if capacity is None else int(capacity)
+    dev = mask.device
+    out = {"row_pair": torch.empty(max(B * P, 1), dtype=torch.int32, device=dev),
+           "row_ptr": torch.empty(B * P + 1, dtype=torch.int32, device=dev),
+           "ev_chunk": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+           "grp_pred": torch.empty(max(B * P * G, 1), dtype=torch.int32, device=dev),
+           "snap_slot": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+           "counts": torch.zeros(4, dtype=torch.int32, device=dev)}
+    ev = GdnEvents(*(out[n].data_ptr() for n in ("row_pair", "row_ptr", "ev_chunk", "grp_pred", "snap_slot",
+                                                  "counts")), cap)
+    shape = GdnShape(B, C * 64, P, 2 * P, 128, 128, GDN_BF16)
+    lib = load()
+    with torch.cuda.device(dev):
+        _check("gdn_select_events", lib.gdn_select_events(ctypes.byref(shape), _ptr(mask), ctypes.byref(ev),
+                                                          _stream(stream)))
+    out["_struct"] = ev
+    return out
+
+
+def gdn_events_status(events: dict, stream=None) -> int:
+    return int(load().gdn_events_status(ctypes.byref(events["_struct"]), _stream(stream)))
+
+
+def gdn_workspace_status(workspace, stream=None) -> int:
+    buf = workspace.buf if isinstance(workspace, Workspace) else workspace
+    return int(load().gdn_workspace_status(_ptr(buf), _stream(stream)))
+
+
+def gdn_version() -> int:
+    return int(load().gdn_version())
+
+
+def gdn_profile_enable(enable: bool = True) -> None:
+    """Record per-stage CUDA events in the following prefills (see include/gdn.h)."""
+    _check("gdn_profile_enable", load().gdn_profile_enable(int(enable)))
+
+
+def gdn_profile_read() -> tuple[dict, int]:
+    """Summed milliseconds per stage over the recorded prefills, and their count."""
+    ms = (ctypes.c_float * len(STAGES))()
+    n = ctypes.c_int32(0)
+    _check("gdn_profile_read", load().gdn_profile_read(ms, len(STAGES), ctypes.byref(n)))
+    return {name: float(ms[i]) for i, name in enumerate(STAGES)}, int(n.value)

@@ -1,0 +1,288 @@
+// gdn_api.cu -- the extern "C" entry points of libgdn (declared in include/gdn.h):
+// argument validation, workspace carving and the launch sequence of the
+// prefill pipeline.  No allocation, no synchronisation (except the status
+// queries), no host copy of the event count.
+#include <cstring>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// ---- stage profiler (benchmark aid; see gdn_profile_enable) ----------------
+constexpr int kStages = 6;
+constexpr int kProfSlots = 256;
+struct Profiler {
+    bool on = false, created = false;
+    int used = 0;
+    int dev = -1;
+    cudaEvent_t ev[kProfSlots][kStages + 1];
+};
+Profiler g_prof;
+
+// Returns the event row of this prefill, or nullptr when not profiling.
+cudaEvent_t *prof_slot() {
+    if (!g_prof.on || g_prof.used >= kProfSlots) return nullptr;
+    return g_prof.ev[g_prof.used++];
+}
+
+int device_ok() {
+    // cache per device: 0 unknown, 1 ok, 2 not a compute-capability 10.3 part
+    static int state[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (state[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return 0;
+        state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return state[dev] == 1;
+}
+
+gdn_status check_shape(const gdn_shape *s) {
+    if (!s) return GDN_ERR_NULL;
+    if (s->dtype != GDN_BF16 && s->dtype != GDN_F32) return GDN_ERR_DTYPE;
+    if (s->B < 0 || s->T < 0 || s->Nq <= 0 || s->Nv != 2 * s->Nq) return GDN_ERR_SHAPE;
+    if (s->d != kDim || s->dv != kDim) return GDN_ERR_UNSUPPORTED;
+    if (s->T % kChunk != 0) return GDN_ERR_UNSUPPORTED;
+    // index arithmetic uses int32 for chunk/row/event counts
+    const int64_t C = s->T / kChunk;
+    if ((int64_t)s->B * s->Nq * C >= (int64_t)1 << 30) return GDN_ERR_SHAPE;
+    if ((int64_t)s->B * s->Nq > 8192) return GDN_ERR_UNSUPPORTED;  // compaction keeps rows in shared memory
+    return GDN_OK;
+}
+
+void fill_problem(const gdn_shape *s, gdn_solver solver, Problem *pb) {
+    std::memset(pb, 0, sizeof(*pb));
+    pb->B = s->B; pb->T = s->T; pb->Nq = s->Nq; pb->Nv = s->Nv; pb->d = s->d; pb->dv = s->dv;
+    pb->C = s->T / kChunk;
+    pb->G = (pb->C + 1) / 2;
+    pb->P = s->Nq;
+    pb->R = s->B * s->Nq;
+    pb->dtype = s->dtype;
+    pb->solver = solver;
+    pb->nblk = solver == GDN_SOLVER_EXACT ? kBlkFull : kBlkAdj;
+}
+
+size_t elem_size(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
+
+}  // namespace
+
+size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
+    const int64_t R = pb.R, C = pb.C, G = pb.G;
+    const size_t es = elem_size(pb.dtype);
+    const int64_t ev_cap = R * C;            // every chunk of every pair may be an event
+    const int64_t snap_cap = R * G;          // at most one predecessor per group
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+    const size_t o_counts = take(4 * sizeof(int32_t));
+    const size_t o_row_pair = take(R * sizeof(int32_t));
+    const size_t o_row_ptr = take((R + 1) * sizeof(int32_t));
+    const size_t o_ev_chunk = take(ev_cap * sizeof(int32_t));
+    const size_t o_grp_pred = take(R * G * sizeof(int32_t));
+    const size_t o_snap_slot = take(ev_cap * sizeof(int32_t));
+    const size_t o_P = take((size_t)pb.B * pb.Nv * (C + 1) * sizeof(double));
+    const size_t o_U = take((size_t)pb.B * pb.T * pb.Nv * pb.dv * es);
+    const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
+    const size_t o_W = take((size_t)ev_cap * 2 * kChunk * pb.d * es);
+    const size_t o_snap = take((size_t)snap_cap * 2 * pb.d * pb.dv * sizeof(float));
+    if (ws) {
+        char *b = (char *)base;
+        ws->counts = (int32_t *)(b + o_counts);
+        ws->row_pair = (int32_t *)(b + o_row_pair);
+        ws->row_ptr = (int32_t *)(b + o_row_ptr);
+        ws->ev_chunk = (int32_t *)(b + o_ev_chunk);
+        ws->grp_pred = (int32_t *)(b + o_grp_pred);
+        ws->snap_slot = (int32_t *)(b + o_snap_slot);
+        ws->P = (double *)(b + o_P);
+        ws->U = b + o_U;
+        ws->cbar = (float *)(b + o_cbar);
+        ws->W = b + o_W;
+        ws->snap = (float *)(b + o_snap);
+        ws->ev_cap = ev_cap;
+        ws->snap_cap = snap_cap;
+    }
+    return off;
+}
+
+namespace {
+
+gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *beta,
+                       const float *g, const float *h0, const uint8_t *mask, bool sparse, gdn_solver solver,
+                       void *o, float *s_final, float *score, void *workspace, size_t workspace_bytes,
+                       void *stream) {
+    gdn_status st = check_shape(shape);
+    if (st != GDN_OK) return st;
+    if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return GDN_ERR_DTYPE;
+    const bool has_tokens = shape->B > 0 && shape->T > 0;
+    if (shape->B > 0 && !s_final) return GDN_ERR_NULL;
+    if (has_tokens && (!q || !k || !v || !beta || !g || !o || (sparse && !mask))) return GDN_ERR_NULL;
+    if (shape->B > 0 && !workspace) return GDN_ERR_NULL;
+    const void *ptrs[] = {q, k, v, beta, g, h0, o, s_final, score};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGN;
+    if (workspace && ((uintptr_t)workspace % kAlign) != 0) return GDN_ERR_ALIGN;
+    Problem pb;
+    fill_problem(shape, solver, &pb);
+    if (shape->B == 0) return GDN_OK;
+    const size_t need = workspace_layout(pb, nullptr, nullptr);
+    if (workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if (!device_ok()) return GDN_ERR_DEVICE;
+    pb.q = q; pb.k = k; pb.v = v; pb.beta = beta; pb.g = g; pb.h0 = h0;
+    pb.mask = sparse ? mask : nullptr;
+    pb.o = o; pb.s_final = s_final; pb.score = score;
+    pb.stream = (cudaStream_t)stream;
+    Workspace ws;
+    workspace_layout(pb, workspace, &ws);
+
+    gdn_events ev;
+    ev.row_pair = ws.row_pair; ev.row_ptr = ws.row_ptr; ev.ev_chunk = ws.ev_chunk;
+    ev.grp_pred = ws.grp_pred; ev.snap_slot = ws.snap_slot; ev.counts = ws.counts;
+    ev.capacity = (int32_t)ws.ev_cap;
+    cudaEvent_t *prof = prof_slot();
+    auto mark = [&](int i) { if (prof) cudaEventRecord(prof[i], pb.stream); };
+    mark(0);
+    cudaError_t e = launch_select(pb, ev, ws.snap_cap);
+    mark(1);
+    if (e == cudaSuccess) e = launch_prefix(pb, ws);
+    mark(2);
+    if (e == cudaSuccess) e = launch_intra(pb, ws);
+    mark(3);
+    if (e == cudaSuccess) e = launch_wbuild(pb, ws);
+    mark(4);
+    if (e == cudaSuccess) e = launch_scan(pb, ws);
+    mark(5);
+    if (e == cudaSuccess) e = launch_output(pb, ws);
+    mark(6);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status read_status(const int32_t *counts, void *stream) {
+    if (!counts) return GDN_ERR_NULL;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+    int32_t host[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(host, counts, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    return host[2] ? GDN_ERR_CAPACITY : GDN_OK;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+size_t gdn_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse) {
+    (void)sparse;  // both paths share one layout: the dense path is the all-events case
+    if (check_shape(shape) != GDN_OK) return 0;
+    if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return 0;
+    Problem pb;
+    fill_problem(shape, solver, &pb);
+    return workspace_layout(pb, nullptr, nullptr);
+}
+
+gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask, gdn_events *events, void *stream) {
+    gdn_status st = check_shape(shape);
+    if (st != GDN_OK) return st;
+    if (!events) return GDN_ERR_NULL;
+    Problem pb;
+    fill_problem(shape, GDN_SOLVER_BLOCK_ADJ, &pb);
+    if (pb.R == 0) return GDN_OK;
+    if (!events->row_pair || !events->row_ptr || !events->grp_pred || !events->counts) return GDN_ERR_NULL;
+    if (pb.C > 0 && (!mask || !events->ev_chunk || !events->snap_slot)) return GDN_ERR_NULL;
+    if (events->capacity < 0) return GDN_ERR_SHAPE;
+    const void *ptrs[] = {mask, events->row_pair, events->row_ptr, events->ev_chunk, events->grp_pred,
+                          events->snap_slot, events->counts};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGN;
+    if (!device_ok()) return GDN_ERR_DEVICE;
+    pb.mask = mask;
+    pb.stream = (cudaStream_t)stream;
+    // the snapshot numbering needs no capacity of its own: it never exceeds E
+    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_events_status(const gdn_events *events, void *stream) {
+    if (!events) return GDN_ERR_NULL;
+    return read_status(events->counts, stream);
+}
+
+gdn_status gdn_prefill_dense(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                             const float *beta, const float *g, const float *h0, gdn_solver solver, void *o,
+                             float *s_final, float *score, void *workspace, size_t workspace_bytes, void *stream) {
+    return run_prefill(shape, q, k, v, beta, g, h0, nullptr, false, solver, o, s_final, score, workspace,
+                       workspace_bytes, stream);
+}
+
+gdn_status gdn_prefill_sparse(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                              const float *beta, const float *g, const float *h0, const uint8_t *mask,
+                              gdn_solver solver, void *o, float *s_final, float *score, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    return run_prefill(shape, q, k, v, beta, g, h0, mask, true, solver, o, s_final, score, workspace,
+                       workspace_bytes, stream);
+}
+
+gdn_status gdn_workspace_status(const void *workspace, void *stream) {
+    if (!workspace) return GDN_ERR_NULL;
+    // counts live at offset 0 of the workspace
+    return read_status((const int32_t *)workspace, stream);
+}
+
+const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_NULL: return "a required pointer is NULL";
+        case GDN_ERR_SHAPE: return "unsupported or inconsistent sizes";
+        case GDN_ERR_DTYPE: return "unknown dtype or solver";
+        case GDN_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
+        case GDN_ERR_WORKSPACE: return "workspace smaller than gdn_workspace_bytes()";
+        case GDN_ERR_UNSUPPORTED: return "request not implemented by this build (needs d == dv == 128, T % 64 == 0)";
+        case GDN_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+        case GDN_ERR_DEVICE: return "current device is not a compute-capability 10.3 (GB300) GPU";
+        case GDN_ERR_CAPACITY: return "device-side event or snapshot capacity exceeded";
+    }
+    return "unknown status";
+}
+
+int32_t gdn_version(void) { return 100; }
+
+gdn_status gdn_profile_enable(int enable) {
+    if (enable && !g_prof.created) {
+        if (!device_ok()) return GDN_ERR_DEVICE;
+        for (int i = 0; i < kProfSlots; ++i)
+            for (int j = 0; j <= kStages; ++j)
+                if (cudaEventCreate(&g_prof.ev[i][j]) != cudaSuccess) return GDN_ERR_CUDA;
+        g_prof.created = true;
+    }
+    g_prof.on = enable != 0;
+    g_prof.used = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills) {
+    if (!stage_ms || !n_prefills) return GDN_ERR_NULL;
+    if (n_stages < 0 || n_stages > kStages) return GDN_ERR_SHAPE;
+    for (int j = 0; j < n_stages; ++j) stage_ms[j] = 0.f;
+    *n_prefills = g_prof.created ? g_prof.used : 0;
+    for (int i = 0; i < *n_prefills; ++i) {
+        if (cudaEventSynchronize(g_prof.ev[i][kStages]) != cudaSuccess) return GDN_ERR_CUDA;
+        for (int j = 0; j < n_stages; ++j) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, g_prof.ev[i][j], g_prof.ev[i][j + 1]) != cudaSuccess) return GDN_ERR_CUDA;
+            stage_ms[j] += ms;
+        }
+    }
+    g_prof.used = 0;
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// gdn_internal.cuh -- shared declarations of libgdn's kernels (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;     // L: tokens per chunk
+constexpr int kBlk = 16;       // solver block size
+constexpr int kDim = 128;      // d == dv supported by this version
+constexpr int kBlkAdj = 7;     // kept 16x16 blocks of the block-adjacent solver
+constexpr int kBlkFull = 10;   // lower 16x16 blocks of the exact solver
+
+// Compact coefficient blocks, stored in this order: the four diagonal blocks,
+// the three sub-diagonal ones, then (exact solver only) the far blocks.
+__host__ __device__ constexpr int blk_row(int b) {
+    return b < 4 ? b : (b < 7 ? b - 3 : (b == 7 ? 2 : (b == 8 ? 3 : 3)));
+}
+__host__ __device__ constexpr int blk_col(int b) {
+    return b < 4 ? b : (b < 7 ? b - 4 : (b == 7 ? 0 : (b == 8 ? 1 : 0)));
+}
+
+// Status bits latched in counts[2].
+constexpr int kStatusEventOverflow = 1;
+constexpr int kStatusSnapOverflow = 2;
+
+// ---- storage-type helpers --------------------------------------------------
+template <typename T> struct io;
+template <> struct io<float> {
+    static __device__ __forceinline__ float ld(const float *p) { return *p; }
+    static __device__ __forceinline__ void st(float *p, float x) { *p = x; }
+};
+template <> struct io<__nv_bfloat16> {
+    static __device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ void st(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+// ---- problem description shared by the launchers -------------------------
+struct Problem {
+    int B, T, Nq, Nv, d, dv, C, G, P, R;
+    gdn_dtype dtype;
+    gdn_solver solver;
+    int nblk;                  // 7 (block-adjacent) or 10 (exact)
+    const void *q, *k, *v;
+    const float *beta, *g, *h0;
+    const uint8_t *mask;       // NULL: every chunk is an event
+    void *o;
+    float *s_final, *score;
+    cudaStream_t stream;
+};
+
+// Workspace layout (all offsets 256-byte aligned).
+struct Workspace {
+    int32_t *counts;           // [4]: E, n_snap, status, reserved
+    int32_t *row_pair, *row_ptr, *ev_chunk, *grp_pred, *snap_slot;
+    double *P;                 // [B, Nv, C+1] log2 decay prefix (Eq. 19)
+    void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
+    float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks
+    void *W;                   // [ev_cap, 2, 64, d] dtype, deferred W of events
+    float *snap;               // [snap_cap, 2, d, dv] post-event state snapshots
+    int64_t ev_cap, snap_cap;
+};
+
+size_t workspace_layout(const Problem &pb, void *base, Workspace *ws);
+
+// ---- launchers (each returns cudaGetLastError()) --------------------------
+cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap);
+cudaError_t launch_prefix(const Problem &pb, const Workspace &ws);
+cudaError_t launch_intra(const Problem &pb, const Workspace &ws);
+cudaError_t launch_wbuild(const Problem &pb, const Workspace &ws);
+cudaError_t launch_scan(const Problem &pb, const Workspace &ws);
+cudaError_t launch_output(const Problem &pb, const Workspace &ws);
+
+}  // namespace gdn

@@ -26,8 +26,9 @@ loads, which are not available):
       chunks 0 and C-1 are always kept plus k_p - 2 others uniformly without
       replacement.  Each sequence of a batch draws its own mask.
 
-Seeds follow 1000*config + 100*layer + batch_index; every draw uses numpy's
-PCG64 generator so the same bits come out on x86 and Arm hosts.
+Seeds follow 1000*config + 100*layer + batch_index.  Every draw uses numpy's
+PCG64 generator; tensors are drawn in blocks of 2048 tokens, each from its own
+SeedSequence child, so the same bits come out on any host and thread count.
 """
 from __future__ import annotations
 
@@ -89,13 +90,40 @@ class Inputs:
 
 
 def _l2n(x: np.ndarray) -> np.ndarray:
-    n = np.sqrt((x.astype(np.float64) ** 2).sum(-1, keepdims=True))
-    return (x / np.maximum(n, 1e-30)).astype(np.float32)
+    n = np.sqrt(np.einsum("...i,...i->...", x, x, dtype=np.float32))[..., None]
+    return (x / np.maximum(n, np.float32(1e-30))).astype(np.float32)
 
 
 def _round(x: np.ndarray, dtype: str) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     return bf16_bits_to_f32(f32_to_bf16_bits(x)) if dtype == "bf16" else x
+
+
+TOKEN_BLOCK = 2048  # tokens per independently seeded generation block
+
+
+def _blocks(B: int, T: int):
+    return [(b, t0, min(T, t0 + TOKEN_BLOCK)) for b in range(B) for t0 in range(0, T, TOKEN_BLOCK)]
+
+
+def _fill(seed: int, tag: int, out: np.ndarray, draw) -> None:
+    """Fill out[b, t0:t1] block by block; block (b, t0) draws from its own
+    SeedSequence child [seed, tag, b, t0 // TOKEN_BLOCK], so the result does
+    not depend on thread scheduling or the host."""
+    import concurrent.futures as cf
+
+    def work(blk):
+        b, t0, t1 = blk
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, b, t0 // TOKEN_BLOCK])))
+        out[b, t0:t1] = draw(rng, (t1 - t0,) + out.shape[2:])
+
+    blocks = _blocks(out.shape[0], out.shape[1])
+    if len(blocks) <= 1:
+        for blk in blocks:
+            work(blk)
+        return
+    with cf.ThreadPoolExecutor(max_workers=min(16, len(blocks))) as ex:
+        list(ex.map(work, blocks))
 
 
 def make_mask(rng: np.random.Generator, B: int, P: int, C: int, kind: str,
@@ -141,22 +169,28 @@ def make_inputs(B: int, T: int, Nq: int, Nv: int, d: int = 128, dv: int = 128,
     """Draw one seeded layer of inputs; see the module docstring for the recipe."""
     if Nv != 2 * Nq:
         raise ValueError("value heads come in adjacent pairs per query/key head (Nv == 2*Nq)")
-    rng = np.random.default_rng(seed)
-    q = _l2n(rng.standard_normal((B, T, Nq, d), dtype=np.float32))
-    k = _l2n(rng.standard_normal((B, T, Nq, d), dtype=np.float32))
-    v = rng.standard_normal((B, T, Nv, dv), dtype=np.float32)
-    beta = (1.0 / (1.0 + np.exp(-rng.standard_normal((B, T, Nv), dtype=np.float32)))).astype(np.float32)
-    a = -rng.uniform(0.001, 0.05, size=(B, T, Nv)).astype(np.float32)
+    q = np.empty((B, T, Nq, d), np.float32)
+    k = np.empty((B, T, Nq, d), np.float32)
+    v = np.empty((B, T, Nv, dv), np.float32)
+    beta = np.empty((B, T, Nv), np.float32)
+    a = np.empty((B, T, Nv), np.float32)
+    normal_qk = lambda r, shp: _round(_l2n(r.standard_normal(shp, dtype=np.float32)), dtype)
+    _fill(seed, 1, q, normal_qk)
+    _fill(seed, 2, k, normal_qk)
+    _fill(seed, 3, v, lambda r, shp: _round(r.standard_normal(shp, dtype=np.float32), dtype))
+    _fill(seed, 4, beta, lambda r, shp: (1.0 / (1.0 + np.exp(-r.standard_normal(shp, dtype=np.float32)))).astype(np.float32))
+    _fill(seed, 5, a, lambda r, shp: -r.uniform(0.001, 0.05, size=shp).astype(np.float32))
     C = (T + CHUNK - 1) // CHUNK
     g = np.empty_like(a)
-    for c in range(C):
-        t0, t1 = c * CHUNK, min(T, (c + 1) * CHUNK)
-        g[:, t0:t1] = np.cumsum(a[:, t0:t1], axis=1, dtype=np.float32)
+    if T:
+        full = (T // CHUNK) * CHUNK
+        g[:, :full] = np.cumsum(a[:, :full].reshape(B, T // CHUNK, CHUNK, Nv), axis=2, dtype=np.float32).reshape(B, full, Nv)
+        if full < T:
+            g[:, full:] = np.cumsum(a[:, full:], axis=1, dtype=np.float32)
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0]))
     m = make_mask(rng, B, Nv // 2, C, mask, retention)
     h0 = rng.standard_normal((B, Nv, d, dv), dtype=np.float32) * np.float32(0.1) if with_h0 else None
-    return Inputs(B, T, Nq, Nv, d, dv, dtype,
-                  _round(q, dtype), _round(k, dtype), _round(v, dtype),
-                  beta, g, m, h0,
+    return Inputs(B, T, Nq, Nv, d, dv, dtype, q, k, v, beta, g, m, h0,
                   meta={"seed": seed, "mask": mask, "retention_target": retention})
 
 

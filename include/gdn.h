@@ -1,0 +1,171 @@
+/*
+ * gdn.h -- C ABI of libgdn: the chunkwise (64-token) Gated Delta Network
+ * prefill core on NVIDIA GB300 (sm_103a), dense and event-sparse forms.
+ *
+ * Source of the operator: "SparseGDN: Chunk Sparse in Linear Attention"
+ * (arXiv 2610.41420v1), as paraphrased by its Chinese reading notes:
+ *   Sec. 2.1, Eqs. 1-4   dense chunkwise recurrence and chunk output
+ *   Sec. 2.3, Eqs. 5-9   local Delta system, block-adjacent solver, Tail-16 score
+ *   Sec. 2.5, Eqs. 15-16 deferred W, CSR event layout, device-resident event count
+ *   Sec. 2.6, Eqs. 17-21 event-sparse propagation and prefix-gap recovery
+ *   Sec. 2.7, Eqs. 22-25 two-chunk group output from compact state snapshots
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Shapes.  B sequences of T tokens; Nq query/key heads of width d; Nv = 2*Nq
+ * value heads of width dv.  Value heads 2p and 2p+1 form head pair p and read
+ * query/key head p.  C = T/64 chunks, G = ceil(C/2) output groups, P = Nq
+ * pairs.  This version requires d == dv == 128 and T % 64 == 0 (T == 0 and
+ * B == 0 are accepted).
+ *
+ * Layouts (row-major, contiguous, innermost last):
+ *   q, k      [B, T, Nq, d]      dtype (bf16 or fp32)
+ *   v, o      [B, T, Nv, dv]     dtype
+ *   beta      [B, T, Nv]         fp32, per-token update strength
+ *   g         [B, T, Nv]         fp32, log2 retention accumulated inside each
+ *                                64-token chunk, inclusive of the token's own
+ *                                gate (the pages' g_{c,h,i})
+ *   mask      [B, P, C]          uint8 0/1 event mask, shared by a head pair
+ *   h0, s_final [B, Nv, d, dv]   fp32 recurrent state (key dim x value dim)
+ *   score     [B, Nv, C]         fp32 Tail-16 write score s_{c,h} (Eq. 9)
+ *   O is the GDN-core output before RMSNorm, output gate and projection,
+ *   scaled by 1/sqrt(d).
+ *
+ * Memory and streams.  Every pointer is a caller-owned DEVICE pointer on the
+ * current CUDA device, 16-byte aligned (the workspace: 256-byte aligned).  The
+ * library never allocates, never frees and never synchronises, except
+ * gdn_workspace_status().  Work is enqueued on `stream` (a cudaStream_t; NULL
+ * = legacy default stream) and is complete only when that stream is.  The
+ * event count E never leaves the device.  Calls on distinct workspaces are
+ * independent; two calls that share a workspace must be stream-ordered.
+ *
+ * Errors.  Argument problems are detected on the host before anything is
+ * enqueued and returned synchronously (GDN_ERR_NULL / SHAPE / DTYPE / ALIGN /
+ * WORKSPACE / UNSUPPORTED / DEVICE).  A failed launch returns GDN_ERR_CUDA.
+ * Conditions only the GPU can see (event or snapshot capacity exceeded) are
+ * latched in a device status word; the kernels never write past a capacity,
+ * and gdn_workspace_status() / gdn_events_status() report the latch.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDN_ERR_SHAPE = 2,       /* unsupported or inconsistent sizes */
+    GDN_ERR_DTYPE = 3,       /* unknown dtype or solver enum */
+    GDN_ERR_ALIGN = 4,       /* a pointer is not 16-byte (workspace: 256-byte) aligned */
+    GDN_ERR_WORKSPACE = 5,   /* workspace smaller than gdn_workspace_bytes() */
+    GDN_ERR_UNSUPPORTED = 6, /* valid request this build does not implement */
+    GDN_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+    GDN_ERR_DEVICE = 8,      /* current device is not a compute-capability 10.3 GPU */
+    GDN_ERR_CAPACITY = 9     /* (device-latched) more events or snapshots than capacity */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
+
+/* Intra-chunk solver for M = I + A_Delta (Sec. 2.3).
+ * EXACT ("Full64"): C = M^-1.  BLOCK_ADJ: only the four diagonal and three
+ * sub-diagonal 16x16 blocks of M^-1 are kept (Eq. 7). */
+typedef enum { GDN_SOLVER_EXACT = 0, GDN_SOLVER_BLOCK_ADJ = 1 } gdn_solver;
+
+typedef struct {
+    int32_t B, T, Nq, Nv, d, dv;
+    gdn_dtype dtype; /* storage type of q, k, v, o (and of internal U / W) */
+} gdn_shape;
+
+/* CSR event lists (Sec. 2.5).  One row per (sequence b, head pair p), physical
+ * row id i = b*P + p.  Rows are ordered by event count descending, ties by
+ * physical id ascending ("long chains first"; a caller mask carries no tiers).
+ * Events inside a row ascend in chunk index.  All arrays are caller-owned
+ * device memory written by gdn_select_events(). */
+typedef struct {
+    int32_t *row_pair;  /* [B*P]       physical id of row j */
+    int32_t *row_ptr;   /* [B*P+1]     offset of row j's first event; row_ptr[B*P] = E */
+    int32_t *ev_chunk;  /* [capacity]  chunk index of event e */
+    int32_t *grp_pred;  /* [B*P*G]     indexed by physical id: global index of the last
+                                       event of that pair with chunk < 2r, or -1 */
+    int32_t *snap_slot; /* [capacity]  dense number (in event order) of the events some
+                                       group reads as predecessor, else -1 */
+    int32_t *counts;    /* [4]         E, number of snapshots, status bits, reserved */
+    int32_t capacity;   /* entries available in ev_chunk and snap_slot */
+} gdn_events;
+
+/* Bytes of workspace the prefill entry points need for `shape` (sparse != 0:
+ * gdn_prefill_sparse, else gdn_prefill_dense).  0 for invalid shapes. */
+GDN_API size_t gdn_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse);
+
+/* Event compaction (Sec. 2.5, Eq. 16): turn the [B,P,C] 0/1 mask into CSR
+ * event lists, the per-group predecessor event and the snapshot numbering.
+ * E = sum of the mask stays on the device (counts[0]).  If E > capacity the
+ * status bit 1 is set in counts[2], nothing past capacity is written and
+ * gdn_events_status() returns GDN_ERR_CAPACITY.  No workspace needed. */
+GDN_API gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask,
+                             gdn_events *events, void *stream);
+
+/* Synchronises `stream` and reports the status bits of an events struct. */
+GDN_API gdn_status gdn_events_status(const gdn_events *events, void *stream);
+
+/* Dense prefill (Secs. 2.1 and 2.3; Eqs. 1-8): every chunk is a recurrent
+ * event.  Writes o and s_final (the state after the last chunk, for decoding).
+ * h0 may be NULL (zero initial state); score may be NULL. */
+GDN_API gdn_status gdn_prefill_dense(const gdn_shape *shape,
+                             const void *q, const void *k, const void *v,
+                             const float *beta, const float *g, const float *h0,
+                             gdn_solver solver, void *o, float *s_final, float *score,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* Event-sparse prefill (Secs. 2.3-2.7; Eqs. 5-25).  Runs the whole pipeline on
+ * the GPU: intra-chunk solve and Tail-16 score for every chunk, mask -> CSR
+ * compaction, deferred W for selected events only, the event scan (read and
+ * write only on selected events, decay always), and the two-chunk group
+ * output from compact state snapshots.  Selected chunks write U' in place of
+ * U; unselected chunks keep U.  mask: [B,P,C] uint8 0/1.  h0 and score may be
+ * NULL. */
+GDN_API gdn_status gdn_prefill_sparse(const gdn_shape *shape,
+                              const void *q, const void *k, const void *v,
+                              const float *beta, const float *g, const float *h0,
+                              const uint8_t *mask, gdn_solver solver,
+                              void *o, float *s_final, float *score,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream` and reports the device-latched status of the last
+ * prefill that used `workspace` (GDN_OK or GDN_ERR_CAPACITY). */
+GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream);
+
+GDN_API const char *gdn_status_string(gdn_status status);
+
+/* Stage timing for benchmarks.  While enabled, each prefill records a CUDA
+ * event before its first and after each of its six kernels on its own stream
+ * (stages: 0 select/compaction, 1 log-decay prefix, 2 intra, 3 deferred W,
+ * 4 scan, 5 group output), for up to 256 prefills.  Enabling (again) drops
+ * earlier records.  Not thread-safe: one host thread drives the profiler.
+ * The events are created on the first enable (no device memory). */
+GDN_API gdn_status gdn_profile_enable(int enable);
+
+/* Synchronises on the recorded events, writes the summed milliseconds of each
+ * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 6),
+ * the number of recorded prefills to *n_prefills, and clears the records. */
+GDN_API gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+GDN_API int32_t gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

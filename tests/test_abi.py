@@ -1,0 +1,111 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/gdn.h declares, sizes workspaces, and rejects bad arguments on the host
+before anything is enqueued (only argument errors are exercised here, so no
+pointer is ever dereferenced and no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_16_gb300 as gdn
+from gated_delta_rule_16_gb300 import _binding as bnd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_16_gb300 import build
+    build.build()
+    return gdn.load()
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]*?\b(gdn_\w+)\s*\(", text)))
+
+
+def test_exports_match_header(lib):
+    names = declared_entry_points()
+    assert names == sorted(bnd.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert gdn.gdn_version() == 100
+    for code in range(10):
+        assert lib.gdn_status_string(code)
+    assert lib.gdn_status_string(0) == b"ok"
+
+
+def shape(B=1, T=4096, Nq=16, Nv=32, d=128, dv=128, dtype=bnd.GDN_BF16):
+    return bnd.GdnShape(B, T, Nq, Nv, d, dv, dtype)
+
+
+def test_workspace_bytes(lib):
+    s = shape()
+    n_ex = gdn.gdn_workspace_bytes(s, "exact")
+    n_ba = gdn.gdn_workspace_bytes(s, "block_adj")
+    assert n_ex > n_ba > 0
+    # U alone is B*T*Nv*dv*2 bytes for bf16; the workspace holds at least that
+    assert n_ba > 1 * 4096 * 32 * 128 * 2
+    assert gdn.gdn_workspace_bytes(shape(d=64, dv=64)) == 0
+    assert gdn.gdn_workspace_bytes(shape(T=100)) == 0
+    assert gdn.gdn_workspace_bytes(shape(Nv=31)) == 0
+    assert gdn.gdn_workspace_bytes(shape(T=0)) > 0
+    # grows linearly with the batch
+    assert gdn.gdn_workspace_bytes(shape(B=2)) > 1.9 * n_ba
+
+
+FAKE = 1 << 20  # aligned fake address: never dereferenced, every call below fails validation first
+
+
+def call_dense(lib, s, ptrs=None, ws=FAKE, ws_bytes=1 << 40, solver=1):
+    p = ptrs or {}
+    get = lambda n: ctypes.c_void_p(p.get(n, FAKE))
+    return lib.gdn_prefill_dense(ctypes.byref(s), get("q"), get("k"), get("v"), get("beta"), get("g"),
+                                 ctypes.c_void_p(p.get("h0")), solver, get("o"), get("s"),
+                                 ctypes.c_void_p(p.get("score")), ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_host_validation(lib):
+    assert call_dense(lib, shape(d=64, dv=64)) == 6          # UNSUPPORTED
+    assert call_dense(lib, shape(T=100)) == 6                 # UNSUPPORTED: T % 64
+    assert call_dense(lib, shape(Nv=31)) == 2                 # SHAPE
+    assert call_dense(lib, shape(dtype=7)) == 3               # DTYPE
+    assert call_dense(lib, shape(), solver=5) == 3            # DTYPE (solver)
+    assert call_dense(lib, shape(), ptrs={"q": 0}) == 1       # NULL
+    assert call_dense(lib, shape(), ptrs={"o": FAKE + 4}) == 4  # ALIGN
+    assert call_dense(lib, shape(), ws=FAKE + 16) == 4        # ALIGN: workspace needs 256 bytes
+    assert call_dense(lib, shape(), ws_bytes=1024) == 5       # WORKSPACE
+    assert call_dense(lib, shape(), ws=0) == 1                # NULL workspace
+    # B == 0 is a valid empty call: nothing to do, nothing touched
+    assert call_dense(lib, shape(B=0), ptrs={n: 0 for n in ("q", "k", "v", "beta", "g", "o", "s")}, ws=0) == 0
+
+
+def test_sparse_requires_mask(lib):
+    s = shape()
+    get = ctypes.c_void_p(FAKE)
+    rc = lib.gdn_prefill_sparse(ctypes.byref(s), get, get, get, get, get, None, None, 1, get, get, None,
+                                get, 1 << 40, None)
+    assert rc == 1
+
+
+def test_select_events_validation(lib):
+    ev = bnd.GdnEvents(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 10)
+    assert lib.gdn_select_events(ctypes.byref(shape()), None, ctypes.byref(ev), None) == 1
+    ev2 = bnd.GdnEvents(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1)
+    assert lib.gdn_select_events(ctypes.byref(shape()), ctypes.c_void_p(FAKE), ctypes.byref(ev2), None) == 2
+    ev3 = bnd.GdnEvents(FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, 10)
+    assert lib.gdn_select_events(ctypes.byref(shape()), ctypes.c_void_p(FAKE), ctypes.byref(ev3), None) == 4
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        bnd._lib, saved = None, bnd._lib
+        try:
+            bnd.load(str(tmp_path / "missing.so"))
+        finally:
+            bnd._lib = saved

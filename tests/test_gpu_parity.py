@@ -1,0 +1,180 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU fp64 oracle.
+
+Element-by-element comparisons on seeded inputs at sizes the oracle finishes
+in seconds (several chunks, groups, pairs, sequences, and an odd chunk count),
+plus the full-size sparse layer (T = 32768) checked on sampled head pairs.
+CSR event lists are compared bit for bit.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import gdn_synth
+import oracle
+from gpu_helpers import TOL, assert_close, dev, max_rel_err, run_gpu, slice_pairs, to_dev
+
+import gated_delta_rule_16_gb300 as gdn
+
+pytestmark = pytest.mark.gpu
+
+SOLVER = {"exact": oracle.SOLVER_EXACT, "block_adj": oracle.SOLVER_BLOCK_ADJ}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from gated_delta_rule_16_gb300 import build
+    build.build()
+    gdn.load()
+
+
+def oracle_run(x, solver, sparse=True, mask=None, h0="inputs", debug=False):
+    m = (x.mask if mask is None else mask) if sparse else None
+    h = x.h0 if isinstance(h0, str) else h0
+    return oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=m, h0=h, solver=SOLVER[solver], debug=debug)
+
+
+# ------------------------------------------------------------- tiny fp32 ---
+
+@pytest.mark.parametrize("solver", ["exact", "block_adj"])
+@pytest.mark.parametrize("sparse", [True, False])
+def test_tiny_fp32(solver, sparse):
+    x = gdn_synth.make_workload("tiny_fp32_T256")
+    res = run_gpu(x, solver=solver, sparse=sparse)
+    assert_close(res, oracle_run(x, solver, sparse), "f32", f"tiny {solver} sparse={sparse}")
+
+
+@pytest.mark.parametrize("solver", ["exact", "block_adj"])
+def test_tiny_fp32_all_16_masks(solver):
+    x = gdn_synth.make_workload("tiny_fp32_T256", with_h0=True)
+    for bits in itertools.product([0, 1], repeat=4):
+        m = np.array(bits, np.uint8).reshape(1, 1, 4)
+        for h0 in (None, x.h0):
+            res = run_gpu(x, solver=solver, mask=m, h0=h0 if h0 is not None else np.zeros_like(x.h0))
+            ref = oracle_run(x, solver, mask=m, h0=h0)
+            assert_close(res, ref, "f32", f"mask {bits} h0={h0 is not None}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ragged_groups_batch_and_h0(dtype):
+    # 5 chunks (last group has one chunk), 3 pairs, 2 sequences, random masks and an initial state
+    x = gdn_synth.make_inputs(2, 320, 3, 6, dtype=dtype, seed=21, mask="bernoulli", retention=0.5, with_h0=True)
+    for solver in ("exact", "block_adj"):
+        res = run_gpu(x, solver=solver, score=True)
+        ref = oracle_run(x, solver, debug=True)
+        assert_close(res, ref, dtype, f"ragged {dtype} {solver}")
+        rel = np.abs(res["score"] - ref["score"]) / np.maximum(ref["score"], 1e-30)
+        assert rel.max() <= TOL[dtype]
+
+
+def test_single_chunk_and_empty_sequence():
+    x = gdn_synth.make_inputs(1, 64, 2, 4, dtype="f32", seed=22, mask="ones", with_h0=True)
+    for sparse in (True, False):
+        assert_close(run_gpu(x, sparse=sparse), oracle_run(x, "block_adj", sparse), "f32", "T=64")
+    # T = 0: the final state is the initial state
+    t = to_dev(x)
+    e = lambda *s: torch.empty(*s, device=dev())
+    q = e((1, 0, 2, 128)); v = e((1, 0, 4, 128)); bg = e((1, 0, 4))
+    o, s = gdn.gdn_prefill_dense(q, q, v, bg, bg, h0=t["h0"])
+    torch.cuda.synchronize()
+    assert torch.equal(s, t["h0"])
+    o, s = gdn.gdn_prefill_dense(q, q, v, bg, bg)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(s).item() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_zero_mask_decay_only(dtype):
+    x = gdn_synth.make_inputs(1, 512, 2, 4, dtype=dtype, seed=23, mask="zeros", with_h0=True)
+    assert_close(run_gpu(x), oracle_run(x, "block_adj"), dtype, "zero mask with h0")
+    r = run_gpu(x, h0=np.zeros_like(x.h0))
+    assert np.count_nonzero(r["s_final"]) == 0
+
+
+def test_all_ones_sparse_equals_dense_bitwise():
+    x = gdn_synth.make_inputs(1, 512, 2, 4, dtype="bf16", seed=24, mask="ones")
+    for solver in ("exact", "block_adj"):
+        a = run_gpu(x, solver=solver, sparse=True)
+        b = run_gpu(x, solver=solver, sparse=False)
+        assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["s_final"], b["s_final"])
+
+
+# ----------------------------------------------------------------- CSR ---
+
+@pytest.mark.parametrize("shape,p", [((1, 1, 4), 0.5), ((2, 3, 7), 0.4), ((3, 16, 33), 0.29),
+                                     ((1, 16, 512), 0.29), ((8, 16, 512), 0.29), ((2, 3, 6), 1.0),
+                                     ((2, 3, 6), 0.0), ((1, 16, 2048), 0.1), ((4, 5, 1), 0.5)])
+def test_csr_bit_exact(shape, p):
+    rng = np.random.default_rng(sum(shape))
+    m = (rng.random(shape) < p).astype(np.uint8)
+    ev = gdn.gdn_select_events(torch.from_numpy(m).to(dev()))
+    assert gdn.gdn_events_status(ev) == 0
+    ref = oracle.events(m)
+    E = ref["n_events"]
+    counts = ev["counts"].cpu().numpy()
+    assert counts[0] == E and counts[1] == ref["n_snap"] and counts[2] == 0
+    B, P, C = shape
+    assert np.array_equal(ev["row_pair"].cpu().numpy()[:B * P], ref["row_pair"])
+    assert np.array_equal(ev["row_ptr"].cpu().numpy(), ref["row_ptr"])
+    assert np.array_equal(ev["ev_chunk"].cpu().numpy()[:E], ref["ev_chunk"])
+    assert np.array_equal(ev["grp_pred"].cpu().numpy()[:B * P * ((C + 1) // 2)], ref["grp_pred"].ravel())
+    assert np.array_equal(ev["snap_slot"].cpu().numpy()[:E], ref["snap_slot"])
+
+
+def test_csr_all_16_masks():
+    for bits in itertools.product([0, 1], repeat=4):
+        m = np.array(bits, np.uint8).reshape(1, 1, 4)
+        ev = gdn.gdn_select_events(torch.from_numpy(m).to(dev()))
+        ref = oracle.events(m)
+        E = ref["n_events"]
+        assert np.array_equal(ev["ev_chunk"].cpu().numpy()[:E], ref["ev_chunk"])
+        assert np.array_equal(ev["grp_pred"].cpu().numpy()[:2], ref["grp_pred"].ravel())
+        assert np.array_equal(ev["snap_slot"].cpu().numpy()[:E], ref["snap_slot"])
+
+
+def test_csr_capacity_overflow_latched():
+    m = np.ones((1, 2, 8), np.uint8)
+    ev = gdn.gdn_select_events(torch.from_numpy(m).to(dev()), capacity=5)
+    assert gdn.gdn_events_status(ev) == 9
+    assert ev["counts"][0].item() == 16
+
+
+# ------------------------------------------------------- layer-sized bf16 ---
+
+@pytest.mark.parametrize("solver", ["exact", "block_adj"])
+def test_dense_layer_T4096(solver):
+    x = gdn_synth.make_workload("qwen35_4b_layer_T4096_dense")
+    res = run_gpu(x, solver=solver, sparse=False)
+    assert_close(res, oracle_run(x, solver, sparse=False), "bf16", f"T=4096 dense {solver}")
+
+
+def test_sparse_layer_T32768_sampled_pairs():
+    x = gdn_synth.make_workload("qwen35_4b_layer_T32768_sparse29")
+    res = run_gpu(x, solver="block_adj")
+    counts = x.mask[0].sum(-1)
+    pairs = [int(np.argmax(counts)), int(np.argmin(counts)), 7]
+    for p in pairs:
+        y = slice_pairs(x, 0, [p])
+        ref = oracle_run(y, "block_adj")
+        got = {"o": res["o"][:, :, 2 * p:2 * p + 2], "s_final": res["s_final"][:, 2 * p:2 * p + 2]}
+        assert_close(got, ref, "bf16", f"T=32768 pair {p} ({counts[p]} events)")
+
+
+def test_batch8_T32768_sampled_pairs():
+    x = gdn_synth.make_workload("qwen35_4b_layer_B8_T32768_sparse29")
+    res = run_gpu(x, solver="block_adj")
+    for b, p in ((0, 3), (5, 11), (7, 0)):
+        y = slice_pairs(x, b, [p])
+        ref = oracle_run(y, "block_adj")
+        got = {"o": res["o"][b:b + 1, :, 2 * p:2 * p + 2], "s_final": res["s_final"][b:b + 1, 2 * p:2 * p + 2]}
+        assert_close(got, ref, "bf16", f"B=8 seq {b} pair {p}")
+
+
+def test_workspace_status_ok_after_prefill():
+    x = gdn_synth.make_inputs(1, 256, 1, 2, dtype="bf16", seed=25, mask="two_of_four")
+    ws = gdn.Workspace()
+    run_gpu(x, workspace=ws)
+    assert gdn.gdn_workspace_status(ws) == 0
