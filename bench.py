@@ -1,0 +1,348 @@
+#!/usr/bin/env python3
+"""GDN-core prefill throughput on one GB300: tokens/s per layer and % of roofline.
+
+One step = one pass of the whole hot path over one synthetic layer: mask ->
+CSR compaction, log-decay prefix, intra-chunk solve, deferred W, event scan and
+group output, all in libgdn's CUDA kernels through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+Default workload: one Qwen3.5-4B-shaped GDN layer, B=1, T=32768, N_q=16,
+N_v=32, d=d_v=128, bf16, event-sparse path at 29% retention (Beta(2,5)
+per-pair budgets), block-adjacent solver.  Under torchrun every rank runs its
+own independent sequence (weak scaling, no collective on the data path).
+
+--impl reference times the CPU fp64 oracle (the only reference this build has)
+on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "GDN-core prefill tokens/s per layer at T=32K, 29% events; % of roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen35_4b_layer_T32768_sparse29")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------ accounting ---
+
+def algorithmic_bytes(x, kernel: str, n_snap: int = 0) -> float:
+    """Compulsory bytes of one launch: inputs read once, outputs written once.
+
+    step   : q, k, v, beta, g, mask in; o and s_final out (the whole core).
+    output : q, k, U' (the workspace U buffer), g in; o out; plus one entry
+             state per (group, value head) read from the fp32 snapshots.
+    intra  : k, v, beta, g in; U (dtype) and the compact C-bar blocks (fp32) out.
+    scan   : per selected (pair-)event, for both value heads: W and U read, U'
+             written (dtype), K read once per pair; g in; the post-event fp32
+             snapshots that output groups reference written; s_final out.
+    """
+    es = 2 if x.dtype == "bf16" else 4
+    B, T, Nq, Nv, d, dv, C = x.B, x.T, x.Nq, x.Nv, x.d, x.dv, x.C
+    G = (C + 1) // 2
+    qk = B * T * Nq * d * es
+    vo = B * T * Nv * dv * es
+    bg = B * T * Nv * 4
+    if kernel == "step":
+        return 2 * qk + 2 * vo + 2 * bg + B * Nv * d * dv * 4 + x.mask.size
+    if kernel == "output":
+        return 2 * qk + 2 * vo + bg + B * Nv * G * d * dv * 4
+    if kernel == "intra":
+        return qk + 2 * vo + 2 * bg + B * Nv * C * 7 * 256 * 4
+    if kernel == "scan":
+        E = int(x.mask.sum())
+        per_event = 64 * d * es + 2 * (2 * 64 * d * es + 2 * 64 * dv * es + 64 * 4)
+        return E * per_event + n_snap * 2 * d * dv * 4 + B * Nv * d * dv * 4
+    raise ValueError(kernel)
+
+
+# ------------------------------------------------------------------ clocks ---
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# -------------------------------------------------------------- the oracle ---
+
+def oracle_sample(x, pairs, t_tokens, nthreads):
+    """Time the oracle on head pairs `pairs` of sequence 0 over the first t_tokens tokens."""
+    import oracle
+    vi = [2 * p + j for p in pairs for j in (0, 1)]
+    C = t_tokens // 64
+    sl = lambda a, idx: np.ascontiguousarray(a[0:1, :t_tokens][:, :, idx])
+    q, k = sl(x.q, pairs), sl(x.k, pairs)
+    v, beta, g = sl(x.v, vi), sl(x.beta, vi), sl(x.g, vi)
+    mask = np.ascontiguousarray(x.mask[0:1][:, pairs, :C])
+    t0 = time.perf_counter()
+    oracle.prefill(q, k, v, beta, g, mask=mask, solver=oracle.SOLVER_BLOCK_ADJ, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    # tokens of the whole layer this sample stands for: t_tokens x (fraction of the layer's heads)
+    return t_tokens * len(pairs) / x.Nq / dt, dt, min(nthreads, 2 * len(pairs))
+
+
+def cpu_baseline(x):
+    cores = os.cpu_count() or 1
+    npairs = max(1, min(x.Nq, cores))
+    pairs = list(range(npairs))
+    t_tokens = min(x.T, 16384)
+    value, dt, used = oracle_sample(x, pairs, t_tokens, nthreads=min(2 * npairs, cores))
+    return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"fp64 C oracle, head pairs 0..{npairs - 1} of {x.Nq}, tokens 0..{t_tokens - 1} of sequence 0 "
+                      f"({dt:.1f} s wall, {used} threads); tokens/s scaled to the full layer by the head fraction"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import gdn_synth
+    x = gdn_synth.make_workload(args.workload)
+    cores = os.cpu_count() or 1
+    npairs = max(1, min(x.Nq, cores // 2, 4))
+    t_tokens = min(x.T, 4096)
+    times, vals = [], []
+    used = 1
+    for step in range(args.warmup + args.steps):
+        pairs = [(step * npairs + i) % x.Nq for i in range(npairs)]
+        v, dt, used = oracle_sample(x, pairs, t_tokens, nthreads=2 * npairs)
+        if step >= args.warmup:
+            times.append(dt)
+            vals.append(v)
+    ms = 1000.0 * statistics.mean(times)
+    value = t_tokens * npairs / x.Nq / (ms / 1000.0)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "B": x.B, "T": x.T, "Nq": x.Nq, "Nv": x.Nv, "d": x.d, "dv": x.dv,
+                       "retention": round(x.retention(), 4), "solver": "block_adj"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": f"each step: {npairs} head pairs (cycling) x tokens 0..{t_tokens - 1} of "
+                                       f"sequence 0; tokens/s scaled to the full layer by the head fraction"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------ our CUDA path ---
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_16_gb300 as gdn
+    import gdn_synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    x = gdn_synth.make_workload(args.workload, batch_index=rank)   # each rank: its own independent sequence(s)
+    tok = x.B * x.T
+    st = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+    host = {
+        "q": torch.from_numpy(x.q).to(st).pin_memory(), "k": torch.from_numpy(x.k).to(st).pin_memory(),
+        "v": torch.from_numpy(x.v).to(st).pin_memory(), "beta": torch.from_numpy(x.beta).pin_memory(),
+        "g": torch.from_numpy(x.g).pin_memory(), "mask": torch.from_numpy(x.mask).pin_memory(),
+    }
+    d_in = {n: t.to(dev) for n, t in host.items()}
+    o = torch.empty((x.B, x.T, x.Nv, x.dv), dtype=st, device=dev)
+    s_final = torch.empty((x.B, x.Nv, x.d, x.dv), dtype=torch.float32, device=dev)
+    ws = gdn.Workspace()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdn.gdn_prefill_sparse(d_in["q"], d_in["k"], d_in["v"], d_in["beta"], d_in["g"], d_in["mask"],
+                               solver="block_adj", o=o, s_final=s_final, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if gdn.gdn_workspace_status(ws) != 0:
+        raise RuntimeError("device-side capacity overflow in the warm-up")
+    # the library's device counters at workspace offset 0: E, snapshots written, status
+    n_events, n_snap = (int(v) for v in ws.buf[:8].view(torch.int32).cpu().tolist())
+
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    gdn.gdn_profile_enable(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    stage_ms, nrec = gdn.gdn_profile_read()
+    gdn.gdn_profile_enable(False)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = tok * world / (ms / 1000.0)
+
+    # end to end through the public API: pinned host inputs -> device -> prefill -> host outputs
+    h_o = torch.empty(o.shape, dtype=st).pin_memory()
+    h_s = torch.empty(s_final.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_o.numel() * h_o.element_size() + h_s.numel() * h_s.element_size()
+
+    def e2e_step():
+        dd = {n: t.to(dev, non_blocking=True) for n, t in host.items()}
+        oo, ss = gdn.gdn_prefill_sparse(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["mask"],
+                                        solver="block_adj", workspace=ws, stream=stream)
+        h_o.copy_(oo, non_blocking=True)
+        h_s.copy_(ss, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peak, peak_kind = peaks()
+    per_stage = {k: v / max(nrec, 1) for k, v in stage_ms.items()}
+    dom = max(per_stage, key=per_stage.get)
+    dom_kernel = dom if dom in ("output", "intra", "scan") else "step"
+    dom_ms = per_stage[dom] if dom_kernel != "step" else ms
+    achieved = algorithmic_bytes(x, dom_kernel, n_snap) / (dom_ms / 1000.0) / 1e9
+    step_gbs = algorithmic_bytes(x, "step") / (ms / 1000.0) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": x.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "B": x.B, "T": x.T, "Nq": x.Nq, "Nv": x.Nv, "d": x.d, "dv": x.dv,
+                   "retention": round(x.retention(), 4), "events": n_events, "snapshots": n_snap,
+                   "solver": "block_adj",
+                   "l2": "inputs larger than L2 (%.0f MB compulsory bytes per step), no flush" %
+                         (algorithmic_bytes(x, "step") / 1e6),
+                   "parallelism": "one independent sequence per GPU" if world > 1 else "single GPU"},
+        "clocks": clk,
+        "e2e": {"value": tok * world / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": len(gdn.STAGES) * args.steps,
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                     "step_frac": step_gbs / peak,
+                     "note": f"achieved = compulsory bytes of one {dom_kernel} launch / its mean CUDA-event time; "
+                             f"frac of {peak_kind} HBM copy bandwidth"},
+        "stages_ms": {k: round(v, 4) for k, v in per_stage.items()},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
