@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     gdn_events_status,
     gdn_prefill_dense,
     gdn_prefill_sparse,
+    gdn_prefill_sparse_noalloc,
     gdn_profile_enable,
     gdn_profile_read,
     gdn_select_events,

@@ -23,7 +23,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE"
           9: "GDN_ERR_CAPACITY"}
 EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn_prefill_dense",
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
-           "gdn_profile_enable", "gdn_profile_read")
+           "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc")
 STAGES = ("select", "prefix", "intra", "wbuild", "scan", "output")
 
 
@@ -70,6 +70,8 @@ def load(path: str | None = None):
             lib.gdn_prefill_dense.restype = i32
             lib.gdn_prefill_sparse.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
             lib.gdn_prefill_sparse.restype = i32
+            lib.gdn_prefill_sparse_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+            lib.gdn_prefill_sparse_noalloc.restype = i32
             lib.gdn_workspace_status.argtypes = [vp, vp]
             lib.gdn_workspace_status.restype = i32
             lib.gdn_status_string.argtypes = [i32]
@@ -201,6 +203,39 @@ def gdn_prefill_sparse(q, k, v, beta, g, mask, *, h0=None, solver="block_adj", o
         raise ValueError("gdn_prefill_sparse needs an event mask")
     return _prefill("gdn_prefill_sparse", q, k, v, beta, g, mask, h0, solver, o, s_final, score, workspace,
                     stream)
+
+
+def gdn_prefill_sparse_noalloc(q, k, v, beta, g, mask, *, h0=None, solver="block_adj", o=None, s_final=None,
+                               score=None, stream=None):
+    """Allocation-free event-sparse prefill (library-owned 64 MiB scratch); returns (o, s_final).
+
+    For callers that cannot allocate device memory; see include/gdn.h.  The
+    outputs must be passed in by such callers (o, s_final); when omitted here
+    they are created with torch for convenience.
+    """
+    B, T, Nq, d = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    C = (T + 63) // 64
+    _need(q, "q", shape=(B, T, Nq, d))
+    _need(k, "k", dtype=q.dtype, shape=(B, T, Nq, d))
+    _need(v, "v", dtype=q.dtype, shape=(B, T, Nv, dv))
+    _need(beta, "beta", torch.float32, (B, T, Nv))
+    _need(g, "g", torch.float32, (B, T, Nv))
+    _need(h0, "h0", torch.float32, (B, Nv, d, dv))
+    _need(mask, "mask", torch.uint8, (B, Nv // 2, C))
+    if o is None:
+        o = torch.empty((B, T, Nv, dv), dtype=q.dtype, device=q.device)
+    if s_final is None:
+        s_final = torch.empty((B, Nv, d, dv), dtype=torch.float32, device=q.device)
+    _need(o, "o", q.dtype, (B, T, Nv, dv))
+    _need(s_final, "s_final", torch.float32, (B, Nv, d, dv))
+    _need(score, "score", torch.float32, (B, Nv, C))
+    shape = shape_of(q, v)
+    with torch.cuda.device(q.device):
+        _check("gdn_prefill_sparse_noalloc", load().gdn_prefill_sparse_noalloc(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(mask),
+            SOLVERS[solver], _ptr(o), _ptr(s_final), _ptr(score), _stream(stream)))
+    return o, s_final
 
 
 def gdn_select_events(mask: torch.Tensor, Nq: int | None = None, capacity: int | None = None, stream=None):

@@ -142,6 +142,35 @@ GDN_API gdn_status gdn_prefill_sparse(const gdn_shape *shape,
                               void *o, float *s_final, float *score,
                               void *workspace, size_t workspace_bytes, void *stream);
 
+/* Allocation-free event-sparse prefill.  The paper has no counterpart: this
+ * is a deployment aid for callers that cannot allocate device memory -- for
+ * example a plugin inside a host runtime that owns all device memory and
+ * passes the plugin only its inputs and outputs, or a latency-critical server
+ * that forbids cudaMalloc after start-up.  Same arguments, pipeline and
+ * results as gdn_prefill_sparse(), but no workspace argument: the scratch is a
+ * fixed array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) in the library's device
+ * memory, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing and calls no allocating routine.
+ *   - Size limit: shapes with gdn_workspace_bytes(shape, solver, 1) above
+ *     64 MiB are rejected with GDN_ERR_WORKSPACE before anything is enqueued
+ *     (with this version's workspace layout: B=1, Nq=16, bf16,
+ *     block-adjacent up to T = 1792; one head pair in fp32 up to T = 20352).
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress, with that device current).  Make that
+ *     first call before any stream capture.
+ *   - Sharing: every call uses the same array and it keeps the last call's
+ *     contents.  Nothing in it must start at zero (each value read is written
+ *     earlier in the same call), but calls that overlap on the GPU (other
+ *     streams, other host threads) race on it: serialise them.
+ *   - The device status word lives in that array: read it with
+ *     gdn_workspace_status() only on a workspace you own, not here. */
+#define GDN_NOALLOC_SCRATCH_BYTES (64ull << 20)
+GDN_API gdn_status gdn_prefill_sparse_noalloc(const gdn_shape *shape,
+                                      const void *q, const void *k, const void *v,
+                                      const float *beta, const float *g, const float *h0,
+                                      const uint8_t *mask, gdn_solver solver,
+                                      void *o, float *s_final, float *score, void *stream);
+
 /* Synchronises `stream` and reports the device-latched status of the last
  * prefill that used `workspace` (GDN_OK or GDN_ERR_CAPACITY). */
 GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream);
