@@ -302,7 +302,7 @@ def run_ours(args):
     peak, peak_kind = peaks()
     per_stage = {k: v / max(nrec, 1) for k, v in stage_ms.items()}
     dom = max(per_stage, key=per_stage.get)
-    dom_kernel = dom if dom in ("output", "intra", "scan") else "step"
+    dom_kernel = dom if dom in ("output", "intra") else "step"
     dom_ms = per_stage[dom] if dom_kernel != "step" else ms
     achieved = algorithmic_bytes(x, dom_kernel, n_snap) / (dom_ms / 1000.0) / 1e9
     step_gbs = algorithmic_bytes(x, "step") / (ms / 1000.0) / 1e9

@@ -20,11 +20,11 @@ GDN_BF16, GDN_F32 = 0, 1
 SOLVERS = {"exact": 0, "block_adj": 1}
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE", 4: "GDN_ERR_ALIGN",
           5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_UNSUPPORTED", 7: "GDN_ERR_CUDA", 8: "GDN_ERR_DEVICE",
-          9: "GDN_ERR_CAPACITY"}
+          9: "GDN_ERR_CAPACITY", 10: "GDN_ERR_TIMEOUT"}
 EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn_prefill_dense",
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
            "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc")
-STAGES = ("select", "prefix", "intra", "wbuild", "scan", "output")
+STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output")
 
 
 class GdnError(RuntimeError):

@@ -16,7 +16,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // ---- stage profiler (benchmark aid; see gdn_profile_enable) ----------------
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr int kProfSlots = 256;
 struct Profiler {
     bool on = false, created = false;
@@ -55,7 +55,9 @@ gdn_status check_shape(const gdn_shape *s) {
     if (s->T % kChunk != 0) return GDN_ERR_UNSUPPORTED;
     // index arithmetic uses int32 for chunk/row/event counts
     const int64_t C = s->T / kChunk;
-    if ((int64_t)s->B * s->Nq * C >= (int64_t)1 << 30) return GDN_ERR_SHAPE;
+    // event tiles are addressed by int32 TMA row coordinates: events x 128 rows < 2^31
+    if ((int64_t)s->B * s->Nq * C >= (int64_t)1 << 24) return GDN_ERR_SHAPE;
+    if ((int64_t)s->B * s->T >= (int64_t)1 << 31) return GDN_ERR_SHAPE;
     if ((int64_t)s->B * s->Nq > 8192) return GDN_ERR_UNSUPPORTED;  // compaction keeps rows in shared memory
     return GDN_OK;
 }
@@ -94,6 +96,11 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
     const size_t o_W = take((size_t)ev_cap * 2 * kChunk * pb.d * es);
     const size_t o_snap = take((size_t)snap_cap * 2 * pb.d * pb.dv * sizeof(float));
+    const int64_t nr = pb.dtype == GDN_BF16 ? (C + kRunChunks - 1) / kRunChunks : 0;
+    const size_t run_elems = (size_t)R * 2 * nr * kDim * kDim;
+    const size_t o_amap = take(run_elems * 2);
+    const size_t o_bmap = take(run_elems * sizeof(float));
+    const size_t o_entry = take(run_elems * sizeof(float));
     if (ws) {
         char *b = (char *)base;
         ws->counts = (int32_t *)(b + o_counts);
@@ -107,6 +114,9 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
         ws->cbar = (float *)(b + o_cbar);
         ws->W = b + o_W;
         ws->snap = (float *)(b + o_snap);
+        ws->amap = b + o_amap;
+        ws->bmap = (float *)(b + o_bmap);
+        ws->entry = (float *)(b + o_entry);
         ws->ev_cap = ev_cap;
         ws->snap_cap = snap_cap;
     }
@@ -158,10 +168,15 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     mark(3);
     if (e == cudaSuccess) e = launch_wbuild(pb, ws);
     mark(4);
-    if (e == cudaSuccess) e = launch_scan(pb, ws);
+    const bool tc = pb.dtype == GDN_BF16;   // tensor-core path for bf16 storage
+    if (e == cudaSuccess && tc) e = launch_scan_tc(pb, ws, 0);
     mark(5);
-    if (e == cudaSuccess) e = launch_output(pb, ws);
+    if (e == cudaSuccess && tc) e = launch_scan_tc(pb, ws, 1);
     mark(6);
+    if (e == cudaSuccess) e = tc ? launch_scan_tc(pb, ws, 2) : launch_scan(pb, ws);
+    mark(7);
+    if (e == cudaSuccess) e = launch_output(pb, ws);
+    mark(8);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -170,6 +185,7 @@ gdn_status read_status(const int32_t *counts, void *stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
     int32_t host[4] = {0, 0, 0, 0};
     if (cudaMemcpy(host, counts, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    if (host[2] & kStatusTimeout) return GDN_ERR_TIMEOUT;
     return host[2] ? GDN_ERR_CAPACITY : GDN_OK;
 }
 
@@ -249,6 +265,7 @@ const char *gdn_status_string(gdn_status status) {
         case GDN_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
         case GDN_ERR_DEVICE: return "current device is not a compute-capability 10.3 (GB300) GPU";
         case GDN_ERR_CAPACITY: return "device-side event or snapshot capacity exceeded";
+        case GDN_ERR_TIMEOUT: return "a kernel gave up waiting after its time limit (device-latched)";
     }
     return "unknown status";
 }

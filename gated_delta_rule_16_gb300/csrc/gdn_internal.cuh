@@ -27,6 +27,10 @@ __host__ __device__ constexpr int blk_col(int b) {
 // Status bits latched in counts[2].
 constexpr int kStatusEventOverflow = 1;
 constexpr int kStatusSnapOverflow = 2;
+constexpr int kStatusTimeout = 4;     // a kernel gave up a wait after its time limit
+
+// Chunks per run of the tensor-core scan (the serial chain inside a run).
+constexpr int kRunChunks = 16;
 
 // ---- storage-type helpers --------------------------------------------------
 template <typename T> struct io;
@@ -62,6 +66,10 @@ struct Workspace {
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks
     void *W;                   // [ev_cap, 2, 64, d] dtype, deferred W of events
     float *snap;               // [snap_cap, 2, d, dv] post-event state snapshots
+    // tensor-core scan (bf16 storage only; NR = ceil(C / kRunChunks))
+    void *amap;                // [R, 2, NR, 128, 128] bf16: A_r^T of each run
+    float *bmap;               // [R, 2, NR, 128, 128] B_r^T of each run
+    float *entry;              // [R, 2, NR, 128, 128] S^T entering each run
     int64_t ev_cap, snap_cap;
 };
 
@@ -74,5 +82,7 @@ cudaError_t launch_intra(const Problem &pb, const Workspace &ws);
 cudaError_t launch_wbuild(const Problem &pb, const Workspace &ws);
 cudaError_t launch_scan(const Problem &pb, const Workspace &ws);
 cudaError_t launch_output(const Problem &pb, const Workspace &ws);
+// part 0: run maps, 1: chain over runs, 2: per-run fix-up (writes U' and snapshots)
+cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part);
 
 }  // namespace gdn

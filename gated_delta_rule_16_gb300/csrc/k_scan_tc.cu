@@ -1,0 +1,469 @@
+// k_scan_tc.cu -- the event-sparse state scan (SparseGDN Secs. 2.1, 2.6;
+// Eqs. 1-2, 17-21) on tcgen05 tensor cores, for bf16 storage.
+//
+// Splitting the serial chain.  A CSR row (one head pair) can hold hundreds of
+// events, and each event needs the state left by the previous one.  Every
+// event, and every skipped chunk, maps the state affinely:
+//     S -> 2^gamma S + K^T D (U - W S) = A_e S + B_e,    D = diag(2^(gamma - g)),
+// so a run of 16 chunks maps its entry state S_r to A_r S_r + B_r.  Three
+// launches replace the row-long chain:
+//   1. scan_run_kernel, "map" mode, all runs in parallel: the run's events
+//      applied to the identity with U = 0 give A_r (homogeneous part), applied
+//      to 0 with the true U give B_r (inhomogeneous part);
+//   2. scan_chain_kernel, per (row, head): S_{r+1} = A_r S_r + B_r, one
+//      128x128x128 MMA per run; writes every run's entry state and S_final;
+//   3. scan_run_kernel, "fix-up" mode, all runs in parallel: the run's events
+//      from the true entry state, writing U' = U - W S in place of U and the
+//      post-event snapshots that output groups read.
+// The longest serial chain is then 16 events (plus one MMA per run), not a row.
+//
+// Layout.  Columns of S evolve independently, so the CTA works on S^T: TMEM
+// lane / state row = a column of S (d_v index), 128 rows; 256 threads, thread
+// (row, half) holds 64 of the row's 128 fp32 entries in registers.  Per event:
+//   MMA1  U'^T_acc[128 x 64]  = S^T[128 x 128] . W^T      (A: S^T bf16 K-major; B: W [t][d] K-major)
+//   U'^T = U^T - U'^T_acc;  U''^T = U'^T * 2^(gamma - g_t)        (registers)
+//   MMA2  dS^T[128 x 128]     = U''^T[128 x 64] . K        (A: U''^T K-major; B: K [t][d] MN-major)
+//   S^T <- 2^gamma S^T + dS^T                                      (registers)
+// W, K and U tiles of the next event are TMA-prefetched (double buffer).
+#include "gdn_internal.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 256;
+constexpr int kRun = kRunChunks;
+constexpr uint32_t kSlab = 16384;        // [128 rows][128 B]
+constexpr uint32_t OFF_A1 = 0;           // S^T bf16, K-major, 2 slabs
+constexpr uint32_t OFF_A2 = 2 * kSlab;   // U''^T bf16, K-major, 1 slab
+constexpr uint32_t OFF_BUF = 3 * kSlab;  // two event buffers follow
+constexpr uint32_t BUF_W = 0;            // W [64 t][128 d]: 2 K-slabs of [64][128 B], 8192 apart
+constexpr uint32_t BUF_K = 16384;        // K MN-major: 2 stacks of [64 t][64 d], 8192 apart
+constexpr uint32_t BUF_U = 32768;        // U [64 t][128 dv] bf16, unswizzled
+constexpr uint32_t BUF_BYTES = 49152;
+constexpr uint32_t kRunSmem = 1024 + OFF_BUF + 2 * BUF_BYTES;
+constexpr uint32_t TM_U = 0;             // TMEM columns [0, 64): U'^T accumulator
+constexpr uint32_t TM_S = 64;            // TMEM columns [64, 192): dS^T accumulator
+constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab;
+
+enum { kModeHomog = 0, kModeInhom = 1, kModeFixup = 2 };
+
+struct ScanParams {
+    const int32_t *row_pair, *row_ptr, *ev_chunk, *snap_slot;
+    const double *P;
+    const float *g, *h0;
+    __nv_bfloat16 *U;       // [B,T,Nv,128]: U, replaced by U' for events (fix-up mode)
+    __nv_bfloat16 *amap;    // [R,2,NR,128,128] A_r^T (row m' = column m' of A_r)
+    float *bmap;            // [R,2,NR,128,128] B_r^T
+    float *entry;           // [R,2,NR,128,128] S_r^T entering each run
+    float *snap;            // [snap_cap,2,128 d,128 dv] post-event states (fp32)
+    float *s_final;         // [B,Nv,128 d,128 dv]
+    int32_t *status;
+    int P_, T_, Nv, C, NR;
+    int64_t ev_cap, snap_cap;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void fail(const ScanParams &a, int *abort_flag) {
+    *abort_flag = 1;
+    atomicOr(a.status, kStatusTimeout);
+}
+
+// grid: (runs NR, map mode: 2 heads x {homog, inhom} | fix-up: 2 heads, CSR rows R)
+__global__ void __launch_bounds__(kThreads, 1)
+scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tK,
+                const __grid_constant__ CUtensorMap tU, ScanParams a, int fixup) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = align1024(smraw);
+    __shared__ uint64_t bar_tma[2], bar_mma1, bar_mma2;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_s, n_ev_s, e_first_s;
+    __shared__ int ev_c[kRun], ev_slot[kRun];
+    __shared__ double Pl[kRun + 1];
+    __shared__ float gl[kRun][kChunk];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int rho = blockIdx.x, j = blockIdx.z;
+    const int hh = fixup ? (int)blockIdx.y : (int)(blockIdx.y >> 1);
+    const int mode = fixup ? kModeFixup : (int)(blockIdx.y & 1);
+    const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
+    const int c_lo = rho * kRun, c_hi = min(a.C, c_lo + kRun);
+
+    if (tid == 0) {
+        const int64_t e0 = min((int64_t)a.row_ptr[j], a.ev_cap), e1 = min((int64_t)a.row_ptr[j + 1], a.ev_cap);
+        int64_t lo = e0, hi = e1;
+        while (lo < hi) {
+            const int64_t m = (lo + hi) >> 1;
+            if (a.ev_chunk[m] < c_lo) lo = m + 1; else hi = m;
+        }
+        const int64_t first = lo;
+        hi = e1;
+        while (lo < hi) {
+            const int64_t m = (lo + hi) >> 1;
+            if (a.ev_chunk[m] < c_hi) lo = m + 1; else hi = m;
+        }
+        n_ev_s = (int)(lo - first);
+        e_first_s = (int)first;
+        abort_s = 0;
+    }
+    __syncthreads();
+    const int n_ev = n_ev_s;
+    if (n_ev == 0) return;  // a run without events: the chain kernel applies its decay
+    const int e_first = e_first_s;
+    const int64_t ubase = (((int64_t)i * 2 + hh) * a.NR + rho) * (kDim * kDim);
+    if (tid < n_ev) {
+        ev_c[tid] = a.ev_chunk[e_first + tid];
+        ev_slot[tid] = a.snap_slot[e_first + tid];
+    }
+    const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
+    if (tid <= c_hi - c_lo) Pl[tid] = Pu[c_lo + tid];
+    if (tid == 0) {
+        mbar_init(&bar_tma[0], 1);
+        mbar_init(&bar_tma[1], 1);
+        mbar_init(&bar_mma1, 1);
+        mbar_init(&bar_mma2, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc<256>(&tmem_base);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    for (int idx = tid; idx < n_ev * kChunk; idx += kThreads) {
+        const int k = idx >> 6, t = idx & 63;
+        gl[k][t] = a.g[((int64_t)b * a.T_ + (int64_t)ev_c[k] * kChunk + t) * a.Nv + h];
+    }
+    const uint32_t tbase = tmem_base;
+    uint8_t *A1 = sm + OFF_A1;
+    uint8_t *A2 = sm + OFF_A2;
+    const uint32_t tx_bytes = mode == kModeHomog ? 32768u : 49152u;
+    auto issue_tma = [&](int k) {
+        uint8_t *buf = sm + OFF_BUF + (k & 1) * BUF_BYTES;
+        const int wrow = ((e_first + k) * 2 + hh) * kChunk;
+        const int tok = b * a.T_ + ev_c[k] * kChunk;
+        uint64_t *bar = &bar_tma[k & 1];
+        mbar_arrive_expect_tx(bar, tx_bytes);
+        tma_load_3d(buf + BUF_W, &tW, 0, wrow, 0, bar);
+        tma_load_3d(buf + BUF_W + 8192, &tW, 64, wrow, 0, bar);
+        tma_load_3d(buf + BUF_K, &tK, 0, p, tok, bar);
+        tma_load_3d(buf + BUF_K + 8192, &tK, 64, p, tok, bar);
+        if (mode != kModeHomog) tma_load_3d(buf + BUF_U, &tU, 0, h, tok, bar);
+    };
+    int tma_issued = 0;  // thread 0: events whose tiles were requested
+    if (tid == 0) {
+        issue_tma(0);
+        tma_issued = 1;
+    }
+
+    float S[64];
+    if (mode == kModeHomog) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) S[jj] = (64 * hf + jj == row) ? 1.f : 0.f;
+    } else if (mode == kModeInhom) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) S[jj] = 0.f;
+    } else {
+        const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase + row * kDim + 64 * hf);
+#pragma unroll
+        for (int v4 = 0; v4 < 16; ++v4) {
+            const float4 x = src[v4];
+            S[4 * v4] = x.x; S[4 * v4 + 1] = x.y; S[4 * v4 + 2] = x.z; S[4 * v4 + 3] = x.w;
+        }
+    }
+    __syncthreads();  // gl[] complete
+
+    const uint32_t id1 = idesc_bf16(128, 64, false, false);
+    const uint32_t id2 = idesc_bf16(128, 128, false, true);
+    int cur = c_lo;
+    int k = 0;
+    for (; k < n_ev; ++k) {
+        const int c = ev_c[k];
+        uint8_t *buf = sm + OFF_BUF + (k & 1) * BUF_BYTES;
+        const float gap = exp2f((float)(Pl[c - c_lo] - Pl[cur - c_lo]));
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) S[jj] *= gap;
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(A1 + hf * kSlab, row, k0, &S[k0]);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            if (!mbar_wait(&bar_tma[k & 1], (k >> 1) & 1)) {
+                fail(a, &abort_s);
+            } else {
+                tc_fence_after();
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(A1), ks, kSlab),
+                             kmajor_desc(smem_addr(buf + BUF_W), ks, 8192), id1, ks > 0);
+                mma_commit(&bar_mma1);
+                if (k + 1 < n_ev) {
+                    issue_tma(k + 1);
+                    tma_issued = k + 2;
+                }
+            }
+        }
+        __syncthreads();
+        if (abort_s) break;
+        if (!mbar_wait(&bar_mma1, k & 1)) fail(a, &abort_s);
+        tc_fence_after();
+        float acc[32];
+        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 32 * hf), acc);
+        tmem_ld_wait();
+        const __nv_bfloat16 *Ut = reinterpret_cast<const __nv_bfloat16 *>(buf + BUF_U);
+        const float gam = gl[k][kChunk - 1];
+        const int64_t tok0 = (int64_t)b * a.T_ + (int64_t)c * kChunk;
+        float up[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const int tt = 32 * hf + t;
+            const float u = mode == kModeHomog ? 0.f : __bfloat162float(Ut[tt * kDim + row]);
+            const float v = u - acc[t];
+            if (mode == kModeFixup) a.U[((tok0 + tt) * a.Nv + h) * kDim + row] = __float2bfloat16_rn(v);
+            up[t] = v * exp2f(gam - gl[k][tt]);
+        }
+#pragma unroll
+        for (int t0 = 0; t0 < 32; t0 += 8) st_sw128_8(A2, row, 32 * hf + t0, &up[t0]);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (abort_s) break;
+        if (tid == 0) {
+            tc_fence_after();
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tbase + TM_S, kmajor_desc(smem_addr(A2), ks, kSlab),
+                         mnmajor_desc(smem_addr(buf + BUF_K), ks, 8192), id2, ks > 0);
+            mma_commit(&bar_mma2);
+        }
+        if (!mbar_wait(&bar_mma2, k & 1)) fail(a, &abort_s);
+        tc_fence_after();
+        float d0[32], d1[32];
+        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + 64 * hf), d0);
+        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + 64 * hf + 32), d1);
+        tmem_ld_wait();
+        const float dg = exp2f(gam);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            S[jj] = dg * S[jj] + d0[jj];
+            S[32 + jj] = dg * S[32 + jj] + d1[jj];
+        }
+        if (mode == kModeFixup) {
+            const int slot = ev_slot[k];
+            if (slot >= 0 && slot < a.snap_cap) {
+                float *sn = a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim);
+#pragma unroll
+                for (int jj = 0; jj < 64; ++jj) sn[(64 * hf + jj) * kDim + row] = S[jj];
+            }
+        }
+        cur = c + 1;
+        tc_fence_before();
+        __syncthreads();
+        if (abort_s) break;
+    }
+    if (!abort_s && mode != kModeFixup) {
+        const float fin = exp2f((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
+        if (mode == kModeHomog) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.amap + ubase + row * kDim + 64 * hf);
+#pragma unroll
+            for (int v8 = 0; v8 < 8; ++v8) {
+                __nv_bfloat162 w[4];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2)
+                    w[q2] = __floats2bfloat162_rn(S[8 * v8 + 2 * q2] * fin, S[8 * v8 + 2 * q2 + 1] * fin);
+                dst[v8] = *reinterpret_cast<uint4 *>(w);
+            }
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(a.bmap + ubase + row * kDim + 64 * hf);
+#pragma unroll
+            for (int v4 = 0; v4 < 16; ++v4)
+                dst[v4] = make_float4(S[4 * v4] * fin, S[4 * v4 + 1] * fin, S[4 * v4 + 2] * fin, S[4 * v4 + 3] * fin);
+        }
+    }
+    if (abort_s && tid == 0) {
+        // drain: tiles still in flight into shared memory, and the MMAs issued so far
+        for (int kk = k + 1; kk < tma_issued; ++kk) mbar_wait(&bar_tma[kk & 1], (kk >> 1) & 1);
+        mma_commit(&bar_mma2);
+        mbar_wait(&bar_mma2, (k + 1) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<256>(tbase);
+}
+
+// grid: (2 heads, CSR rows R).  S_{r+1}^T = S_r^T A_r^T + B_r^T over the runs.
+__global__ void __launch_bounds__(kThreads, 1)
+scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = align1024(smraw);
+    __shared__ uint64_t bar_tma[2], bar_mma;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int hh = blockIdx.x, j = blockIdx.y;
+    const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
+    const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
+    const int64_t e0 = min((int64_t)a.row_ptr[j], a.ev_cap), e1 = min((int64_t)a.row_ptr[j + 1], a.ev_cap);
+    const int64_t sbase = ((int64_t)b * a.Nv + h) * (kDim * kDim);
+    const int64_t rbase = ((int64_t)i * 2 + hh) * a.NR;
+
+    if (tid == 0) {
+        mbar_init(&bar_tma[0], 1);
+        mbar_init(&bar_tma[1], 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        abort_s = 0;
+    }
+    if (warp == 0) tmem_alloc<128>(&tmem_base);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base;
+    uint8_t *Atile = sm;
+    uint8_t *Mbuf = sm + 2 * kSlab;
+
+    float S[64];
+#pragma unroll
+    for (int jj = 0; jj < 64; ++jj) S[jj] = a.h0 ? a.h0[sbase + (int64_t)(64 * hf + jj) * kDim + row] : 0.f;
+
+    // next run (>= r) holding an event of this row, from event cursor e; NR if none
+    auto next_run = [&](int64_t e) -> int { return e < e1 ? a.ev_chunk[e] / kRun : a.NR; };
+    int64_t ecur = e0;
+    int n_loads = 0, n_mma = 0;
+    int pending_run = -1;
+    if (tid == 0) {
+        const int r0 = next_run(ecur);
+        if (r0 < a.NR) {
+            mbar_arrive_expect_tx(&bar_tma[0], 2 * kSlab);
+            tma_load_3d(Mbuf, &tA, 0, (int)((rbase + r0) * kDim), 0, &bar_tma[0]);
+            tma_load_3d(Mbuf + kSlab, &tA, 64, (int)((rbase + r0) * kDim), 0, &bar_tma[0]);
+            pending_run = r0;
+            n_loads = 1;
+        }
+    }
+    const uint32_t idesc = idesc_bf16(128, 128, false, true);
+    int used = 0;  // map tiles consumed
+    for (int r = 0; r < a.NR; ++r) {
+        const int c_lo = r * kRun, c_hi = min(a.C, c_lo + kRun);
+        float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim) + row * kDim + 64 * hf);
+#pragma unroll
+        for (int v4 = 0; v4 < 16; ++v4) ent[v4] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+        const bool has = ecur < e1 && a.ev_chunk[ecur] < c_hi;
+        if (!has) {
+            const float f = exp2f((float)(Pu[c_hi] - Pu[c_lo]));
+#pragma unroll
+            for (int jj = 0; jj < 64; ++jj) S[jj] *= f;
+            continue;
+        }
+        while (ecur < e1 && a.ev_chunk[ecur] < c_hi) ++ecur;
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(Atile + hf * kSlab, row, k0, &S[k0]);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        const int bufi = used & 1;
+        if (tid == 0) {
+            if (!mbar_wait(&bar_tma[bufi], (used >> 1) & 1)) {
+                fail(a, &abort_s);
+            } else {
+                tc_fence_after();
+                uint8_t *mt = Mbuf + bufi * 2 * kSlab;
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tbase, kmajor_desc(smem_addr(Atile), ks, kSlab), mnmajor_desc(smem_addr(mt), ks, kSlab),
+                             idesc, ks > 0);
+                mma_commit(&bar_mma);
+                const int rn = next_run(ecur);
+                if (rn < a.NR) {
+                    const int nb = (used + 1) & 1;
+                    uint8_t *dst = Mbuf + nb * 2 * kSlab;
+                    mbar_arrive_expect_tx(&bar_tma[nb], 2 * kSlab);
+                    tma_load_3d(dst, &tA, 0, (int)((rbase + rn) * kDim), 0, &bar_tma[nb]);
+                    tma_load_3d(dst + kSlab, &tA, 64, (int)((rbase + rn) * kDim), 0, &bar_tma[nb]);
+                    ++n_loads;
+                }
+            }
+        }
+        // B_r^T row, fetched while the MMA runs
+        float Bm[64];
+        const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r) * (kDim * kDim) + row * kDim + 64 * hf);
+#pragma unroll
+        for (int v4 = 0; v4 < 16; ++v4) {
+            const float4 x = bsrc[v4];
+            Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
+        }
+        __syncthreads();
+        if (abort_s) break;
+        if (!mbar_wait(&bar_mma, n_mma & 1)) fail(a, &abort_s);
+        ++n_mma;
+        ++used;
+        tc_fence_after();
+        float d0[32], d1[32];
+        tmem_ld32(tmem_addr(tbase, quarter * 32, 64 * hf), d0);
+        tmem_ld32(tmem_addr(tbase, quarter * 32, 64 * hf + 32), d1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            S[jj] = d0[jj] + Bm[jj];
+            S[32 + jj] = d1[jj] + Bm[32 + jj];
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (abort_s) break;
+    }
+    if (!abort_s) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) a.s_final[sbase + (int64_t)(64 * hf + jj) * kDim + row] = S[jj];
+    } else if (tid == 0) {
+        for (int u = used + 1; u < n_loads; ++u) mbar_wait(&bar_tma[u & 1], (u >> 1) & 1);
+        mma_commit(&bar_mma);
+        mbar_wait(&bar_mma, n_mma & 1);
+    }
+    (void)pending_run;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<128>(tbase);
+}
+
+}  // namespace
+
+cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
+    if (pb.R == 0) return cudaSuccess;
+    const int NR = (pb.C + kRun - 1) / kRun;
+    ScanParams a;
+    a.row_pair = ws.row_pair; a.row_ptr = ws.row_ptr; a.ev_chunk = ws.ev_chunk; a.snap_slot = ws.snap_slot;
+    a.P = ws.P; a.g = pb.g; a.h0 = pb.h0;
+    a.U = (__nv_bfloat16 *)ws.U; a.amap = (__nv_bfloat16 *)ws.amap; a.bmap = ws.bmap; a.entry = ws.entry;
+    a.snap = ws.snap; a.s_final = pb.s_final; a.status = ws.counts + 2;
+    a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.NR = NR;
+    a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
+    if (part == 1) {  // chain
+        CUtensorMap tA;
+        if (!make_tmap_bf16_3d(&tA, ws.amap, kDim, (uint64_t)pb.R * 2 * (NR > 0 ? NR : 1) * kDim, 1, kDim * 2,
+                               (uint64_t)pb.R * 2 * (NR > 0 ? NR : 1) * kDim * kDim * 2, 64, 128, 1, true))
+            return cudaErrorInvalidValue;
+        cudaFuncSetAttribute(scan_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
+        scan_chain_kernel<<<dim3(2, pb.R), kThreads, kChainSmem, pb.stream>>>(tA, a);
+        return cudaGetLastError();
+    }
+    if (NR == 0 || pb.C == 0) return cudaSuccess;
+    CUtensorMap tW, tK, tU;
+    const uint64_t BT = (uint64_t)pb.B * pb.T;
+    if (!make_tmap_bf16_3d(&tW, ws.W, kDim, (uint64_t)ws.ev_cap * 2 * kChunk, 1, kDim * 2,
+                           (uint64_t)ws.ev_cap * 2 * kChunk * kDim * 2, 64, 64, 1, true) ||
+        !make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 64, true) ||
+        !make_tmap_bf16_3d(&tU, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 128, 1, 64, false))
+        return cudaErrorInvalidValue;
+    cudaFuncSetAttribute(scan_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmem);
+    const int fixup = part == 2;
+    scan_run_kernel<<<dim3(NR, fixup ? 2 : 4, pb.R), kThreads, kRunSmem, pb.stream>>>(tW, tK, tU, a, fixup);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -26,11 +26,12 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }
 
 // A rank-3 bf16 tensor: dims[0] contiguous (elements), strides of dims 1 and 2
-// in bytes (multiples of 16), box {box0 (64 -> 128 B rows), box1, box2}.
-// Out-of-range box elements read as zero.  Returns false if encoding fails.
+// in bytes (multiples of 16), box {box0, box1, box2}.  swizzle128: the
+// 128-byte swizzle (box0 = 64), else rows land unswizzled.  Out-of-range box
+// elements read as zero.  Returns false if encoding fails.
 inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
-                              uint32_t box2) {
+                              uint32_t box2, bool swizzle128 = true) {
     auto enc = tmap_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -38,7 +39,7 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, u
     cuuint32_t box[3] = {box0, box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

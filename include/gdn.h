@@ -42,9 +42,11 @@
  * Errors.  Argument problems are detected on the host before anything is
  * enqueued and returned synchronously (GDN_ERR_NULL / SHAPE / DTYPE / ALIGN /
  * WORKSPACE / UNSUPPORTED / DEVICE).  A failed launch returns GDN_ERR_CUDA.
- * Conditions only the GPU can see (event or snapshot capacity exceeded) are
- * latched in a device status word; the kernels never write past a capacity,
- * and gdn_workspace_status() / gdn_events_status() report the latch.
+ * Conditions only the GPU can see (event or snapshot capacity exceeded, a
+ * wait inside a kernel that ran past its time limit) are latched in a device
+ * status word; the kernels never write past a capacity and never wait
+ * without a limit, and gdn_workspace_status() / gdn_events_status() report
+ * the latch.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -72,7 +74,8 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = 6, /* valid request this build does not implement */
     GDN_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
     GDN_ERR_DEVICE = 8,      /* current device is not a compute-capability 10.3 GPU */
-    GDN_ERR_CAPACITY = 9     /* (device-latched) more events or snapshots than capacity */
+    GDN_ERR_CAPACITY = 9,    /* (device-latched) more events or snapshots than capacity */
+    GDN_ERR_TIMEOUT = 10     /* (device-latched) a kernel wait exceeded its 2 s limit and was abandoned */
 } gdn_status;
 
 typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
@@ -178,15 +181,17 @@ GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream);
 GDN_API const char *gdn_status_string(gdn_status status);
 
 /* Stage timing for benchmarks.  While enabled, each prefill records a CUDA
- * event before its first and after each of its six kernels on its own stream
+ * event before its first and after each pipeline stage on its own stream
  * (stages: 0 select/compaction, 1 log-decay prefix, 2 intra, 3 deferred W,
- * 4 scan, 5 group output), for up to 256 prefills.  Enabling (again) drops
+ * 4 scan run maps, 5 scan chain over runs, 6 scan (fix-up, or the whole
+ * scan for fp32 storage), 7 group output; stages 4-5 are empty for fp32
+ * storage), for up to 256 prefills.  Enabling (again) drops
  * earlier records.  Not thread-safe: one host thread drives the profiler.
  * The events are created on the first enable (no device memory). */
 GDN_API gdn_status gdn_profile_enable(int enable);
 
 /* Synchronises on the recorded events, writes the summed milliseconds of each
- * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 6),
+ * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 8),
  * the number of recorded prefills to *n_prefills, and clears the records. */
 GDN_API gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills);
 

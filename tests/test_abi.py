@@ -35,7 +35,7 @@ def test_exports_match_header(lib):
 
 def test_version_and_status_strings(lib):
     assert gdn.gdn_version() == 100
-    for code in range(10):
+    for code in range(11):
         assert lib.gdn_status_string(code)
     assert lib.gdn_status_string(0) == b"ok"
 
