@@ -95,7 +95,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_U = take((size_t)pb.B * pb.T * pb.Nv * pb.dv * es);
     const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
     const size_t o_W = take((size_t)ev_cap * 2 * kChunk * pb.d * es);
-    const size_t o_snap = take((size_t)snap_cap * 2 * pb.d * pb.dv * sizeof(float));
+    const size_t o_snap = take((size_t)snap_cap * 2 * pb.d * pb.dv * es);
     const int64_t nr = pb.dtype == GDN_BF16 ? (C + kRunChunks - 1) / kRunChunks : 0;
     const size_t run_elems = (size_t)R * 2 * nr * kDim * kDim;
     const size_t o_amap = take(run_elems * 2);
@@ -113,7 +113,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
         ws->U = b + o_U;
         ws->cbar = (float *)(b + o_cbar);
         ws->W = b + o_W;
-        ws->snap = (float *)(b + o_snap);
+        ws->snap = b + o_snap;
         ws->amap = b + o_amap;
         ws->bmap = (float *)(b + o_bmap);
         ws->entry = (float *)(b + o_entry);
@@ -175,7 +175,7 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     mark(6);
     if (e == cudaSuccess) e = tc ? launch_scan_tc(pb, ws, 2) : launch_scan(pb, ws);
     mark(7);
-    if (e == cudaSuccess) e = launch_output(pb, ws);
+    if (e == cudaSuccess) e = tc ? launch_output_tc(pb, ws) : launch_output(pb, ws);
     mark(8);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

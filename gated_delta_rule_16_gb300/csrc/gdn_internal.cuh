@@ -65,7 +65,7 @@ struct Workspace {
     void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks
     void *W;                   // [ev_cap, 2, 64, d] dtype, deferred W of events
-    float *snap;               // [snap_cap, 2, d, dv] post-event state snapshots
+    void *snap;                // [snap_cap, 2, d, dv] post-event state snapshots (fp32; bf16 for bf16 storage)
     // tensor-core scan (bf16 storage only; NR = ceil(C / kRunChunks))
     void *amap;                // [R, 2, NR, 128, 128] bf16: A_r^T of each run
     float *bmap;               // [R, 2, NR, 128, 128] B_r^T of each run
@@ -84,5 +84,6 @@ cudaError_t launch_scan(const Problem &pb, const Workspace &ws);
 cudaError_t launch_output(const Problem &pb, const Workspace &ws);
 // part 0: run maps, 1: chain over runs, 2: per-run fix-up (writes U' and snapshots)
 cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part);
+cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws);
 
 }  // namespace gdn

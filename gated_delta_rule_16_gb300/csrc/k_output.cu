@@ -161,14 +161,14 @@ cudaError_t launch_output(const Problem &pb, const Workspace &ws) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
         kern<<<grid, kThreads, kOutSmem, pb.stream>>>(
             (const __nv_bfloat16 *)pb.q, (const __nv_bfloat16 *)pb.k, (const __nv_bfloat16 *)ws.U, pb.g, pb.h0, ws.P,
-            ws.ev_chunk, ws.grp_pred, ws.snap_slot, ws.snap, pb.P, pb.T, pb.Nq, pb.Nv, pb.C, pb.G, ws.ev_cap,
+            ws.ev_chunk, ws.grp_pred, ws.snap_slot, (float *)ws.snap, pb.P, pb.T, pb.Nq, pb.Nv, pb.C, pb.G, ws.ev_cap,
             ws.snap_cap, (__nv_bfloat16 *)pb.o);
     } else {
         auto kern = output_kernel<float>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
         kern<<<grid, kThreads, kOutSmem, pb.stream>>>(
             (const float *)pb.q, (const float *)pb.k, (const float *)ws.U, pb.g, pb.h0, ws.P, ws.ev_chunk,
-            ws.grp_pred, ws.snap_slot, ws.snap, pb.P, pb.T, pb.Nq, pb.Nv, pb.C, pb.G, ws.ev_cap, ws.snap_cap,
+            ws.grp_pred, ws.snap_slot, (float *)ws.snap, pb.P, pb.T, pb.Nq, pb.Nv, pb.C, pb.G, ws.ev_cap, ws.snap_cap,
             (float *)pb.o);
     }
     return cudaGetLastError();

@@ -1,0 +1,294 @@
+// k_output_tc.cu -- mapped two-chunk group output (SparseGDN Sec. 2.7,
+// Eqs. 22-24) on tcgen05 tensor cores, for bf16 storage.
+//
+// One CTA per (group r, head pair p, sequence b): 128 query tokens (chunks
+// c = 2r and c+1) against 128 key tokens.  TMEM holds three 128x128 fp32
+// accumulators:
+//   QK  = Q K^T                   (A: Q [tok][d] K-major; B: K [tok][d] K-major), shared by the pair
+//   QS  = Q S_c                   (B: snapshot S [d][dv] bf16, MN-major)
+//   AU  = A U'                    (A: decayed, masked QK in bf16, K-major; B: U' [tok][dv] MN-major)
+// per value head, where the mask/decay of A is
+//   same chunk, j <= i : 2^(g_i - g_j);   i in c+1, j in c : 2^(g_i + gamma_c - g_j);   else 0
+// and the epilogue forms O_i = (f 2^(g_i + shift_i) QS_i + AU_i) / sqrt(d) with
+// f = 2^(P_c - P_(e+1)) the gap decay of the predecessor snapshot (Eq. 21) and
+// shift_i = gamma_c for tokens of chunk c+1.  Operands arrive by TMA.
+#include "gdn_internal.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 256;
+constexpr uint32_t kSlab = 16384;          // [128 rows][128 B]
+constexpr uint32_t OFF_Q = 0;              // Q: 2 K-slabs
+constexpr uint32_t OFF_K = 2 * kSlab;      // K: 2 K-slabs; later S of head 1 (2 MN-stacks)
+constexpr uint32_t OFF_S0 = 4 * kSlab;     // S of head 0: 2 MN-stacks [128 d][64 dv]
+constexpr uint32_t OFF_U0 = 6 * kSlab;     // U' of head 0: 2 MN-stacks [128 tok][64 dv]
+constexpr uint32_t OFF_U1 = 8 * kSlab;     // U' of head 1
+constexpr uint32_t OFF_A = 10 * kSlab;     // decayed masked A: 2 K-slabs [128 q][64 k]
+constexpr uint32_t kOutSmem = 1024 + 12 * kSlab;
+constexpr uint32_t TM_QK = 0, TM_QS = 128, TM_AU = 256;
+
+struct OutParams {
+    const float *g, *h0;
+    const double *P;
+    const int32_t *ev_chunk, *grp_pred, *snap_slot;
+    __nv_bfloat16 *O;
+    int32_t *status;
+    int P_, T_, Nv, C, G;
+    int64_t ev_cap, snap_cap;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tK,
+                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tS, OutParams a) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = align1024(smraw);
+    __shared__ uint64_t bar_qk_ld, bar_h_ld[2], bar_s1, bar_qk_mma, bar_h_mma, bar_drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_s;
+    __shared__ float gs[2][128];
+    __shared__ float fscale[2];
+    __shared__ int has_s[2], slot_s[2];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int row = quarter * 32 + lane;  // query token inside the group
+    const int r = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
+    const int c0 = 2 * r;
+    const bool two = c0 + 1 < a.C;
+    const int tok0 = b * a.T_ + c0 * kChunk;
+
+    if (tid < 2) {
+        const int hh = tid, h = 2 * p + hh;
+        const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
+        const int pred = a.grp_pred[((int64_t)b * a.P_ + p) * a.G + r];
+        int has = 0, slot = -1;
+        float f = 0.f;
+        if (pred >= 0 && pred < a.ev_cap) {
+            slot = a.snap_slot[pred];
+            if (slot >= 0 && slot < a.snap_cap) {
+                has = 1;
+                f = exp2f((float)(Pu[c0] - Pu[a.ev_chunk[pred] + 1]));
+            }
+        } else if (a.h0) {
+            has = 2;  // initial state: converted by the threads below
+            f = exp2f((float)Pu[c0]);
+        }
+        has_s[hh] = has;
+        slot_s[hh] = slot;
+        fscale[hh] = f;
+    }
+    for (int idx = tid; idx < 256; idx += kThreads) {
+        const int hh = idx >> 7, t = idx & 127;
+        const bool valid = t < 64 || two;
+        gs[hh][t] = valid ? a.g[((int64_t)tok0 + t) * a.Nv + 2 * p + hh] : 0.f;
+    }
+    if (tid == 0) {
+        mbar_init(&bar_qk_ld, 1);
+        mbar_init(&bar_h_ld[0], 1);
+        mbar_init(&bar_h_ld[1], 1);
+        mbar_init(&bar_s1, 1);
+        mbar_init(&bar_qk_mma, 1);
+        mbar_init(&bar_h_mma, 1);
+        mbar_init(&bar_drain, 1);
+        fence_mbar_init();
+        abort_s = 0;
+    }
+    if (warp == 0) tmem_alloc<512>(&tmem_base);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base;
+
+    // initial-state path (no predecessor event, h0 given): S = h0 in bf16, MN-major stacks
+    auto fill_h0 = [&](int hh, uint8_t *dst) {
+        const float *src = a.h0 + ((int64_t)b * a.Nv + 2 * p + hh) * (kDim * kDim);
+        for (int idx = tid; idx < kDim * 16; idx += kThreads) {  // (d row, 8-wide dv chunk)
+            const int d = idx >> 4, ch = idx & 15;
+            float v[8];
+#pragma unroll
+            for (int q2 = 0; q2 < 8; ++q2) v[q2] = src[d * kDim + ch * 8 + q2];
+            st_sw128_8(dst + (ch >> 3) * kSlab, d, (ch & 7) * 8, v);
+        }
+        fence_async_smem();
+    };
+
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar_qk_ld, 4 * kSlab);
+        tma_load_3d(sm + OFF_Q, &tQ, 0, p, tok0, &bar_qk_ld);
+        tma_load_3d(sm + OFF_Q + kSlab, &tQ, 64, p, tok0, &bar_qk_ld);
+        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_qk_ld);
+        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_qk_ld);
+        for (int hh = 0; hh < 2; ++hh) {
+            uint8_t *ud = sm + (hh ? OFF_U1 : OFF_U0);
+            const bool snap0 = hh == 0 && has_s[0] == 1;
+            mbar_arrive_expect_tx(&bar_h_ld[hh], 2 * kSlab + (snap0 ? 2 * kSlab : 0));
+            tma_load_3d(ud, &tU, 0, 2 * p + hh, tok0, &bar_h_ld[hh]);
+            tma_load_3d(ud + kSlab, &tU, 64, 2 * p + hh, tok0, &bar_h_ld[hh]);
+            if (snap0) {
+                tma_load_3d(sm + OFF_S0, &tS, 0, slot_s[0] * 2 * kDim, 0, &bar_h_ld[0]);
+                tma_load_3d(sm + OFF_S0 + kSlab, &tS, 64, slot_s[0] * 2 * kDim, 0, &bar_h_ld[0]);
+            }
+        }
+    }
+    if (has_s[0] == 2) fill_h0(0, sm + OFF_S0);
+    __syncthreads();
+
+    const uint32_t id_kk = idesc_bf16(128, 128, false, false);
+    const uint32_t id_km = idesc_bf16(128, 128, false, true);
+    const float inv_sqrt_d = rsqrtf((float)kDim);
+    bool ok = true;
+    bool s1_issued = false;  // thread 0
+    if (tid == 0) {
+        ok = mbar_wait(&bar_qk_ld, 0);
+        if (ok) {
+            tc_fence_after();
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tbase + TM_QK, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                         kmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id_kk, ks > 0);
+            mma_commit(&bar_qk_mma);
+        }
+        if (!ok) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+    }
+    __syncthreads();
+
+    for (int hh = 0; hh < 2 && !abort_s; ++hh) {
+        // 1. A_h from QK (waits for the QK MMA; for head 1 also for head 0's AU MMA to free the A tile)
+        if (!mbar_wait(hh == 0 ? &bar_qk_mma : &bar_h_mma, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+        tc_fence_after();
+        {
+            const float *g = gs[hh];
+            const int ci = row >> 6;
+            const float gi = g[row];
+            const float gam0 = g[63];
+            for (int half32 = 0; half32 < 2; ++half32) {
+                float qk[32];
+                const int j0 = 64 * hf + 32 * half32;
+                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QK + j0), qk);
+                tmem_ld_wait();
+                float w[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int jj = j0 + t, cj = jj >> 6;
+                    float m = 0.f;
+                    if (ci == cj) m = jj <= row ? exp2f(gi - g[jj]) : 0.f;
+                    else if (ci == 1) m = exp2f(gi + gam0 - g[jj]);
+                    w[t] = (ci == 1 && !two) ? 0.f : qk[t] * m;
+                }
+#pragma unroll
+                for (int t0 = 0; t0 < 32; t0 += 8) st_sw128_8(sm + OFF_A + hf * kSlab, row, 32 * half32 + t0, &w[t0]);
+            }
+        }
+        if (hh == 1 && has_s[1] == 2) fill_h0(1, sm + OFF_K);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (abort_s) break;
+        // 2. QS_h and AU_h
+        if (tid == 0) {
+            const bool landed = mbar_wait(&bar_h_ld[hh], 0) && !(hh == 1 && has_s[1] == 1 && !mbar_wait(&bar_s1, 0));
+            if (!landed) {
+                abort_s = 1;
+                atomicOr(a.status, kStatusTimeout);
+            } else {
+                tc_fence_after();
+                uint8_t *st = sm + (hh ? OFF_K : OFF_S0);
+                uint8_t *ut = sm + (hh ? OFF_U1 : OFF_U0);
+                if (has_s[hh])
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16(tbase + TM_QS, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                                 mnmajor_desc(smem_addr(st), ks, kSlab), id_km, ks > 0);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tbase + TM_AU, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
+                             mnmajor_desc(smem_addr(ut), ks, kSlab), id_km, ks > 0);
+                mma_commit(&bar_h_mma);
+            }
+        }
+        __syncthreads();
+        if (abort_s) break;
+        if (!mbar_wait(&bar_h_mma, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+        tc_fence_after();
+        // the K tile is free once QK is done: fetch head 1's snapshot into it
+        if (hh == 0 && tid == 0 && has_s[1] == 1) {
+            mbar_arrive_expect_tx(&bar_s1, 2 * kSlab);
+            tma_load_3d(sm + OFF_K, &tS, 0, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s1);
+            tma_load_3d(sm + OFF_K + kSlab, &tS, 64, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s1);
+            s1_issued = true;
+        }
+        // 3. epilogue of head hh
+        {
+            const float f = fscale[hh] * exp2f(gs[hh][row] + (row >= 64 ? gs[hh][63] : 0.f));
+            const bool has = has_s[hh] != 0;
+            const bool store = row < 64 || two;
+            __nv_bfloat16 *orow = a.O + (((int64_t)tok0 + row) * a.Nv + 2 * p + hh) * kDim + 64 * hf;
+            for (int half32 = 0; half32 < 2; ++half32) {
+                float qs[32], au[32];
+                const int col = 64 * hf + 32 * half32;
+                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_AU + col), au);
+                if (has) tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QS + col), qs);
+                tmem_ld_wait();
+                if (store) {
+#pragma unroll
+                    for (int v8 = 0; v8 < 4; ++v8) {
+                        __nv_bfloat162 w[4];
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const int t = 8 * v8 + 2 * q2;
+                            const float o0 = ((has ? f * qs[t] : 0.f) + au[t]) * inv_sqrt_d;
+                            const float o1 = ((has ? f * qs[t + 1] : 0.f) + au[t + 1]) * inv_sqrt_d;
+                            w[q2] = __floats2bfloat162_rn(o0, o1);
+                        }
+                        reinterpret_cast<uint4 *>(orow + 32 * half32)[v8] = *reinterpret_cast<uint4 *>(w);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    if (abort_s && tid == 0) {
+        // let every copy and MMA issued so far land before the CTA releases its memory
+        mbar_wait(&bar_qk_ld, 0);
+        mbar_wait(&bar_h_ld[0], 0);
+        mbar_wait(&bar_h_ld[1], 0);
+        if (s1_issued) mbar_wait(&bar_s1, 0);
+        mma_commit(&bar_drain);
+        mbar_wait(&bar_drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<512>(tbase);
+}
+
+}  // namespace
+
+cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
+    if (pb.B == 0 || pb.C == 0) return cudaSuccess;
+    CUtensorMap tQ, tK, tU, tS;
+    const uint64_t BT = (uint64_t)pb.B * pb.T;
+    const uint64_t snap_rows = (uint64_t)(ws.snap_cap > 0 ? ws.snap_cap : 1) * 2 * kDim;
+    if (!make_tmap_bf16_3d(&tQ, pb.q, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
+        !make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
+        !make_tmap_bf16_3d(&tU, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
+        !make_tmap_bf16_3d(&tS, ws.snap, kDim, snap_rows, 1, kDim * 2, snap_rows * kDim * 2, 64, 128, 1))
+        return cudaErrorInvalidValue;
+    OutParams a;
+    a.g = pb.g; a.h0 = pb.h0; a.P = ws.P;
+    a.ev_chunk = ws.ev_chunk; a.grp_pred = ws.grp_pred; a.snap_slot = ws.snap_slot;
+    a.O = (__nv_bfloat16 *)pb.o; a.status = ws.counts + 2;
+    a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.G = pb.G;
+    a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
+    cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
+    output_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream>>>(tQ, tK, tU, tS, a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -209,13 +209,13 @@ cudaError_t launch_scan(const Problem &pb, const Workspace &ws) {
         kern<<<grid, kThreads, kScanSmem, pb.stream>>>(
             (const __nv_bfloat16 *)pb.k, (const __nv_bfloat16 *)ws.W, (__nv_bfloat16 *)ws.U, pb.g, pb.h0, ws.P,
             ws.counts, ws.row_pair, ws.row_ptr, ws.ev_chunk, ws.snap_slot, pb.P, pb.T, pb.Nq, pb.Nv, pb.C, ws.ev_cap,
-            ws.snap_cap, ws.snap, pb.s_final);
+            ws.snap_cap, (float *)ws.snap, pb.s_final);
     } else {
         auto kern = scan_kernel<float>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
         kern<<<grid, kThreads, kScanSmem, pb.stream>>>(
             (const float *)pb.k, (const float *)ws.W, (float *)ws.U, pb.g, pb.h0, ws.P, ws.counts, ws.row_pair,
-            ws.row_ptr, ws.ev_chunk, ws.snap_slot, pb.P, pb.T, pb.Nq, pb.Nv, pb.C, ws.ev_cap, ws.snap_cap, ws.snap,
+            ws.row_ptr, ws.ev_chunk, ws.snap_slot, pb.P, pb.T, pb.Nq, pb.Nv, pb.C, ws.ev_cap, ws.snap_cap, (float *)ws.snap,
             pb.s_final);
     }
     return cudaGetLastError();

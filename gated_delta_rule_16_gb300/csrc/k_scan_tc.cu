@@ -25,6 +25,8 @@
 //   MMA2  dS^T[128 x 128]     = U''^T[128 x 64] . K        (A: U''^T K-major; B: K [t][d] MN-major)
 //   S^T <- 2^gamma S^T + dS^T                                      (registers)
 // W, K and U tiles of the next event are TMA-prefetched (double buffer).
+// Snapshots are stored in bf16 as S [d][dv], the MN-major operand the output
+// kernel's Q S product loads by TMA.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -59,7 +61,7 @@ struct ScanParams {
     __nv_bfloat16 *amap;    // [R,2,NR,128,128] A_r^T (row m' = column m' of A_r)
     float *bmap;            // [R,2,NR,128,128] B_r^T
     float *entry;           // [R,2,NR,128,128] S_r^T entering each run
-    float *snap;            // [snap_cap,2,128 d,128 dv] post-event states (fp32)
+    __nv_bfloat16 *snap;    // [snap_cap,2,128 d,128 dv] post-event states (bf16)
     float *s_final;         // [B,Nv,128 d,128 dv]
     int32_t *status;
     int P_, T_, Nv, C, NR;
@@ -256,9 +258,9 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         if (mode == kModeFixup) {
             const int slot = ev_slot[k];
             if (slot >= 0 && slot < a.snap_cap) {
-                float *sn = a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim);
+                __nv_bfloat16 *sn = a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim);
 #pragma unroll
-                for (int jj = 0; jj < 64; ++jj) sn[(64 * hf + jj) * kDim + row] = S[jj];
+                for (int jj = 0; jj < 64; ++jj) sn[(64 * hf + jj) * kDim + row] = __float2bfloat16_rn(S[jj]);
             }
         }
         cur = c + 1;
@@ -440,7 +442,7 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
     a.row_pair = ws.row_pair; a.row_ptr = ws.row_ptr; a.ev_chunk = ws.ev_chunk; a.snap_slot = ws.snap_slot;
     a.P = ws.P; a.g = pb.g; a.h0 = pb.h0;
     a.U = (__nv_bfloat16 *)ws.U; a.amap = (__nv_bfloat16 *)ws.amap; a.bmap = ws.bmap; a.entry = ws.entry;
-    a.snap = ws.snap; a.s_final = pb.s_final; a.status = ws.counts + 2;
+    a.snap = (__nv_bfloat16 *)ws.snap; a.s_final = pb.s_final; a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.NR = NR;
     a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
     if (part == 1) {  // chain
