@@ -164,11 +164,11 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     mark(1);
     if (e == cudaSuccess) e = launch_prefix(pb, ws);
     mark(2);
-    if (e == cudaSuccess) e = launch_intra(pb, ws);
+    const bool tc = pb.dtype == GDN_BF16;   // tensor-core path for bf16 storage
+    if (e == cudaSuccess) e = tc ? launch_intra_tc(pb, ws) : launch_intra(pb, ws);
     mark(3);
     if (e == cudaSuccess) e = launch_wbuild(pb, ws);
     mark(4);
-    const bool tc = pb.dtype == GDN_BF16;   // tensor-core path for bf16 storage
     if (e == cudaSuccess && tc) e = launch_scan_tc(pb, ws, 0);
     mark(5);
     if (e == cudaSuccess && tc) e = launch_scan_tc(pb, ws, 1);

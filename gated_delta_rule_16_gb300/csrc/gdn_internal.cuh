@@ -85,5 +85,6 @@ cudaError_t launch_output(const Problem &pb, const Workspace &ws);
 // part 0: run maps, 1: chain over runs, 2: per-run fix-up (writes U' and snapshots)
 cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part);
 cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws);
+cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws);
 
 }  // namespace gdn

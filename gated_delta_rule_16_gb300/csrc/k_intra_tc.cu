@@ -1,0 +1,266 @@
+// k_intra_tc.cu -- intra-chunk step (SparseGDN Sec. 2.3, Eqs. 5-9) on tcgen05
+// tensor cores, for bf16 storage.
+//
+// One CTA per (group of two chunks, head pair, sequence): 128 tokens.
+//   Gram  G = K K^T [128 x 128]        (A = B = the K tile, K-major, by TMA), shared by the pair
+// per value head:
+//   A_Delta[t,s] = beta_t G[t,s] 2^(g_t - g_s), s < t in the same chunk; M = I + A_Delta
+//   C = M^-1 (exact) or the block-adjacent approximation (Eq. 7), fp32 on CUDA cores:
+//       C_ii = M_ii^-1 (forward substitution), C_ij = -C_ii sum_{k=j}^{i-1} M_ik C_kj
+//   U = C diag(beta) V                  (A: C diag(beta) bf16, block-diagonal over the
+//                                        two chunks, K-major; B: V [tok][dv] MN-major by TMA)
+//   C-bar = C diag(beta 2^g) as compact 16x16 fp32 blocks; s = ||U[48:64,:]||_F.
+#include "gdn_internal.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 256;
+constexpr uint32_t kSlab = 16384;
+constexpr uint32_t OFF_K = 0;            // K tile: 2 K-slabs [128 tok][64 d]
+constexpr uint32_t OFF_V = 2 * kSlab;    // V tiles of the two heads: 2 MN-stacks [128 tok][64 dv] each
+constexpr uint32_t OFF_A = 6 * kSlab;    // C diag(beta) bf16: 2 K-slabs [128 t][64 s]
+constexpr uint32_t OFF_F = 8 * kSlab;    // fp32 work area
+constexpr int MS = kChunk + 1;           // row stride of the fp32 64x64 tiles
+constexpr uint32_t F_M = 0;                              // [2][64][65] M
+constexpr uint32_t F_C = F_M + 2 * kChunk * MS * 4;      // [2][64][65] C
+constexpr uint32_t F_T = F_C + 2 * kChunk * MS * 4;      // [2][3][256] block products
+constexpr uint32_t F_B = F_T + 2 * 3 * 256 * 4;          // [128] beta
+constexpr uint32_t F_G = F_B + 128 * 4;                  // [128] g
+constexpr uint32_t F_S = F_G + 128 * 4;                  // [2] score partial sums
+constexpr uint32_t kIntraTcSmem = 1024 + OFF_F + F_S + 64;
+constexpr uint32_t TM_G = 0, TM_U = 128;
+
+struct IntraParams {
+    const float *beta, *g;
+    __nv_bfloat16 *U;
+    float *cbar, *score;
+    int32_t *status;
+    int P_, T_, Nv, C, nblk, exact;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV, IntraParams a) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = align1024(smraw);
+    __shared__ uint64_t bar_ld, bar_g, bar_u, bar_drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_s;
+    float *Ms = reinterpret_cast<float *>(sm + OFF_F + F_M);
+    float *Cs = reinterpret_cast<float *>(sm + OFF_F + F_C);
+    float *Tb = reinterpret_cast<float *>(sm + OFF_F + F_T);
+    float *bet = reinterpret_cast<float *>(sm + OFF_F + F_B);
+    float *gg = reinterpret_cast<float *>(sm + OFF_F + F_G);
+    float *ssum = reinterpret_cast<float *>(sm + OFF_F + F_S);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int row = quarter * 32 + lane;  // token inside the group
+    const int ct = row >> 6, tl = row & 63;
+    const int r = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
+    const int c0 = 2 * r;
+    const int nch = c0 + 1 < a.C ? 2 : 1;
+    const int tok0 = b * a.T_ + c0 * kChunk;
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_g, 1);
+        mbar_init(&bar_u, 1);
+        mbar_init(&bar_drain, 1);
+        fence_mbar_init();
+        abort_s = 0;
+    }
+    if (warp == 0) tmem_alloc<256>(&tmem_base);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar_ld, 6 * kSlab);
+        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_ld);
+        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_ld);
+        for (int hh = 0; hh < 2; ++hh) {
+            uint8_t *vd = sm + OFF_V + hh * 2 * kSlab;
+            tma_load_3d(vd, &tV, 0, 2 * p + hh, tok0, &bar_ld);
+            tma_load_3d(vd + kSlab, &tV, 64, 2 * p + hh, tok0, &bar_ld);
+        }
+        if (!mbar_wait(&bar_ld, 0)) {
+            abort_s = 1;
+            atomicOr(a.status, kStatusTimeout);
+        } else {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 128, false, false);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tbase + TM_G, kmajor_desc(smem_addr(sm + OFF_K), ks, kSlab),
+                         kmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id, ks > 0);
+            mma_commit(&bar_g);
+        }
+    }
+    __syncthreads();
+    const int max_off = a.exact ? 3 : 1;
+    for (int hh = 0; hh < 2 && !abort_s; ++hh) {
+        const int h = 2 * p + hh;
+        if (tid < 128) {
+            const bool valid = (tid >> 6) < nch;
+            bet[tid] = valid ? a.beta[((int64_t)tok0 + tid) * a.Nv + h] : 0.f;
+            gg[tid] = valid ? a.g[((int64_t)tok0 + tid) * a.Nv + h] : 0.f;
+        }
+        if (tid < 2) ssum[tid] = 0.f;
+        for (int idx = tid; idx < 2 * kChunk * MS; idx += kThreads) Cs[idx] = 0.f;
+        __syncthreads();
+        // 1. M from the Gram block of the row's chunk: thread (row, half) covers 32 columns
+        if (hh == 0 && !mbar_wait(&bar_g, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+        tc_fence_after();
+        {
+            float gv[32];
+            tmem_ld32(tmem_addr(tbase, quarter * 32, TM_G + 64 * ct + 32 * hf), gv);
+            tmem_ld_wait();
+            const float bt = bet[row], gt = gg[row];
+            float *mrow = Ms + (ct * kChunk + tl) * MS;
+#pragma unroll
+            for (int q2 = 0; q2 < 32; ++q2) {
+                const int s = 32 * hf + q2;
+                mrow[s] = s < tl ? bt * gv[q2] * exp2f(gt - gg[64 * ct + s]) : (s == tl ? 1.f : 0.f);
+            }
+        }
+        __syncthreads();
+        // 2. solve: diagonal 16x16 blocks by forward substitution, one thread per (chunk, column)
+        if (tid < 128) {
+            const int cc = tid >> 6, jcol = tid & 63, r1 = (jcol & ~15) + kBlk;
+            float *Cm = Cs + cc * kChunk * MS;
+            const float *Mm = Ms + cc * kChunk * MS;
+            Cm[jcol * MS + jcol] = 1.f;
+            for (int i2 = jcol + 1; i2 < r1; ++i2) {
+                float acc = 0.f;
+                for (int s = jcol; s < i2; ++s) acc += Mm[i2 * MS + s] * Cm[s * MS + jcol];
+                Cm[i2 * MS + jcol] = -acc;
+            }
+        }
+        __syncthreads();
+        for (int off = 1; off <= max_off; ++off) {
+            const int nb = 4 - off;
+            for (int idx = tid; idx < 2 * nb * 256; idx += kThreads) {
+                const int cc = idx / (nb * 256), rem = idx % (nb * 256);
+                const int bi = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
+                const int ib = bi + off, jb = bi;
+                const float *Mm = Ms + cc * kChunk * MS;
+                const float *Cm = Cs + cc * kChunk * MS;
+                float acc = 0.f;
+                for (int kk = jb * kBlk; kk < ib * kBlk; ++kk)
+                    acc += Mm[(ib * kBlk + rr) * MS + kk] * Cm[kk * MS + jb * kBlk + col];
+                Tb[cc * 768 + rem] = acc;
+            }
+            __syncthreads();
+            for (int idx = tid; idx < 2 * nb * 256; idx += kThreads) {
+                const int cc = idx / (nb * 256), rem = idx % (nb * 256);
+                const int bi = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
+                const int ib = bi + off, jb = bi;
+                float *Cm = Cs + cc * kChunk * MS;
+                float acc = 0.f;
+                for (int m = 0; m < kBlk; ++m)
+                    acc += Cm[(ib * kBlk + rr) * MS + ib * kBlk + m] * Tb[cc * 768 + (bi << 8) + m * 16 + col];
+                Cm[(ib * kBlk + rr) * MS + jb * kBlk + col] = -acc;
+            }
+            __syncthreads();
+        }
+        // 3. A tile C diag(beta) (bf16, block-diagonal) and the compact C-bar blocks
+        {
+            float w[64];
+            const float *crow = Cs + (ct * kChunk + tl) * MS;
+#pragma unroll
+            for (int q2 = 0; q2 < 64; ++q2) w[q2] = (hf == ct) ? crow[q2] * bet[64 * ct + q2] : 0.f;
+#pragma unroll
+            for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(sm + OFF_A + hf * kSlab, row, k0, &w[k0]);
+        }
+        for (int idx = tid; idx < nch * a.nblk * 256; idx += kThreads) {
+            const int cc = idx / (a.nblk * 256), rem = idx % (a.nblk * 256);
+            const int blk = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
+            const int rw = blk_row(blk) * kBlk + rr, cl = blk_col(blk) * kBlk + col;
+            a.cbar[(((int64_t)b * a.Nv + h) * a.C + c0 + cc) * a.nblk * 256 + rem] =
+                Cs[(cc * kChunk + rw) * MS + cl] * bet[64 * cc + cl] * exp2f(gg[64 * cc + cl]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // 4. U = (C diag(beta)) V
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 128, false, true);
+            uint8_t *vt = sm + OFF_V + hh * 2 * kSlab;
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
+                         mnmajor_desc(smem_addr(vt), ks, kSlab), id, ks > 0);
+            mma_commit(&bar_u);
+        }
+        if (!mbar_wait(&bar_u, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+        tc_fence_after();
+        {
+            float sq = 0.f;
+            __nv_bfloat16 *urow = a.U + (((int64_t)tok0 + row) * a.Nv + h) * kDim + 64 * hf;
+            const bool store = ct < nch;
+            for (int half32 = 0; half32 < 2; ++half32) {
+                float u[32];
+                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 64 * hf + 32 * half32), u);
+                tmem_ld_wait();
+                if (store) {
+#pragma unroll
+                    for (int v8 = 0; v8 < 4; ++v8) {
+                        __nv_bfloat162 w2[4];
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2)
+                            w2[q2] = __floats2bfloat162_rn(u[8 * v8 + 2 * q2], u[8 * v8 + 2 * q2 + 1]);
+                        reinterpret_cast<uint4 *>(urow + 32 * half32)[v8] = *reinterpret_cast<uint4 *>(w2);
+                    }
+                }
+                if (tl >= kChunk - kBlk) {
+#pragma unroll
+                    for (int q2 = 0; q2 < 32; ++q2) sq += u[q2] * u[q2];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            if (lane == 0 && sq != 0.f) atomicAdd(&ssum[ct], sq);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid < nch && a.score) a.score[((int64_t)b * a.Nv + h) * a.C + c0 + tid] = sqrtf(ssum[tid]);
+        __syncthreads();
+    }
+    if (abort_s && tid == 0) {
+        mbar_wait(&bar_ld, 0);
+        mma_commit(&bar_drain);
+        mbar_wait(&bar_drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<256>(tbase);
+}
+
+}  // namespace
+
+cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws) {
+    if (pb.B == 0 || pb.C == 0) return cudaSuccess;
+    CUtensorMap tK, tV;
+    const uint64_t BT = (uint64_t)pb.B * pb.T;
+    if (!make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
+        !make_tmap_bf16_3d(&tV, pb.v, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128))
+        return cudaErrorInvalidValue;
+    IntraParams a;
+    a.beta = pb.beta; a.g = pb.g; a.U = (__nv_bfloat16 *)ws.U; a.cbar = ws.cbar; a.score = pb.score;
+    a.status = ws.counts + 2;
+    a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;
+    a.exact = pb.solver == GDN_SOLVER_EXACT;
+    cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraTcSmem);
+    intra_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream>>>(tK, tV, a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn
