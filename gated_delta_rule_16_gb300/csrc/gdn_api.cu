@@ -53,6 +53,7 @@ gdn_status check_shape(const gdn_shape *s) {
     if (s->B < 0 || s->T < 0 || s->Nq <= 0 || s->Nv != 2 * s->Nq) return GDN_ERR_SHAPE;
     if (s->d != kDim || s->dv != kDim) return GDN_ERR_UNSUPPORTED;
     if (s->T % kChunk != 0) return GDN_ERR_UNSUPPORTED;
+    if (s->T / kChunk > 16384) return GDN_ERR_UNSUPPORTED;  // compaction stages a row's mask bits in shared memory
     // index arithmetic uses int32 for chunk/row/event counts
     const int64_t C = s->T / kChunk;
     // event tiles are addressed by int32 TMA row coordinates: events x 128 rows < 2^31
@@ -91,6 +92,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_ev_chunk = take(ev_cap * sizeof(int32_t));
     const size_t o_grp_pred = take(R * G * sizeof(int32_t));
     const size_t o_snap_slot = take(ev_cap * sizeof(int32_t));
+    const size_t o_ev_of = take(R * C * sizeof(int32_t));
     const size_t o_P = take((size_t)pb.B * pb.Nv * (C + 1) * sizeof(double));
     const size_t o_U = take((size_t)pb.B * pb.T * pb.Nv * pb.dv * es);
     const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
@@ -109,6 +111,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
         ws->ev_chunk = (int32_t *)(b + o_ev_chunk);
         ws->grp_pred = (int32_t *)(b + o_grp_pred);
         ws->snap_slot = (int32_t *)(b + o_snap_slot);
+        ws->ev_of = (int32_t *)(b + o_ev_of);
         ws->P = (double *)(b + o_P);
         ws->U = b + o_U;
         ws->cbar = (float *)(b + o_cbar);
@@ -160,14 +163,14 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     cudaEvent_t *prof = prof_slot();
     auto mark = [&](int i) { if (prof) cudaEventRecord(prof[i], pb.stream); };
     mark(0);
-    cudaError_t e = launch_select(pb, ev, ws.snap_cap);
+    cudaError_t e = launch_select(pb, ev, ws.snap_cap, ws.ev_of);
     mark(1);
     if (e == cudaSuccess) e = launch_prefix(pb, ws);
     mark(2);
     const bool tc = pb.dtype == GDN_BF16;   // tensor-core path for bf16 storage
     if (e == cudaSuccess) e = tc ? launch_intra_tc(pb, ws) : launch_intra(pb, ws);
     mark(3);
-    if (e == cudaSuccess) e = launch_wbuild(pb, ws);
+    if (e == cudaSuccess && !tc) e = launch_wbuild(pb, ws);  // bf16: W is built inside intra
     mark(4);
     if (e == cudaSuccess && tc) e = launch_scan_tc(pb, ws, 0);
     mark(5);
@@ -223,7 +226,7 @@ gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask, gdn_ev
     pb.mask = mask;
     pb.stream = (cudaStream_t)stream;
     // the snapshot numbering needs no capacity of its own: it never exceeds E
-    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity);
+    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity, nullptr);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

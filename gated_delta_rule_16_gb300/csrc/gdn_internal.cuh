@@ -61,6 +61,7 @@ struct Problem {
 struct Workspace {
     int32_t *counts;           // [4]: E, n_snap, status, reserved
     int32_t *row_pair, *row_ptr, *ev_chunk, *grp_pred, *snap_slot;
+    int32_t *ev_of;            // [R, C] event index of each (physical row, chunk), or -1
     double *P;                 // [B, Nv, C+1] log2 decay prefix (Eq. 19)
     void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks
@@ -76,7 +77,8 @@ struct Workspace {
 size_t workspace_layout(const Problem &pb, void *base, Workspace *ws);
 
 // ---- launchers (each returns cudaGetLastError()) --------------------------
-cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap);
+// ev_of (may be NULL): [R, C] event index of each (physical row, chunk), -1 when not selected
+cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of);
 cudaError_t launch_prefix(const Problem &pb, const Workspace &ws);
 cudaError_t launch_intra(const Problem &pb, const Workspace &ws);
 cudaError_t launch_wbuild(const Problem &pb, const Workspace &ws);

@@ -9,7 +9,11 @@
 //       C_ii = M_ii^-1 (forward substitution), C_ij = -C_ii sum_{k=j}^{i-1} M_ik C_kj
 //   U = C diag(beta) V                  (A: C diag(beta) bf16, block-diagonal over the
 //                                        two chunks, K-major; B: V [tok][dv] MN-major by TMA)
-//   C-bar = C diag(beta 2^g) as compact 16x16 fp32 blocks; s = ||U[48:64,:]||_F.
+//   s = ||U[48:64,:]||_F (Tail-16 write score)
+//   W = C diag(beta 2^g) K for the chunks that are events (Eq. 15): A = C-bar bf16,
+//       block-diagonal, K-major; B = the K tile read as MN-major (token rows, d
+//       columns: the same bytes as the K-major Gram operand).  W is written at the
+//       event's index, so it is never built for skipped chunks.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -33,12 +37,13 @@ constexpr uint32_t F_B = F_T + 2 * 3 * 256 * 4;          // [128] beta
 constexpr uint32_t F_G = F_B + 128 * 4;                  // [128] g
 constexpr uint32_t F_S = F_G + 128 * 4;                  // [2] score partial sums
 constexpr uint32_t kIntraTcSmem = 1024 + OFF_F + F_S + 64;
-constexpr uint32_t TM_G = 0, TM_U = 128;
+constexpr uint32_t TM_G = 0, TM_U = 128, TM_W = 256;
 
 struct IntraParams {
     const float *beta, *g;
-    __nv_bfloat16 *U;
-    float *cbar, *score;
+    const int32_t *ev_of;
+    __nv_bfloat16 *U, *W;
+    float *score;
     int32_t *status;
     int P_, T_, Nv, C, nblk, exact;
 };
@@ -52,6 +57,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     __shared__ uint64_t bar_ld, bar_g, bar_u, bar_drain;
+    __shared__ int ev_s[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
     float *Ms = reinterpret_cast<float *>(sm + OFF_F + F_M);
@@ -78,11 +84,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         fence_mbar_init();
         abort_s = 0;
     }
-    if (warp == 0) tmem_alloc<256>(&tmem_base);
+    if (tid < 2) ev_s[tid] = tid < nch ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
+    if (warp == 0) tmem_alloc<512>(&tmem_base);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
+    const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar_ld, 6 * kSlab);
         tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_ld);
@@ -171,26 +179,28 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             }
             __syncthreads();
         }
-        // 3. A tile C diag(beta) (bf16, block-diagonal) and the compact C-bar blocks
+        // 3. A tiles: C diag(beta) for U, and C diag(beta 2^g) for W (built in the
+        //    fp32 M area, free once the solve is done); both bf16, block-diagonal
         {
-            float w[64];
             const float *crow = Cs + (ct * kChunk + tl) * MS;
+            for (int part = 0; part < (any_event ? 2 : 1); ++part) {
+                uint8_t *dst = part == 0 ? sm + OFF_A : reinterpret_cast<uint8_t *>(Ms);
+                for (int k0 = 0; k0 < 64; k0 += 8) {
+                    float w[8];
 #pragma unroll
-            for (int q2 = 0; q2 < 64; ++q2) w[q2] = (hf == ct) ? crow[q2] * bet[64 * ct + q2] : 0.f;
-#pragma unroll
-            for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(sm + OFF_A + hf * kSlab, row, k0, &w[k0]);
-        }
-        for (int idx = tid; idx < nch * a.nblk * 256; idx += kThreads) {
-            const int cc = idx / (a.nblk * 256), rem = idx % (a.nblk * 256);
-            const int blk = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
-            const int rw = blk_row(blk) * kBlk + rr, cl = blk_col(blk) * kBlk + col;
-            a.cbar[(((int64_t)b * a.Nv + h) * a.C + c0 + cc) * a.nblk * 256 + rem] =
-                Cs[(cc * kChunk + rw) * MS + cl] * bet[64 * cc + cl] * exp2f(gg[64 * cc + cl]);
+                    for (int q2 = 0; q2 < 8; ++q2) {
+                        const int sidx = 64 * ct + k0 + q2;
+                        const float f = part == 0 ? bet[sidx] : bet[sidx] * exp2f(gg[sidx]);
+                        w[q2] = (hf == ct) ? crow[k0 + q2] * f : 0.f;
+                    }
+                    st_sw128_8(dst + hf * kSlab, row, k0, w);
+                }
+            }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // 4. U = (C diag(beta)) V
+        // 4. U = (C diag(beta)) V and, for events, W = (C diag(beta 2^g)) K
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 128, false, true);
@@ -198,6 +208,10 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
                          mnmajor_desc(smem_addr(vt), ks, kSlab), id, ks > 0);
+            if (any_event)
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tbase + TM_W, kmajor_desc(smem_addr(Ms), ks, kSlab),
+                             mnmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id, ks > 0);
             mma_commit(&bar_u);
         }
         if (!mbar_wait(&bar_u, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
@@ -228,6 +242,23 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 #pragma unroll
             for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
             if (lane == 0 && sq != 0.f) atomicAdd(&ssum[ct], sq);
+            const int ev = ev_s[ct];
+            if (ev >= 0) {
+                __nv_bfloat16 *wrow = a.W + (((int64_t)ev * 2 + hh) * kChunk + tl) * kDim + 64 * hf;
+                for (int half32 = 0; half32 < 2; ++half32) {
+                    float w[32];
+                    tmem_ld32(tmem_addr(tbase, quarter * 32, TM_W + 64 * hf + 32 * half32), w);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int v8 = 0; v8 < 4; ++v8) {
+                        __nv_bfloat162 w2[4];
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2)
+                            w2[q2] = __floats2bfloat162_rn(w[8 * v8 + 2 * q2], w[8 * v8 + 2 * q2 + 1]);
+                        reinterpret_cast<uint4 *>(wrow + 32 * half32)[v8] = *reinterpret_cast<uint4 *>(w2);
+                    }
+                }
+            }
         }
         tc_fence_before();
         __syncthreads();
@@ -241,7 +272,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc<256>(tbase);
+    if (warp == 0) tmem_dealloc<512>(tbase);
 }
 
 }  // namespace
@@ -254,7 +285,8 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws) {
         !make_tmap_bf16_3d(&tV, pb.v, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128))
         return cudaErrorInvalidValue;
     IntraParams a;
-    a.beta = pb.beta; a.g = pb.g; a.U = (__nv_bfloat16 *)ws.U; a.cbar = ws.cbar; a.score = pb.score;
+    a.beta = pb.beta; a.g = pb.g; a.ev_of = ws.ev_of;
+    a.U = (__nv_bfloat16 *)ws.U; a.W = (__nv_bfloat16 *)ws.W; a.score = pb.score;
     a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;
     a.exact = pb.solver == GDN_SOLVER_EXACT;

@@ -62,16 +62,19 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
               int32_t *__restrict__ row_pair, int32_t *__restrict__ row_ptr,
               int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
               int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
-              int64_t ev_cap, int64_t snap_cap) {
+              int32_t *__restrict__ ev_of, int64_t ev_cap, int64_t snap_cap) {
     extern __shared__ int sm[];
+    const int NW = (C + 31) >> 5;   // 32-chunk mask words per row
     int *cnt = sm;               // [R]   events per physical row
     int *order = cnt + R;        // [R]   physical id of sorted row j
     int *sorted_cnt = order + R; // [R]
     int *ptr = sorted_cnt + R;   // [R+1] row offsets
     int *refc = ptr + R + 1;     // [R]   referenced events per sorted row
     int *refb = refc + R;        // [R+1] snapshot base per sorted row
+    unsigned *words = reinterpret_cast<unsigned *>(refb + R + 1);  // [kWarps][NW] one row's mask bits
     __shared__ int warp_tot[33];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned *wrow = words + warp * NW;
 
     // 1. events per row
     for (int i = warp; i < R; i += kWarps) {
@@ -97,83 +100,91 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     // 3. row offsets
     block_exclusive_scan(sorted_cnt, ptr, R, warp_tot);
     const int64_t E = ptr[R];
-    // 4. per row: event chunks, predecessor of each group, referenced-event count
+    // 4. per row (one warp): stage the mask bits, write event chunks, the chunk -> event
+    //    map, each group's predecessor, and count the events some group references
+    //    (event at chunk c, next event of the row at cn or none: referenced iff the
+    //    smallest even chunk index m > c satisfies m <= cn and m <= 2(G-1)).
     for (int j = warp; j < R; j += kWarps) {
         const int i = order[j];
         const int base = ptr[j];
-        int run = 0;  // events of this row with chunk < current word start
-        for (int w0 = 0; w0 < C; w0 += 32) {
-            const int c = w0 + lane;
-            const bool s = c < C && is_set(mask, i, C, c);
-            const unsigned bits = __ballot_sync(0xffffffffu, s);
+        for (int w = 0; w < NW; ++w) {
+            const int c = 32 * w + lane;
+            const unsigned bits = __ballot_sync(0xffffffffu, c < C && is_set(mask, i, C, c));
+            if (lane == 0) wrow[w] = bits;
+        }
+        __syncwarp();
+        int run = 0, nref = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int c = 32 * w + lane;
+            const unsigned bits = wrow[w];
+            const bool s = (bits >> lane) & 1u;
             const int before = __popc(bits & ((1u << lane) - 1u));
-            if (s && (int64_t)base + run + before < ev_cap) ev_chunk[base + run + before] = c;
-            // groups r with 2r in [w0, w0+32): lane l < 16 handles 2r = w0 + 2l
-            if (lane < 16) {
-                const int r = (w0 >> 1) + lane;
+            const int e = base + run + before;
+            if (s && (int64_t)e < ev_cap) ev_chunk[e] = c;
+            if (ev_of && c < C) ev_of[(int64_t)i * C + c] = s ? e : -1;
+            if (lane < 16) {  // groups r with 2r = 32w + 2 lane
+                const int r = 16 * w + lane;
                 if (r < G) {
                     const int n_before = run + __popc(bits & ((1u << (2 * lane)) - 1u));
                     grp_pred[(int64_t)i * G + r] = n_before > 0 ? base + n_before - 1 : -1;
                 }
             }
-            run += __popc(bits);
-        }
-        // referenced events: need the next event's chunk, re-read from the mask
-        int nref = 0;
-        for (int w0 = 0; w0 < C; w0 += 32) {
-            const int c = w0 + lane;
-            const bool s = c < C && is_set(mask, i, C, c);
-            const unsigned bits = __ballot_sync(0xffffffffu, s);
-            bool ref = false;
-            if (s) {
-                const int m = (c & ~1) + 2;  // smallest even chunk index > c
-                int cn = 0x7fffffff;         // next event chunk of this row
-                const unsigned later = lane < 31 ? bits >> (lane + 1) : 0u;
-                if (later) {
-                    cn = c + 1 + __ffs(later) - 1;
-                } else {
-                    for (int c2 = w0 + 32; c2 < C; ++c2)
-                        if (is_set(mask, i, C, c2)) { cn = c2; break; }
-                }
-                ref = m <= 2 * (G - 1) && m <= cn;
-            }
-            nref += __popc(__ballot_sync(0xffffffffu, ref));
-        }
-        if (lane == 0) refc[j] = nref;
-    }
-    __syncthreads();
-    block_exclusive_scan(refc, refb, R, warp_tot);
-    // 5. snapshot slots
-    for (int j = warp; j < R; j += kWarps) {
-        const int i = order[j];
-        const int base = ptr[j];
-        int run = 0, rrun = refb[j];
-        for (int w0 = 0; w0 < C; w0 += 32) {
-            const int c = w0 + lane;
-            const bool s = c < C && is_set(mask, i, C, c);
-            const unsigned bits = __ballot_sync(0xffffffffu, s);
             bool ref = false;
             if (s) {
                 const int m = (c & ~1) + 2;
                 int cn = 0x7fffffff;
                 const unsigned later = lane < 31 ? bits >> (lane + 1) : 0u;
                 if (later) {
-                    cn = c + 1 + __ffs(later) - 1;
+                    cn = c + __ffs(later);
                 } else {
-                    for (int c2 = w0 + 32; c2 < C; ++c2)
-                        if (is_set(mask, i, C, c2)) { cn = c2; break; }
+                    for (int w2 = w + 1; w2 < NW; ++w2)
+                        if (wrow[w2]) { cn = 32 * w2 + __ffs(wrow[w2]) - 1; break; }
+                }
+                ref = m <= 2 * (G - 1) && m <= cn;
+            }
+            nref += __popc(__ballot_sync(0xffffffffu, ref));
+            run += __popc(bits);
+        }
+        if (lane == 0) refc[j] = nref;
+        __syncwarp();
+    }
+    __syncthreads();
+    block_exclusive_scan(refc, refb, R, warp_tot);
+    // 5. snapshot slots (the row's bits are staged again)
+    for (int j = warp; j < R; j += kWarps) {
+        const int i = order[j];
+        const int base = ptr[j];
+        for (int w = 0; w < NW; ++w) {
+            const int c = 32 * w + lane;
+            const unsigned bits = __ballot_sync(0xffffffffu, c < C && is_set(mask, i, C, c));
+            if (lane == 0) wrow[w] = bits;
+        }
+        __syncwarp();
+        int run = 0, rrun = refb[j];
+        for (int w = 0; w < NW; ++w) {
+            const int c = 32 * w + lane;
+            const unsigned bits = wrow[w];
+            const bool s = (bits >> lane) & 1u;
+            bool ref = false;
+            if (s) {
+                const int m = (c & ~1) + 2;
+                int cn = 0x7fffffff;
+                const unsigned later = lane < 31 ? bits >> (lane + 1) : 0u;
+                if (later) {
+                    cn = c + __ffs(later);
+                } else {
+                    for (int w2 = w + 1; w2 < NW; ++w2)
+                        if (wrow[w2]) { cn = 32 * w2 + __ffs(wrow[w2]) - 1; break; }
                 }
                 ref = m <= 2 * (G - 1) && m <= cn;
             }
             const unsigned rb = __ballot_sync(0xffffffffu, ref);
             const int e = base + run + __popc(bits & ((1u << lane) - 1u));
-            if (s && (int64_t)e < ev_cap) {
-                const int slot = rrun + __popc(rb & ((1u << lane) - 1u));
-                snap_slot[e] = ref ? slot : -1;
-            }
+            if (s && (int64_t)e < ev_cap) snap_slot[e] = ref ? rrun + __popc(rb & ((1u << lane) - 1u)) : -1;
             run += __popc(bits);
             rrun += __popc(rb);
         }
+        __syncwarp();
     }
     for (int j = threadIdx.x; j < R; j += kThreads) row_pair[j] = order[j];
     for (int j = threadIdx.x; j <= R; j += kThreads) row_ptr[j] = ptr[j];
@@ -191,15 +202,15 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
 
 }  // namespace
 
-cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap) {
-    const size_t smem = sizeof(int) * (6 * (size_t)pb.R + 2);
+cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of) {
+    const size_t smem = sizeof(int) * (6 * (size_t)pb.R + 2 + (size_t)kWarps * ((pb.C + 31) / 32));
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     select_kernel<<<1, kThreads, smem, pb.stream>>>(pb.mask, pb.R, pb.C, pb.G, ev.row_pair, ev.row_ptr,
                                                     ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts,
-                                                    (int64_t)ev.capacity, snap_cap);
+                                                    ev_of, (int64_t)ev.capacity, snap_cap);
     return cudaGetLastError();
 }
 
