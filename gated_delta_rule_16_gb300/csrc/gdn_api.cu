@@ -93,6 +93,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_grp_pred = take(R * G * sizeof(int32_t));
     const size_t o_snap_slot = take(ev_cap * sizeof(int32_t));
     const size_t o_ev_of = take(R * C * sizeof(int32_t));
+    const size_t o_run_first = take(R * ((C + kRunChunks - 1) / kRunChunks + 1) * sizeof(int32_t));
     const size_t o_P = take((size_t)pb.B * pb.Nv * (C + 1) * sizeof(double));
     const size_t o_U = take((size_t)pb.B * pb.T * pb.Nv * pb.dv * es);
     const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
@@ -112,6 +113,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
         ws->grp_pred = (int32_t *)(b + o_grp_pred);
         ws->snap_slot = (int32_t *)(b + o_snap_slot);
         ws->ev_of = (int32_t *)(b + o_ev_of);
+        ws->run_first = (int32_t *)(b + o_run_first);
         ws->P = (double *)(b + o_P);
         ws->U = b + o_U;
         ws->cbar = (float *)(b + o_cbar);
@@ -163,7 +165,7 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     cudaEvent_t *prof = prof_slot();
     auto mark = [&](int i) { if (prof) cudaEventRecord(prof[i], pb.stream); };
     mark(0);
-    cudaError_t e = launch_select(pb, ev, ws.snap_cap, ws.ev_of);
+    cudaError_t e = launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first);
     mark(1);
     if (e == cudaSuccess) e = launch_prefix(pb, ws);
     mark(2);
@@ -226,7 +228,7 @@ gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask, gdn_ev
     pb.mask = mask;
     pb.stream = (cudaStream_t)stream;
     // the snapshot numbering needs no capacity of its own: it never exceeds E
-    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity, nullptr);
+    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity, nullptr, nullptr);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -30,7 +30,7 @@ constexpr int kStatusSnapOverflow = 2;
 constexpr int kStatusTimeout = 4;     // a kernel gave up a wait after its time limit
 
 // Chunks per run of the tensor-core scan (the serial chain inside a run).
-constexpr int kRunChunks = 16;
+constexpr int kRunChunks = 16;  // the compaction kernel emits two runs per 32-chunk mask word
 
 // ---- storage-type helpers --------------------------------------------------
 template <typename T> struct io;
@@ -62,6 +62,7 @@ struct Workspace {
     int32_t *counts;           // [4]: E, n_snap, status, reserved
     int32_t *row_pair, *row_ptr, *ev_chunk, *grp_pred, *snap_slot;
     int32_t *ev_of;            // [R, C] event index of each (physical row, chunk), or -1
+    int32_t *run_first;        // [R, NR+1] first event of each run, per CSR row
     double *P;                 // [B, Nv, C+1] log2 decay prefix (Eq. 19)
     void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks
@@ -77,8 +78,11 @@ struct Workspace {
 size_t workspace_layout(const Problem &pb, void *base, Workspace *ws);
 
 // ---- launchers (each returns cudaGetLastError()) --------------------------
-// ev_of (may be NULL): [R, C] event index of each (physical row, chunk), -1 when not selected
-cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of);
+// ev_of (may be NULL): [R, C] event index of each (physical row, chunk), -1 when not selected.
+// run_first (may be NULL): [R, NR+1] per CSR row, index of the first event of each run of
+// kRunChunks chunks (entry NR: the row's end).  Both need kRunChunks = 16 (two runs per mask word).
+cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of,
+                          int32_t *run_first);
 cudaError_t launch_prefix(const Problem &pb, const Workspace &ws);
 cudaError_t launch_intra(const Problem &pb, const Workspace &ws);
 cudaError_t launch_wbuild(const Problem &pb, const Workspace &ws);

@@ -33,9 +33,10 @@ constexpr int MS = kChunk + 1;           // row stride of the fp32 64x64 tiles
 constexpr uint32_t F_M = 0;                              // [2][64][65] M
 constexpr uint32_t F_C = F_M + 2 * kChunk * MS * 4;      // [2][64][65] C
 constexpr uint32_t F_T = F_C + 2 * kChunk * MS * 4;      // [2][3][256] block products
-constexpr uint32_t F_B = F_T + 2 * 3 * 256 * 4;          // [128] beta
-constexpr uint32_t F_G = F_B + 128 * 4;                  // [128] g
-constexpr uint32_t F_S = F_G + 128 * 4;                  // [2] score partial sums
+constexpr uint32_t F_B = F_T + 2 * 3 * 256 * 4;          // [2 heads][128] beta
+constexpr uint32_t F_G = F_B + 2 * 128 * 4;              // [2 heads][128] g
+constexpr uint32_t F_BG = F_G + 2 * 128 * 4;             // [128] beta 2^g of the current head
+constexpr uint32_t F_S = F_BG + 128 * 4;                 // [2] score partial sums
 constexpr uint32_t kIntraTcSmem = 1024 + OFF_F + F_S + 64;
 constexpr uint32_t TM_G = 0, TM_U = 128, TM_W = 256;
 
@@ -53,7 +54,9 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV, IntraParams a) {
+intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
+                const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tU64,
+                const __grid_constant__ CUtensorMap tW, IntraParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     __shared__ uint64_t bar_ld, bar_g, bar_u, bar_drain;
@@ -63,8 +66,9 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     float *Ms = reinterpret_cast<float *>(sm + OFF_F + F_M);
     float *Cs = reinterpret_cast<float *>(sm + OFF_F + F_C);
     float *Tb = reinterpret_cast<float *>(sm + OFF_F + F_T);
-    float *bet = reinterpret_cast<float *>(sm + OFF_F + F_B);
-    float *gg = reinterpret_cast<float *>(sm + OFF_F + F_G);
+    float *bet2 = reinterpret_cast<float *>(sm + OFF_F + F_B);
+    float *gg2 = reinterpret_cast<float *>(sm + OFF_F + F_G);
+    float *bgs = reinterpret_cast<float *>(sm + OFF_F + F_BG);
     float *ssum = reinterpret_cast<float *>(sm + OFF_F + F_S);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -85,6 +89,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         abort_s = 0;
     }
     if (tid < 2) ev_s[tid] = tid < nch ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
+    {   // beta and g of both heads, fetched once while the tiles load
+        const int hh = tid >> 7, t = tid & 127;
+        const bool valid = (t >> 6) < nch;
+        const int64_t gi = ((int64_t)tok0 + t) * a.Nv + 2 * p + hh;
+        bet2[tid] = valid ? a.beta[gi] : 0.f;
+        gg2[tid] = valid ? a.g[gi] : 0.f;
+    }
     if (warp == 0) tmem_alloc<512>(&tmem_base);
     tc_fence_before();
     __syncthreads();
@@ -116,11 +127,10 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     const int max_off = a.exact ? 3 : 1;
     for (int hh = 0; hh < 2 && !abort_s; ++hh) {
         const int h = 2 * p + hh;
-        if (tid < 128) {
-            const bool valid = (tid >> 6) < nch;
-            bet[tid] = valid ? a.beta[((int64_t)tok0 + tid) * a.Nv + h] : 0.f;
-            gg[tid] = valid ? a.g[((int64_t)tok0 + tid) * a.Nv + h] : 0.f;
-        }
+        const float *bet = bet2 + 128 * hh;
+        const float *gg = gg2 + 128 * hh;
+        if (tid == 0) bulk_wait_read();  // the W store of the previous head has left the A tile
+        if (tid < 128) bgs[tid] = bet[tid] * exp2f(gg[tid]);
         if (tid < 2) ssum[tid] = 0.f;
         for (int idx = tid; idx < 2 * kChunk * MS; idx += kThreads) Cs[idx] = 0.f;
         __syncthreads();
@@ -140,17 +150,27 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             }
         }
         __syncthreads();
-        // 2. solve: diagonal 16x16 blocks by forward substitution, one thread per (chunk, column)
-        if (tid < 128) {
-            const int cc = tid >> 6, jcol = tid & 63, r1 = (jcol & ~15) + kBlk;
-            float *Cm = Cs + cc * kChunk * MS;
-            const float *Mm = Ms + cc * kChunk * MS;
-            Cm[jcol * MS + jcol] = 1.f;
-            for (int i2 = jcol + 1; i2 < r1; ++i2) {
+        // 2. solve.  Diagonal 16x16 blocks by forward substitution: warp w < 4 takes
+        //    blocks 2w and 2w+1 (8 blocks: 2 chunks x 4), one lane per column, the
+        //    column of C_ii in registers and the rows of M_ii broadcast from shared memory:
+        //    C_ii[i][j] = -sum_{s<i} M_ii[i][s] C_ii[s][j]   (C_ii[s][j] = 0 for s < j, 1 for s = j)
+        if (warp < 4) {
+            const int blk = 2 * warp + (lane >> 4), j = lane & 15;
+            const int cc = blk >> 2, r0 = (blk & 3) * kBlk;
+            const float *Mb = Ms + (cc * kChunk + r0) * MS + r0;
+            float x[kBlk];
+#pragma unroll
+            for (int i2 = 0; i2 < kBlk; ++i2) x[i2] = i2 == j ? 1.f : 0.f;
+#pragma unroll
+            for (int i2 = 1; i2 < kBlk; ++i2) {
                 float acc = 0.f;
-                for (int s = jcol; s < i2; ++s) acc += Mm[i2 * MS + s] * Cm[s * MS + jcol];
-                Cm[i2 * MS + jcol] = -acc;
+#pragma unroll
+                for (int s2 = 0; s2 < i2; ++s2) acc += Mb[i2 * MS + s2] * x[s2];
+                if (i2 > j) x[i2] = -acc;
             }
+            float *Cb = Cs + (cc * kChunk + r0) * MS + r0 + j;
+#pragma unroll
+            for (int i2 = 0; i2 < kBlk; ++i2) Cb[i2 * MS] = x[i2];
         }
         __syncthreads();
         for (int off = 1; off <= max_off; ++off) {
@@ -184,16 +204,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         {
             const float *crow = Cs + (ct * kChunk + tl) * MS;
             for (int part = 0; part < (any_event ? 2 : 1); ++part) {
-                uint8_t *dst = part == 0 ? sm + OFF_A : reinterpret_cast<uint8_t *>(Ms);
+                uint8_t *dst = (part == 0 ? sm + OFF_A : reinterpret_cast<uint8_t *>(Ms)) + hf * kSlab;
+                const float *f = (part == 0 ? bet : bgs) + 64 * ct;
                 for (int k0 = 0; k0 < 64; k0 += 8) {
                     float w[8];
 #pragma unroll
-                    for (int q2 = 0; q2 < 8; ++q2) {
-                        const int sidx = 64 * ct + k0 + q2;
-                        const float f = part == 0 ? bet[sidx] : bet[sidx] * exp2f(gg[sidx]);
-                        w[q2] = (hf == ct) ? crow[k0 + q2] * f : 0.f;
-                    }
-                    st_sw128_8(dst + hf * kSlab, row, k0, w);
+                    for (int q2 = 0; q2 < 8; ++q2) w[q2] = hf == ct ? crow[k0 + q2] * f[k0 + q2] : 0.f;
+                    st_sw128_8(dst, row, k0, w);
                 }
             }
         }
@@ -216,24 +233,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         }
         if (!mbar_wait(&bar_u, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
         tc_fence_after();
-        {
+        {   // U rows staged in this head's V tile (free once the MMAs are done), W rows in the A tile
             float sq = 0.f;
-            __nv_bfloat16 *urow = a.U + (((int64_t)tok0 + row) * a.Nv + h) * kDim + 64 * hf;
-            const bool store = ct < nch;
+            uint8_t *ustage = sm + OFF_V + hh * 2 * kSlab + hf * kSlab;
             for (int half32 = 0; half32 < 2; ++half32) {
                 float u[32];
                 tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 64 * hf + 32 * half32), u);
                 tmem_ld_wait();
-                if (store) {
 #pragma unroll
-                    for (int v8 = 0; v8 < 4; ++v8) {
-                        __nv_bfloat162 w2[4];
-#pragma unroll
-                        for (int q2 = 0; q2 < 4; ++q2)
-                            w2[q2] = __floats2bfloat162_rn(u[8 * v8 + 2 * q2], u[8 * v8 + 2 * q2 + 1]);
-                        reinterpret_cast<uint4 *>(urow + 32 * half32)[v8] = *reinterpret_cast<uint4 *>(w2);
-                    }
-                }
+                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(ustage, row, 32 * half32 + 8 * v8, &u[8 * v8]);
                 if (tl >= kChunk - kBlk) {
 #pragma unroll
                     for (int q2 = 0; q2 < 32; ++q2) sq += u[q2] * u[q2];
@@ -242,29 +250,40 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 #pragma unroll
             for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
             if (lane == 0 && sq != 0.f) atomicAdd(&ssum[ct], sq);
-            const int ev = ev_s[ct];
-            if (ev >= 0) {
-                __nv_bfloat16 *wrow = a.W + (((int64_t)ev * 2 + hh) * kChunk + tl) * kDim + 64 * hf;
+            if (ev_s[ct] >= 0) {
+                uint8_t *wstage = sm + OFF_A + hf * kSlab;
                 for (int half32 = 0; half32 < 2; ++half32) {
                     float w[32];
                     tmem_ld32(tmem_addr(tbase, quarter * 32, TM_W + 64 * hf + 32 * half32), w);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int v8 = 0; v8 < 4; ++v8) {
-                        __nv_bfloat162 w2[4];
-#pragma unroll
-                        for (int q2 = 0; q2 < 4; ++q2)
-                            w2[q2] = __floats2bfloat162_rn(w[8 * v8 + 2 * q2], w[8 * v8 + 2 * q2 + 1]);
-                        reinterpret_cast<uint4 *>(wrow + 32 * half32)[v8] = *reinterpret_cast<uint4 *>(w2);
-                    }
+                    for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(wstage, row, 32 * half32 + 8 * v8, &w[8 * v8]);
                 }
             }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            uint8_t *ust = sm + OFF_V + hh * 2 * kSlab;
+            const CUtensorMap *m = nch == 2 ? &tU : &tU64;  // a final single-chunk group writes 64 rows only
+            tma_store_3d(m, 0, h, tok0, ust);
+            tma_store_3d(m, 64, h, tok0, ust + kSlab);
+            for (int cc = 0; cc < nch; ++cc) {
+                const int ev = ev_s[cc];
+                if (ev < 0) continue;
+                const int wrow = (ev * 2 + hh) * kChunk;
+                tma_store_3d(&tW, 0, wrow, 0, sm + OFF_A + cc * 8192);
+                tma_store_3d(&tW, 64, wrow, 0, sm + OFF_A + kSlab + cc * 8192);
+            }
+            bulk_commit();
         }
         tc_fence_before();
         __syncthreads();
         if (tid < nch && a.score) a.score[((int64_t)b * a.Nv + h) * a.C + c0 + tid] = sqrtf(ssum[tid]);
         __syncthreads();
     }
+    if (tid == 0) bulk_wait_all();
     if (abort_s && tid == 0) {
         mbar_wait(&bar_ld, 0);
         mma_commit(&bar_drain);
@@ -279,10 +298,14 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 
 cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws) {
     if (pb.B == 0 || pb.C == 0) return cudaSuccess;
-    CUtensorMap tK, tV;
+    CUtensorMap tK, tV, tU, tU64, tW;
     const uint64_t BT = (uint64_t)pb.B * pb.T;
+    const uint64_t wrows = (uint64_t)ws.ev_cap * 2 * kChunk;
     if (!make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tV, pb.v, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128))
+        !make_tmap_bf16_3d(&tV, pb.v, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
+        !make_tmap_bf16_3d(&tU, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
+        !make_tmap_bf16_3d(&tU64, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&tW, ws.W, kDim, wrows, 1, kDim * 2, wrows * kDim * 2, 64, 64, 1))
         return cudaErrorInvalidValue;
     IntraParams a;
     a.beta = pb.beta; a.g = pb.g; a.ev_of = ws.ev_of;
@@ -291,7 +314,7 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws) {
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;
     a.exact = pb.solver == GDN_SOLVER_EXACT;
     cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraTcSmem);
-    intra_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream>>>(tK, tV, a);
+    intra_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream>>>(tK, tV, tU, tU64, tW, a);
     return cudaGetLastError();
 }
 

@@ -48,10 +48,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tK,
-                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tS, OutParams a) {
+                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tS,
+                 const __grid_constant__ CUtensorMap tO, const __grid_constant__ CUtensorMap tO64, OutParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
-    __shared__ uint64_t bar_qk_ld, bar_h_ld[2], bar_s1, bar_qk_mma, bar_h_mma, bar_drain;
+    __shared__ uint64_t bar_qk_ld, bar_h_ld[2], bar_s[2], bar_qk_mma, bar_h_mma, bar_drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
     __shared__ float gs[2][128];
@@ -66,6 +67,29 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     const bool two = c0 + 1 < a.C;
     const int tok0 = b * a.T_ + c0 * kChunk;
 
+    if (tid == 0) {  // the tiles that do not depend on the predecessor lookup go first
+        mbar_init(&bar_qk_ld, 1);
+        mbar_init(&bar_h_ld[0], 1);
+        mbar_init(&bar_h_ld[1], 1);
+        mbar_init(&bar_s[0], 1);
+        mbar_init(&bar_s[1], 1);
+        mbar_init(&bar_qk_mma, 1);
+        mbar_init(&bar_h_mma, 1);
+        mbar_init(&bar_drain, 1);
+        fence_mbar_init();
+        abort_s = 0;
+        mbar_arrive_expect_tx(&bar_qk_ld, 4 * kSlab);
+        tma_load_3d(sm + OFF_Q, &tQ, 0, p, tok0, &bar_qk_ld);
+        tma_load_3d(sm + OFF_Q + kSlab, &tQ, 64, p, tok0, &bar_qk_ld);
+        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_qk_ld);
+        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_qk_ld);
+        for (int hh = 0; hh < 2; ++hh) {
+            uint8_t *ud = sm + (hh ? OFF_U1 : OFF_U0);
+            mbar_arrive_expect_tx(&bar_h_ld[hh], 2 * kSlab);
+            tma_load_3d(ud, &tU, 0, 2 * p + hh, tok0, &bar_h_ld[hh]);
+            tma_load_3d(ud + kSlab, &tU, 64, 2 * p + hh, tok0, &bar_h_ld[hh]);
+        }
+    }
     if (tid < 2) {
         const int hh = tid, h = 2 * p + hh;
         const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
@@ -91,17 +115,6 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         const bool valid = t < 64 || two;
         gs[hh][t] = valid ? a.g[((int64_t)tok0 + t) * a.Nv + 2 * p + hh] : 0.f;
     }
-    if (tid == 0) {
-        mbar_init(&bar_qk_ld, 1);
-        mbar_init(&bar_h_ld[0], 1);
-        mbar_init(&bar_h_ld[1], 1);
-        mbar_init(&bar_s1, 1);
-        mbar_init(&bar_qk_mma, 1);
-        mbar_init(&bar_h_mma, 1);
-        mbar_init(&bar_drain, 1);
-        fence_mbar_init();
-        abort_s = 0;
-    }
     if (warp == 0) tmem_alloc<512>(&tmem_base);
     tc_fence_before();
     __syncthreads();
@@ -121,23 +134,10 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         fence_async_smem();
     };
 
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_qk_ld, 4 * kSlab);
-        tma_load_3d(sm + OFF_Q, &tQ, 0, p, tok0, &bar_qk_ld);
-        tma_load_3d(sm + OFF_Q + kSlab, &tQ, 64, p, tok0, &bar_qk_ld);
-        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_qk_ld);
-        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_qk_ld);
-        for (int hh = 0; hh < 2; ++hh) {
-            uint8_t *ud = sm + (hh ? OFF_U1 : OFF_U0);
-            const bool snap0 = hh == 0 && has_s[0] == 1;
-            mbar_arrive_expect_tx(&bar_h_ld[hh], 2 * kSlab + (snap0 ? 2 * kSlab : 0));
-            tma_load_3d(ud, &tU, 0, 2 * p + hh, tok0, &bar_h_ld[hh]);
-            tma_load_3d(ud + kSlab, &tU, 64, 2 * p + hh, tok0, &bar_h_ld[hh]);
-            if (snap0) {
-                tma_load_3d(sm + OFF_S0, &tS, 0, slot_s[0] * 2 * kDim, 0, &bar_h_ld[0]);
-                tma_load_3d(sm + OFF_S0 + kSlab, &tS, 64, slot_s[0] * 2 * kDim, 0, &bar_h_ld[0]);
-            }
-        }
+    if (tid == 0 && has_s[0] == 1) {
+        mbar_arrive_expect_tx(&bar_s[0], 2 * kSlab);
+        tma_load_3d(sm + OFF_S0, &tS, 0, slot_s[0] * 2 * kDim, 0, &bar_s[0]);
+        tma_load_3d(sm + OFF_S0 + kSlab, &tS, 64, slot_s[0] * 2 * kDim, 0, &bar_s[0]);
     }
     if (has_s[0] == 2) fill_h0(0, sm + OFF_S0);
     __syncthreads();
@@ -194,7 +194,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         if (abort_s) break;
         // 2. QS_h and AU_h
         if (tid == 0) {
-            const bool landed = mbar_wait(&bar_h_ld[hh], 0) && !(hh == 1 && has_s[1] == 1 && !mbar_wait(&bar_s1, 0));
+            const bool landed = mbar_wait(&bar_h_ld[hh], 0) && !(has_s[hh] == 1 && !mbar_wait(&bar_s[hh], 0));
             if (!landed) {
                 abort_s = 1;
                 atomicOr(a.status, kStatusTimeout);
@@ -218,48 +218,48 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         tc_fence_after();
         // the K tile is free once QK is done: fetch head 1's snapshot into it
         if (hh == 0 && tid == 0 && has_s[1] == 1) {
-            mbar_arrive_expect_tx(&bar_s1, 2 * kSlab);
-            tma_load_3d(sm + OFF_K, &tS, 0, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s1);
-            tma_load_3d(sm + OFF_K + kSlab, &tS, 64, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s1);
+            mbar_arrive_expect_tx(&bar_s[1], 2 * kSlab);
+            tma_load_3d(sm + OFF_K, &tS, 0, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s[1]);
+            tma_load_3d(sm + OFF_K + kSlab, &tS, 64, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s[1]);
             s1_issued = true;
         }
-        // 3. epilogue of head hh
+        // 3. epilogue of head hh: O rows staged (bf16, 128B-swizzled) in the U' tile
+        //    this head no longer needs, then written by one TMA store
         {
             const float f = fscale[hh] * exp2f(gs[hh][row] + (row >= 64 ? gs[hh][63] : 0.f));
             const bool has = has_s[hh] != 0;
-            const bool store = row < 64 || two;
-            __nv_bfloat16 *orow = a.O + (((int64_t)tok0 + row) * a.Nv + 2 * p + hh) * kDim + 64 * hf;
+            uint8_t *stage = sm + (hh ? OFF_U1 : OFF_U0) + hf * kSlab;
             for (int half32 = 0; half32 < 2; ++half32) {
                 float qs[32], au[32];
                 const int col = 64 * hf + 32 * half32;
                 tmem_ld32(tmem_addr(tbase, quarter * 32, TM_AU + col), au);
                 if (has) tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QS + col), qs);
                 tmem_ld_wait();
-                if (store) {
 #pragma unroll
-                    for (int v8 = 0; v8 < 4; ++v8) {
-                        __nv_bfloat162 w[4];
+                for (int t = 0; t < 32; ++t) au[t] = ((has ? f * qs[t] : 0.f) + au[t]) * inv_sqrt_d;
 #pragma unroll
-                        for (int q2 = 0; q2 < 4; ++q2) {
-                            const int t = 8 * v8 + 2 * q2;
-                            const float o0 = ((has ? f * qs[t] : 0.f) + au[t]) * inv_sqrt_d;
-                            const float o1 = ((has ? f * qs[t + 1] : 0.f) + au[t + 1]) * inv_sqrt_d;
-                            w[q2] = __floats2bfloat162_rn(o0, o1);
-                        }
-                        reinterpret_cast<uint4 *>(orow + 32 * half32)[v8] = *reinterpret_cast<uint4 *>(w);
-                    }
-                }
+                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(stage, row, 32 * half32 + 8 * v8, &au[8 * v8]);
             }
         }
+        fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (tid == 0) {
+            uint8_t *stage = sm + (hh ? OFF_U1 : OFF_U0);
+            const CUtensorMap *m = two ? &tO : &tO64;  // a final single-chunk group writes 64 rows only
+            tma_store_3d(m, 0, 2 * p + hh, tok0, stage);
+            tma_store_3d(m, 64, 2 * p + hh, tok0, stage + kSlab);
+            bulk_commit();
+        }
     }
+    if (tid == 0) bulk_wait_all();
     if (abort_s && tid == 0) {
         // let every copy and MMA issued so far land before the CTA releases its memory
         mbar_wait(&bar_qk_ld, 0);
         mbar_wait(&bar_h_ld[0], 0);
         mbar_wait(&bar_h_ld[1], 0);
-        if (s1_issued) mbar_wait(&bar_s1, 0);
+        if (has_s[0] == 1) mbar_wait(&bar_s[0], 0);
+        if (s1_issued) mbar_wait(&bar_s[1], 0);
         mma_commit(&bar_drain);
         mbar_wait(&bar_drain, 0);
     }
@@ -272,13 +272,15 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
 
 cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
     if (pb.B == 0 || pb.C == 0) return cudaSuccess;
-    CUtensorMap tQ, tK, tU, tS;
+    CUtensorMap tQ, tK, tU, tS, tO, tO64;
     const uint64_t BT = (uint64_t)pb.B * pb.T;
     const uint64_t snap_rows = (uint64_t)(ws.snap_cap > 0 ? ws.snap_cap : 1) * 2 * kDim;
     if (!make_tmap_bf16_3d(&tQ, pb.q, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
         !make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
         !make_tmap_bf16_3d(&tU, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tS, ws.snap, kDim, snap_rows, 1, kDim * 2, snap_rows * kDim * 2, 64, 128, 1))
+        !make_tmap_bf16_3d(&tS, ws.snap, kDim, snap_rows, 1, kDim * 2, snap_rows * kDim * 2, 64, 128, 1) ||
+        !make_tmap_bf16_3d(&tO, pb.o, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
+        !make_tmap_bf16_3d(&tO64, pb.o, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     OutParams a;
     a.g = pb.g; a.h0 = pb.h0; a.P = ws.P;
@@ -287,7 +289,7 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.G = pb.G;
     a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
     cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
-    output_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream>>>(tQ, tK, tU, tS, a);
+    output_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream>>>(tQ, tK, tU, tS, tO, tO64, a);
     return cudaGetLastError();
 }
 

@@ -50,17 +50,19 @@ constexpr uint32_t kRunSmem = 1024 + OFF_BUF + 2 * BUF_BYTES;
 constexpr uint32_t TM_U = 0;             // TMEM columns [0, 64): U'^T accumulator
 constexpr uint32_t TM_S = 64;            // TMEM columns [64, 192): dS^T accumulator
 constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab;
+constexpr int kMaxRuns = 1024;  // C <= 16384 chunks
 
 enum { kModeHomog = 0, kModeInhom = 1, kModeFixup = 2 };
 
 struct ScanParams {
     const int32_t *row_pair, *row_ptr, *ev_chunk, *snap_slot;
+    const int32_t *run_first;   // [R, NR+1] first event of each run, per CSR row
     const double *P;
     const float *g, *h0;
     __nv_bfloat16 *U;       // [B,T,Nv,128]: U, replaced by U' for events (fix-up mode)
     __nv_bfloat16 *amap;    // [R,2,NR,128,128] A_r^T (row m' = column m' of A_r)
-    float *bmap;            // [R,2,NR,128,128] B_r^T
-    float *entry;           // [R,2,NR,128,128] S_r^T entering each run
+    float *bmap;            // [R,2,NR] tiles of B_r^T, column-quad layout (quad_index)
+    float *entry;           // [R,2,NR] tiles of S_r^T entering each run, column-quad layout
     __nv_bfloat16 *snap;    // [snap_cap,2,128 d,128 dv] post-event states (bf16)
     float *s_final;         // [B,Nv,128 d,128 dv]
     int32_t *status;
@@ -80,7 +82,8 @@ __device__ __forceinline__ void fail(const ScanParams &a, int *abort_flag) {
 // grid: (runs NR, map mode: 2 heads x {homog, inhom} | fix-up: 2 heads, CSR rows R)
 __global__ void __launch_bounds__(kThreads, 1)
 scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tK,
-                const __grid_constant__ CUtensorMap tU, ScanParams a, int fixup) {
+                const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tA, ScanParams a,
+                int fixup) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     __shared__ uint64_t bar_tma[2], bar_mma1, bar_mma2;
@@ -88,7 +91,8 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     __shared__ int abort_s, n_ev_s, e_first_s;
     __shared__ int ev_c[kRun], ev_slot[kRun];
     __shared__ double Pl[kRun + 1];
-    __shared__ float gl[kRun][kChunk];
+    __shared__ float dec[kRun][kChunk];  // 2^(gamma - g_t) of each event chunk
+    __shared__ float gamk[kRun];         // gamma of each event chunk
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, hf = warp >> 2;
@@ -100,20 +104,10 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     const int c_lo = rho * kRun, c_hi = min(a.C, c_lo + kRun);
 
     if (tid == 0) {
-        const int64_t e0 = min((int64_t)a.row_ptr[j], a.ev_cap), e1 = min((int64_t)a.row_ptr[j + 1], a.ev_cap);
-        int64_t lo = e0, hi = e1;
-        while (lo < hi) {
-            const int64_t m = (lo + hi) >> 1;
-            if (a.ev_chunk[m] < c_lo) lo = m + 1; else hi = m;
-        }
-        const int64_t first = lo;
-        hi = e1;
-        while (lo < hi) {
-            const int64_t m = (lo + hi) >> 1;
-            if (a.ev_chunk[m] < c_hi) lo = m + 1; else hi = m;
-        }
-        n_ev_s = (int)(lo - first);
-        e_first_s = (int)first;
+        const int64_t f = min((int64_t)a.run_first[(int64_t)j * (a.NR + 1) + rho], a.ev_cap);
+        const int64_t l = min((int64_t)a.run_first[(int64_t)j * (a.NR + 1) + rho + 1], a.ev_cap);
+        n_ev_s = (int)max((int64_t)0, l - f);
+        e_first_s = (int)f;
         abort_s = 0;
     }
     __syncthreads();
@@ -140,7 +134,10 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     tc_fence_after();
     for (int idx = tid; idx < n_ev * kChunk; idx += kThreads) {
         const int k = idx >> 6, t = idx & 63;
-        gl[k][t] = a.g[((int64_t)b * a.T_ + (int64_t)ev_c[k] * kChunk + t) * a.Nv + h];
+        const int64_t tk = (int64_t)b * a.T_ + (int64_t)ev_c[k] * kChunk;
+        const float gam = a.g[(tk + kChunk - 1) * a.Nv + h];
+        dec[k][t] = exp2f(gam - a.g[(tk + t) * a.Nv + h]);
+        if (t == 0) gamk[k] = gam;
     }
     const uint32_t tbase = tmem_base;
     uint8_t *A1 = sm + OFF_A1;
@@ -172,14 +169,14 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj) S[jj] = 0.f;
     } else {
-        const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase + row * kDim + 64 * hf);
+        const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase) + 16 * hf * 128 + row;
 #pragma unroll
         for (int v4 = 0; v4 < 16; ++v4) {
-            const float4 x = src[v4];
+            const float4 x = src[v4 * 128];
             S[4 * v4] = x.x; S[4 * v4 + 1] = x.y; S[4 * v4 + 2] = x.z; S[4 * v4 + 3] = x.w;
         }
     }
-    __syncthreads();  // gl[] complete
+    __syncthreads();  // dec[] complete
 
     const uint32_t id1 = idesc_bf16(128, 64, false, false);
     const uint32_t id2 = idesc_bf16(128, 128, false, true);
@@ -206,6 +203,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                              kmajor_desc(smem_addr(buf + BUF_W), ks, 8192), id1, ks > 0);
                 mma_commit(&bar_mma1);
                 if (k + 1 < n_ev) {
+                    if (mode == kModeFixup) bulk_wait_read();  // U' of event k-1 left that buffer
                     issue_tma(k + 1);
                     tma_issued = k + 2;
                 }
@@ -218,17 +216,16 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         float acc[32];
         tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 32 * hf), acc);
         tmem_ld_wait();
-        const __nv_bfloat16 *Ut = reinterpret_cast<const __nv_bfloat16 *>(buf + BUF_U);
-        const float gam = gl[k][kChunk - 1];
-        const int64_t tok0 = (int64_t)b * a.T_ + (int64_t)c * kChunk;
+        __nv_bfloat16 *Ut = reinterpret_cast<__nv_bfloat16 *>(buf + BUF_U);
+        const float gam = gamk[k];
         float up[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
             const int tt = 32 * hf + t;
             const float u = mode == kModeHomog ? 0.f : __bfloat162float(Ut[tt * kDim + row]);
             const float v = u - acc[t];
-            if (mode == kModeFixup) a.U[((tok0 + tt) * a.Nv + h) * kDim + row] = __float2bfloat16_rn(v);
-            up[t] = v * exp2f(gam - gl[k][tt]);
+            if (mode == kModeFixup) Ut[tt * kDim + row] = __float2bfloat16_rn(v);  // U' replaces U in the tile
+            up[t] = v * dec[k][tt];
         }
 #pragma unroll
         for (int t0 = 0; t0 < 32; t0 += 8) st_sw128_8(A2, row, 32 * hf + t0, &up[t0]);
@@ -242,6 +239,10 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                 mma_bf16(tbase + TM_S, kmajor_desc(smem_addr(A2), ks, kSlab),
                          mnmajor_desc(smem_addr(buf + BUF_K), ks, 8192), id2, ks > 0);
             mma_commit(&bar_mma2);
+            if (mode == kModeFixup) {  // U' of this event back to the U buffer, in place
+                tma_store_3d(&tU, 0, h, b * a.T_ + c * kChunk, buf + BUF_U);
+                bulk_commit();
+            }
         }
         if (!mbar_wait(&bar_mma2, k & 1)) fail(a, &abort_s);
         tc_fence_after();
@@ -270,23 +271,28 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     }
     if (!abort_s && mode != kModeFixup) {
         const float fin = exp2f((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) S[jj] *= fin;
         if (mode == kModeHomog) {
-            uint4 *dst = reinterpret_cast<uint4 *>(a.amap + ubase + row * kDim + 64 * hf);
+            // A_r^T rows staged as the chain's MN-major operand image, then one TMA store
 #pragma unroll
-            for (int v8 = 0; v8 < 8; ++v8) {
-                __nv_bfloat162 w[4];
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2)
-                    w[q2] = __floats2bfloat162_rn(S[8 * v8 + 2 * q2] * fin, S[8 * v8 + 2 * q2 + 1] * fin);
-                dst[v8] = *reinterpret_cast<uint4 *>(w);
+            for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(A1 + hf * kSlab, row, k0, &S[k0]);
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                const int yrow = (int)((((int64_t)i * 2 + hh) * a.NR + rho) * kDim);
+                tma_store_3d(&tA, 0, yrow, 0, A1);
+                tma_store_3d(&tA, 64, yrow, 0, A1 + kSlab);
+                bulk_commit();
             }
         } else {
-            float4 *dst = reinterpret_cast<float4 *>(a.bmap + ubase + row * kDim + 64 * hf);
+            float4 *dst = reinterpret_cast<float4 *>(a.bmap + ubase) + 16 * hf * 128 + row;
 #pragma unroll
             for (int v4 = 0; v4 < 16; ++v4)
-                dst[v4] = make_float4(S[4 * v4] * fin, S[4 * v4 + 1] * fin, S[4 * v4 + 2] * fin, S[4 * v4 + 3] * fin);
+                dst[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
         }
     }
+    if (tid == 0) bulk_wait_all();
     if (abort_s && tid == 0) {
         // drain: tiles still in flight into shared memory, and the MMAs issued so far
         for (int kk = k + 1; kk < tma_issued; ++kk) mbar_wait(&bar_tma[kk & 1], (kk >> 1) & 1);
@@ -306,13 +312,13 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     __shared__ uint64_t bar_tma[2], bar_mma;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
+    __shared__ int nxt[kMaxRuns + 1];  // nxt[r]: first run >= r holding events of this row (NR if none)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, hf = warp >> 2;
     const int row = quarter * 32 + lane;
     const int hh = blockIdx.x, j = blockIdx.y;
     const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
     const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
-    const int64_t e0 = min((int64_t)a.row_ptr[j], a.ev_cap), e1 = min((int64_t)a.row_ptr[j + 1], a.ev_cap);
     const int64_t sbase = ((int64_t)b * a.Nv + h) * (kDim * kDim);
     const int64_t rbase = ((int64_t)i * 2 + hh) * a.NR;
 
@@ -324,6 +330,27 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         abort_s = 0;
     }
     if (warp == 0) tmem_alloc<128>(&tmem_base);
+    {   // which runs hold events: from the per-run first-event table
+        const int32_t *rf = a.run_first + (int64_t)j * (a.NR + 1);
+        for (int r = tid; r < a.NR; r += kThreads) nxt[r] = rf[r + 1] > rf[r] ? r : a.NR;
+        if (tid == 0) nxt[a.NR] = a.NR;
+    }
+    __syncthreads();
+    if (warp == 0) {  // suffix minimum: nxt[r] = first run >= r with events
+        int carry = a.NR;
+        for (int base = ((a.NR + 31) / 32 - 1) * 32; base >= 0; base -= 32) {
+            const int r = base + lane;
+            int v = r < a.NR ? nxt[r] : a.NR;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_down_sync(0xffffffffu, v, o);
+                if (lane + o < 32) v = min(v, y);
+            }
+            v = min(v, carry);
+            if (r < a.NR) nxt[r] = v;
+            carry = __shfl_sync(0xffffffffu, v, 0);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -335,36 +362,43 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
 #pragma unroll
     for (int jj = 0; jj < 64; ++jj) S[jj] = a.h0 ? a.h0[sbase + (int64_t)(64 * hf + jj) * kDim + row] : 0.f;
 
-    // next run (>= r) holding an event of this row, from event cursor e; NR if none
-    auto next_run = [&](int64_t e) -> int { return e < e1 ? a.ev_chunk[e] / kRun : a.NR; };
-    int64_t ecur = e0;
+    auto next_run = [&](int r) -> int { return r < a.NR ? nxt[r] : a.NR; };
     int n_loads = 0, n_mma = 0;
-    int pending_run = -1;
     if (tid == 0) {
-        const int r0 = next_run(ecur);
+        const int r0 = next_run(0);
         if (r0 < a.NR) {
             mbar_arrive_expect_tx(&bar_tma[0], 2 * kSlab);
             tma_load_3d(Mbuf, &tA, 0, (int)((rbase + r0) * kDim), 0, &bar_tma[0]);
             tma_load_3d(Mbuf + kSlab, &tA, 64, (int)((rbase + r0) * kDim), 0, &bar_tma[0]);
-            pending_run = r0;
             n_loads = 1;
         }
     }
     const uint32_t idesc = idesc_bf16(128, 128, false, true);
     int used = 0;  // map tiles consumed
+    float Bm[64];  // B^T row of the next run with events
+    {
+        const int r0 = next_run(0);
+        if (r0 < a.NR) {
+            const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r0) * (kDim * kDim)) + 16 * hf * 128 + row;
+#pragma unroll
+            for (int v4 = 0; v4 < 16; ++v4) {
+                const float4 x = bsrc[v4 * 128];
+                Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
+            }
+        }
+    }
     for (int r = 0; r < a.NR; ++r) {
         const int c_lo = r * kRun, c_hi = min(a.C, c_lo + kRun);
-        float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim) + row * kDim + 64 * hf);
+        float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim)) + 16 * hf * 128 + row;
 #pragma unroll
-        for (int v4 = 0; v4 < 16; ++v4) ent[v4] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
-        const bool has = ecur < e1 && a.ev_chunk[ecur] < c_hi;
+        for (int v4 = 0; v4 < 16; ++v4) ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+        const bool has = nxt[r] == r;
         if (!has) {
             const float f = exp2f((float)(Pu[c_hi] - Pu[c_lo]));
 #pragma unroll
             for (int jj = 0; jj < 64; ++jj) S[jj] *= f;
             continue;
         }
-        while (ecur < e1 && a.ev_chunk[ecur] < c_hi) ++ecur;
 #pragma unroll
         for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(Atile + hf * kSlab, row, k0, &S[k0]);
         fence_async_smem();
@@ -381,7 +415,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
                     mma_bf16(tbase, kmajor_desc(smem_addr(Atile), ks, kSlab), mnmajor_desc(smem_addr(mt), ks, kSlab),
                              idesc, ks > 0);
                 mma_commit(&bar_mma);
-                const int rn = next_run(ecur);
+                const int rn = next_run(r + 1);
                 if (rn < a.NR) {
                     const int nb = (used + 1) & 1;
                     uint8_t *dst = Mbuf + nb * 2 * kSlab;
@@ -391,14 +425,6 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
                     ++n_loads;
                 }
             }
-        }
-        // B_r^T row, fetched while the MMA runs
-        float Bm[64];
-        const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r) * (kDim * kDim) + row * kDim + 64 * hf);
-#pragma unroll
-        for (int v4 = 0; v4 < 16; ++v4) {
-            const float4 x = bsrc[v4];
-            Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
         }
         __syncthreads();
         if (abort_s) break;
@@ -415,6 +441,18 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
             S[jj] = d0[jj] + Bm[jj];
             S[32 + jj] = d1[jj] + Bm[32 + jj];
         }
+        {   // refill with the next run's B^T row; the loads land during the next step
+            const int rn2 = next_run(r + 1);
+            if (rn2 < a.NR) {
+                const float4 *bsrc =
+                    reinterpret_cast<const float4 *>(a.bmap + (rbase + rn2) * (kDim * kDim)) + 16 * hf * 128 + row;
+#pragma unroll
+                for (int v4 = 0; v4 < 16; ++v4) {
+                    const float4 x = bsrc[v4 * 128];
+                    Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
+                }
+            }
+        }
         tc_fence_before();
         __syncthreads();
         if (abort_s) break;
@@ -427,7 +465,6 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         mma_commit(&bar_mma);
         mbar_wait(&bar_mma, n_mma & 1);
     }
-    (void)pending_run;
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc<128>(tbase);
@@ -440,16 +477,17 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
     const int NR = (pb.C + kRun - 1) / kRun;
     ScanParams a;
     a.row_pair = ws.row_pair; a.row_ptr = ws.row_ptr; a.ev_chunk = ws.ev_chunk; a.snap_slot = ws.snap_slot;
+    a.run_first = ws.run_first;
     a.P = ws.P; a.g = pb.g; a.h0 = pb.h0;
     a.U = (__nv_bfloat16 *)ws.U; a.amap = (__nv_bfloat16 *)ws.amap; a.bmap = ws.bmap; a.entry = ws.entry;
     a.snap = (__nv_bfloat16 *)ws.snap; a.s_final = pb.s_final; a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.NR = NR;
     a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
+    CUtensorMap tA;
+    const uint64_t amap_rows = (uint64_t)pb.R * 2 * (NR > 0 ? NR : 1) * kDim;
+    if (!make_tmap_bf16_3d(&tA, ws.amap, kDim, amap_rows, 1, kDim * 2, amap_rows * kDim * 2, 64, 128, 1, true))
+        return cudaErrorInvalidValue;
     if (part == 1) {  // chain
-        CUtensorMap tA;
-        if (!make_tmap_bf16_3d(&tA, ws.amap, kDim, (uint64_t)pb.R * 2 * (NR > 0 ? NR : 1) * kDim, 1, kDim * 2,
-                               (uint64_t)pb.R * 2 * (NR > 0 ? NR : 1) * kDim * kDim * 2, 64, 128, 1, true))
-            return cudaErrorInvalidValue;
         cudaFuncSetAttribute(scan_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
         scan_chain_kernel<<<dim3(2, pb.R), kThreads, kChainSmem, pb.stream>>>(tA, a);
         return cudaGetLastError();
@@ -464,7 +502,7 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(scan_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmem);
     const int fixup = part == 2;
-    scan_run_kernel<<<dim3(NR, fixup ? 2 : 4, pb.R), kThreads, kRunSmem, pb.stream>>>(tW, tK, tU, a, fixup);
+    scan_run_kernel<<<dim3(NR, fixup ? 2 : 4, pb.R), kThreads, kRunSmem, pb.stream>>>(tW, tK, tU, tA, a, fixup);
     return cudaGetLastError();
 }
 

@@ -62,7 +62,8 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
               int32_t *__restrict__ row_pair, int32_t *__restrict__ row_ptr,
               int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
               int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
-              int32_t *__restrict__ ev_of, int64_t ev_cap, int64_t snap_cap) {
+              int32_t *__restrict__ ev_of, int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
+              int64_t snap_cap) {
     extern __shared__ int sm[];
     const int NW = (C + 31) >> 5;   // 32-chunk mask words per row
     int *cnt = sm;               // [R]   events per physical row
@@ -122,6 +123,10 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
             const int e = base + run + before;
             if (s && (int64_t)e < ev_cap) ev_chunk[e] = c;
             if (ev_of && c < C) ev_of[(int64_t)i * C + c] = s ? e : -1;
+            if (run_first && lane < 2) {  // runs of 16 chunks starting inside this word
+                const int rr = 2 * w + lane;
+                if (rr < NR) run_first[(int64_t)j * (NR + 1) + rr] = base + run + (lane ? __popc(bits & 0xFFFFu) : 0);
+            }
             if (lane < 16) {  // groups r with 2r = 32w + 2 lane
                 const int r = 16 * w + lane;
                 if (r < G) {
@@ -145,7 +150,10 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
             nref += __popc(__ballot_sync(0xffffffffu, ref));
             run += __popc(bits);
         }
-        if (lane == 0) refc[j] = nref;
+        if (lane == 0) {
+            refc[j] = nref;
+            if (run_first) run_first[(int64_t)j * (NR + 1) + NR] = base + run;
+        }
         __syncwarp();
     }
     __syncthreads();
@@ -202,7 +210,8 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
 
 }  // namespace
 
-cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of) {
+cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of,
+                          int32_t *run_first) {
     const size_t smem = sizeof(int) * (6 * (size_t)pb.R + 2 + (size_t)kWarps * ((pb.C + 31) / 32));
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -210,7 +219,8 @@ cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_
     }
     select_kernel<<<1, kThreads, smem, pb.stream>>>(pb.mask, pb.R, pb.C, pb.G, ev.row_pair, ev.row_ptr,
                                                     ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts,
-                                                    ev_of, (int64_t)ev.capacity, snap_cap);
+                                                    ev_of, run_first, (pb.C + kRunChunks - 1) / kRunChunks,
+                                                    (int64_t)ev.capacity, snap_cap);
     return cudaGetLastError();
 }
 

@@ -92,6 +92,19 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// TMA store from shared memory; completion is tracked per issuing thread by bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, const void *smem_src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_addr(smem_src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The shared-memory sources of this thread's committed stores may be overwritten.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's committed stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- fences -------------------------------------------------------------------
 // Generic-proxy writes to shared memory -> visible to the tensor core (async proxy).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -182,6 +195,14 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_saddr, int ks, ui
 // Byte offset of element (row, k) inside a K-major 128B-swizzled slab of bf16.
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t k) {
     return row * 128u + ((((k >> 3) ^ (row & 7u)) & 7u) << 4) + ((k & 7u) << 1);
+}
+
+// fp32 state tiles in global memory use a "column-quad" layout: element
+// (row, col) of a 128x128 tile lives at float index (col / 4) * 512 + row * 4 +
+// col % 4, so that threads owning consecutive rows read or write consecutive
+// 16-byte quads (fully coalesced thread-per-row access).
+__host__ __device__ __forceinline__ uint32_t quad_index(uint32_t row, uint32_t col) {
+    return (col >> 2) * 512u + row * 4u + (col & 3u);
 }
 
 // Stores 8 consecutive K values (k0 % 8 == 0) of one row as one 16-byte chunk.

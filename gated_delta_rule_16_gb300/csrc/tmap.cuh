@@ -32,6 +32,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
                               uint32_t box2, bool swizzle128 = true) {
+    if (reinterpret_cast<uintptr_t>(base) & 15u) return false;
     auto enc = tmap_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
