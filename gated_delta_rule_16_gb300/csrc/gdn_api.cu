@@ -95,6 +95,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_ev_of = take(R * C * sizeof(int32_t));
     const size_t o_run_first = take(R * ((C + kRunChunks - 1) / kRunChunks + 1) * sizeof(int32_t));
     const size_t o_P = take((size_t)pb.B * pb.Nv * (C + 1) * sizeof(double));
+    const size_t o_grp_info = take((size_t)R * G * 16);
     const size_t o_U = take((size_t)pb.B * pb.T * pb.Nv * pb.dv * es);
     const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
     const size_t o_W = take((size_t)ev_cap * 2 * kChunk * pb.d * es);
@@ -115,6 +116,7 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
         ws->ev_of = (int32_t *)(b + o_ev_of);
         ws->run_first = (int32_t *)(b + o_run_first);
         ws->P = (double *)(b + o_P);
+        ws->grp_info = b + o_grp_info;
         ws->U = b + o_U;
         ws->cbar = (float *)(b + o_cbar);
         ws->W = b + o_W;

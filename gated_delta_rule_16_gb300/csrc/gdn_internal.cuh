@@ -64,6 +64,7 @@ struct Workspace {
     int32_t *ev_of;            // [R, C] event index of each (physical row, chunk), or -1
     int32_t *run_first;        // [R, NR+1] first event of each run, per CSR row
     double *P;                 // [B, Nv, C+1] log2 decay prefix (Eq. 19)
+    void *grp_info;            // [B, P, G] int4 {snapshot slot, kind, decay head 0, decay head 1}
     void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks
     void *W;                   // [ev_cap, 2, 64, d] dtype, deferred W of events

@@ -164,13 +164,20 @@ intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__re
     }
 }
 
-// P[b,h,0] = 0, P[b,h,c+1] = P[b,h,c] + gamma_{c}: one warp per (b, h), fp64.
-__global__ void prefix_kernel(const float *__restrict__ g, int B, int T_, int Nv, int C, double *__restrict__ P) {
-    const int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (unit >= B * Nv) return;
-    const int b = unit / Nv, h = unit % Nv;
-    double *Pu = P + (int64_t)unit * (C + 1);
+// P[b,h,0] = 0, P[b,h,c+1] = P[b,h,c] + gamma_c (Eq. 19), fp64: one CTA per
+// (sequence, head pair), one warp per value head.  Then, per output group r of
+// the pair, the entry-state table the group output reads with one load:
+// {snapshot slot or -1, state kind, 2^(P_2r - P_(e+1)) of both heads} where e is
+// the group's predecessor event (kind 1), or {-1, 2, 2^P_2r} when the group
+// starts from h0 (kind 2), or kind 0 (zero state).
+__global__ void prefix_kernel(const float *__restrict__ g, int T_, int Nv, int C, int P_, int G,
+                              const int32_t *__restrict__ grp_pred, const int32_t *__restrict__ snap_slot,
+                              const int32_t *__restrict__ ev_chunk, int64_t ev_cap, int64_t snap_cap, int has_h0,
+                              double *__restrict__ P, int4 *__restrict__ grp_info) {
+    const int bp = blockIdx.x, b = bp / P_, p = bp % P_;
+    const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = 2 * p + hh;
+    double *Pu = P + ((int64_t)b * Nv + h) * (C + 1);
     if (lane == 0) Pu[0] = 0.0;
     double carry = 0.0;
     for (int c0 = 0; c0 < C; c0 += 32) {
@@ -183,6 +190,25 @@ __global__ void prefix_kernel(const float *__restrict__ g, int B, int T_, int Nv
         }
         if (c < C) Pu[c + 1] = carry + x;
         carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (!grp_info) return;
+    __syncthreads();  // P of both heads written by this CTA
+    const double *P0 = P + ((int64_t)b * Nv + 2 * p) * (C + 1);
+    const double *P1 = P0 + (C + 1);
+    for (int r = threadIdx.x; r < G; r += blockDim.x) {
+        const int pred = grp_pred[(int64_t)bp * G + r];
+        int4 info = make_int4(-1, 0, 0, 0);
+        if (pred >= 0 && pred < ev_cap) {
+            const int slot = snap_slot[pred];
+            if (slot >= 0 && slot < snap_cap) {
+                const int e1 = ev_chunk[pred] + 1;
+                info = make_int4(slot, 1, __float_as_int(exp2f((float)(P0[2 * r] - P0[e1]))),
+                                 __float_as_int(exp2f((float)(P1[2 * r] - P1[e1]))));
+            }
+        } else if (has_h0) {
+            info = make_int4(-1, 2, __float_as_int(exp2f((float)P0[2 * r])), __float_as_int(exp2f((float)P1[2 * r])));
+        }
+        grp_info[(int64_t)bp * G + r] = info;
     }
 }
 
@@ -209,9 +235,10 @@ cudaError_t launch_intra(const Problem &pb, const Workspace &ws) {
 }
 
 cudaError_t launch_prefix(const Problem &pb, const Workspace &ws) {
-    const int units = pb.B * pb.Nv;
-    if (units == 0) return cudaSuccess;
-    prefix_kernel<<<(units + 7) / 8, 256, 0, pb.stream>>>(pb.g, pb.B, pb.T, pb.Nv, pb.C, ws.P);
+    if (pb.R == 0) return cudaSuccess;
+    prefix_kernel<<<pb.R, 64, 0, pb.stream>>>(pb.g, pb.T, pb.Nv, pb.C, pb.P, pb.G, ws.grp_pred, ws.snap_slot,
+                                              ws.ev_chunk, ws.ev_cap, ws.snap_cap, pb.h0 != nullptr, ws.P,
+                                              (int4 *)ws.grp_info);
     return cudaGetLastError();
 }
 

@@ -53,6 +53,41 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// Off-diagonal 16x16 blocks at distance OFF of both chunks' C (Eq. 7 generalised):
+// C_ij = -C_ii (sum_{k=j}^{i-1} M_ik C_kj), i = j + OFF, once every block closer to
+// the diagonal is known.  256 threads, one element (row rr, column col) of a block each.
+template <int OFF>
+__device__ __forceinline__ void offdiag_blocks(const float *Ms, float *Cs, float *Tb, int tid) {
+    constexpr int NB = 4 - OFF;
+    const int rr = tid >> 4, col = tid & 15;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int bi = 0; bi < NB; ++bi) {
+            const int ib = bi + OFF, jb = bi;
+            const float *Mr = Ms + (cc * kChunk + ib * kBlk + rr) * MS + jb * kBlk;
+            const float *Cc = Cs + (cc * kChunk + jb * kBlk) * MS + jb * kBlk + col;
+            float acc = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < kBlk * OFF; ++kk) acc += Mr[kk] * Cc[kk * MS];
+            Tb[(cc * NB + bi) * 256 + tid] = acc;
+        }
+    __syncthreads();
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int bi = 0; bi < NB; ++bi) {
+            const int ib = bi + OFF, jb = bi;
+            float *Cr = Cs + (cc * kChunk + ib * kBlk + rr) * MS;
+            const float *Tt = Tb + (cc * NB + bi) * 256 + col;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < kBlk; ++m) acc += Cr[ib * kBlk + m] * Tt[m * 16];
+            Cr[jb * kBlk + col] = -acc;
+        }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tU64,
@@ -80,13 +115,21 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     const int nch = c0 + 1 < a.C ? 2 : 1;
     const int tok0 = b * a.T_ + c0 * kChunk;
 
-    if (tid == 0) {
+    if (tid == 0) {  // barriers, then the tiles: the loads overlap the set-up below
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_g, 1);
         mbar_init(&bar_u, 1);
         mbar_init(&bar_drain, 1);
         fence_mbar_init();
         abort_s = 0;
+        mbar_arrive_expect_tx(&bar_ld, 6 * kSlab);
+        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_ld);
+        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_ld);
+        for (int hh = 0; hh < 2; ++hh) {
+            uint8_t *vd = sm + OFF_V + hh * 2 * kSlab;
+            tma_load_3d(vd, &tV, 0, 2 * p + hh, tok0, &bar_ld);
+            tma_load_3d(vd + kSlab, &tV, 64, 2 * p + hh, tok0, &bar_ld);
+        }
     }
     if (tid < 2) ev_s[tid] = tid < nch ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
     {   // beta and g of both heads, fetched once while the tiles load
@@ -103,14 +146,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     const uint32_t tbase = tmem_base;
     const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_ld, 6 * kSlab);
-        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_ld);
-        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_ld);
-        for (int hh = 0; hh < 2; ++hh) {
-            uint8_t *vd = sm + OFF_V + hh * 2 * kSlab;
-            tma_load_3d(vd, &tV, 0, 2 * p + hh, tok0, &bar_ld);
-            tma_load_3d(vd + kSlab, &tV, 64, 2 * p + hh, tok0, &bar_ld);
-        }
         if (!mbar_wait(&bar_ld, 0)) {
             abort_s = 1;
             atomicOr(a.status, kStatusTimeout);
@@ -173,31 +208,10 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             for (int i2 = 0; i2 < kBlk; ++i2) Cb[i2 * MS] = x[i2];
         }
         __syncthreads();
-        for (int off = 1; off <= max_off; ++off) {
-            const int nb = 4 - off;
-            for (int idx = tid; idx < 2 * nb * 256; idx += kThreads) {
-                const int cc = idx / (nb * 256), rem = idx % (nb * 256);
-                const int bi = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
-                const int ib = bi + off, jb = bi;
-                const float *Mm = Ms + cc * kChunk * MS;
-                const float *Cm = Cs + cc * kChunk * MS;
-                float acc = 0.f;
-                for (int kk = jb * kBlk; kk < ib * kBlk; ++kk)
-                    acc += Mm[(ib * kBlk + rr) * MS + kk] * Cm[kk * MS + jb * kBlk + col];
-                Tb[cc * 768 + rem] = acc;
-            }
-            __syncthreads();
-            for (int idx = tid; idx < 2 * nb * 256; idx += kThreads) {
-                const int cc = idx / (nb * 256), rem = idx % (nb * 256);
-                const int bi = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
-                const int ib = bi + off, jb = bi;
-                float *Cm = Cs + cc * kChunk * MS;
-                float acc = 0.f;
-                for (int m = 0; m < kBlk; ++m)
-                    acc += Cm[(ib * kBlk + rr) * MS + ib * kBlk + m] * Tb[cc * 768 + (bi << 8) + m * 16 + col];
-                Cm[(ib * kBlk + rr) * MS + jb * kBlk + col] = -acc;
-            }
-            __syncthreads();
+        offdiag_blocks<1>(Ms, Cs, Tb, tid);
+        if (max_off == 3) {
+            offdiag_blocks<2>(Ms, Cs, Tb, tid);
+            offdiag_blocks<3>(Ms, Cs, Tb, tid);
         }
         // 3. A tiles: C diag(beta) for U, and C diag(beta 2^g) for W (built in the
         //    fp32 M area, free once the solve is done); both bf16, block-diagonal
@@ -206,11 +220,18 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             for (int part = 0; part < (any_event ? 2 : 1); ++part) {
                 uint8_t *dst = (part == 0 ? sm + OFF_A : reinterpret_cast<uint8_t *>(Ms)) + hf * kSlab;
                 const float *f = (part == 0 ? bet : bgs) + 64 * ct;
-                for (int k0 = 0; k0 < 64; k0 += 8) {
-                    float w[8];
+                if (hf == ct) {  // warp-uniform: this half of the row is the row's own chunk
 #pragma unroll
-                    for (int q2 = 0; q2 < 8; ++q2) w[q2] = hf == ct ? crow[k0 + q2] * f[k0 + q2] : 0.f;
-                    st_sw128_8(dst, row, k0, w);
+                    for (int k0 = 0; k0 < 64; k0 += 8) {
+                        float w[8];
+#pragma unroll
+                        for (int q2 = 0; q2 < 8; ++q2) w[q2] = crow[k0 + q2] * f[k0 + q2];
+                        st_sw128_8(dst, row, k0, w);
+                    }
+                } else {
+                    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(dst, row, k0, z);
                 }
             }
         }

@@ -34,12 +34,10 @@ constexpr uint32_t TM_QK = 0, TM_QS = 128, TM_AU = 256;
 
 struct OutParams {
     const float *g, *h0;
-    const double *P;
-    const int32_t *ev_chunk, *grp_pred, *snap_slot;
+    const int4 *grp_info;   // per group: {snapshot slot, kind, decay head 0, decay head 1}
     __nv_bfloat16 *O;
     int32_t *status;
     int P_, T_, Nv, C, G;
-    int64_t ev_cap, snap_cap;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -90,25 +88,12 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
             tma_load_3d(ud + kSlab, &tU, 64, 2 * p + hh, tok0, &bar_h_ld[hh]);
         }
     }
-    if (tid < 2) {
-        const int hh = tid, h = 2 * p + hh;
-        const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
-        const int pred = a.grp_pred[((int64_t)b * a.P_ + p) * a.G + r];
-        int has = 0, slot = -1;
-        float f = 0.f;
-        if (pred >= 0 && pred < a.ev_cap) {
-            slot = a.snap_slot[pred];
-            if (slot >= 0 && slot < a.snap_cap) {
-                has = 1;
-                f = exp2f((float)(Pu[c0] - Pu[a.ev_chunk[pred] + 1]));
-            }
-        } else if (a.h0) {
-            has = 2;  // initial state: converted by the threads below
-            f = exp2f((float)Pu[c0]);
-        }
-        has_s[hh] = has;
-        slot_s[hh] = slot;
-        fscale[hh] = f;
+    if (tid < 2) {  // entry state of the group: one table load (kind 1 snapshot, 2 h0, 0 zero)
+        const int4 info = a.grp_info[((int64_t)b * a.P_ + p) * a.G + r];
+        const int hh = tid;
+        has_s[hh] = info.y == 2 && !a.h0 ? 0 : info.y;
+        slot_s[hh] = info.x;
+        fscale[hh] = __int_as_float(hh ? info.w : info.z);
     }
     for (int idx = tid; idx < 256; idx += kThreads) {
         const int hh = idx >> 7, t = idx & 127;
@@ -283,11 +268,9 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
         !make_tmap_bf16_3d(&tO64, pb.o, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     OutParams a;
-    a.g = pb.g; a.h0 = pb.h0; a.P = ws.P;
-    a.ev_chunk = ws.ev_chunk; a.grp_pred = ws.grp_pred; a.snap_slot = ws.snap_slot;
+    a.g = pb.g; a.h0 = pb.h0; a.grp_info = (const int4 *)ws.grp_info;
     a.O = (__nv_bfloat16 *)pb.o; a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.G = pb.G;
-    a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
     cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
     output_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream>>>(tQ, tK, tU, tS, tO, tO64, a);
     return cudaGetLastError();
