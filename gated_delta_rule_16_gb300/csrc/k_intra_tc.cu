@@ -165,7 +165,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         const float *bet = bet2 + 128 * hh;
         const float *gg = gg2 + 128 * hh;
         if (tid == 0) bulk_wait_read();  // the W store of the previous head has left the A tile
-        if (tid < 128) bgs[tid] = bet[tid] * exp2f(gg[tid]);
+        if (tid < 128) bgs[tid] = bet[tid] * ex2(gg[tid]);
         if (tid < 2) ssum[tid] = 0.f;
         for (int idx = tid; idx < 2 * kChunk * MS; idx += kThreads) Cs[idx] = 0.f;
         __syncthreads();
@@ -181,7 +181,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 #pragma unroll
             for (int q2 = 0; q2 < 32; ++q2) {
                 const int s = 32 * hf + q2;
-                mrow[s] = s < tl ? bt * gv[q2] * exp2f(gt - gg[64 * ct + s]) : (s == tl ? 1.f : 0.f);
+                mrow[s] = s < tl ? bt * gv[q2] * ex2(gt - gg[64 * ct + s]) : (s == tl ? 1.f : 0.f);
             }
         }
         __syncthreads();

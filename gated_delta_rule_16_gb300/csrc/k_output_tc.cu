@@ -164,8 +164,8 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
                 for (int t = 0; t < 32; ++t) {
                     const int jj = j0 + t, cj = jj >> 6;
                     float m = 0.f;
-                    if (ci == cj) m = jj <= row ? exp2f(gi - g[jj]) : 0.f;
-                    else if (ci == 1) m = exp2f(gi + gam0 - g[jj]);
+                    if (ci == cj) m = jj <= row ? ex2(gi - g[jj]) : 0.f;
+                    else if (ci == 1) m = ex2(gi + gam0 - g[jj]);
                     w[t] = (ci == 1 && !two) ? 0.f : qk[t] * m;
                 }
 #pragma unroll
@@ -211,7 +211,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         // 3. epilogue of head hh: O rows staged (bf16, 128B-swizzled) in the U' tile
         //    this head no longer needs, then written by one TMA store
         {
-            const float f = fscale[hh] * exp2f(gs[hh][row] + (row >= 64 ? gs[hh][63] : 0.f));
+            const float f = fscale[hh] * ex2(gs[hh][row] + (row >= 64 ? gs[hh][63] : 0.f));
             const bool has = has_s[hh] != 0;
             uint8_t *stage = sm + (hh ? OFF_U1 : OFF_U0) + hf * kSlab;
             for (int half32 = 0; half32 < 2; ++half32) {

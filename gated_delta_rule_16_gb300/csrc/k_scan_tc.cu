@@ -136,7 +136,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         const int k = idx >> 6, t = idx & 63;
         const int64_t tk = (int64_t)b * a.T_ + (int64_t)ev_c[k] * kChunk;
         const float gam = a.g[(tk + kChunk - 1) * a.Nv + h];
-        dec[k][t] = exp2f(gam - a.g[(tk + t) * a.Nv + h]);
+        dec[k][t] = ex2(gam - a.g[(tk + t) * a.Nv + h]);
         if (t == 0) gamk[k] = gam;
     }
     const uint32_t tbase = tmem_base;
@@ -185,7 +185,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     for (; k < n_ev; ++k) {
         const int c = ev_c[k];
         uint8_t *buf = sm + OFF_BUF + (k & 1) * BUF_BYTES;
-        const float gap = exp2f((float)(Pl[c - c_lo] - Pl[cur - c_lo]));
+        const float gap = ex2((float)(Pl[c - c_lo] - Pl[cur - c_lo]));
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj) S[jj] *= gap;
 #pragma unroll
@@ -250,7 +250,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + 64 * hf), d0);
         tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + 64 * hf + 32), d1);
         tmem_ld_wait();
-        const float dg = exp2f(gam);
+        const float dg = ex2(gam);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
             S[jj] = dg * S[jj] + d0[jj];
@@ -270,7 +270,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         if (abort_s) break;
     }
     if (!abort_s && mode != kModeFixup) {
-        const float fin = exp2f((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
+        const float fin = ex2((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj) S[jj] *= fin;
         if (mode == kModeHomog) {
@@ -394,7 +394,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         for (int v4 = 0; v4 < 16; ++v4) ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
         const bool has = nxt[r] == r;
         if (!has) {
-            const float f = exp2f((float)(Pu[c_hi] - Pu[c_lo]));
+            const float f = ex2((float)(Pu[c_hi] - Pu[c_lo]));
 #pragma unroll
             for (int jj = 0; jj < 64; ++jj) S[jj] *= f;
             continue;

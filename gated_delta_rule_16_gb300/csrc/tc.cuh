@@ -30,6 +30,15 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 2^x by the hardware approximation instruction (PTX ex2.approx.ftz.f32; its
+// documented relative error, about 2^-22, is far below the bf16 rounding these
+// kernels apply afterwards).  Results below the normal range flush to zero.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
