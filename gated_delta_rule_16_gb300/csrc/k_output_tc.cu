@@ -21,7 +21,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: 4 per TMEM lane quarter, 32 columns each
 constexpr uint32_t kSlab = 16384;          // [128 rows][128 B]
 constexpr uint32_t OFF_Q = 0;              // Q: 2 K-slabs
 constexpr uint32_t OFF_K = 2 * kSlab;      // K: 2 K-slabs; later S of head 1 (2 MN-stacks)
@@ -58,8 +58,8 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     __shared__ int has_s[2], slot_s[2];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, hf = warp >> 2;
-    const int row = quarter * 32 + lane;  // query token inside the group
+    const int quarter = warp & 3, seg = warp >> 2;  // TMEM lane quarter, 32-column segment
+    const int row = quarter * 32 + lane;            // query token inside the group
     const int r = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
     const int c0 = 2 * r;
     const bool two = c0 + 1 < a.C;
@@ -154,9 +154,9 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
             const int ci = row >> 6;
             const float gi = g[row];
             const float gam0 = g[63];
-            for (int half32 = 0; half32 < 2; ++half32) {
+            {
                 float qk[32];
-                const int j0 = 64 * hf + 32 * half32;
+                const int j0 = 32 * seg;
                 tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QK + j0), qk);
                 tmem_ld_wait();
                 float w[32];
@@ -169,7 +169,8 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
                     w[t] = (ci == 1 && !two) ? 0.f : qk[t] * m;
                 }
 #pragma unroll
-                for (int t0 = 0; t0 < 32; t0 += 8) st_sw128_8(sm + OFF_A + hf * kSlab, row, 32 * half32 + t0, &w[t0]);
+                for (int t0 = 0; t0 < 32; t0 += 8)
+                    st_sw128_8(sm + OFF_A + (seg >> 1) * kSlab, row, 32 * (seg & 1) + t0, &w[t0]);
             }
         }
         if (hh == 1 && has_s[1] == 2) fill_h0(1, sm + OFF_K);
@@ -213,17 +214,17 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         {
             const float f = fscale[hh] * ex2(gs[hh][row] + (row >= 64 ? gs[hh][63] : 0.f));
             const bool has = has_s[hh] != 0;
-            uint8_t *stage = sm + (hh ? OFF_U1 : OFF_U0) + hf * kSlab;
-            for (int half32 = 0; half32 < 2; ++half32) {
+            uint8_t *stage = sm + (hh ? OFF_U1 : OFF_U0) + (seg >> 1) * kSlab;
+            {
                 float qs[32], au[32];
-                const int col = 64 * hf + 32 * half32;
+                const int col = 32 * seg;
                 tmem_ld32(tmem_addr(tbase, quarter * 32, TM_AU + col), au);
                 if (has) tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QS + col), qs);
                 tmem_ld_wait();
 #pragma unroll
                 for (int t = 0; t < 32; ++t) au[t] = ((has ? f * qs[t] : 0.f) + au[t]) * inv_sqrt_d;
 #pragma unroll
-                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(stage, row, 32 * half32 + 8 * v8, &au[8 * v8]);
+                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(stage, row, 32 * (seg & 1) + 8 * v8, &au[8 * v8]);
             }
         }
         fence_async_smem();
