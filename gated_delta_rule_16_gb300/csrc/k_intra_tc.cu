@@ -23,7 +23,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: 4 per TMEM lane quarter, 32 columns each
 constexpr uint32_t kSlab = 16384;
 constexpr uint32_t OFF_K = 0;            // K tile: 2 K-slabs [128 tok][64 d]
 constexpr uint32_t OFF_V = 2 * kSlab;    // V tiles of the two heads: 2 MN-stacks [128 tok][64 dv] each
@@ -55,13 +55,13 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 // Off-diagonal 16x16 blocks at distance OFF of both chunks' C (Eq. 7 generalised):
 // C_ij = -C_ii (sum_{k=j}^{i-1} M_ik C_kj), i = j + OFF, once every block closer to
-// the diagonal is known.  256 threads, one element (row rr, column col) of a block each.
+// the diagonal is known.  512 threads: one chunk per half, one element of a block each.
 template <int OFF>
 __device__ __forceinline__ void offdiag_blocks(const float *Ms, float *Cs, float *Tb, int tid) {
     constexpr int NB = 4 - OFF;
-    const int rr = tid >> 4, col = tid & 15;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc)
+    const int cc = tid >> 8, e = tid & 255;  // 512 threads: chunk, element of the 16x16 block
+    const int rr = e >> 4, col = e & 15;
+    {
 #pragma unroll
         for (int bi = 0; bi < NB; ++bi) {
             const int ib = bi + OFF, jb = bi;
@@ -70,11 +70,11 @@ __device__ __forceinline__ void offdiag_blocks(const float *Ms, float *Cs, float
             float acc = 0.f;
 #pragma unroll
             for (int kk = 0; kk < kBlk * OFF; ++kk) acc += Mr[kk] * Cc[kk * MS];
-            Tb[(cc * NB + bi) * 256 + tid] = acc;
+            Tb[(cc * NB + bi) * 256 + e] = acc;
         }
+    }
     __syncthreads();
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc)
+    {
 #pragma unroll
         for (int bi = 0; bi < NB; ++bi) {
             const int ib = bi + OFF, jb = bi;
@@ -85,6 +85,7 @@ __device__ __forceinline__ void offdiag_blocks(const float *Ms, float *Cs, float
             for (int m = 0; m < kBlk; ++m) acc += Cr[ib * kBlk + m] * Tt[m * 16];
             Cr[jb * kBlk + col] = -acc;
         }
+    }
     __syncthreads();
 }
 
@@ -107,8 +108,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     float *ssum = reinterpret_cast<float *>(sm + OFF_F + F_S);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, hf = warp >> 2;
-    const int row = quarter * 32 + lane;  // token inside the group
+    const int quarter = warp & 3, seg = warp >> 2;  // TMEM lane quarter, 32-column segment
+    const int row = quarter * 32 + lane;            // token inside the group
     const int ct = row >> 6, tl = row & 63;
     const int r = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
     const int c0 = 2 * r;
@@ -132,7 +133,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         }
     }
     if (tid < 2) ev_s[tid] = tid < nch ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
-    {   // beta and g of both heads, fetched once while the tiles load
+    if (tid < 256) {  // beta and g of both heads, fetched once while the tiles load
         const int hh = tid >> 7, t = tid & 127;
         const bool valid = (t >> 6) < nch;
         const int64_t gi = ((int64_t)tok0 + t) * a.Nv + 2 * p + hh;
@@ -172,7 +173,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         // 1. M from the Gram block of the row's chunk: thread (row, half) covers 32 columns
         if (hh == 0 && !mbar_wait(&bar_g, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
         tc_fence_after();
-        {
+        if (seg < 2) {
+            const int hf = seg;
             float gv[32];
             tmem_ld32(tmem_addr(tbase, quarter * 32, TM_G + 64 * ct + 32 * hf), gv);
             tmem_ld_wait();
@@ -217,21 +219,22 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         //    fp32 M area, free once the solve is done); both bf16, block-diagonal
         {
             const float *crow = Cs + (ct * kChunk + tl) * MS;
+            const int slab = seg >> 1, c0s = 32 * (seg & 1);  // this thread's 32 columns
             for (int part = 0; part < (any_event ? 2 : 1); ++part) {
-                uint8_t *dst = (part == 0 ? sm + OFF_A : reinterpret_cast<uint8_t *>(Ms)) + hf * kSlab;
+                uint8_t *dst = (part == 0 ? sm + OFF_A : reinterpret_cast<uint8_t *>(Ms)) + slab * kSlab;
                 const float *f = (part == 0 ? bet : bgs) + 64 * ct;
-                if (hf == ct) {  // warp-uniform: this half of the row is the row's own chunk
+                if (slab == ct) {  // warp-uniform: these columns belong to the row's own chunk
 #pragma unroll
-                    for (int k0 = 0; k0 < 64; k0 += 8) {
+                    for (int k0 = 0; k0 < 32; k0 += 8) {
                         float w[8];
 #pragma unroll
-                        for (int q2 = 0; q2 < 8; ++q2) w[q2] = crow[k0 + q2] * f[k0 + q2];
-                        st_sw128_8(dst, row, k0, w);
+                        for (int q2 = 0; q2 < 8; ++q2) w[q2] = crow[c0s + k0 + q2] * f[c0s + k0 + q2];
+                        st_sw128_8(dst, row, c0s + k0, w);
                     }
                 } else {
                     const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(dst, row, k0, z);
+                    for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(dst, row, c0s + k0, z);
                 }
             }
         }
@@ -256,13 +259,14 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         tc_fence_after();
         {   // U rows staged in this head's V tile (free once the MMAs are done), W rows in the A tile
             float sq = 0.f;
-            uint8_t *ustage = sm + OFF_V + hh * 2 * kSlab + hf * kSlab;
-            for (int half32 = 0; half32 < 2; ++half32) {
+            const int slab = seg >> 1, c0s = 32 * (seg & 1);
+            uint8_t *ustage = sm + OFF_V + hh * 2 * kSlab + slab * kSlab;
+            {
                 float u[32];
-                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 64 * hf + 32 * half32), u);
+                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 32 * seg), u);
                 tmem_ld_wait();
 #pragma unroll
-                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(ustage, row, 32 * half32 + 8 * v8, &u[8 * v8]);
+                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(ustage, row, c0s + 8 * v8, &u[8 * v8]);
                 if (tl >= kChunk - kBlk) {
 #pragma unroll
                     for (int q2 = 0; q2 < 32; ++q2) sq += u[q2] * u[q2];
@@ -272,14 +276,12 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
             if (lane == 0 && sq != 0.f) atomicAdd(&ssum[ct], sq);
             if (ev_s[ct] >= 0) {
-                uint8_t *wstage = sm + OFF_A + hf * kSlab;
-                for (int half32 = 0; half32 < 2; ++half32) {
-                    float w[32];
-                    tmem_ld32(tmem_addr(tbase, quarter * 32, TM_W + 64 * hf + 32 * half32), w);
-                    tmem_ld_wait();
+                uint8_t *wstage = sm + OFF_A + slab * kSlab;
+                float w[32];
+                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_W + 32 * seg), w);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(wstage, row, 32 * half32 + 8 * v8, &w[8 * v8]);
-                }
+                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(wstage, row, c0s + 8 * v8, &w[8 * v8]);
             }
         }
         fence_async_smem();
