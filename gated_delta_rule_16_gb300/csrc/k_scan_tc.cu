@@ -18,8 +18,8 @@
 // The longest serial chain is then 16 events (plus one MMA per run), not a row.
 //
 // Layout.  Columns of S evolve independently, so the CTA works on S^T: TMEM
-// lane / state row = a column of S (d_v index), 128 rows; 256 threads, thread
-// (row, half) holds 64 of the row's 128 fp32 entries in registers.  Per event:
+// lane / state row = a column of S (d_v index), 128 rows; 512 threads, thread
+// (row, segment) holds 32 of the row's 128 fp32 entries in registers.  Per event:
 //   MMA1  U'^T_acc[128 x 64]  = S^T[128 x 128] . W^T      (A: S^T bf16 K-major; B: W [t][d] K-major)
 //   U'^T = U^T - U'^T_acc;  U''^T = U'^T * 2^(gamma - g_t)        (registers)
 //   MMA2  dS^T[128 x 128]     = U''^T[128 x 64] . K        (A: U''^T K-major; B: K [t][d] MN-major)
@@ -36,7 +36,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: 4 per TMEM lane quarter, 32 state columns each
 constexpr int kRun = kRunChunks;
 constexpr uint32_t kSlab = 16384;        // [128 rows][128 B]
 constexpr uint32_t OFF_A1 = 0;           // S^T bf16, K-major, 2 slabs
@@ -95,8 +95,9 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     __shared__ float gamk[kRun];         // gamma of each event chunk
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, hf = warp >> 2;
+    const int quarter = warp & 3, seg = warp >> 2;  // TMEM lane quarter, 32-column segment
     const int row = quarter * 32 + lane;
+    const int cs = 32 * seg, slab = seg >> 1, cin = 32 * (seg & 1);  // columns, slab, offset in slab
     const int rho = blockIdx.x, j = blockIdx.z;
     const int hh = fixup ? (int)blockIdx.y : (int)(blockIdx.y >> 1);
     const int mode = fixup ? kModeFixup : (int)(blockIdx.y & 1);
@@ -161,17 +162,17 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         tma_issued = 1;
     }
 
-    float S[64];
+    float S[32];
     if (mode == kModeHomog) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) S[jj] = (64 * hf + jj == row) ? 1.f : 0.f;
+        for (int jj = 0; jj < 32; ++jj) S[jj] = (cs + jj == row) ? 1.f : 0.f;
     } else if (mode == kModeInhom) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) S[jj] = 0.f;
+        for (int jj = 0; jj < 32; ++jj) S[jj] = 0.f;
     } else {
-        const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase) + 16 * hf * 128 + row;
+        const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase) + 8 * seg * 128 + row;
 #pragma unroll
-        for (int v4 = 0; v4 < 16; ++v4) {
+        for (int v4 = 0; v4 < 8; ++v4) {
             const float4 x = src[v4 * 128];
             S[4 * v4] = x.x; S[4 * v4 + 1] = x.y; S[4 * v4 + 2] = x.z; S[4 * v4 + 3] = x.w;
         }
@@ -187,9 +188,9 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         uint8_t *buf = sm + OFF_BUF + (k & 1) * BUF_BYTES;
         const float gap = ex2((float)(Pl[c - c_lo] - Pl[cur - c_lo]));
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) S[jj] *= gap;
+        for (int jj = 0; jj < 32; ++jj) S[jj] *= gap;
 #pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(A1 + hf * kSlab, row, k0, &S[k0]);
+        for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(A1 + slab * kSlab, row, cin + k0, &S[k0]);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -213,22 +214,22 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         if (abort_s) break;
         if (!mbar_wait(&bar_mma1, k & 1)) fail(a, &abort_s);
         tc_fence_after();
-        float acc[32];
-        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 32 * hf), acc);
+        float acc[16];
+        tmem_ld16(tmem_addr(tbase, quarter * 32, TM_U + 16 * seg), acc);
         tmem_ld_wait();
         __nv_bfloat16 *Ut = reinterpret_cast<__nv_bfloat16 *>(buf + BUF_U);
         const float gam = gamk[k];
-        float up[32];
+        float up[16];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-            const int tt = 32 * hf + t;
+        for (int t = 0; t < 16; ++t) {
+            const int tt = 16 * seg + t;
             const float u = mode == kModeHomog ? 0.f : __bfloat162float(Ut[tt * kDim + row]);
             const float v = u - acc[t];
             if (mode == kModeFixup) Ut[tt * kDim + row] = __float2bfloat16_rn(v);  // U' replaces U in the tile
             up[t] = v * dec[k][tt];
         }
 #pragma unroll
-        for (int t0 = 0; t0 < 32; t0 += 8) st_sw128_8(A2, row, 32 * hf + t0, &up[t0]);
+        for (int t0 = 0; t0 < 16; t0 += 8) st_sw128_8(A2, row, 16 * seg + t0, &up[t0]);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -246,22 +247,18 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         }
         if (!mbar_wait(&bar_mma2, k & 1)) fail(a, &abort_s);
         tc_fence_after();
-        float d0[32], d1[32];
-        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + 64 * hf), d0);
-        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + 64 * hf + 32), d1);
+        float d0[32];
+        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + cs), d0);
         tmem_ld_wait();
         const float dg = ex2(gam);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            S[jj] = dg * S[jj] + d0[jj];
-            S[32 + jj] = dg * S[32 + jj] + d1[jj];
-        }
+        for (int jj = 0; jj < 32; ++jj) S[jj] = dg * S[jj] + d0[jj];
         if (mode == kModeFixup) {
             const int slot = ev_slot[k];
             if (slot >= 0 && slot < a.snap_cap) {
                 __nv_bfloat16 *sn = a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim);
 #pragma unroll
-                for (int jj = 0; jj < 64; ++jj) sn[(64 * hf + jj) * kDim + row] = __float2bfloat16_rn(S[jj]);
+                for (int jj = 0; jj < 32; ++jj) sn[(cs + jj) * kDim + row] = __float2bfloat16_rn(S[jj]);
             }
         }
         cur = c + 1;
@@ -272,11 +269,11 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     if (!abort_s && mode != kModeFixup) {
         const float fin = ex2((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) S[jj] *= fin;
+        for (int jj = 0; jj < 32; ++jj) S[jj] *= fin;
         if (mode == kModeHomog) {
             // A_r^T rows staged as the chain's MN-major operand image, then one TMA store
 #pragma unroll
-            for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(A1 + hf * kSlab, row, k0, &S[k0]);
+            for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(A1 + slab * kSlab, row, cin + k0, &S[k0]);
             fence_async_smem();
             __syncthreads();
             if (tid == 0) {
@@ -286,9 +283,9 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                 bulk_commit();
             }
         } else {
-            float4 *dst = reinterpret_cast<float4 *>(a.bmap + ubase) + 16 * hf * 128 + row;
+            float4 *dst = reinterpret_cast<float4 *>(a.bmap + ubase) + 8 * seg * 128 + row;
 #pragma unroll
-            for (int v4 = 0; v4 < 16; ++v4)
+            for (int v4 = 0; v4 < 8; ++v4)
                 dst[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
         }
     }
@@ -314,8 +311,9 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     __shared__ int abort_s;
     __shared__ int nxt[kMaxRuns + 1];  // nxt[r]: first run >= r holding events of this row (NR if none)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, hf = warp >> 2;
+    const int quarter = warp & 3, seg = warp >> 2;
     const int row = quarter * 32 + lane;
+    const int cs = 32 * seg, slab = seg >> 1, cin = 32 * (seg & 1);
     const int hh = blockIdx.x, j = blockIdx.y;
     const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
     const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
@@ -358,9 +356,9 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     uint8_t *Atile = sm;
     uint8_t *Mbuf = sm + 2 * kSlab;
 
-    float S[64];
+    float S[32];
 #pragma unroll
-    for (int jj = 0; jj < 64; ++jj) S[jj] = a.h0 ? a.h0[sbase + (int64_t)(64 * hf + jj) * kDim + row] : 0.f;
+    for (int jj = 0; jj < 32; ++jj) S[jj] = a.h0 ? a.h0[sbase + (int64_t)(cs + jj) * kDim + row] : 0.f;
 
     auto next_run = [&](int r) -> int { return r < a.NR ? nxt[r] : a.NR; };
     int n_loads = 0, n_mma = 0;
@@ -375,13 +373,13 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     }
     const uint32_t idesc = idesc_bf16(128, 128, false, true);
     int used = 0;  // map tiles consumed
-    float Bm[64];  // B^T row of the next run with events
+    float Bm[32];  // B^T row segment of the next run with events
     {
         const int r0 = next_run(0);
         if (r0 < a.NR) {
-            const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r0) * (kDim * kDim)) + 16 * hf * 128 + row;
+            const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r0) * (kDim * kDim)) + 8 * seg * 128 + row;
 #pragma unroll
-            for (int v4 = 0; v4 < 16; ++v4) {
+            for (int v4 = 0; v4 < 8; ++v4) {
                 const float4 x = bsrc[v4 * 128];
                 Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
             }
@@ -389,18 +387,18 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     }
     for (int r = 0; r < a.NR; ++r) {
         const int c_lo = r * kRun, c_hi = min(a.C, c_lo + kRun);
-        float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim)) + 16 * hf * 128 + row;
+        float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim)) + 8 * seg * 128 + row;
 #pragma unroll
-        for (int v4 = 0; v4 < 16; ++v4) ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+        for (int v4 = 0; v4 < 8; ++v4) ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
         const bool has = nxt[r] == r;
         if (!has) {
             const float f = ex2((float)(Pu[c_hi] - Pu[c_lo]));
 #pragma unroll
-            for (int jj = 0; jj < 64; ++jj) S[jj] *= f;
+            for (int jj = 0; jj < 32; ++jj) S[jj] *= f;
             continue;
         }
 #pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 8) st_sw128_8(Atile + hf * kSlab, row, k0, &S[k0]);
+        for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(Atile + slab * kSlab, row, cin + k0, &S[k0]);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -432,22 +430,18 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         ++n_mma;
         ++used;
         tc_fence_after();
-        float d0[32], d1[32];
-        tmem_ld32(tmem_addr(tbase, quarter * 32, 64 * hf), d0);
-        tmem_ld32(tmem_addr(tbase, quarter * 32, 64 * hf + 32), d1);
+        float d0[32];
+        tmem_ld32(tmem_addr(tbase, quarter * 32, cs), d0);
         tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            S[jj] = d0[jj] + Bm[jj];
-            S[32 + jj] = d1[jj] + Bm[32 + jj];
-        }
+        for (int jj = 0; jj < 32; ++jj) S[jj] = d0[jj] + Bm[jj];
         {   // refill with the next run's B^T row; the loads land during the next step
             const int rn2 = next_run(r + 1);
             if (rn2 < a.NR) {
                 const float4 *bsrc =
-                    reinterpret_cast<const float4 *>(a.bmap + (rbase + rn2) * (kDim * kDim)) + 16 * hf * 128 + row;
+                    reinterpret_cast<const float4 *>(a.bmap + (rbase + rn2) * (kDim * kDim)) + 8 * seg * 128 + row;
 #pragma unroll
-                for (int v4 = 0; v4 < 16; ++v4) {
+                for (int v4 = 0; v4 < 8; ++v4) {
                     const float4 x = bsrc[v4 * 128];
                     Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
                 }
@@ -459,7 +453,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     }
     if (!abort_s) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) a.s_final[sbase + (int64_t)(64 * hf + jj) * kDim + row] = S[jj];
+        for (int jj = 0; jj < 32; ++jj) a.s_final[sbase + (int64_t)(cs + jj) * kDim + row] = S[jj];
     } else if (tid == 0) {
         for (int u = used + 1; u < n_loads; ++u) mbar_wait(&bar_tma[u & 1], (u >> 1) & 1);
         mma_commit(&bar_mma);
