@@ -306,7 +306,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         if (tid < nch && a.score) a.score[((int64_t)b * a.Nv + h) * a.C + c0 + tid] = sqrtf(ssum[tid]);
         __syncthreads();
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read();  // the stores only need their shared-memory sources before exit
     if (abort_s && tid == 0) {
         mbar_wait(&bar_ld, 0);
         mma_commit(&bar_drain);

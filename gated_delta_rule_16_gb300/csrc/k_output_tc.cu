@@ -238,7 +238,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
             bulk_commit();
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read();  // the stores only need their shared-memory sources before exit
     if (abort_s && tid == 0) {
         // let every copy and MMA issued so far land before the CTA releases its memory
         mbar_wait(&bar_qk_ld, 0);

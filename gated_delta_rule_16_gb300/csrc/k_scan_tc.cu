@@ -289,7 +289,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                 dst[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read();  // the stores only need their shared-memory sources before exit
     if (abort_s && tid == 0) {
         // drain: tiles still in flight into shared memory, and the MMAs issued so far
         for (int kk = k + 1; kk < tma_issued; ++kk) mbar_wait(&bar_tma[kk & 1], (kk >> 1) & 1);

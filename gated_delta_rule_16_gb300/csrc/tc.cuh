@@ -204,13 +204,15 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 }
 
 // K-major operand: descriptor of the 16-wide K step `ks` of a tile whose slabs
-// of 64 K-elements are `slab_bytes` apart.
+// of 64 K-elements are `slab_bytes` apart.  The start-address field is the
+// descriptor's low 14 bits (address / 16, shared addresses < 256 KiB), so a
+// step is the base descriptor plus the step's byte offset / 16.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_saddr, int ks, uint32_t slab_bytes) {
-    return sdesc_sw128(tile_saddr + (uint32_t)(ks >> 2) * slab_bytes + (uint32_t)(ks & 3) * 32u, 16u, 1024u);
+    return sdesc_sw128(tile_saddr, 16u, 1024u) + (((uint32_t)(ks >> 2) * slab_bytes + (uint32_t)(ks & 3) * 32u) >> 4);
 }
 // MN-major operand: descriptor of K step `ks`; stacks of 64 M/N-elements are `stack_bytes` apart.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_saddr, int ks, uint32_t stack_bytes) {
-    return sdesc_sw128(tile_saddr + (uint32_t)ks * 2048u, stack_bytes, 1024u);
+    return sdesc_sw128(tile_saddr, stack_bytes, 1024u) + (uint64_t)ks * 128u;
 }
 
 // Byte offset of element (row, k) inside a K-major 128B-swizzled slab of bf16.
