@@ -53,6 +53,27 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def rank_batch_index(rank: int) -> int:
+    """Weak scaling: rank r processes its own independent sequence(s), drawn with batch index r."""
+    return rank
+
+
+def reduce_step_ms(ms: float, world: int, device=None) -> float:
+    """Max over ranks of the per-step time (the slowest rank sets the job's step time)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, step_ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (step_ms / 1000.0)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -70,7 +91,8 @@ def algorithmic_bytes(x, kernel: str, n_snap: int = 0) -> float:
     step   : q, k, v, beta, g, mask in; o and s_final out (the whole core).
     output : q, k, U' (the workspace U buffer), g in; o out; plus one entry
              state per (group, value head) read from the fp32 snapshots.
-    intra  : k, v, beta, g in; U (dtype) and the compact C-bar blocks (fp32) out.
+    intra  : k, v, beta, g in; U out, and W of the event chunks out (bf16 storage:
+             W is built inside intra; fp32 storage writes compact C-bar blocks instead).
     scan   : per selected (pair-)event, for both value heads: W and U read, U'
              written (dtype), K read once per pair; g in; the post-event fp32
              snapshots that output groups reference written; s_final out.
@@ -86,6 +108,8 @@ def algorithmic_bytes(x, kernel: str, n_snap: int = 0) -> float:
     if kernel == "output":
         return 2 * qk + 2 * vo + bg + B * Nv * G * d * dv * 4
     if kernel == "intra":
+        if x.dtype == "bf16":
+            return qk + 2 * vo + 2 * bg + int(x.mask.sum()) * 2 * 64 * d * es
         return qk + 2 * vo + 2 * bg + B * Nv * C * 7 * 256 * 4
     if kernel == "scan":
         E = int(x.mask.sum())
@@ -220,7 +244,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    x = gdn_synth.make_workload(args.workload, batch_index=rank)   # each rank: its own independent sequence(s)
+    x = gdn_synth.make_workload(args.workload, batch_index=rank_batch_index(rank))
     tok = x.B * x.T
     st = torch.bfloat16 if x.dtype == "bf16" else torch.float32
     host = {
@@ -263,12 +287,8 @@ def run_ours(args):
     stage_ms, nrec = gdn.gdn_profile_read()
     gdn.gdn_profile_enable(False)
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = tok * world / (ms / 1000.0)
+    ms = reduce_step_ms(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    value = job_throughput(tok, world, ms)
 
     # end to end through the public API: pinned host inputs -> device -> prefill -> host outputs
     h_o = torch.empty(o.shape, dtype=st).pin_memory()
@@ -293,11 +313,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_step_ms(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
 
     peak, peak_kind = peaks()
     per_stage = {k: v / max(nrec, 1) for k, v in stage_ms.items()}
@@ -318,7 +334,7 @@ def run_ours(args):
                          (algorithmic_bytes(x, "step") / 1e6),
                    "parallelism": "one independent sequence per GPU" if world > 1 else "single GPU"},
         "clocks": clk,
-        "e2e": {"value": tok * world / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(tok, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": len(gdn.STAGES) * args.steps,
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",

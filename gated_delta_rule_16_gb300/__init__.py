@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     gdn_profile_enable,
     gdn_profile_read,
     gdn_select_events,
+    gdn_selftest_wait_timeout,
     gdn_version,
     gdn_workspace_bytes,
     gdn_workspace_status,

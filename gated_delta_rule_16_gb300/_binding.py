@@ -23,7 +23,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE"
           9: "GDN_ERR_CAPACITY", 10: "GDN_ERR_TIMEOUT"}
 EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn_prefill_dense",
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
-           "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc")
+           "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout")
 STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output")
 
 
@@ -72,6 +72,8 @@ def load(path: str | None = None):
             lib.gdn_prefill_sparse.restype = i32
             lib.gdn_prefill_sparse_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
             lib.gdn_prefill_sparse_noalloc.restype = i32
+            lib.gdn_selftest_wait_timeout.argtypes = [vp, i32, vp]
+            lib.gdn_selftest_wait_timeout.restype = i32
             lib.gdn_workspace_status.argtypes = [vp, vp]
             lib.gdn_workspace_status.restype = i32
             lib.gdn_status_string.argtypes = [i32]
@@ -269,6 +271,15 @@ def gdn_events_status(events: dict, stream=None) -> int:
 def gdn_workspace_status(workspace, stream=None) -> int:
     buf = workspace.buf if isinstance(workspace, Workspace) else workspace
     return int(load().gdn_workspace_status(_ptr(buf), _stream(stream)))
+
+
+def gdn_selftest_wait_timeout(limit_ms: int = 50, device="cuda:0", stream=None):
+    """Run the bounded-wait self-test; returns (status code, milliseconds waited, status bits)."""
+    st = torch.zeros(4, dtype=torch.int32, device=device)
+    with torch.cuda.device(st.device):
+        rc = int(load().gdn_selftest_wait_timeout(_ptr(st), int(limit_ms), _stream(stream)))
+    host = st.cpu().tolist()
+    return rc, host[3], host[2]
 
 
 def gdn_version() -> int:

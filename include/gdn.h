@@ -174,8 +174,18 @@ GDN_API gdn_status gdn_prefill_sparse_noalloc(const gdn_shape *shape,
                                       const uint8_t *mask, gdn_solver solver,
                                       void *o, float *s_final, float *score, void *stream);
 
+/* Self-test of failure detection: every wait inside the kernels is bounded in
+ * time.  Launches one thread that waits on a barrier nothing arrives at, with
+ * a limit of limit_ms (1..2000) milliseconds; the wait must give up, latch the
+ * timeout bit (status[2] & 4, the same bit a prefill latches as
+ * GDN_ERR_TIMEOUT) and return, leaving the context usable.  status: caller
+ * device buffer of 4 int32 (status[3] receives the milliseconds waited).
+ * Synchronises `stream`.  Returns GDN_OK when the wait timed out as designed,
+ * GDN_ERR_DEVICE when it did not. */
+GDN_API gdn_status gdn_selftest_wait_timeout(int32_t *status, int32_t limit_ms, void *stream);
+
 /* Synchronises `stream` and reports the device-latched status of the last
- * prefill that used `workspace` (GDN_OK or GDN_ERR_CAPACITY). */
+ * prefill that used `workspace` (GDN_OK, GDN_ERR_CAPACITY or GDN_ERR_TIMEOUT). */
 GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream);
 
 GDN_API const char *gdn_status_string(gdn_status status);

@@ -178,3 +178,24 @@ def test_workspace_status_ok_after_prefill():
     ws = gdn.Workspace()
     run_gpu(x, workspace=ws)
     assert gdn.gdn_workspace_status(ws) == 0
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    # a barrier nothing arrives at: the wait must give up after its limit and latch the bit
+    rc, waited_ms, bits = gdn.gdn_selftest_wait_timeout(50)
+    assert rc == 0 and bits & 4 and 50 <= waited_ms < 2000
+    # the context is still usable: a prefill right after runs and matches the oracle
+    x = gdn_synth.make_workload("tiny_fp32_T256")
+    assert_close(run_gpu(x), oracle_run(x, "block_adj"), "f32", "after timeout self-test")
+
+
+@pytest.mark.parametrize("layer", [0, 23])
+def test_long_context_T131072_layer_sampled_pair(layer):
+    # one layer of the 24-layer, 128K-token prefill; its final state (and output) on a sampled pair
+    x = gdn_synth.make_workload("qwen35_4b_24layers_T131072_sparse29", layer=layer)
+    res = run_gpu(x, solver="block_adj")
+    p = (5 * layer + 2) % x.Nq
+    y = slice_pairs(x, 0, [p])
+    ref = oracle_run(y, "block_adj")
+    got = {"o": res["o"][:, :, 2 * p:2 * p + 2], "s_final": res["s_final"][:, 2 * p:2 * p + 2]}
+    assert_close(got, ref, "bf16", f"T=131072 layer {layer} pair {p}")
