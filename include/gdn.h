@@ -157,7 +157,7 @@ GDN_API gdn_status gdn_prefill_sparse(const gdn_shape *shape,
  *   - Size limit: shapes with gdn_workspace_bytes(shape, solver, 1) above
  *     64 MiB are rejected with GDN_ERR_WORKSPACE before anything is enqueued
  *     (with this version's workspace layout: B=1, Nq=16, bf16,
- *     block-adjacent up to T = 1792; one head pair in fp32 up to T = 20352).
+ *     block-adjacent up to T = 1984; one head pair in fp32 up to T = 20352).
  *   - Set-up: the first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress, with that device current).  Make that
  *     first call before any stream capture.
