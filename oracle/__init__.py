@@ -14,6 +14,8 @@ Parity status of each function (pins live in ``tests/test_oracle_pins.py``):
   prefill (block-adjacent solver)                 pinned: kept blocks equal M^-1's
                                                   blocks; special inputs where it is exact
   events (CSR)                                    pinned: brute enumeration
+  select (online selector, Eqs. 10-14)            pinned: nominal retention range and E bound of
+                                                  the pages, constructed inputs with known tiers
   tail score                                      pinned: Frobenius norm by numpy
 """
 from __future__ import annotations
@@ -59,6 +61,9 @@ def _load():
             lib.gdn_oracle_prefill.argtypes = [ctypes.c_int] * 6 + [D] * 6 + [U8, ctypes.c_int, ctypes.c_int] + [D] * 9
             lib.gdn_oracle_events.restype = ctypes.c_int
             lib.gdn_oracle_events.argtypes = [ctypes.c_int] * 3 + [U8, ctypes.c_int] + [I] * 7
+            F = ctypes.POINTER(ctypes.c_float)
+            lib.gdn_oracle_select.restype = ctypes.c_int
+            lib.gdn_oracle_select.argtypes = [ctypes.c_int] * 3 + [F, F, F, U8, I, I]
             _lib = lib
     return _lib
 
@@ -136,3 +141,26 @@ def events(mask, capacity=None):
     return {"overflow": rc == 1, "n_events": E, "n_snap": int(ns[0]),
             "row_pair": row_pair, "row_ptr": row_ptr, "ev_chunk": ev_chunk[:E] if rc == 0 else None,
             "grp_pred": grp_pred[:R * G].reshape(B, P, G), "snap_slot": snap_slot[:E] if rc == 0 else None}
+
+
+def select(score, gamma, eta=None):
+    """Online event selection (SparseGDN Sec. 2.4, Eqs. 10-14) for 16 head pairs.
+
+    score, gamma: [B, Nv=32, C] fp32 (Tail-16 scores and chunk gate tails); eta: [B, Nv] or None.
+    Returns dict: mask [B, 16, C] uint8, tier [B, 16] (0 L, 1 M, 2 H), k (k_L, k_M, k_H).
+    """
+    lib = _load()
+    sc = np.ascontiguousarray(score, dtype=np.float32)
+    gm = np.ascontiguousarray(gamma, dtype=np.float32)
+    B, Nv, C = sc.shape
+    et = None if eta is None else np.ascontiguousarray(eta, dtype=np.float32)
+    mask = np.zeros((B, Nv // 2, C), np.uint8)
+    tier = np.zeros((B, Nv // 2), np.int32)
+    k = np.zeros(3, np.int32)
+    F = lambda a: None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+    I = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+    rc = lib.gdn_oracle_select(B, Nv, C, F(sc), F(gm), F(et), mask.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                               I(tier), I(k))
+    if rc != 0:
+        raise ValueError("gdn_oracle_select rejected its arguments (needs 16 head pairs)")
+    return {"mask": mask, "tier": tier, "k": tuple(int(v) for v in k)}

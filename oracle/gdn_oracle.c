@@ -421,3 +421,173 @@ int gdn_oracle_events(int B, int P, int C, const unsigned char *mask, int capaci
     free(cnt);
     return 0;
 }
+
+/* ---- online event selection (Sec. 2.4, Eqs. 10-14) -----------------------
+ * Per sequence, from the Tail-16 scores s[h][c] (Eq. 9), the chunk gate tails
+ * gamma[h][c] and an optional output-visibility energy eta[h]:
+ *   norm_h = ||s_{.,h}||_2 (sum of squares in fp64, rounded to fp32, fp32 sqrt)
+ *   q_c    = 0.5 (s_{c,h0} / norm_h0 + s_{c,h1} / norm_h1), fp32 (Eq. 10); a zero norm adds 0
+ *   r_h    = mean of 2^gamma over the last min(16, C) chunks; L_h = sum_{j=1}^{C-2} r_h^j (Eq. 11)
+ *   G_h    = sqrt(eta_h / mean eta), or 1 without eta (Eq. 11)
+ *   k_l    = clip(round_half_even(rho_l C), 2, C), rho = (0.08, 0.30, 0.95); C = 1 keeps its chunk
+ *   C_l    = anchors {0, C-1} plus the k_l - 2 best non-anchor chunks by q (ties: lower index)
+ *            -- nested sets C_L in C_M in C_H (Eq. 13)
+ *   gains  Delta_{a->b} = sum_{c in C_b \ C_a} sum_{h in pair} s_{c,h} L_h G_h (Eq. 12), fp64
+ *   x      = gains / mean over pairs (0 when the mean is 0)
+ *   B(x,k) = k (n-k) / n (mean of the k largest - mean of the rest)^2 (Eq. 14)
+ *   n_H    = argmax_{k in 1..4} B(x_H sorted desc, k), n = 16 (ties: smaller k); the n_H pairs
+ *            with the largest x_H (ties: lower pair id) take tier H
+ *   n_M    = argmax over the row {1: 11-13, 2: 7-9, 3: 3-5, 4: 0} of B(x_M of the other pairs), n = 16 - n_H;
+ *            the n_M best of the other pairs by x_M take tier M; the rest tier L.
+ *   mask[p][c] = [c in C_tier(p)], shared by the pair.
+ * Only defined for 16 head pairs (the pages' tier table).  Returns 0, or -1. */
+typedef struct { float q; int c; } ranked_t;
+
+/* q descending, ties: lower chunk index first */
+static int cmp_ranked(const void *a, const void *b)
+{
+    const ranked_t *x = (const ranked_t *)a, *y = (const ranked_t *)b;
+    if (x->q != y->q) return x->q > y->q ? -1 : 1;
+    return x->c < y->c ? -1 : (x->c > y->c);
+}
+
+/* B(x, k) for x sorted descending (Eq. 14) */
+static double separation(const double *xs, int n, int k)
+{
+    double top = 0.0, rest = 0.0;
+    for (int i = 0; i < k; ++i) top += xs[i];
+    for (int i = k; i < n; ++i) rest += xs[i];
+    top /= k;
+    rest = n > k ? rest / (n - k) : 0.0;
+    return (double)k * (n - k) / n * (top - rest) * (top - rest);
+}
+
+/* sort pair ids by x descending, ties: lower id first (insertion sort, n <= 16) */
+static void order_pairs(const double *x, int *ids, int n)
+{
+    for (int i = 1; i < n; ++i) {
+        int v = ids[i], j = i - 1;
+        while (j >= 0 && (x[ids[j]] < x[v] || (x[ids[j]] == x[v] && ids[j] > v))) {
+            ids[j + 1] = ids[j];
+            --j;
+        }
+        ids[j + 1] = v;
+    }
+}
+
+int gdn_oracle_select(int B, int Nv, int C, const float *score, const float *gamma, const float *eta,
+                      unsigned char *mask, int *tier_out, int *k_out)
+{
+    enum { NP = 16 };
+    if (Nv != 2 * NP || C < 0 || B < 0) return -1;
+    const double rho[3] = {0.08, 0.30, 0.95};       /* tiers L, M, H */
+    static const int nm_lo[5] = {0, 11, 7, 3, 0}, nm_hi[5] = {0, 13, 9, 5, 0};
+    int k[3];
+    for (int l = 0; l < 3; ++l) {
+        int kk = (int)nearbyint(rho[l] * C);          /* round half to even */
+        kk = kk < 2 ? 2 : kk;
+        k[l] = kk > C ? C : kk;
+    }
+    if (k_out) for (int l = 0; l < 3; ++l) k_out[l] = k[l];
+    const int n_in = C > 2 ? C - 2 : 0;               /* non-anchor chunks 1 .. C-2 */
+    ranked_t *rk = (ranked_t *)malloc(sizeof(ranked_t) * (n_in > 0 ? n_in : 1));
+    int *rank = (int *)malloc(sizeof(int) * (size_t)NP * (C > 0 ? C : 1));  /* -1: anchor */
+
+    for (int b = 0; b < B; ++b) {
+        const float *s = score + (size_t)b * Nv * C;  /* s[h * C + c] */
+        const float *gm = gamma + (size_t)b * Nv * C;
+        float norm[2 * NP];
+        double L[2 * NP], G[2 * NP];
+        /* Eq. 11: norms, memory lifetime, output visibility */
+        for (int h = 0; h < Nv; ++h) {
+            double ss = 0.0;
+            for (int c = 0; c < C; ++c) ss += (double)s[h * C + c] * (double)s[h * C + c];
+            norm[h] = sqrtf((float)ss);
+            const int c0 = C > 16 ? C - 16 : 0;
+            double r = 0.0;
+            for (int c = c0; c < C; ++c) r += exp2((double)gm[h * C + c]);
+            r = C > c0 ? r / (C - c0) : 0.0;
+            double Lh = 0.0, pw = 1.0;
+            for (int j = 1; j <= C - 2; ++j) { pw *= r; Lh += pw; }
+            L[h] = Lh;
+        }
+        double emean = 0.0;
+        if (eta) {
+            for (int h = 0; h < Nv; ++h) emean += eta[(size_t)b * Nv + h];
+            emean /= Nv;
+        }
+        for (int h = 0; h < Nv; ++h)
+            G[h] = !eta ? 1.0 : (emean > 0.0 ? sqrt(eta[(size_t)b * Nv + h] / emean) : 0.0);
+
+        /* Eqs. 10, 12, 13: in-pair ranking, nested candidate sets, upgrade gains */
+        double gain_LM[NP], gain_MH[NP];
+        for (int p = 0; p < NP; ++p) {
+            const int h0 = 2 * p, h1 = 2 * p + 1;
+            for (int i = 0; i < n_in; ++i) {
+                const int c = i + 1;
+                const float a0 = norm[h0] > 0.f ? s[h0 * C + c] / norm[h0] : 0.f;
+                const float a1 = norm[h1] > 0.f ? s[h1 * C + c] / norm[h1] : 0.f;
+                rk[i].q = 0.5f * (a0 + a1);
+                rk[i].c = c;
+            }
+            qsort(rk, n_in, sizeof(ranked_t), cmp_ranked);
+            int *rp = rank + (size_t)p * C;
+            for (int c = 0; c < C; ++c) rp[c] = -1;
+            for (int i = 0; i < n_in; ++i) rp[rk[i].c] = i;
+            gain_LM[p] = gain_MH[p] = 0.0;
+            for (int i = 0; i < n_in; ++i) {
+                const int c = rk[i].c;
+                const double w = (double)s[h0 * C + c] * L[h0] * G[h0] + (double)s[h1 * C + c] * L[h1] * G[h1];
+                if (i >= k[0] - 2 && i < k[1] - 2) gain_LM[p] += w;   /* in C_M, not in C_L */
+                if (i >= k[1] - 2 && i < k[2] - 2) gain_MH[p] += w;   /* in C_H, not in C_M */
+            }
+        }
+
+        /* Eq. 14: dynamic tier counts */
+        double mLM = 0.0, mMH = 0.0, xM[NP], xH[NP], xs[NP];
+        for (int p = 0; p < NP; ++p) { mLM += gain_LM[p]; mMH += gain_MH[p]; }
+        mLM /= NP;
+        mMH /= NP;
+        for (int p = 0; p < NP; ++p) {
+            xM[p] = mLM != 0.0 ? gain_LM[p] / mLM : 0.0;
+            xH[p] = mMH != 0.0 ? gain_MH[p] / mMH : 0.0;
+        }
+        int ids[NP], tier[NP];
+        for (int p = 0; p < NP; ++p) { ids[p] = p; tier[p] = 0; }
+        order_pairs(xH, ids, NP);
+        for (int i = 0; i < NP; ++i) xs[i] = xH[ids[i]];
+        int nH = 1;
+        double best = separation(xs, NP, 1);
+        for (int kk = 2; kk <= 4; ++kk) {
+            const double v = separation(xs, NP, kk);
+            if (v > best) { best = v; nH = kk; }
+        }
+        for (int i = 0; i < nH; ++i) tier[ids[i]] = 2;
+        int rest[NP], nr = 0;
+        for (int p = 0; p < NP; ++p)
+            if (tier[p] != 2) rest[nr++] = p;
+        order_pairs(xM, rest, nr);
+        for (int i = 0; i < nr; ++i) xs[i] = xM[rest[i]];
+        int nM = 0;
+        if (nm_hi[nH] > 0) {
+            nM = nm_lo[nH];
+            best = separation(xs, nr, nM);
+            for (int kk = nm_lo[nH] + 1; kk <= nm_hi[nH]; ++kk) {
+                const double v = separation(xs, nr, kk);
+                if (v > best) { best = v; nM = kk; }
+            }
+        }
+        for (int i = 0; i < nM; ++i) tier[rest[i]] = 1;
+
+        /* the mask of each pair: anchors plus its tier's best k - 2 chunks */
+        for (int p = 0; p < NP; ++p) {
+            if (tier_out) tier_out[(size_t)b * NP + p] = tier[p];
+            const int *rp = rank + (size_t)p * C;
+            for (int c = 0; c < C; ++c)
+                mask[((size_t)b * NP + p) * C + c] = (rp[c] < 0 || rp[c] < k[tier[p]] - 2) ? 1 : 0;
+        }
+    }
+    free(rk);
+    free(rank);
+    return 0;
+}
