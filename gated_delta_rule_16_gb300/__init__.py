@@ -14,9 +14,11 @@ from ._binding import (  # noqa: F401
     gdn_prefill_dense,
     gdn_prefill_sparse,
     gdn_prefill_sparse_noalloc,
+    gdn_prefill_sparse_online,
     gdn_profile_enable,
     gdn_profile_read,
     gdn_select_events,
+    gdn_select_events_scored,
     gdn_selftest_wait_timeout,
     gdn_version,
     gdn_workspace_bytes,

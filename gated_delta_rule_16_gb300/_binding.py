@@ -23,8 +23,9 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE"
           9: "GDN_ERR_CAPACITY", 10: "GDN_ERR_TIMEOUT"}
 EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn_prefill_dense",
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
-           "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout")
-STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output")
+           "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout",
+           "gdn_prefill_sparse_online", "gdn_select_events_scored", "gdn_select_scored_workspace_bytes")
+STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output", "selector")
 
 
 class GdnError(RuntimeError):
@@ -70,6 +71,13 @@ def load(path: str | None = None):
             lib.gdn_prefill_dense.restype = i32
             lib.gdn_prefill_sparse.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
             lib.gdn_prefill_sparse.restype = i32
+            lib.gdn_prefill_sparse_online.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                                      vp, sz, vp]
+            lib.gdn_prefill_sparse_online.restype = i32
+            lib.gdn_select_events_scored.argtypes = [shp, vp, vp, vp, vp, vp, vp, sz, vp]
+            lib.gdn_select_events_scored.restype = i32
+            lib.gdn_select_scored_workspace_bytes.argtypes = [shp]
+            lib.gdn_select_scored_workspace_bytes.restype = sz
             lib.gdn_prefill_sparse_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
             lib.gdn_prefill_sparse_noalloc.restype = i32
             lib.gdn_selftest_wait_timeout.argtypes = [vp, i32, vp]
@@ -130,7 +138,8 @@ def _need(t, name, dtype=None, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def gdn_workspace_bytes(shape: GdnShape, solver: str = "block_adj", sparse: bool = True) -> int:
+def gdn_workspace_bytes(shape: GdnShape, solver: str = "block_adj", sparse: int = 1) -> int:
+    """sparse: 0 dense, 1 sparse with a given mask, 2 sparse with online selection."""
     return int(load().gdn_workspace_bytes(ctypes.byref(shape), SOLVERS[solver], int(sparse)))
 
 
@@ -180,7 +189,7 @@ def _prefill(fn, q, k, v, beta, g, mask, h0, solver, o, s_final, score, workspac
     _need(s_final, "s_final", torch.float32, (B, Nv, d, dv))
     _need(score, "score", torch.float32, (B, Nv, C))
     shape = shape_of(q, v)
-    nbytes = gdn_workspace_bytes(shape, solver, mask is not None)
+    nbytes = gdn_workspace_bytes(shape, solver, 1 if mask is not None else 0)
     ws = _workspace(workspace, nbytes, dev)
     lib = load()
     args = [ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0)]
@@ -238,6 +247,70 @@ def gdn_prefill_sparse_noalloc(q, k, v, beta, g, mask, *, h0=None, solver="block
             ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(mask),
             SOLVERS[solver], _ptr(o), _ptr(s_final), _ptr(score), _stream(stream)))
     return o, s_final
+
+
+def gdn_prefill_sparse_online(q, k, v, beta, g, *, h0=None, eta=None, solver="block_adj", o=None,
+                              s_final=None, score=None, mask_out=None, tier_out=None, workspace=None, stream=None):
+    """Event-sparse prefill that selects its own events (Tail-16 scores, Eqs. 10-14).
+
+    16 head pairs only.  Returns (o, s_final, mask [B,16,C] uint8, tier [B,16] int32).
+    """
+    B, T, Nq, d = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    C = (T + 63) // 64
+    _need(q, "q", shape=(B, T, Nq, d))
+    _need(k, "k", dtype=q.dtype, shape=(B, T, Nq, d))
+    _need(v, "v", dtype=q.dtype, shape=(B, T, Nv, dv))
+    _need(beta, "beta", torch.float32, (B, T, Nv))
+    _need(g, "g", torch.float32, (B, T, Nv))
+    _need(h0, "h0", torch.float32, (B, Nv, d, dv))
+    _need(eta, "eta", torch.float32, (B, Nv))
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, T, Nv, dv), dtype=q.dtype, device=dev)
+    if s_final is None:
+        s_final = torch.empty((B, Nv, d, dv), dtype=torch.float32, device=dev)
+    if mask_out is None:
+        mask_out = torch.empty((B, Nq, C), dtype=torch.uint8, device=dev)
+    if tier_out is None:
+        tier_out = torch.empty((B, Nq), dtype=torch.int32, device=dev)
+    _need(o, "o", q.dtype, (B, T, Nv, dv))
+    _need(s_final, "s_final", torch.float32, (B, Nv, d, dv))
+    _need(score, "score", torch.float32, (B, Nv, C))
+    _need(mask_out, "mask_out", torch.uint8, (B, Nq, C))
+    _need(tier_out, "tier_out", torch.int32, (B, Nq))
+    shape = shape_of(q, v)
+    ws = _workspace(workspace, gdn_workspace_bytes(shape, solver, 2), dev)
+    with torch.cuda.device(dev):
+        _check("gdn_prefill_sparse_online", load().gdn_prefill_sparse_online(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(eta),
+            SOLVERS[solver], _ptr(o), _ptr(s_final), _ptr(score), _ptr(mask_out), _ptr(tier_out), _ptr(ws),
+            ws.numel(), _stream(stream)))
+    return o, s_final, mask_out, tier_out
+
+
+def gdn_select_events_scored(score: torch.Tensor, g: torch.Tensor, eta=None, *, mask_out=None, tier_out=None,
+                             workspace=None, stream=None):
+    """Online selection from Tail-16 scores [B,32,C] and gates g [B,T,32]; returns (mask, tier)."""
+    _need(score, "score", torch.float32)
+    B, Nv, C = score.shape
+    _need(g, "g", torch.float32, (B, C * 64, Nv))
+    _need(eta, "eta", torch.float32, (B, Nv))
+    dev = score.device
+    if mask_out is None:
+        mask_out = torch.empty((B, Nv // 2, C), dtype=torch.uint8, device=dev)
+    if tier_out is None:
+        tier_out = torch.empty((B, Nv // 2), dtype=torch.int32, device=dev)
+    _need(mask_out, "mask_out", torch.uint8, (B, Nv // 2, C))
+    _need(tier_out, "tier_out", torch.int32, (B, Nv // 2))
+    shape = GdnShape(B, C * 64, Nv // 2, Nv, 128, 128, GDN_BF16)
+    lib = load()
+    ws = _workspace(workspace, int(lib.gdn_select_scored_workspace_bytes(ctypes.byref(shape))), dev)
+    with torch.cuda.device(dev):
+        _check("gdn_select_events_scored", lib.gdn_select_events_scored(
+            ctypes.byref(shape), _ptr(score), _ptr(g), _ptr(eta), _ptr(mask_out), _ptr(tier_out), _ptr(ws),
+            ws.numel(), _stream(stream)))
+    return mask_out, tier_out
 
 
 def gdn_select_events(mask: torch.Tensor, Nq: int | None = None, capacity: int | None = None, stream=None):

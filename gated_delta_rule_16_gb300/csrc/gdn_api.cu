@@ -16,13 +16,14 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // ---- stage profiler (benchmark aid; see gdn_profile_enable) ----------------
-constexpr int kStages = 8;
+// Stages: 0 select (compaction), 1 prefix, 2 intra, 3 deferred W, 4 scan run maps,
+// 5 scan chain, 6 scan (fix-up / whole scan), 7 output, 8 online selector.
+constexpr int kStages = 9;
 constexpr int kProfSlots = 256;
 struct Profiler {
     bool on = false, created = false;
     int used = 0;
-    int dev = -1;
-    cudaEvent_t ev[kProfSlots][kStages + 1];
+    cudaEvent_t ev[kProfSlots][2 * kStages];  // start and end of every stage
 };
 Profiler g_prof;
 
@@ -100,6 +101,9 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
     const size_t o_W = take((size_t)ev_cap * 2 * kChunk * pb.d * es);
     const size_t o_snap = take((size_t)snap_cap * 2 * pb.d * pb.dv * es);
+    const size_t o_sel_ws = take(pb.online ? selector_workspace_bytes(pb.B, (int)C) : 0);
+    const size_t o_sel_score = take(pb.online ? (size_t)pb.B * pb.Nv * C * sizeof(float) : 0);
+    const size_t o_sel_mask = take(pb.online ? (size_t)R * C : 0);
     const int64_t nr = pb.dtype == GDN_BF16 ? (C + kRunChunks - 1) / kRunChunks : 0;
     const size_t run_elems = (size_t)R * 2 * nr * kDim * kDim;
     const size_t o_amap = take(run_elems * 2);
@@ -121,6 +125,9 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
         ws->cbar = (float *)(b + o_cbar);
         ws->W = b + o_W;
         ws->snap = b + o_snap;
+        ws->sel_ws = b + o_sel_ws;
+        ws->sel_score = (float *)(b + o_sel_score);
+        ws->sel_mask = (uint8_t *)(b + o_sel_mask);
         ws->amap = b + o_amap;
         ws->bmap = (float *)(b + o_bmap);
         ws->entry = (float *)(b + o_entry);
@@ -132,33 +139,44 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
 
 namespace {
 
+enum PrefillMode { kDense = 0, kSparse = 1, kOnline = 2 };
+
 gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *beta,
-                       const float *g, const float *h0, const uint8_t *mask, bool sparse, gdn_solver solver,
-                       void *o, float *s_final, float *score, void *workspace, size_t workspace_bytes,
-                       void *stream) {
+                       const float *g, const float *h0, const uint8_t *mask, const float *eta, PrefillMode mode,
+                       gdn_solver solver, void *o, float *s_final, float *score, uint8_t *mask_out,
+                       int32_t *tier_out, void *workspace, size_t workspace_bytes, void *stream) {
     gdn_status st = check_shape(shape);
     if (st != GDN_OK) return st;
     if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return GDN_ERR_DTYPE;
+    if (mode == kOnline && shape->Nv != 32) return GDN_ERR_UNSUPPORTED;  // the tier table is for 16 pairs
     const bool has_tokens = shape->B > 0 && shape->T > 0;
     if (shape->B > 0 && !s_final) return GDN_ERR_NULL;
-    if (has_tokens && (!q || !k || !v || !beta || !g || !o || (sparse && !mask))) return GDN_ERR_NULL;
+    if (has_tokens && (!q || !k || !v || !beta || !g || !o || (mode == kSparse && !mask))) return GDN_ERR_NULL;
     if (shape->B > 0 && !workspace) return GDN_ERR_NULL;
-    const void *ptrs[] = {q, k, v, beta, g, h0, o, s_final, score};
+    const void *ptrs[] = {q, k, v, beta, g, h0, o, s_final, score, eta, tier_out};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return GDN_ERR_ALIGN;
     if (workspace && ((uintptr_t)workspace % kAlign) != 0) return GDN_ERR_ALIGN;
     Problem pb;
     fill_problem(shape, solver, &pb);
+    pb.online = mode == kOnline;
     if (shape->B == 0) return GDN_OK;
     const size_t need = workspace_layout(pb, nullptr, nullptr);
     if (workspace_bytes < need) return GDN_ERR_WORKSPACE;
     if (!device_ok()) return GDN_ERR_DEVICE;
     pb.q = q; pb.k = k; pb.v = v; pb.beta = beta; pb.g = g; pb.h0 = h0;
-    pb.mask = sparse ? mask : nullptr;
-    pb.o = o; pb.s_final = s_final; pb.score = score;
+    pb.o = o; pb.s_final = s_final;
     pb.stream = (cudaStream_t)stream;
     Workspace ws;
     workspace_layout(pb, workspace, &ws);
+    pb.score = score;
+    if (mode == kOnline) {
+        if (!pb.score) pb.score = ws.sel_score;
+        if (!mask_out) mask_out = ws.sel_mask;
+        pb.mask = mask_out;
+    } else {
+        pb.mask = mode == kSparse ? mask : nullptr;
+    }
 
     gdn_events ev;
     ev.row_pair = ws.row_pair; ev.row_ptr = ws.row_ptr; ev.ev_chunk = ws.ev_chunk;
@@ -166,24 +184,32 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     ev.capacity = (int32_t)ws.ev_cap;
     cudaEvent_t *prof = prof_slot();
     auto mark = [&](int i) { if (prof) cudaEventRecord(prof[i], pb.stream); };
-    mark(0);
-    cudaError_t e = launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first);
-    mark(1);
-    if (e == cudaSuccess) e = launch_prefix(pb, ws);
-    mark(2);
     const bool tc = pb.dtype == GDN_BF16;   // tensor-core path for bf16 storage
-    if (e == cudaSuccess) e = tc ? launch_intra_tc(pb, ws) : launch_intra(pb, ws);
-    mark(3);
-    if (e == cudaSuccess && !tc) e = launch_wbuild(pb, ws);  // bf16: W is built inside intra
-    mark(4);
-    if (e == cudaSuccess && tc) e = launch_scan_tc(pb, ws, 0);
-    mark(5);
-    if (e == cudaSuccess && tc) e = launch_scan_tc(pb, ws, 1);
-    mark(6);
-    if (e == cudaSuccess) e = tc ? launch_scan_tc(pb, ws, 2) : launch_scan(pb, ws);
-    mark(7);
-    if (e == cudaSuccess) e = tc ? launch_output_tc(pb, ws) : launch_output(pb, ws);
-    mark(8);
+    cudaError_t e = cudaSuccess;
+    auto stage = [&](int id, auto &&launch) {
+        mark(2 * id);
+        if (e == cudaSuccess) e = launch();
+        mark(2 * id + 1);
+    };
+    auto none = [] { return cudaSuccess; };
+    if (mode == kOnline) {
+        // intra first (its Tail-16 scores drive the selection), then the rest of the pipeline
+        stage(2, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
+        stage(8, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
+        stage(0, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
+        stage(1, [&] { return launch_prefix(pb, ws); });
+        stage(3, [&] { return launch_wbuild(pb, ws); });
+    } else {
+        stage(0, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
+        stage(1, [&] { return launch_prefix(pb, ws); });
+        stage(2, [&] { return tc ? launch_intra_tc(pb, ws, false) : launch_intra(pb, ws); });
+        stage(3, [&] { return tc ? none() : launch_wbuild(pb, ws); });  // bf16: W is built inside intra
+        stage(8, none);
+    }
+    stage(4, [&] { return tc ? launch_scan_tc(pb, ws, 0) : none(); });
+    stage(5, [&] { return tc ? launch_scan_tc(pb, ws, 1) : none(); });
+    stage(6, [&] { return tc ? launch_scan_tc(pb, ws, 2) : launch_scan(pb, ws); });
+    stage(7, [&] { return tc ? launch_output_tc(pb, ws) : launch_output(pb, ws); });
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -204,11 +230,13 @@ using namespace gdn;
 extern "C" {
 
 size_t gdn_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse) {
-    (void)sparse;  // both paths share one layout: the dense path is the all-events case
+    // dense and sparse share one layout (the dense path is the all-events case);
+    // sparse == 2 (online selection) adds the selector's buffers
     if (check_shape(shape) != GDN_OK) return 0;
     if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return 0;
     Problem pb;
     fill_problem(shape, solver, &pb);
+    pb.online = sparse == 2;
     return workspace_layout(pb, nullptr, nullptr);
 }
 
@@ -242,16 +270,51 @@ gdn_status gdn_events_status(const gdn_events *events, void *stream) {
 gdn_status gdn_prefill_dense(const gdn_shape *shape, const void *q, const void *k, const void *v,
                              const float *beta, const float *g, const float *h0, gdn_solver solver, void *o,
                              float *s_final, float *score, void *workspace, size_t workspace_bytes, void *stream) {
-    return run_prefill(shape, q, k, v, beta, g, h0, nullptr, false, solver, o, s_final, score, workspace,
-                       workspace_bytes, stream);
+    return run_prefill(shape, q, k, v, beta, g, h0, nullptr, nullptr, kDense, solver, o, s_final, score, nullptr,
+                       nullptr, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_prefill_sparse(const gdn_shape *shape, const void *q, const void *k, const void *v,
                               const float *beta, const float *g, const float *h0, const uint8_t *mask,
                               gdn_solver solver, void *o, float *s_final, float *score, void *workspace,
                               size_t workspace_bytes, void *stream) {
-    return run_prefill(shape, q, k, v, beta, g, h0, mask, true, solver, o, s_final, score, workspace,
-                       workspace_bytes, stream);
+    return run_prefill(shape, q, k, v, beta, g, h0, mask, nullptr, kSparse, solver, o, s_final, score, nullptr,
+                       nullptr, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_prefill_sparse_online(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                                     const float *beta, const float *g, const float *h0, const float *eta,
+                                     gdn_solver solver, void *o, float *s_final, float *score, uint8_t *mask_out,
+                                     int32_t *tier_out, void *workspace, size_t workspace_bytes, void *stream) {
+    return run_prefill(shape, q, k, v, beta, g, h0, nullptr, eta, kOnline, solver, o, s_final, score, mask_out,
+                       tier_out, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_select_events_scored(const gdn_shape *shape, const float *score, const float *g, const float *eta,
+                                    uint8_t *mask_out, int32_t *tier_out, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    gdn_status st = check_shape(shape);
+    if (st != GDN_OK) return st;
+    if (shape->Nv != 32) return GDN_ERR_UNSUPPORTED;
+    Problem pb;
+    fill_problem(shape, GDN_SOLVER_BLOCK_ADJ, &pb);
+    if (pb.B == 0 || pb.C == 0) return GDN_OK;
+    if (!score || !g || !mask_out || !workspace) return GDN_ERR_NULL;
+    const void *ptrs[] = {score, g, eta, tier_out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGN;
+    if (((uintptr_t)workspace % kAlign) != 0) return GDN_ERR_ALIGN;
+    if (workspace_bytes < gdn_select_scored_workspace_bytes(shape)) return GDN_ERR_WORKSPACE;
+    if (!device_ok()) return GDN_ERR_DEVICE;
+    pb.g = g;
+    pb.stream = (cudaStream_t)stream;
+    const cudaError_t e = launch_selector(pb, score, eta, mask_out, tier_out, workspace);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+size_t gdn_select_scored_workspace_bytes(const gdn_shape *shape) {
+    if (check_shape(shape) != GDN_OK || shape->Nv != 32) return 0;
+    return align_up(selector_workspace_bytes(shape->B, (int)(shape->T / kChunk)) + 1);
 }
 
 gdn_status gdn_workspace_status(const void *workspace, void *stream) {
@@ -283,7 +346,7 @@ gdn_status gdn_profile_enable(int enable) {
     if (enable && !g_prof.created) {
         if (!device_ok()) return GDN_ERR_DEVICE;
         for (int i = 0; i < kProfSlots; ++i)
-            for (int j = 0; j <= kStages; ++j)
+            for (int j = 0; j < 2 * kStages; ++j)
                 if (cudaEventCreate(&g_prof.ev[i][j]) != cudaSuccess) return GDN_ERR_CUDA;
         g_prof.created = true;
     }
@@ -298,10 +361,11 @@ gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefil
     for (int j = 0; j < n_stages; ++j) stage_ms[j] = 0.f;
     *n_prefills = g_prof.created ? g_prof.used : 0;
     for (int i = 0; i < *n_prefills; ++i) {
-        if (cudaEventSynchronize(g_prof.ev[i][kStages]) != cudaSuccess) return GDN_ERR_CUDA;
         for (int j = 0; j < n_stages; ++j) {
             float ms = 0.f;
-            if (cudaEventElapsedTime(&ms, g_prof.ev[i][j], g_prof.ev[i][j + 1]) != cudaSuccess) return GDN_ERR_CUDA;
+            if (cudaEventSynchronize(g_prof.ev[i][2 * j + 1]) != cudaSuccess) return GDN_ERR_CUDA;
+            if (cudaEventElapsedTime(&ms, g_prof.ev[i][2 * j], g_prof.ev[i][2 * j + 1]) != cudaSuccess)
+                return GDN_ERR_CUDA;
             stage_ms[j] += ms;
         }
     }

@@ -49,6 +49,7 @@ struct Problem {
     gdn_dtype dtype;
     gdn_solver solver;
     int nblk;                  // 7 (block-adjacent) or 10 (exact)
+    int online;                // workspace also holds the online-selection buffers
     const void *q, *k, *v;
     const float *beta, *g, *h0;
     const uint8_t *mask;       // NULL: every chunk is an event
@@ -73,6 +74,10 @@ struct Workspace {
     void *amap;                // [R, 2, NR, 128, 128] bf16: A_r^T of each run
     float *bmap;               // [R, 2, NR, 128, 128] B_r^T of each run
     float *entry;              // [R, 2, NR, 128, 128] S^T entering each run
+    // online selection only
+    void *sel_ws;              // online selector scratch (selector_workspace_bytes)
+    float *sel_score;          // [B, Nv, C] Tail-16 scores when the caller passes none
+    uint8_t *sel_mask;         // [B, P, C] selected mask when the caller passes none
     int64_t ev_cap, snap_cap;
 };
 
@@ -92,6 +97,13 @@ cudaError_t launch_output(const Problem &pb, const Workspace &ws);
 // part 0: run maps, 1: chain over runs, 2: per-run fix-up (writes U' and snapshots)
 cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part);
 cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws);
-cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws);
+// write_cbar: store the compact C-bar blocks (W is built later, after online selection)
+cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_cbar);
+// online selection: mask [B,16,C] (and tiers [B,16], may be NULL) from scores [B,Nv,C]
+// Online selection (Eqs. 10-14) for 16 head pairs: score [B,32,C] -> mask [B,16,C],
+// tier_out [B,16] (may be NULL); ws holds selector_workspace_bytes(B, C).
+size_t selector_workspace_bytes(int B, int C);
+cudaError_t launch_selector(const Problem &pb, const float *score, const float *eta, uint8_t *mask,
+                            int32_t *tier_out, void *ws);
 
 }  // namespace gdn

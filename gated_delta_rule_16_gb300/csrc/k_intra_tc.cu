@@ -42,8 +42,9 @@ constexpr uint32_t TM_G = 0, TM_U = 128, TM_W = 256;
 
 struct IntraParams {
     const float *beta, *g;
-    const int32_t *ev_of;
+    const int32_t *ev_of;   // NULL: no W here (online selection builds W later from C-bar)
     __nv_bfloat16 *U, *W;
+    float *cbar;            // non-NULL: write the compact C-bar blocks [B,Nv,C,nblk,16,16]
     float *score;
     int32_t *status;
     int P_, T_, Nv, C, nblk, exact;
@@ -132,7 +133,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             tma_load_3d(vd + kSlab, &tV, 64, 2 * p + hh, tok0, &bar_ld);
         }
     }
-    if (tid < 2) ev_s[tid] = tid < nch ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
+    if (tid < 2) ev_s[tid] = (a.ev_of && tid < nch) ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
     if (tid < 256) {  // beta and g of both heads, fetched once while the tiles load
         const int hh = tid >> 7, t = tid & 127;
         const bool valid = (t >> 6) < nch;
@@ -238,6 +239,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 }
             }
         }
+        if (a.cbar) {  // compact C-bar = C diag(beta 2^g) for the W kernel that runs after selection
+            for (int idx = tid; idx < nch * a.nblk * 256; idx += kThreads) {
+                const int cc = idx / (a.nblk * 256), rem = idx % (a.nblk * 256);
+                const int blk = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
+                const int rw = blk_row(blk) * kBlk + rr, cl = blk_col(blk) * kBlk + col;
+                a.cbar[(((int64_t)b * a.Nv + h) * a.C + c0 + cc) * a.nblk * 256 + rem] =
+                    Cs[(cc * kChunk + rw) * MS + cl] * bgs[64 * cc + cl];
+            }
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -319,7 +329,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 
 }  // namespace
 
-cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws) {
+cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_cbar) {
     if (pb.B == 0 || pb.C == 0) return cudaSuccess;
     CUtensorMap tK, tV, tU, tU64, tW;
     const uint64_t BT = (uint64_t)pb.B * pb.T;
@@ -331,7 +341,8 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws) {
         !make_tmap_bf16_3d(&tW, ws.W, kDim, wrows, 1, kDim * 2, wrows * kDim * 2, 64, 64, 1))
         return cudaErrorInvalidValue;
     IntraParams a;
-    a.beta = pb.beta; a.g = pb.g; a.ev_of = ws.ev_of;
+    a.beta = pb.beta; a.g = pb.g; a.ev_of = write_cbar ? nullptr : ws.ev_of;
+    a.cbar = write_cbar ? ws.cbar : nullptr;
     a.U = (__nv_bfloat16 *)ws.U; a.W = (__nv_bfloat16 *)ws.W; a.score = pb.score;
     a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;

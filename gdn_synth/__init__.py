@@ -173,25 +173,51 @@ def make_inputs(B: int, T: int, Nq: int, Nv: int, d: int = 128, dv: int = 128,
     k = np.empty((B, T, Nq, d), np.float32)
     v = np.empty((B, T, Nv, dv), np.float32)
     beta = np.empty((B, T, Nv), np.float32)
-    a = np.empty((B, T, Nv), np.float32)
     normal_qk = lambda r, shp: _round(_l2n(r.standard_normal(shp, dtype=np.float32)), dtype)
     _fill(seed, 1, q, normal_qk)
     _fill(seed, 2, k, normal_qk)
     _fill(seed, 3, v, lambda r, shp: _round(r.standard_normal(shp, dtype=np.float32), dtype))
     _fill(seed, 4, beta, lambda r, shp: (1.0 / (1.0 + np.exp(-r.standard_normal(shp, dtype=np.float32)))).astype(np.float32))
-    _fill(seed, 5, a, lambda r, shp: -r.uniform(0.001, 0.05, size=shp).astype(np.float32))
+    g = make_gates(B, T, Nv, seed)
     C = (T + CHUNK - 1) // CHUNK
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0]))
+    m = make_mask(rng, B, Nv // 2, C, mask, retention)
+    h0 = rng.standard_normal((B, Nv, d, dv), dtype=np.float32) * np.float32(0.1) if with_h0 else None
+    return Inputs(B, T, Nq, Nv, d, dv, dtype, q, k, v, beta, g, m, h0,
+                  meta={"seed": seed, "mask": mask, "retention_target": retention})
+
+
+def make_gates(B: int, T: int, Nv: int, seed: int) -> np.ndarray:
+    """g [B,T,Nv] fp32: per-token log2 retention -U(0.001, 0.05), summed inside each chunk."""
+    a = np.empty((B, T, Nv), np.float32)
+    _fill(seed, 5, a, lambda r, shp: -r.uniform(0.001, 0.05, size=shp).astype(np.float32))
     g = np.empty_like(a)
     if T:
         full = (T // CHUNK) * CHUNK
         g[:, :full] = np.cumsum(a[:, :full].reshape(B, T // CHUNK, CHUNK, Nv), axis=2, dtype=np.float32).reshape(B, full, Nv)
         if full < T:
             g[:, full:] = np.cumsum(a[:, full:], axis=1, dtype=np.float32)
-    rng = np.random.default_rng(np.random.SeedSequence([seed, 0]))
-    m = make_mask(rng, B, Nv // 2, C, mask, retention)
-    h0 = rng.standard_normal((B, Nv, d, dv), dtype=np.float32) * np.float32(0.1) if with_h0 else None
-    return Inputs(B, T, Nq, Nv, d, dv, dtype, q, k, v, beta, g, m, h0,
-                  meta={"seed": seed, "mask": mask, "retention_target": retention})
+    return g
+
+
+def make_scores(B: int, Nv: int, C: int, seed: int, kind: str = "lognormal") -> np.ndarray:
+    """Stand-in Tail-16 write scores [B,Nv,C] fp32 (non-negative, like norms).
+
+    "lognormal": |N(0,1)| times a per-head scale exp(N(0, 0.7)), with a few hot
+    chunks (x4) per head; "ties": the same, rounded to 1/4 so many values tie;
+    "zero_heads": lognormal with every fourth head all zero.
+    """
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 7]))
+    s = np.abs(rng.standard_normal((B, Nv, C))) * np.exp(0.7 * rng.standard_normal((B, Nv, 1)))
+    hot = rng.random((B, Nv, C)) < 0.05
+    s = np.where(hot, 4.0 * s, s)
+    if kind == "ties":
+        s = np.round(4.0 * s) / 4.0
+    elif kind == "zero_heads":
+        s[:, ::4] = 0.0
+    elif kind != "lognormal":
+        raise ValueError(f"unknown score kind {kind!r}")
+    return s.astype(np.float32)
 
 
 # The five workloads of the SparseGDN GDN-core study, by what they are.

@@ -107,8 +107,9 @@ typedef struct {
     int32_t capacity;   /* entries available in ev_chunk and snap_slot */
 } gdn_events;
 
-/* Bytes of workspace the prefill entry points need for `shape` (sparse != 0:
- * gdn_prefill_sparse, else gdn_prefill_dense).  0 for invalid shapes. */
+/* Bytes of workspace the prefill entry points need for `shape`: sparse = 0
+ * gdn_prefill_dense, 1 gdn_prefill_sparse, 2 gdn_prefill_sparse_online.
+ * 0 for invalid shapes. */
 GDN_API size_t gdn_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse);
 
 /* Event compaction (Sec. 2.5, Eq. 16): turn the [B,P,C] 0/1 mask into CSR
@@ -118,6 +119,21 @@ GDN_API size_t gdn_workspace_bytes(const gdn_shape *shape, gdn_solver solver, in
  * gdn_events_status() returns GDN_ERR_CAPACITY.  No workspace needed. */
 GDN_API gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask,
                              gdn_events *events, void *stream);
+
+/* Online event selection (Sec. 2.4, Eqs. 10-14) for 16 head pairs (Nv == 32):
+ * from the Tail-16 scores score [B,Nv,C] (fp32, Eq. 9), the gates g [B,T,Nv]
+ * (gamma = g at each chunk's last token) and an optional output-visibility
+ * energy eta [B,Nv] (NULL: G_h = 1), choose per sequence the tier of every pair
+ * (Eq. 14) and its chunks (anchors 0 and C-1 plus the best k_tier - 2 chunks by
+ * the in-pair rank q, Eqs. 10 and 13); writes mask_out [B,16,C] (0/1) and, if
+ * non-NULL, tier_out [B,16] (0 low, 1 mid, 2 high).  Ties: q descending then
+ * lower chunk; pair gains descending then lower pair; B(x,k) ties take the
+ * smaller k.  Workspace: gdn_select_scored_workspace_bytes(shape), 256-byte
+ * aligned.  Other head counts return GDN_ERR_UNSUPPORTED. */
+GDN_API gdn_status gdn_select_events_scored(const gdn_shape *shape, const float *score, const float *g,
+                                    const float *eta, uint8_t *mask_out, int32_t *tier_out,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+GDN_API size_t gdn_select_scored_workspace_bytes(const gdn_shape *shape);
 
 /* Synchronises `stream` and reports the status bits of an events struct. */
 GDN_API gdn_status gdn_events_status(const gdn_events *events, void *stream);
@@ -144,6 +160,21 @@ GDN_API gdn_status gdn_prefill_sparse(const gdn_shape *shape,
                               const uint8_t *mask, gdn_solver solver,
                               void *o, float *s_final, float *score,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Event-sparse prefill with online selection, the pages' full pipeline
+ * (Secs. 2.3-2.7): intra step (U, Tail-16 scores, compact C-bar), online
+ * selection (as gdn_select_events_scored), compaction, deferred W for the
+ * selected events only, event scan, group output.  16 head pairs only.
+ * score (may be NULL) receives the Tail-16 scores, mask_out (may be NULL) the
+ * selected mask [B,16,C], tier_out (may be NULL) the tiers [B,16]; eta may be
+ * NULL.  Workspace: gdn_workspace_bytes(shape, solver, 2). */
+GDN_API gdn_status gdn_prefill_sparse_online(const gdn_shape *shape,
+                                     const void *q, const void *k, const void *v,
+                                     const float *beta, const float *g, const float *h0,
+                                     const float *eta, gdn_solver solver,
+                                     void *o, float *s_final, float *score, uint8_t *mask_out,
+                                     int32_t *tier_out, void *workspace, size_t workspace_bytes,
+                                     void *stream);
 
 /* Allocation-free event-sparse prefill.  The paper has no counterpart: this
  * is a deployment aid for callers that cannot allocate device memory -- for
@@ -192,16 +223,16 @@ GDN_API const char *gdn_status_string(gdn_status status);
 
 /* Stage timing for benchmarks.  While enabled, each prefill records a CUDA
  * event before its first and after each pipeline stage on its own stream
- * (stages: 0 select/compaction, 1 log-decay prefix, 2 intra, 3 deferred W,
- * 4 scan run maps, 5 scan chain over runs, 6 scan (fix-up, or the whole
- * scan for fp32 storage), 7 group output; stages 4-5 are empty for fp32
- * storage), for up to 256 prefills.  Enabling (again) drops
+ * (stages: 0 compaction, 1 log-decay prefix, 2 intra, 3 deferred W, 4 scan
+ * run maps, 5 scan chain over runs, 6 scan (fix-up, or the whole scan for fp32
+ * storage), 7 group output, 8 online selector; a stage a path does not run
+ * reads 0), for up to 256 prefills.  Enabling (again) drops
  * earlier records.  Not thread-safe: one host thread drives the profiler.
  * The events are created on the first enable (no device memory). */
 GDN_API gdn_status gdn_profile_enable(int enable);
 
 /* Synchronises on the recorded events, writes the summed milliseconds of each
- * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 8),
+ * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 9),
  * the number of recorded prefills to *n_prefills, and clears the records. */
 GDN_API gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills);
 

@@ -42,7 +42,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (portable flags only: it also builds on Arm hosts)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-Wall", "-shared", "-fPIC",
                                "-o", tmp, _SRC, "-lpthread", "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH

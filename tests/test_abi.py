@@ -109,3 +109,33 @@ def test_binding_fails_loudly_without_library(tmp_path):
             bnd.load(str(tmp_path / "missing.so"))
         finally:
             bnd._lib = saved
+
+
+def test_online_workspace_and_validation(lib):
+    s = shape()
+    assert gdn.gdn_workspace_bytes(s, "block_adj", 2) > gdn.gdn_workspace_bytes(s, "block_adj", 1)
+    assert lib.gdn_select_scored_workspace_bytes(ctypes.byref(s)) > 16 * 64 * 4
+    assert lib.gdn_select_scored_workspace_bytes(ctypes.byref(shape(Nq=2, Nv=4))) == 0
+    f = ctypes.c_void_p(FAKE)
+
+    def online(sh, ws_bytes=1 << 40, **kw):
+        get = lambda n: ctypes.c_void_p(kw.get(n, FAKE))
+        return lib.gdn_prefill_sparse_online(ctypes.byref(sh), get("q"), get("k"), get("v"), get("beta"),
+                                             get("g"), None, None, 1, get("o"), get("s"), None, None, None,
+                                             f, ws_bytes, None)
+
+    assert online(shape(Nq=2, Nv=4)) == 6                     # UNSUPPORTED: the tier table is for 16 pairs
+    assert online(shape(), q=0) == 1                          # NULL
+    assert online(shape(), o=FAKE + 4) == 4                   # ALIGN
+    assert online(shape(), ws_bytes=4096) == 5                # WORKSPACE
+
+    def scored(sh, score=FAKE, g=FAKE, mask=FAKE, ws_bytes=1 << 40):
+        return lib.gdn_select_events_scored(ctypes.byref(sh), ctypes.c_void_p(score), ctypes.c_void_p(g), None,
+                                            ctypes.c_void_p(mask), None, f, ws_bytes, None)
+
+    assert scored(shape(Nq=2, Nv=4)) == 6
+    assert scored(shape(), score=0) == 1
+    assert scored(shape(), mask=0) == 1
+    assert scored(shape(), score=FAKE + 4) == 4
+    assert scored(shape(), ws_bytes=64) == 5
+    assert scored(shape(B=0), score=0, g=0, mask=0) == 0

@@ -1,0 +1,149 @@
+"""Parity of the online event selector (SparseGDN Sec. 2.4, Eqs. 10-14) and of
+the prefill that selects its own events, through the C ABI.
+
+The selection is a deterministic function of the Tail-16 scores and the gates,
+so the GPU's masks and tiers must equal the oracle's bit for bit on the same
+scores.  The prefill that selects online is checked in three parts: its scores
+against the oracle's (floating-point tolerance), its mask against the oracle's
+selection on the GPU's own scores (bit for bit; near-equal scores may rank
+either way, so the oracle's own scores are not the reference for the mask),
+and its outputs against the oracle prefill run with that mask.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdn_synth
+import oracle
+from gpu_helpers import TOL, assert_close, dev, slice_pairs, to_dev
+
+import gated_delta_rule_16_gb300 as gdn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from gated_delta_rule_16_gb300 import build
+    build.build()
+    gdn.load()
+
+
+def chunk_gamma(g, C):
+    """gamma[b,h,c] = g at the last token of chunk c."""
+    return np.ascontiguousarray(np.moveaxis(g[:, 63::64, :][:, :C], 1, 2))
+
+
+def gpu_select(score, g, eta=None):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    mask, tier = gdn.gdn_select_events_scored(t(score), t(g), None if eta is None else t(eta))
+    torch.cuda.synchronize()
+    return mask.cpu().numpy(), tier.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,C,kind", [(1, 1, "lognormal"), (1, 2, "lognormal"), (1, 3, "lognormal"),
+                                      (2, 5, "ties"), (1, 15, "lognormal"), (1, 25, "zero_heads"),
+                                      (3, 64, "lognormal"), (2, 64, "ties"), (1, 512, "lognormal"),
+                                      (4, 512, "zero_heads"), (2, 2048, "lognormal"), (1, 1000, "ties")])
+@pytest.mark.parametrize("with_eta", [False, True])
+def test_selector_bit_exact(B, C, kind, with_eta):
+    seed = 31 * B + C
+    score = gdn_synth.make_scores(B, 32, C, seed, kind)
+    g = gdn_synth.make_gates(B, 64 * C, 32, seed)
+    eta = None
+    if with_eta:
+        eta = np.abs(np.random.default_rng(seed).standard_normal((B, 32))).astype(np.float32)
+        eta[:, 5] = 0.0
+    mask, tier = gpu_select(score, g, eta)
+    ref = oracle.select(score, chunk_gamma(g, C), eta)
+    assert np.array_equal(tier, ref["tier"]), f"tiers {tier} != {ref['tier']}"
+    assert np.array_equal(mask, ref["mask"]), f"{np.count_nonzero(mask != ref['mask'])} mask bytes differ"
+
+
+def test_selector_all_zero_scores_and_eta():
+    score = np.zeros((2, 32, 40), np.float32)
+    g = gdn_synth.make_gates(2, 64 * 40, 32, 5)
+    eta = np.zeros((2, 32), np.float32)
+    for e in (None, eta):
+        mask, tier = gpu_select(score, g, e)
+        ref = oracle.select(score, chunk_gamma(g, 40), e)
+        assert np.array_equal(tier, ref["tier"]) and np.array_equal(mask, ref["mask"])
+
+
+def test_selector_rejects_other_head_counts():
+    score = torch.zeros((1, 4, 8), device=dev())
+    g = torch.zeros((1, 512, 4), device=dev())
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.gdn_select_events_scored(score, g)
+    assert ei.value.status == 6
+
+
+def run_online(x, solver="block_adj", eta=None):
+    t = to_dev(x)
+    sc = torch.full((x.B, x.Nv, x.C), -1.0, device=dev())
+    et = None if eta is None else torch.from_numpy(eta).to(dev())
+    o, s, mask, tier = gdn.gdn_prefill_sparse_online(t["q"], t["k"], t["v"], t["beta"], t["g"], h0=t["h0"],
+                                                     eta=et, solver=solver, score=sc)
+    torch.cuda.synchronize()
+    return {"o": o.float().cpu().numpy().astype(np.float64), "s_final": s.cpu().numpy().astype(np.float64),
+            "score": sc.cpu().numpy(), "mask": mask.cpu().numpy(), "tier": tier.cpu().numpy()}
+
+
+def check_selection(x, res, eta=None):
+    ref = oracle.select(res["score"], chunk_gamma(x.g, x.C), eta)
+    assert np.array_equal(res["tier"], ref["tier"])
+    assert np.array_equal(res["mask"], ref["mask"])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("solver", ["exact", "block_adj"])
+def test_online_prefill_small(dtype, solver):
+    # 2 sequences x 16 head pairs x 23 chunks (odd: the last group has one chunk), with h0
+    x = gdn_synth.make_inputs(2, 23 * 64, 16, 32, dtype=dtype, seed=41, mask="ones", with_h0=True)
+    res = run_online(x, solver)
+    ref = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=res["mask"], h0=x.h0,
+                         solver={"exact": oracle.SOLVER_EXACT, "block_adj": oracle.SOLVER_BLOCK_ADJ}[solver],
+                         debug=True)
+    rel = np.abs(res["score"] - ref["score"]) / np.maximum(ref["score"], 1e-30)
+    assert rel.max() <= TOL[dtype]
+    check_selection(x, res)
+    assert_close(res, ref, dtype, f"online {dtype} {solver}")
+
+
+def test_online_prefill_with_eta():
+    x = gdn_synth.make_inputs(1, 40 * 64, 16, 32, dtype="bf16", seed=42, mask="ones")
+    eta = np.abs(np.random.default_rng(42).standard_normal((1, 32))).astype(np.float32)
+    res = run_online(x, eta=eta)
+    check_selection(x, res, eta)
+    ref = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=res["mask"], solver=oracle.SOLVER_BLOCK_ADJ)
+    assert_close(res, ref, "bf16", "online with eta")
+
+
+def test_online_layer_T32768_sampled_pairs():
+    x = gdn_synth.make_workload("qwen35_4b_layer_T32768_sparse29")
+    res = run_online(x)
+    check_selection(x, res)
+    # the selection keeps the tier budget: retention in [0.08, 0.95], the high tier 1..4 pairs
+    ret = res["mask"].mean()
+    assert 0.08 <= ret <= 0.95
+    assert 1 <= (res["tier"] == 2).sum() <= 4
+    for p in (int(np.argmax(res["mask"][0].sum(-1))), int(np.argmin(res["mask"][0].sum(-1)))):
+        y = slice_pairs(x, 0, [p])
+        ref = oracle.prefill(y.q, y.k, y.v, y.beta, y.g, mask=res["mask"][:, p:p + 1], h0=None,
+                             solver=oracle.SOLVER_BLOCK_ADJ)
+        got = {"o": res["o"][:, :, 2 * p:2 * p + 2], "s_final": res["s_final"][:, 2 * p:2 * p + 2]}
+        assert_close(got, ref, "bf16", f"online T=32768 pair {p}")
+
+
+def test_online_matches_given_mask_path():
+    # the prefill with the selected mask handed in gives the same result within rounding
+    x = gdn_synth.make_inputs(1, 4096, 16, 32, dtype="bf16", seed=43, mask="ones")
+    res = run_online(x)
+    t = to_dev(x)
+    o, s = gdn.gdn_prefill_sparse(t["q"], t["k"], t["v"], t["beta"], t["g"],
+                                  torch.from_numpy(res["mask"]).to(dev()))
+    torch.cuda.synchronize()
+    other = {"o": o.float().cpu().numpy().astype(np.float64), "s_final": s.cpu().numpy().astype(np.float64)}
+    assert_close(res, other, "bf16", "online vs given mask")
