@@ -198,7 +198,7 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
         stage(8, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
         stage(0, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
         stage(1, [&] { return launch_prefix(pb, ws); });
-        stage(3, [&] { return launch_wbuild(pb, ws); });
+        stage(3, [&] { return tc ? launch_wbuild_tc(pb, ws) : launch_wbuild(pb, ws); });
     } else {
         stage(0, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
         stage(1, [&] { return launch_prefix(pb, ws); });

@@ -67,7 +67,7 @@ struct Workspace {
     double *P;                 // [B, Nv, C+1] log2 decay prefix (Eq. 19)
     void *grp_info;            // [B, P, G] int4 {snapshot slot, kind, decay head 0, decay head 1}
     void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
-    float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks
+    float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks (bf16 on the tensor-core path)
     void *W;                   // [ev_cap, 2, 64, d] dtype, deferred W of events
     void *snap;                // [snap_cap, 2, d, dv] post-event state snapshots (fp32; bf16 for bf16 storage)
     // tensor-core scan (bf16 storage only; NR = ceil(C / kRunChunks))
@@ -100,6 +100,9 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws);
 // write_cbar: store the compact C-bar blocks (W is built later, after online selection)
 cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_cbar);
 // online selection: mask [B,16,C] (and tiers [B,16], may be NULL) from scores [B,Nv,C]
+// Deferred W on tensor cores for the selected events, from the compact bf16 C-bar
+// blocks that launch_intra_tc(..., write_cbar = true) stored (bf16 storage only).
+cudaError_t launch_wbuild_tc(const Problem &pb, const Workspace &ws);
 // Online selection (Eqs. 10-14) for 16 head pairs: score [B,32,C] -> mask [B,16,C],
 // tier_out [B,16] (may be NULL); ws holds selector_workspace_bytes(B, C).
 size_t selector_workspace_bytes(int B, int C);

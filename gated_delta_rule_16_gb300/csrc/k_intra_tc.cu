@@ -44,7 +44,7 @@ struct IntraParams {
     const float *beta, *g;
     const int32_t *ev_of;   // NULL: no W here (online selection builds W later from C-bar)
     __nv_bfloat16 *U, *W;
-    float *cbar;            // non-NULL: write the compact C-bar blocks [B,Nv,C,nblk,16,16]
+    __nv_bfloat16 *cbar;    // non-NULL: write the compact C-bar blocks [B,Nv,C,nblk,16,16] (bf16)
     float *score;
     int32_t *status;
     int P_, T_, Nv, C, nblk, exact;
@@ -239,13 +239,19 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 }
             }
         }
-        if (a.cbar) {  // compact C-bar = C diag(beta 2^g) for the W kernel that runs after selection
-            for (int idx = tid; idx < nch * a.nblk * 256; idx += kThreads) {
-                const int cc = idx / (a.nblk * 256), rem = idx % (a.nblk * 256);
-                const int blk = rem >> 8, rr = (rem >> 4) & 15, col = rem & 15;
-                const int rw = blk_row(blk) * kBlk + rr, cl = blk_col(blk) * kBlk + col;
-                a.cbar[(((int64_t)b * a.Nv + h) * a.C + c0 + cc) * a.nblk * 256 + rem] =
-                    Cs[(cc * kChunk + rw) * MS + cl] * bgs[64 * cc + cl];
+        if (a.cbar) {  // compact C-bar = C diag(beta 2^g), bf16 as in the W operand, for the W kernel after selection
+            for (int idx = tid; idx < nch * a.nblk * 32; idx += kThreads) {  // 8 coefficients (16 bytes) each
+                const int cc = idx / (a.nblk * 32), rem = idx % (a.nblk * 32);
+                const int blk = rem >> 5, rr = (rem >> 1) & 15, col0 = (rem & 1) * 8;
+                const int rw = blk_row(blk) * kBlk + rr, cl = blk_col(blk) * kBlk + col0;
+                const float *cr = Cs + (cc * kChunk + rw) * MS + cl;
+                const float *bg = bgs + 64 * cc + cl;
+                __nv_bfloat162 p2[4];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2)
+                    p2[q2] = __floats2bfloat162_rn(cr[2 * q2] * bg[2 * q2], cr[2 * q2 + 1] * bg[2 * q2 + 1]);
+                *reinterpret_cast<uint4 *>(a.cbar + (((int64_t)b * a.Nv + h) * a.C + c0 + cc) * a.nblk * 256 +
+                                           blk * 256 + rr * 16 + col0) = *reinterpret_cast<uint4 *>(p2);
             }
         }
         fence_async_smem();
@@ -342,7 +348,7 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
         return cudaErrorInvalidValue;
     IntraParams a;
     a.beta = pb.beta; a.g = pb.g; a.ev_of = write_cbar ? nullptr : ws.ev_of;
-    a.cbar = write_cbar ? ws.cbar : nullptr;
+    a.cbar = write_cbar ? reinterpret_cast<__nv_bfloat16 *>(ws.cbar) : nullptr;
     a.U = (__nv_bfloat16 *)ws.U; a.W = (__nv_bfloat16 *)ws.W; a.score = pb.score;
     a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;

@@ -15,9 +15,13 @@
 //   n_H    = argmax_{1..4} B(x_H), n_M = argmax over the table row of B(x_M of the rest) (Eq. 14)
 // The ranking of each pair is a bitonic sort in shared memory of 64-bit keys
 // (~bits(q) << 32 | chunk), i.e. q descending then chunk ascending (q >= 0: the
-// scores are norms).  The gains are summed by one thread in rank order, so every
-// decision is taken from the same fp32 q values and the same fp64 sums as the
-// sequential definition and the masks are reproducible bit for bit.
+// scores are norms); q is computed with IEEE fp32 division from the fp32 norms,
+// as in the sequential definition.  The fp64 quantities behind the tier choice
+// (sums of squares, L_h, gains, separations) are reduced in parallel: they
+// differ from a sequential evaluation only in rounding order (and exp2's last
+// ulp), so a tier choice can only differ where two candidates are within fp64
+// rounding of each other.  GB300's fp64 units are slow (a dependent fp64 add
+// costs on the order of a hundred cycles), so no step here is a long serial chain.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -26,6 +30,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kPairs = 16;
 
+// B(x, k) of Eq. 14 for sorted x[0..n): k (n - k) / n (mean of the top k - mean of the rest)^2
 __device__ double separation(const double *xs, int n, int k) {
     double top = 0.0, rest = 0.0;
     for (int i = 0; i < k; ++i) top += xs[i];
@@ -35,17 +40,40 @@ __device__ double separation(const double *xs, int n, int k) {
     return (double)k * (n - k) / n * (top - rest) * (top - rest);
 }
 
-// pair ids by x descending, ties to the lower id (insertion sort, n <= 16)
-__device__ void order_pairs(const double *x, int *ids, int n) {
-    for (int i = 1; i < n; ++i) {
-        const int v = ids[i];
-        int j = i - 1;
-        while (j >= 0 && (x[ids[j]] < x[v] || (x[ids[j]] == x[v] && ids[j] > v))) {
-            ids[j + 1] = ids[j];
-            --j;
-        }
-        ids[j + 1] = v;
+// position of element i in x sorted descending, ties to the lower index
+__device__ __forceinline__ int desc_position(const double *x, const int *ids, int n, int i) {
+    const double v = x[ids[i]];
+    int pos = 0;
+    for (int j = 0; j < n; ++j) {
+        const double u = x[ids[j]];
+        pos += (u > v || (u == v && ids[j] < ids[i])) ? 1 : 0;
     }
+    return pos;
+}
+
+// x^n for n >= 1 by binary exponentiation (a short dependent chain: fp64 is slow here)
+__device__ __forceinline__ double ipow(double x, int n) {
+    double r = 1.0;
+    while (n) {
+        if (n & 1) r *= x;
+        x *= x;
+        n >>= 1;
+    }
+    return r;
+}
+
+template <int NT>
+__device__ double block_sum(double v, double *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    double t = lane < NT / 32 ? red[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
 }
 
 __device__ __forceinline__ int tier_size(int l, int C) {
@@ -60,46 +88,69 @@ __device__ __forceinline__ int tier_size(int l, int C) {
 // anchors) and gains[2] = {gain_LM, gain_MH}.
 __global__ void __launch_bounds__(kThreads)
 selector_pair_kernel(const float *__restrict__ score, const float *__restrict__ g, const float *__restrict__ eta,
-                     int T_, int Nv, int C, int npow2, int32_t *__restrict__ rank_ws, double *__restrict__ wbuf,
-                     double *__restrict__ gains) {
+                     int T_, int Nv, int C, int npow2, int32_t *__restrict__ rank_ws, double *__restrict__ gains) {
     extern __shared__ unsigned long long keys[];  // [npow2]
     __shared__ float norm[2];
-    __shared__ double L[2], G[2];
+    __shared__ double L[2], G[2], rr[2], red[kThreads / 32], red2[kThreads / 32];
     const int p = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int h0 = 2 * p;
     const float *s0 = score + ((int64_t)b * Nv + h0) * C;
     const float *s1 = s0 + C;
     int32_t *rank = rank_ws + ((int64_t)b * kPairs + p) * C;
-    double *w = wbuf + ((int64_t)b * kPairs + p) * C;
 
-    // Eq. 11 for the two heads: thread j handles head h0 + j.  Every sum runs in index
-    // order and every product is rounded on its own (no fused multiply-add), so the
-    // fp64 values are those of the sequential definition.
-    if (tid < 2) {
-        const int h = h0 + tid;
-        const float *sh = tid ? s1 : s0;
-        double ss = 0.0;
-        for (int c = 0; c < C; ++c) ss = __dadd_rn(ss, __dmul_rn((double)sh[c], (double)sh[c]));
-        norm[tid] = sqrtf((float)ss);
-        const int c0 = C > 16 ? C - 16 : 0;
-        double r = 0.0;
-        for (int c = c0; c < C; ++c)
-            r = __dadd_rn(r, exp2((double)g[((int64_t)b * T_ + (int64_t)c * kChunk + kChunk - 1) * Nv + h]));
-        r = C > c0 ? r / (C - c0) : 0.0;
-        double Lh = 0.0, pw = 1.0;
-        for (int j = 1; j <= C - 2; ++j) {
-            pw = __dmul_rn(pw, r);
-            Lh = __dadd_rn(Lh, pw);
+    // Eq. 11 for the two heads, each by half of the CTA (256 threads)
+    const int half = tid >> 8, ht = tid & 255;
+    const int h = h0 + half;
+    const float *sh = half ? s1 : s0;
+    double ss = 0.0;
+    for (int c = ht; c < C; c += 256) ss += (double)sh[c] * (double)sh[c];
+    // r_h: mean of 2^gamma over the last min(16, C) chunks
+    const int c0 = C > 16 ? C - 16 : 0;
+    double e2 = 0.0;
+    if (ht < C - c0) e2 = exp2((double)g[((int64_t)b * T_ + (int64_t)(c0 + ht) * kChunk + kChunk - 1) * Nv + h]);
+    // both half-sums at once: lanes reduce within the warp, warps of a half combine in shared memory
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        e2 += __shfl_xor_sync(0xffffffffu, e2, o);
+    }
+    if ((tid & 31) == 0) { red[tid >> 5] = ss; red2[tid >> 5] = e2; }
+    __syncthreads();
+    if (ht == 0) {
+        double a = 0.0, r = 0.0;
+        for (int w8 = 0; w8 < 8; ++w8) { a += red[8 * half + w8]; r += red2[8 * half + w8]; }
+        norm[half] = sqrtf((float)a);
+        rr[half] = C > c0 ? r / (C - c0) : 0.0;
+    }
+    __syncthreads();
+    // L_h = sum_{j=1}^{C-2} r^j: thread ht sums the powers j in its segment
+    {
+        const double r = rr[half];
+        const int n = C - 2, m = (n + 255) / 256;
+        const int j0 = ht * m + 1, j1 = min(n, j0 + m - 1);
+        double part = 0.0;
+        if (j0 <= j1 && r > 0.0) {
+            double pw = ipow(r, j0);
+            for (int j = j0; j <= j1; ++j) { part += pw; pw *= r; }
         }
-        double Gh = 1.0;
-        if (eta) {
-            double m = 0.0;
-            for (int j = 0; j < Nv; ++j) m = __dadd_rn(m, (double)eta[(int64_t)b * Nv + j]);
-            m /= Nv;
-            Gh = m > 0.0 ? sqrt((double)eta[(int64_t)b * Nv + h] / m) : 0.0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        __syncthreads();
+        if ((tid & 31) == 0) red[tid >> 5] = part;
+        __syncthreads();
+        if (ht == 0) {
+            double Lh = 0.0;
+            for (int w8 = 0; w8 < 8; ++w8) Lh += red[8 * half + w8];
+            double Gh = 1.0;
+            if (eta) {
+                double em = 0.0;
+                for (int j = 0; j < Nv; ++j) em += (double)eta[(int64_t)b * Nv + j];
+                em /= Nv;
+                Gh = em > 0.0 ? sqrt((double)eta[(int64_t)b * Nv + h] / em) : 0.0;
+            }
+            L[half] = Lh;
+            G[half] = Gh;
         }
-        L[tid] = Lh;
-        G[tid] = Gh;
     }
     __syncthreads();
     const int n_in = C > 2 ? C - 2 : 0;
@@ -130,73 +181,101 @@ selector_pair_kernel(const float *__restrict__ score, const float *__restrict__ 
             __syncthreads();
         }
     }
-    // ranks, and the Eq. 12 summands in rank order
+    // ranks, and the Eq. 12 gains of the upgrades L -> M (ranks [k_L-2, k_M-2)) and
+    // M -> H (ranks [k_M-2, k_H-2))
     const double L0 = L[0], L1 = L[1], G0 = G[0], G1 = G[1];
+    const int kL = tier_size(0, C) - 2, kM = tier_size(1, C) - 2, kH = tier_size(2, C) - 2;
+    double wLM = 0.0, wMH = 0.0;
     for (int i = tid; i < n_in; i += kThreads) {
         const int c = (int)(keys[i] & 0xffffffffu);
         rank[c] = i;
-        w[i] = __dadd_rn(__dmul_rn(__dmul_rn((double)s0[c], L0), G0), __dmul_rn(__dmul_rn((double)s1[c], L1), G1));
+        const double w = (double)s0[c] * L0 * G0 + (double)s1[c] * L1 * G1;
+        if (i >= kL && i < kM) wLM += w;
+        if (i >= kM && i < kH) wMH += w;
     }
     if (tid == 0 && C > 0) {
         rank[0] = -1;
         rank[C - 1] = -1;
     }
-    __syncthreads();
-    // Eq. 12 in rank order: C_M \ C_L and C_H \ C_M (two threads, sequential sums)
-    if (tid < 2) {
-        const int lo = tier_size(tid, C) - 2, hi = tier_size(tid + 1, C) - 2;
-        double t = 0.0;
-        for (int i = lo; i < hi; ++i) t = __dadd_rn(t, w[i]);
-        gains[((int64_t)b * kPairs + p) * 2 + tid] = t;
+    const double tLM = block_sum<kThreads>(wLM, red);
+    const double tMH = block_sum<kThreads>(wMH, red2);
+    if (tid == 0) {
+        gains[((int64_t)b * kPairs + p) * 2 + 0] = tLM;
+        gains[((int64_t)b * kPairs + p) * 2 + 1] = tMH;
     }
 }
 
 // Eq. 14 for one sequence, then the mask of every pair: anchors plus its tier's
-// best k - 2 chunks.
+// best k - 2 chunks.  Thread p < 16 normalises pair p's gains and finds its place
+// in the descending orders; candidate counts are scored one per thread.
 __global__ void __launch_bounds__(256)
 selector_tier_kernel(int C, const int32_t *__restrict__ rank_ws, const double *__restrict__ gains,
                      uint8_t *__restrict__ mask, int32_t *__restrict__ tier_out) {
-    __shared__ double xM[kPairs], xH[kPairs], xs[kPairs];
-    __shared__ int ids[kPairs], rest[kPairs], tier[kPairs], kk[3];
+    __shared__ double gLM[kPairs], gMH[kPairs], xM[kPairs], xH[kPairs], xs[kPairs], sep[kPairs];
+    __shared__ int ids[kPairs], rest[kPairs], tier[kPairs], kk[3], nH_s, nr_s;
     const int b = blockIdx.x, tid = threadIdx.x;
-    if (tid == 0) {
-        for (int l = 0; l < 3; ++l) kk[l] = tier_size(l, C);
-        const double *gb = gains + (int64_t)b * kPairs * 2;
-        double mLM = 0.0, mMH = 0.0;
-        for (int p = 0; p < kPairs; ++p) { mLM += gb[2 * p]; mMH += gb[2 * p + 1]; }
+    if (tid < kPairs) {
+        gLM[tid] = gains[((int64_t)b * kPairs + tid) * 2];
+        gMH[tid] = gains[((int64_t)b * kPairs + tid) * 2 + 1];
+        ids[tid] = tid;
+    }
+    if (tid < 3) kk[tid] = tier_size(tid, C);
+    __syncthreads();
+    if (tid < 32) {  // means over the 16 pairs by a shuffle tree, then x = gain / mean
+        double mLM = tid < kPairs ? gLM[tid] : 0.0, mMH = tid < kPairs ? gMH[tid] : 0.0;
+#pragma unroll
+        for (int o = 8; o; o >>= 1) {
+            mLM += __shfl_xor_sync(0xffffffffu, mLM, o);
+            mMH += __shfl_xor_sync(0xffffffffu, mMH, o);
+        }
         mLM /= kPairs;
         mMH /= kPairs;
-        for (int p = 0; p < kPairs; ++p) {
-            xM[p] = mLM != 0.0 ? gb[2 * p] / mLM : 0.0;
-            xH[p] = mMH != 0.0 ? gb[2 * p + 1] / mMH : 0.0;
-            ids[p] = p;
-            tier[p] = 0;
+        if (tid < kPairs) {
+            xM[tid] = mLM != 0.0 ? gLM[tid] / mLM : 0.0;
+            xH[tid] = mMH != 0.0 ? gMH[tid] / mMH : 0.0;
         }
-        order_pairs(xH, ids, kPairs);
-        for (int i = 0; i < kPairs; ++i) xs[i] = xH[ids[i]];
+    }
+    __syncthreads();
+    // high tier: x_H sorted descending, B(x_H, k) for k = 1..4, the first maximum wins
+    if (tid < kPairs) {
+        const int pos = desc_position(xH, ids, kPairs, tid);
+        xs[pos] = xH[tid];
+        rest[pos] = tid;  // pair at each position of the x_H order
+    }
+    __syncthreads();
+    if (tid < 4) sep[tid] = separation(xs, kPairs, tid + 1);
+    __syncthreads();
+    if (tid == 0) {
         int nH = 1;
-        double best = separation(xs, kPairs, 1);
-        for (int k = 2; k <= 4; ++k) {
-            const double v = separation(xs, kPairs, k);
-            if (v > best) { best = v; nH = k; }
-        }
-        for (int i = 0; i < nH; ++i) tier[ids[i]] = 2;
+        for (int k = 2; k <= 4; ++k)
+            if (sep[k - 1] > sep[nH - 1]) nH = k;
+        nH_s = nH;
+        for (int p = 0; p < kPairs; ++p) tier[p] = 0;
+        for (int i = 0; i < nH; ++i) tier[rest[i]] = 2;
         int nr = 0;
         for (int p = 0; p < kPairs; ++p)
-            if (tier[p] != 2) rest[nr++] = p;
-        order_pairs(xM, rest, nr);
-        for (int i = 0; i < nr; ++i) xs[i] = xM[rest[i]];
-        // admissible counts of mid-tier pairs for each high-tier count
-        const int lo = nH == 1 ? 11 : (nH == 2 ? 7 : (nH == 3 ? 3 : 0));
-        const int hi = nH == 1 ? 13 : (nH == 2 ? 9 : (nH == 3 ? 5 : 0));
+            if (tier[p] != 2) ids[nr++] = p;  // the remaining pairs, in pair order
+        nr_s = nr;
+    }
+    __syncthreads();
+    // mid tier among the rest: x_M sorted descending, B over the table row of n_H
+    const int nH = nH_s, nr = nr_s;
+    const int lo = nH == 1 ? 11 : (nH == 2 ? 7 : (nH == 3 ? 3 : 0));
+    const int hi = nH == 1 ? 13 : (nH == 2 ? 9 : (nH == 3 ? 5 : 0));
+    if (tid < nr) {
+        const int pos = desc_position(xM, ids, nr, tid);
+        xs[pos] = xM[ids[tid]];
+        rest[pos] = ids[tid];
+    }
+    __syncthreads();
+    if (hi > 0 && tid <= hi - lo) sep[tid] = separation(xs, nr, lo + tid);
+    __syncthreads();
+    if (tid == 0) {
         int nM = 0;
         if (hi > 0) {
             nM = lo;
-            best = separation(xs, nr, lo);
-            for (int k = lo + 1; k <= hi; ++k) {
-                const double v = separation(xs, nr, k);
-                if (v > best) { best = v; nM = k; }
-            }
+            for (int k = lo + 1; k <= hi; ++k)
+                if (sep[k - lo] > sep[nM - lo]) nM = k;
         }
         for (int i = 0; i < nM; ++i) tier[rest[i]] = 1;
     }
@@ -214,7 +293,7 @@ selector_tier_kernel(int C, const int32_t *__restrict__ rank_ws, const double *_
 }  // namespace
 
 size_t selector_workspace_bytes(int B, int C) {
-    return (size_t)B * kPairs * C * (sizeof(int32_t) + sizeof(double)) + (size_t)B * kPairs * 2 * sizeof(double);
+    return (size_t)B * kPairs * 2 * sizeof(double) + (size_t)B * kPairs * C * sizeof(int32_t);
 }
 
 cudaError_t launch_selector(const Problem &pb, const float *score, const float *eta, uint8_t *mask,
@@ -225,12 +304,10 @@ cudaError_t launch_selector(const Problem &pb, const float *score, const float *
     const size_t smem = (size_t)npow2 * sizeof(unsigned long long);
     cudaError_t e = cudaFuncSetAttribute(selector_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const size_t n = (size_t)pb.B * kPairs * pb.C;
-    double *wbuf = (double *)ws;                  // [B,16,C] fp64, rank order
-    double *gains = wbuf + n;                     // [B,16,2]
+    double *gains = (double *)ws;                                    // [B,16,2]
     int32_t *rank = (int32_t *)(gains + (size_t)pb.B * kPairs * 2);  // [B,16,C]
     selector_pair_kernel<<<dim3(kPairs, pb.B), kThreads, smem, pb.stream>>>(score, pb.g, eta, pb.T, pb.Nv, pb.C,
-                                                                            npow2, rank, wbuf, gains);
+                                                                            npow2, rank, gains);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     selector_tier_kernel<<<pb.B, 256, 0, pb.stream>>>(pb.C, rank, gains, mask, tier_out);
