@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen35_4b_layer_T32768_sparse29")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     return ap.parse_args()
 
 
@@ -231,6 +231,37 @@ def run_reference(args):
 
 # ------------------------------------------------------------ our CUDA path ---
 
+def online_variant(gdn, d_in, x, ws, stream, steps, world, dev):
+    """The same step with the events chosen on the GPU from the Tail-16 scores
+    (SparseGDN Sec. 2.4) instead of the given mask: time, stages and retention."""
+    import torch
+    if x.Nv != 32:
+        return None
+
+    def step():
+        return gdn.gdn_prefill_sparse_online(d_in["q"], d_in["k"], d_in["v"], d_in["beta"], d_in["g"],
+                                             solver="block_adj", workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    gdn.gdn_profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        out = step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stage_ms, nrec, n_launch = gdn.gdn_profile_read(with_launches=True)
+    gdn.gdn_profile_enable(False)
+    ms = reduce_step_ms(e0.elapsed_time(e1) / steps, world, dev)
+    return {"ms_per_step": ms, "value": job_throughput(x.B * x.T, world, ms), "unit": UNIT,
+            "retention": round(float(out[2].float().mean().item()), 4),
+            "tiers_low_mid_high": [int((out[3] == t).sum().item()) for t in range(3)],
+            "gpu_launches": n_launch,
+            "stages_ms": {k: round(v / max(nrec, 1), 4) for k, v in stage_ms.items()}}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -284,36 +315,51 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    stage_ms, nrec = gdn.gdn_profile_read()
+    stage_ms, nrec, n_launch = gdn.gdn_profile_read(with_launches=True)
     gdn.gdn_profile_enable(False)
     clk = clocks.stop()
     ms = reduce_step_ms(ev0.elapsed_time(ev1) / args.steps, world, dev)
     value = job_throughput(tok, world, ms)
 
-    # end to end through the public API: pinned host inputs -> device -> prefill -> host outputs
-    h_o = torch.empty(o.shape, dtype=st).pin_memory()
-    h_s = torch.empty(s_final.shape, dtype=torch.float32).pin_memory()
+    # end to end through the C ABI with host buffers (gdn_prefill_host): each step copies its
+    # inputs from pinned host memory, runs the prefill and copies O and S_final back.  Serial:
+    # one stream.  Pipelined (the e2e value): two workspaces on two streams, so one step's
+    # copies overlap the other step's kernels; every step still does all of its own copies.
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = h_o.numel() * h_o.element_size() + h_s.numel() * h_s.element_size()
+    d2h = o.numel() * o.element_size() + s_final.numel() * s_final.element_size()
+    streams = [stream, torch.cuda.Stream(dev)]
+    wss = [gdn.Workspace(), gdn.Workspace()]
+    h_out = [(torch.empty(o.shape, dtype=st).pin_memory(), torch.empty(s_final.shape, dtype=torch.float32).pin_memory())
+             for _ in range(2)]
 
-    def e2e_step():
-        dd = {n: t.to(dev, non_blocking=True) for n, t in host.items()}
-        oo, ss = gdn.gdn_prefill_sparse(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["mask"],
-                                        solver="block_adj", workspace=ws, stream=stream)
-        h_o.copy_(oo, non_blocking=True)
-        h_s.copy_(ss, non_blocking=True)
+    def e2e_step(j):
+        gdn.gdn_prefill_host(host["q"], host["k"], host["v"], host["beta"], host["g"], host["mask"],
+                             solver="block_adj", o=h_out[j][0], s_final=h_out[j][1], workspace=wss[j],
+                             device=dev, stream=streams[j])
 
-    e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_step_ms(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    def time_e2e(pipelined):
+        for i in range(2):
+            e2e_step(i % 2 if pipelined else 0)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(streams[0])
+        streams[1].wait_event(e0)
+        for i in range(args.e2e_steps):
+            e2e_step(i % 2 if pipelined else 0)
+        streams[0].wait_stream(streams[1])
+        e1.record(streams[0])
+        torch.cuda.synchronize()
+        return reduce_step_ms(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+
+    e2e_serial_ms = time_e2e(False)
+    e2e_ms = time_e2e(True)
+    # the host copy of O must equal the device-path result of the same inputs
+    if not torch.equal(h_out[(args.e2e_steps - 1) % 2][0], o.cpu()):
+        raise RuntimeError("host-buffer prefill disagrees with the device-buffer prefill")
+
+    online = online_variant(gdn, d_in, x, ws, stream, args.steps, world, dev)
 
     peak, peak_kind = peaks()
     per_stage = {k: v / max(nrec, 1) for k, v in stage_ms.items()}
@@ -335,14 +381,16 @@ def run_ours(args):
                    "parallelism": "one independent sequence per GPU" if world > 1 else "single GPU"},
         "clocks": clk,
         "e2e": {"value": job_throughput(tok, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": len(gdn.STAGES) * args.steps,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": "gdn_prefill_host (C ABI, host buffers)",
+                "pipelining": "2 streams x 2 workspaces", "serial_ms_per_step": e2e_serial_ms},
+        "gpu_launches": n_launch,
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
                      "step_frac": step_gbs / peak,
                      "note": f"achieved = compulsory bytes of one {dom_kernel} launch / its mean CUDA-event time; "
                              f"frac of {peak_kind} HBM copy bandwidth"},
         "stages_ms": {k: round(v, 4) for k, v in per_stage.items()},
+        "variants": {"online_selection": online},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x)

@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     Workspace,
     gdn_events_status,
     gdn_prefill_dense,
+    gdn_prefill_host,
     gdn_prefill_sparse,
     gdn_prefill_sparse_noalloc,
     gdn_prefill_sparse_online,

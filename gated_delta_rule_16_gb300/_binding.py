@@ -24,7 +24,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE"
 EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn_prefill_dense",
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
            "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout",
-           "gdn_prefill_sparse_online", "gdn_select_events_scored", "gdn_select_scored_workspace_bytes")
+           "gdn_prefill_sparse_online", "gdn_select_events_scored", "gdn_select_scored_workspace_bytes",
+           "gdn_prefill_host", "gdn_prefill_host_workspace_bytes")
 STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output", "selector")
 
 
@@ -78,6 +79,10 @@ def load(path: str | None = None):
             lib.gdn_select_events_scored.restype = i32
             lib.gdn_select_scored_workspace_bytes.argtypes = [shp]
             lib.gdn_select_scored_workspace_bytes.restype = sz
+            lib.gdn_prefill_host.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+            lib.gdn_prefill_host.restype = i32
+            lib.gdn_prefill_host_workspace_bytes.argtypes = [shp, i32, i32]
+            lib.gdn_prefill_host_workspace_bytes.restype = sz
             lib.gdn_prefill_sparse_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
             lib.gdn_prefill_sparse_noalloc.restype = i32
             lib.gdn_selftest_wait_timeout.argtypes = [vp, i32, vp]
@@ -91,7 +96,7 @@ def load(path: str | None = None):
             lib.gdn_profile_enable.argtypes = [i32]
             lib.gdn_profile_enable.restype = i32
             lib.gdn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int32,
-                                             ctypes.POINTER(ctypes.c_int32)]
+                                             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]
             lib.gdn_profile_read.restype = i32
             _lib = lib
     return _lib
@@ -313,6 +318,54 @@ def gdn_select_events_scored(score: torch.Tensor, g: torch.Tensor, eta=None, *, 
     return mask_out, tier_out
 
 
+def _need_host(t, name, dtype=None, shape=None):
+    if t is None:
+        return
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def gdn_prefill_host(q, k, v, beta, g, mask=None, *, h0=None, solver="block_adj", o=None, s_final=None,
+                     workspace=None, device="cuda:0", stream=None):
+    """Prefill with host (CPU, preferably pinned) inputs and outputs; returns (o, s_final).
+
+    The copies and kernels are enqueued on `stream`; the call does not wait, so
+    synchronise the stream before reading the outputs.
+    """
+    B, T, Nq, d = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    C = (T + 63) // 64
+    _need_host(q, "q", shape=(B, T, Nq, d))
+    _need_host(k, "k", dtype=q.dtype, shape=(B, T, Nq, d))
+    _need_host(v, "v", dtype=q.dtype, shape=(B, T, Nv, dv))
+    _need_host(beta, "beta", torch.float32, (B, T, Nv))
+    _need_host(g, "g", torch.float32, (B, T, Nv))
+    _need_host(h0, "h0", torch.float32, (B, Nv, d, dv))
+    _need_host(mask, "mask", torch.uint8, (B, Nq, C))
+    if o is None:
+        o = torch.empty((B, T, Nv, dv), dtype=q.dtype).pin_memory()
+    if s_final is None:
+        s_final = torch.empty((B, Nv, d, dv), dtype=torch.float32).pin_memory()
+    _need_host(o, "o", q.dtype, (B, T, Nv, dv))
+    _need_host(s_final, "s_final", torch.float32, (B, Nv, d, dv))
+    shape = shape_of(q, v)
+    dev = torch.device(device)
+    lib = load()
+    nbytes = int(lib.gdn_prefill_host_workspace_bytes(ctypes.byref(shape), SOLVERS[solver], int(mask is not None)))
+    ws = _workspace(workspace, nbytes, dev)
+    with torch.cuda.device(dev):
+        _check("gdn_prefill_host", lib.gdn_prefill_host(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(mask),
+            SOLVERS[solver], _ptr(o), _ptr(s_final), _ptr(ws), ws.numel(), _stream(stream)))
+    return o, s_final
+
+
 def gdn_select_events(mask: torch.Tensor, Nq: int | None = None, capacity: int | None = None, stream=None):
     """Mask [B,P,C] uint8 -> CSR event lists on the device (dict of int32 tensors)."""
     _need(mask, "mask", torch.uint8)
@@ -364,9 +417,12 @@ def gdn_profile_enable(enable: bool = True) -> None:
     _check("gdn_profile_enable", load().gdn_profile_enable(int(enable)))
 
 
-def gdn_profile_read() -> tuple[dict, int]:
-    """Summed milliseconds per stage over the recorded prefills, and their count."""
+def gdn_profile_read(with_launches: bool = False):
+    """Summed milliseconds per stage over the recorded prefills and their count
+    (and, with_launches, the number of kernels they launched)."""
     ms = (ctypes.c_float * len(STAGES))()
     n = ctypes.c_int32(0)
-    _check("gdn_profile_read", load().gdn_profile_read(ms, len(STAGES), ctypes.byref(n)))
-    return {name: float(ms[i]) for i, name in enumerate(STAGES)}, int(n.value)
+    nl = ctypes.c_int64(0)
+    _check("gdn_profile_read", load().gdn_profile_read(ms, len(STAGES), ctypes.byref(n), ctypes.byref(nl)))
+    stages = {name: float(ms[i]) for i, name in enumerate(STAGES)}
+    return (stages, int(n.value), int(nl.value)) if with_launches else (stages, int(n.value))

@@ -23,6 +23,7 @@ constexpr int kProfSlots = 256;
 struct Profiler {
     bool on = false, created = false;
     int used = 0;
+    int64_t launches = 0;                      // kernels launched by the recorded prefills
     cudaEvent_t ev[kProfSlots][2 * kStages];  // start and end of every stage
 };
 Profiler g_prof;
@@ -186,30 +187,32 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     auto mark = [&](int i) { if (prof) cudaEventRecord(prof[i], pb.stream); };
     const bool tc = pb.dtype == GDN_BF16;   // tensor-core path for bf16 storage
     cudaError_t e = cudaSuccess;
-    auto stage = [&](int id, auto &&launch) {
+    // kernels: how many kernels the stage's launcher issues (0 for an empty stage)
+    auto stage = [&](int id, int kernels, auto &&launch) {
         mark(2 * id);
         if (e == cudaSuccess) e = launch();
         mark(2 * id + 1);
+        if (prof) g_prof.launches += kernels;
     };
     auto none = [] { return cudaSuccess; };
     if (mode == kOnline) {
         // intra first (its Tail-16 scores drive the selection), then the rest of the pipeline
-        stage(2, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
-        stage(8, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
-        stage(0, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
-        stage(1, [&] { return launch_prefix(pb, ws); });
-        stage(3, [&] { return tc ? launch_wbuild_tc(pb, ws) : launch_wbuild(pb, ws); });
+        stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
+        stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
+        stage(1, 1, [&] { return launch_prefix(pb, ws); });
+        stage(3, 1, [&] { return tc ? launch_wbuild_tc(pb, ws) : launch_wbuild(pb, ws); });
     } else {
-        stage(0, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
-        stage(1, [&] { return launch_prefix(pb, ws); });
-        stage(2, [&] { return tc ? launch_intra_tc(pb, ws, false) : launch_intra(pb, ws); });
-        stage(3, [&] { return tc ? none() : launch_wbuild(pb, ws); });  // bf16: W is built inside intra
-        stage(8, none);
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
+        stage(1, 1, [&] { return launch_prefix(pb, ws); });
+        stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, false) : launch_intra(pb, ws); });
+        stage(3, tc ? 0 : 1, [&] { return tc ? none() : launch_wbuild(pb, ws); });  // bf16: W is built inside intra
+        stage(8, 0, none);
     }
-    stage(4, [&] { return tc ? launch_scan_tc(pb, ws, 0) : none(); });
-    stage(5, [&] { return tc ? launch_scan_tc(pb, ws, 1) : none(); });
-    stage(6, [&] { return tc ? launch_scan_tc(pb, ws, 2) : launch_scan(pb, ws); });
-    stage(7, [&] { return tc ? launch_output_tc(pb, ws) : launch_output(pb, ws); });
+    stage(4, tc ? 1 : 0, [&] { return tc ? launch_scan_tc(pb, ws, 0) : none(); });
+    stage(5, tc ? 1 : 0, [&] { return tc ? launch_scan_tc(pb, ws, 1) : none(); });
+    stage(6, 1, [&] { return tc ? launch_scan_tc(pb, ws, 2) : launch_scan(pb, ws); });
+    stage(7, 1, [&] { return tc ? launch_output_tc(pb, ws) : launch_output(pb, ws); });
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -220,6 +223,25 @@ gdn_status read_status(const int32_t *counts, void *stream) {
     if (cudaMemcpy(host, counts, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
     if (host[2] & kStatusTimeout) return GDN_ERR_TIMEOUT;
     return host[2] ? GDN_ERR_CAPACITY : GDN_OK;
+}
+
+// Device staging of gdn_prefill_host: q, k, v, beta, g, h0, mask, o, s_final (each 256-byte aligned).
+struct HostStaging {
+    size_t q, k, v, beta, g, h0, mask, o, s, total;
+};
+
+HostStaging host_staging(const gdn_shape *sh) {
+    const size_t es = elem_size(sh->dtype), BT = (size_t)sh->B * sh->T;
+    const size_t qk = BT * sh->Nq * sh->d * es, vo = BT * sh->Nv * sh->dv * es, bg = BT * sh->Nv * sizeof(float);
+    const size_t st = (size_t)sh->B * sh->Nv * sh->d * sh->dv * sizeof(float);
+    const size_t mk = (size_t)sh->B * sh->Nq * (sh->T / kChunk);
+    HostStaging h;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+    h.q = take(qk); h.k = take(qk); h.v = take(vo); h.beta = take(bg); h.g = take(bg);
+    h.h0 = take(st); h.mask = take(mk); h.o = take(vo); h.s = take(st);
+    h.total = off;
+    return h;
 }
 
 }  // namespace
@@ -280,6 +302,54 @@ gdn_status gdn_prefill_sparse(const gdn_shape *shape, const void *q, const void 
                               size_t workspace_bytes, void *stream) {
     return run_prefill(shape, q, k, v, beta, g, h0, mask, nullptr, kSparse, solver, o, s_final, score, nullptr,
                        nullptr, workspace, workspace_bytes, stream);
+}
+
+size_t gdn_prefill_host_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse) {
+    const size_t w = gdn_workspace_bytes(shape, solver, sparse ? 1 : 0);
+    return w ? w + host_staging(shape).total : 0;
+}
+
+gdn_status gdn_prefill_host(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *beta,
+                            const float *g, const float *h0, const uint8_t *mask, gdn_solver solver, void *o,
+                            float *s_final, void *workspace, size_t workspace_bytes, void *stream) {
+    gdn_status st = check_shape(shape);
+    if (st != GDN_OK) return st;
+    if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return GDN_ERR_DTYPE;
+    if (shape->B == 0) return GDN_OK;
+    const bool sparse = mask != nullptr;
+    const size_t wbytes = gdn_workspace_bytes(shape, solver, sparse ? 1 : 0);
+    const HostStaging hs = host_staging(shape);
+    if (!workspace) return GDN_ERR_NULL;
+    if (((uintptr_t)workspace % kAlign) != 0) return GDN_ERR_ALIGN;
+    if (workspace_bytes < wbytes + hs.total) return GDN_ERR_WORKSPACE;
+    const bool has_tokens = shape->T > 0;
+    if (!s_final || (has_tokens && (!q || !k || !v || !beta || !g || !o))) return GDN_ERR_NULL;
+    if (!device_ok()) return GDN_ERR_DEVICE;
+    char *stg = (char *)workspace + wbytes;
+    const cudaStream_t cs = (cudaStream_t)stream;
+    const size_t es = elem_size(shape->dtype), BT = (size_t)shape->B * shape->T;
+    const size_t qk = BT * shape->Nq * shape->d * es, vo = BT * shape->Nv * shape->dv * es;
+    const size_t bg = BT * shape->Nv * sizeof(float);
+    const size_t stb = (size_t)shape->B * shape->Nv * shape->d * shape->dv * sizeof(float);
+    const size_t mk = (size_t)shape->B * shape->Nq * (shape->T / kChunk);
+    cudaError_t e = cudaSuccess;
+    auto h2d = [&](size_t off, const void *src, size_t n) {
+        if (e == cudaSuccess && n) e = cudaMemcpyAsync(stg + off, src, n, cudaMemcpyHostToDevice, cs);
+    };
+    if (has_tokens) {
+        h2d(hs.q, q, qk); h2d(hs.k, k, qk); h2d(hs.v, v, vo); h2d(hs.beta, beta, bg); h2d(hs.g, g, bg);
+        if (sparse) h2d(hs.mask, mask, mk);
+    }
+    if (h0) h2d(hs.h0, h0, stb);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    st = run_prefill(shape, stg + hs.q, stg + hs.k, stg + hs.v, (const float *)(stg + hs.beta),
+                     (const float *)(stg + hs.g), h0 ? (const float *)(stg + hs.h0) : nullptr,
+                     sparse ? (const uint8_t *)(stg + hs.mask) : nullptr, nullptr, sparse ? kSparse : kDense,
+                     solver, stg + hs.o, (float *)(stg + hs.s), nullptr, nullptr, nullptr, workspace, wbytes, stream);
+    if (st != GDN_OK) return st;
+    if (has_tokens) e = cudaMemcpyAsync(o, stg + hs.o, vo, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(s_final, stg + hs.s, stb, cudaMemcpyDeviceToHost, cs);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 gdn_status gdn_prefill_sparse_online(const gdn_shape *shape, const void *q, const void *k, const void *v,
@@ -352,11 +422,13 @@ gdn_status gdn_profile_enable(int enable) {
     }
     g_prof.on = enable != 0;
     g_prof.used = 0;
+    g_prof.launches = 0;
     return GDN_OK;
 }
 
-gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills) {
+gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills, int64_t *n_launches) {
     if (!stage_ms || !n_prefills) return GDN_ERR_NULL;
+    if (n_launches) *n_launches = g_prof.launches;
     if (n_stages < 0 || n_stages > kStages) return GDN_ERR_SHAPE;
     for (int j = 0; j < n_stages; ++j) stage_ms[j] = 0.f;
     *n_prefills = g_prof.created ? g_prof.used : 0;
@@ -370,6 +442,7 @@ gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefil
         }
     }
     g_prof.used = 0;
+    g_prof.launches = 0;
     return GDN_OK;
 }
 

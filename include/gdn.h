@@ -176,6 +176,26 @@ GDN_API gdn_status gdn_prefill_sparse_online(const gdn_shape *shape,
                                      int32_t *tier_out, void *workspace, size_t workspace_bytes,
                                      void *stream);
 
+/* Prefill with HOST inputs and outputs: the same computation as
+ * gdn_prefill_sparse (mask != NULL) or gdn_prefill_dense (mask == NULL), with
+ * q, k, v, beta, g, h0 (may be NULL), mask and the outputs o, s_final in host
+ * memory, laid out as in those calls.  On `stream` the call enqueues one
+ * cudaMemcpyAsync per input into device staging carved from the workspace, the
+ * prefill, and one cudaMemcpyAsync per output back to the host; it returns
+ * without waiting (synchronise the stream before reading o and s_final).  Host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister): otherwise
+ * the copies do not overlap with other work.  Calls on different streams with
+ * different workspaces run concurrently, so a caller can overlap one call's
+ * copies with another call's kernels.  Workspace (device, 256-byte aligned):
+ * gdn_prefill_host_workspace_bytes(shape, solver, mask != NULL). */
+GDN_API gdn_status gdn_prefill_host(const gdn_shape *shape,
+                            const void *q, const void *k, const void *v,
+                            const float *beta, const float *g, const float *h0,
+                            const uint8_t *mask, gdn_solver solver,
+                            void *o, float *s_final, void *workspace, size_t workspace_bytes,
+                            void *stream);
+GDN_API size_t gdn_prefill_host_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse);
+
 /* Allocation-free event-sparse prefill.  The paper has no counterpart: this
  * is a deployment aid for callers that cannot allocate device memory -- for
  * example a plugin inside a host runtime that owns all device memory and
@@ -233,8 +253,10 @@ GDN_API gdn_status gdn_profile_enable(int enable);
 
 /* Synchronises on the recorded events, writes the summed milliseconds of each
  * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 9),
- * the number of recorded prefills to *n_prefills, and clears the records. */
-GDN_API gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills);
+ * the number of recorded prefills to *n_prefills, the number of kernels those
+ * prefills launched to *n_launches (may be NULL), and clears the records. */
+GDN_API gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills,
+                                    int64_t *n_launches);
 
 /* Library ABI version (major*10000 + minor*100 + patch). */
 GDN_API int32_t gdn_version(void);

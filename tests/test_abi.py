@@ -139,3 +139,23 @@ def test_online_workspace_and_validation(lib):
     assert scored(shape(), score=FAKE + 4) == 4
     assert scored(shape(), ws_bytes=64) == 5
     assert scored(shape(B=0), score=0, g=0, mask=0) == 0
+
+
+def test_host_prefill_validation(lib):
+    s = shape()
+    dev_bytes = gdn.gdn_workspace_bytes(s, "block_adj", 1)
+    host_bytes = lib.gdn_prefill_host_workspace_bytes(ctypes.byref(s), 1, 1)
+    # staging holds q, k, v, beta, g, h0, mask, o and s_final on top of the workspace
+    assert host_bytes > dev_bytes + 2 * (4096 * 16 * 128 * 2) + 2 * (4096 * 32 * 128 * 2)
+    f = ctypes.c_void_p(FAKE)
+
+    def host(sh, ws=FAKE, ws_bytes=1 << 40, q=FAKE):
+        return lib.gdn_prefill_host(ctypes.byref(sh), ctypes.c_void_p(q), f, f, f, f, None, f, 1, f, f,
+                                    ctypes.c_void_p(ws), ws_bytes, None)
+
+    assert host(shape(T=100)) == 6
+    assert host(shape(), ws=0) == 1
+    assert host(shape(), ws=FAKE + 16) == 4
+    assert host(shape(), ws_bytes=dev_bytes) == 5     # the staging does not fit
+    assert host(shape(), q=0) == 1
+    assert host(shape(B=0), ws=0, q=0) == 0

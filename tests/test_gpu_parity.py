@@ -199,3 +199,19 @@ def test_long_context_T131072_layer_sampled_pair(layer):
     ref = oracle_run(y, "block_adj")
     got = {"o": res["o"][:, :, 2 * p:2 * p + 2], "s_final": res["s_final"][:, 2 * p:2 * p + 2]}
     assert_close(got, ref, "bf16", f"T=131072 layer {layer} pair {p}")
+
+
+@pytest.mark.parametrize("dtype,sparse", [("bf16", True), ("bf16", False), ("f32", True)])
+def test_host_buffer_prefill_equals_device_path(dtype, sparse):
+    # gdn_prefill_host: the same kernels behind host copies, so the same bits
+    x = gdn_synth.make_inputs(2, 640, 16, 32, dtype=dtype, seed=26, mask="beta", with_h0=True)
+    res = run_gpu(x, sparse=sparse)
+    st = torch.bfloat16 if dtype == "bf16" else torch.float32
+    h = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dt).pin_memory()
+    stream = torch.cuda.Stream()
+    o, s = gdn.gdn_prefill_host(h(x.q, st), h(x.k, st), h(x.v, st), h(x.beta, torch.float32),
+                                h(x.g, torch.float32), h(x.mask, torch.uint8) if sparse else None,
+                                h0=h(x.h0, torch.float32), stream=stream)
+    stream.synchronize()
+    assert np.array_equal(o.float().numpy().astype(np.float64), res["o"])
+    assert np.array_equal(s.numpy().astype(np.float64), res["s_final"])
