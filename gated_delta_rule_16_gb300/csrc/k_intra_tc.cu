@@ -29,9 +29,12 @@ constexpr uint32_t OFF_K = 0;            // K tile: 2 K-slabs [128 tok][64 d]
 constexpr uint32_t OFF_V = 2 * kSlab;    // V tiles of the two heads: 2 MN-stacks [128 tok][64 dv] each
 constexpr uint32_t OFF_A = 6 * kSlab;    // C diag(beta) bf16: 2 K-slabs [128 t][64 s]
 constexpr uint32_t OFF_F = 8 * kSlab;    // fp32 work area
-constexpr int MS = kChunk + 1;           // row stride of the fp32 64x64 tiles
-constexpr uint32_t F_M = 0;                              // [2][64][65] M
-constexpr uint32_t F_C = F_M + 2 * kChunk * MS * 4;      // [2][64][65] C
+// Row stride of the fp32 64x64 tiles: 68 floats keeps rows 16-byte aligned, and a
+// 16-byte access by eight threads owning eight consecutive rows (one shared-memory
+// wavefront) touches 8 x 4 distinct banks.
+constexpr int MS = kChunk + 4;
+constexpr uint32_t F_M = 0;                              // [2][64][68] M
+constexpr uint32_t F_C = F_M + 2 * kChunk * MS * 4;      // [2][64][68] C
 constexpr uint32_t F_T = F_C + 2 * kChunk * MS * 4;      // [2][3][256] block products
 constexpr uint32_t F_B = F_T + 2 * 3 * 256 * 4;          // [2 heads][128] beta
 constexpr uint32_t F_G = F_B + 2 * 128 * 4;              // [2 heads][128] g
@@ -54,38 +57,53 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
+    acc.x += a * b.x;
+    acc.y += a * b.y;
+    acc.z += a * b.z;
+    acc.w += a * b.w;
+}
+
 // Off-diagonal 16x16 blocks at distance OFF of both chunks' C (Eq. 7 generalised):
 // C_ij = -C_ii (sum_{k=j}^{i-1} M_ik C_kj), i = j + OFF, once every block closer to
-// the diagonal is known.  512 threads: one chunk per half, one element of a block each.
+// the diagonal is known.  Thread (chunk, block, row, column quad): 4 outputs from
+// 16-byte shared-memory loads (a row of M or C_ii, a quad of a row of C or T).
 template <int OFF>
 __device__ __forceinline__ void offdiag_blocks(const float *Ms, float *Cs, float *Tb, int tid) {
     constexpr int NB = 4 - OFF;
-    const int cc = tid >> 8, e = tid & 255;  // 512 threads: chunk, element of the 16x16 block
-    const int rr = e >> 4, col = e & 15;
-    {
+    const bool act = tid < 2 * NB * 64;
+    const int cc = tid / (NB * 64), rem = tid % (NB * 64);
+    const int bi = rem >> 6, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
+    const int ib = bi + OFF, jb = bi;
+    if (act) {  // T = sum_k M_{ib,k} C_{k,jb}: row rr, columns q4 .. q4+3
+        const float *Mr = Ms + (cc * kChunk + ib * kBlk + rr) * MS + jb * kBlk;
+        const float *Cc = Cs + (cc * kChunk + jb * kBlk) * MS + jb * kBlk + q4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int bi = 0; bi < NB; ++bi) {
-            const int ib = bi + OFF, jb = bi;
-            const float *Mr = Ms + (cc * kChunk + ib * kBlk + rr) * MS + jb * kBlk;
-            const float *Cc = Cs + (cc * kChunk + jb * kBlk) * MS + jb * kBlk + col;
-            float acc = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < kBlk * OFF; ++kk) acc += Mr[kk] * Cc[kk * MS];
-            Tb[(cc * NB + bi) * 256 + e] = acc;
+        for (int k4 = 0; k4 < kBlk * OFF; k4 += 4) {
+            const float4 m = ld4(Mr + k4);
+            fma4(acc, m.x, ld4(Cc + (k4 + 0) * MS));
+            fma4(acc, m.y, ld4(Cc + (k4 + 1) * MS));
+            fma4(acc, m.z, ld4(Cc + (k4 + 2) * MS));
+            fma4(acc, m.w, ld4(Cc + (k4 + 3) * MS));
         }
+        *reinterpret_cast<float4 *>(Tb + (cc * NB + bi) * 256 + rr * 16 + q4) = acc;
     }
     __syncthreads();
-    {
+    if (act) {  // C_{ib,jb} = -C_{ib,ib} T
+        float *Cr = Cs + (cc * kChunk + ib * kBlk + rr) * MS;
+        const float *Tt = Tb + (cc * NB + bi) * 256 + q4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int bi = 0; bi < NB; ++bi) {
-            const int ib = bi + OFF, jb = bi;
-            float *Cr = Cs + (cc * kChunk + ib * kBlk + rr) * MS;
-            const float *Tt = Tb + (cc * NB + bi) * 256 + col;
-            float acc = 0.f;
-#pragma unroll
-            for (int m = 0; m < kBlk; ++m) acc += Cr[ib * kBlk + m] * Tt[m * 16];
-            Cr[jb * kBlk + col] = -acc;
+        for (int m4 = 0; m4 < kBlk; m4 += 4) {
+            const float4 c = ld4(Cr + ib * kBlk + m4);
+            fma4(acc, c.x, ld4(Tt + (m4 + 0) * 16));
+            fma4(acc, c.y, ld4(Tt + (m4 + 1) * 16));
+            fma4(acc, c.z, ld4(Tt + (m4 + 2) * 16));
+            fma4(acc, c.w, ld4(Tt + (m4 + 3) * 16));
         }
+        *reinterpret_cast<float4 *>(Cr + jb * kBlk + q4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
 }
@@ -169,7 +187,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         if (tid == 0) bulk_wait_read();  // the W store of the previous head has left the A tile
         if (tid < 128) bgs[tid] = bet[tid] * ex2(gg[tid]);
         if (tid < 2) ssum[tid] = 0.f;
-        for (int idx = tid; idx < 2 * kChunk * MS; idx += kThreads) Cs[idx] = 0.f;
         __syncthreads();
         // 1. M from the Gram block of the row's chunk: thread (row, half) covers 32 columns
         if (hh == 0 && !mbar_wait(&bar_g, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
@@ -180,12 +197,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             tmem_ld32(tmem_addr(tbase, quarter * 32, TM_G + 64 * ct + 32 * hf), gv);
             tmem_ld_wait();
             const float bt = bet[row], gt = gg[row];
-            float *mrow = Ms + (ct * kChunk + tl) * MS;
+            float4 *mrow = reinterpret_cast<float4 *>(Ms + (ct * kChunk + tl) * MS + 32 * hf);
 #pragma unroll
             for (int q2 = 0; q2 < 32; ++q2) {
                 const int s = 32 * hf + q2;
-                mrow[s] = s < tl ? bt * gv[q2] * ex2(gt - gg[64 * ct + s]) : (s == tl ? 1.f : 0.f);
+                gv[q2] = s < tl ? bt * gv[q2] * ex2(gt - gg[64 * ct + s]) : (s == tl ? 1.f : 0.f);
             }
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                mrow[q4] = make_float4(gv[4 * q4], gv[4 * q4 + 1], gv[4 * q4 + 2], gv[4 * q4 + 3]);
         }
         __syncthreads();
         // 2. solve.  Diagonal 16x16 blocks by forward substitution: warp w < 4 takes
@@ -227,10 +247,16 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 if (slab == ct) {  // warp-uniform: these columns belong to the row's own chunk
 #pragma unroll
                     for (int k0 = 0; k0 < 32; k0 += 8) {
-                        float w[8];
-#pragma unroll
-                        for (int q2 = 0; q2 < 8; ++q2) w[q2] = crow[c0s + k0 + q2] * f[c0s + k0 + q2];
-                        st_sw128_8(dst, row, c0s + k0, w);
+                        // blocks the solver does not keep (and those above the diagonal) are zero
+                        const int col = c0s + k0, jb = col >> 4, ib = tl >> 4;
+                        float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        if (jb <= ib && (max_off == 3 || jb + 1 >= ib)) {
+                            const float4 c0 = ld4(crow + col), c1 = ld4(crow + col + 4);
+                            const float4 f0 = ld4(f + col), f1 = ld4(f + col + 4);
+                            w[0] = c0.x * f0.x; w[1] = c0.y * f0.y; w[2] = c0.z * f0.z; w[3] = c0.w * f0.w;
+                            w[4] = c1.x * f1.x; w[5] = c1.y * f1.y; w[6] = c1.z * f1.z; w[7] = c1.w * f1.w;
+                        }
+                        st_sw128_8(dst, row, col, w);
                     }
                 } else {
                     const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
