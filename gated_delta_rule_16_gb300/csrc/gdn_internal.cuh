@@ -69,7 +69,7 @@ struct Workspace {
     void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks (bf16 on the tensor-core path)
     void *W;                   // [ev_cap, 2, 64, d] dtype, deferred W of events
-    void *snap;                // [snap_cap, 2, d, dv] post-event state snapshots (fp32; bf16 for bf16 storage)
+    void *snap;                // post-event state snapshots: fp32 [snap_cap, 2, d, dv]; bf16 storage: S^T [snap_cap, 2, dv, d]
     // tensor-core scan (bf16 storage only; NR = ceil(C / kRunChunks))
     void *amap;                // [R, 2, NR, 128, 128] bf16: A_r^T of each run
     float *bmap;               // [R, 2, NR, 128, 128] B_r^T of each run

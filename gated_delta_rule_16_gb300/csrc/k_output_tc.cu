@@ -5,7 +5,7 @@
 // c = 2r and c+1) against 128 key tokens.  TMEM holds three 128x128 fp32
 // accumulators:
 //   QK  = Q K^T                   (A: Q [tok][d] K-major; B: K [tok][d] K-major), shared by the pair
-//   QS  = Q S_c                   (B: snapshot S [d][dv] bf16, MN-major)
+//   QS  = Q S_c                   (B: snapshot S^T [dv][d] bf16, K-major)
 //   AU  = A U'                    (A: decayed, masked QK in bf16, K-major; B: U' [tok][dv] MN-major)
 // per value head, where the mask/decay of A is
 //   same chunk, j <= i : 2^(g_i - g_j);   i in c+1, j in c : 2^(g_i + gamma_c - g_j);   else 0
@@ -24,8 +24,8 @@ using namespace tc;
 constexpr int kThreads = 512;  // 16 warps: 4 per TMEM lane quarter, 32 columns each
 constexpr uint32_t kSlab = 16384;          // [128 rows][128 B]
 constexpr uint32_t OFF_Q = 0;              // Q: 2 K-slabs
-constexpr uint32_t OFF_K = 2 * kSlab;      // K: 2 K-slabs; later S of head 1 (2 MN-stacks)
-constexpr uint32_t OFF_S0 = 4 * kSlab;     // S of head 0: 2 MN-stacks [128 d][64 dv]
+constexpr uint32_t OFF_K = 2 * kSlab;      // K: 2 K-slabs; later S^T of head 1 (2 K-slabs)
+constexpr uint32_t OFF_S0 = 4 * kSlab;     // S^T of head 0: 2 K-slabs [128 dv][64 d]
 constexpr uint32_t OFF_U0 = 6 * kSlab;     // U' of head 0: 2 MN-stacks [128 tok][64 dv]
 constexpr uint32_t OFF_U1 = 8 * kSlab;     // U' of head 1
 constexpr uint32_t OFF_A = 10 * kSlab;     // decayed masked A: 2 K-slabs [128 q][64 k]
@@ -106,15 +106,15 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tbase = tmem_base;
 
-    // initial-state path (no predecessor event, h0 given): S = h0 in bf16, MN-major stacks
+    // initial-state path (no predecessor event, h0 given): S^T = h0^T in bf16, K-major slabs
     auto fill_h0 = [&](int hh, uint8_t *dst) {
         const float *src = a.h0 + ((int64_t)b * a.Nv + 2 * p + hh) * (kDim * kDim);
-        for (int idx = tid; idx < kDim * 16; idx += kThreads) {  // (d row, 8-wide dv chunk)
-            const int d = idx >> 4, ch = idx & 15;
+        for (int idx = tid; idx < kDim * 16; idx += kThreads) {  // (dv row, 8-wide d chunk)
+            const int dv = idx & 127, ch = idx >> 7;
             float v[8];
 #pragma unroll
-            for (int q2 = 0; q2 < 8; ++q2) v[q2] = src[d * kDim + ch * 8 + q2];
-            st_sw128_8(dst + (ch >> 3) * kSlab, d, (ch & 7) * 8, v);
+            for (int q2 = 0; q2 < 8; ++q2) v[q2] = src[(ch * 8 + q2) * kDim + dv];
+            st_sw128_8(dst + (ch >> 3) * kSlab, dv, (ch & 7) * 8, v);
         }
         fence_async_smem();
     };
@@ -191,7 +191,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
                 if (has_s[hh])
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16(tbase + TM_QS, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
-                                 mnmajor_desc(smem_addr(st), ks, kSlab), id_km, ks > 0);
+                                 kmajor_desc(smem_addr(st), ks, kSlab), id_kk, ks > 0);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tbase + TM_AU, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
                              mnmajor_desc(smem_addr(ut), ks, kSlab), id_km, ks > 0);

@@ -19,14 +19,21 @@
 //
 // Layout.  Columns of S evolve independently, so the CTA works on S^T: TMEM
 // lane / state row = a column of S (d_v index), 128 rows; 512 threads, thread
-// (row, segment) holds 32 of the row's 128 fp32 entries in registers.  Per event:
+// (row, segment) handles 32 of the row's 128 entries.  The state lives in TMEM
+// (fp32, 128 columns), which keeps the registers per thread low enough for two
+// CTAs per SM: one CTA's barriers and MMA round trips overlap the other's work.
+// Per event:
+//   S^T <- 2^(P_c - P_cur) S^T (gap decay): read from TMEM, written as the bf16
+//          operand of MMA1, and 2^gamma S^T written back to TMEM
 //   MMA1  U'^T_acc[128 x 64]  = S^T[128 x 128] . W^T      (A: S^T bf16 K-major; B: W [t][d] K-major)
 //   U'^T = U^T - U'^T_acc;  U''^T = U'^T * 2^(gamma - g_t)        (registers)
-//   MMA2  dS^T[128 x 128]     = U''^T[128 x 64] . K        (A: U''^T K-major; B: K [t][d] MN-major)
-//   S^T <- 2^gamma S^T + dS^T                                      (registers)
-// W, K and U tiles of the next event are TMA-prefetched (double buffer).
-// Snapshots are stored in bf16 as S [d][dv], the MN-major operand the output
-// kernel's Q S product loads by TMA.
+//   MMA2  S^T += U''^T[128 x 64] . K                      (A: U''^T K-major; B: K [t][d] MN-major)
+// The W, K and U tiles are single-buffered; each buffer is refilled for the next
+// event as soon as its reader is done (W after MMA1, U after the U' pass, K after
+// MMA2), so every load has most of an event to land.  U' is written over U in the
+// U tile and TMA-stored.  Snapshots are stored in bf16 as S^T [dv][d] (each thread's
+// 32 state entries are 64 contiguous bytes), the K-major operand of the output
+// kernel's Q S product.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -41,14 +48,12 @@ constexpr int kRun = kRunChunks;
 constexpr uint32_t kSlab = 16384;        // [128 rows][128 B]
 constexpr uint32_t OFF_A1 = 0;           // S^T bf16, K-major, 2 slabs
 constexpr uint32_t OFF_A2 = 2 * kSlab;   // U''^T bf16, K-major, 1 slab
-constexpr uint32_t OFF_BUF = 3 * kSlab;  // two event buffers follow
-constexpr uint32_t BUF_W = 0;            // W [64 t][128 d]: 2 K-slabs of [64][128 B], 8192 apart
-constexpr uint32_t BUF_K = 16384;        // K MN-major: 2 stacks of [64 t][64 d], 8192 apart
-constexpr uint32_t BUF_U = 32768;        // U [64 t][128 dv] bf16, unswizzled
-constexpr uint32_t BUF_BYTES = 49152;
-constexpr uint32_t kRunSmem = 1024 + OFF_BUF + 2 * BUF_BYTES;
+constexpr uint32_t OFF_W = 3 * kSlab;    // W [64 t][128 d]: 2 K-slabs of [64][128 B], 8192 apart
+constexpr uint32_t OFF_K = 4 * kSlab;    // K MN-major: 2 stacks of [64 t][64 d], 8192 apart
+constexpr uint32_t OFF_U = 5 * kSlab;    // U [64 t][128 dv] bf16, unswizzled
+constexpr uint32_t kRunSmem = 1024 + 6 * kSlab;
 constexpr uint32_t TM_U = 0;             // TMEM columns [0, 64): U'^T accumulator
-constexpr uint32_t TM_S = 64;            // TMEM columns [64, 192): dS^T accumulator
+constexpr uint32_t TM_S = 128;           // TMEM columns [128, 256): the state S^T
 constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab;
 constexpr int kMaxRuns = 1024;  // C <= 16384 chunks
 
@@ -63,7 +68,7 @@ struct ScanParams {
     __nv_bfloat16 *amap;    // [R,2,NR,128,128] A_r^T (row m' = column m' of A_r)
     float *bmap;            // [R,2,NR] tiles of B_r^T, column-quad layout (quad_index)
     float *entry;           // [R,2,NR] tiles of S_r^T entering each run, column-quad layout
-    __nv_bfloat16 *snap;    // [snap_cap,2,128 d,128 dv] post-event states (bf16)
+    __nv_bfloat16 *snap;    // [snap_cap,2,128 dv,128 d] post-event states S^T (bf16)
     float *s_final;         // [B,Nv,128 d,128 dv]
     int32_t *status;
     int P_, T_, Nv, C, NR;
@@ -80,13 +85,13 @@ __device__ __forceinline__ void fail(const ScanParams &a, int *abort_flag) {
 }
 
 // grid: (runs NR, map mode: 2 heads x {homog, inhom} | fix-up: 2 heads, CSR rows R)
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tK,
                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tA, ScanParams a,
                 int fixup) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
-    __shared__ uint64_t bar_tma[2], bar_mma1, bar_mma2;
+    __shared__ uint64_t bar_w, bar_k, bar_u, bar_mma1, bar_mma2, bar_drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s, n_ev_s, e_first_s;
     __shared__ int ev_c[kRun], ev_slot[kRun];
@@ -123,10 +128,12 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
     if (tid <= c_hi - c_lo) Pl[tid] = Pu[c_lo + tid];
     if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
+        mbar_init(&bar_w, 1);
+        mbar_init(&bar_k, 1);
+        mbar_init(&bar_u, 1);
         mbar_init(&bar_mma1, 1);
         mbar_init(&bar_mma2, 1);
+        mbar_init(&bar_drain, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc<256>(&tmem_base);
@@ -141,43 +148,70 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         if (t == 0) gamk[k] = gam;
     }
     const uint32_t tbase = tmem_base;
+    const uint32_t t_s = tmem_addr(tbase, quarter * 32, TM_S + cs);
     uint8_t *A1 = sm + OFF_A1;
     uint8_t *A2 = sm + OFF_A2;
-    const uint32_t tx_bytes = mode == kModeHomog ? 32768u : 49152u;
-    auto issue_tma = [&](int k) {
-        uint8_t *buf = sm + OFF_BUF + (k & 1) * BUF_BYTES;
+    const bool with_u = mode != kModeHomog;
+    // loads of event k (thread 0), each once its buffer is free
+    auto load_w = [&](int k) {
         const int wrow = ((e_first + k) * 2 + hh) * kChunk;
-        const int tok = b * a.T_ + ev_c[k] * kChunk;
-        uint64_t *bar = &bar_tma[k & 1];
-        mbar_arrive_expect_tx(bar, tx_bytes);
-        tma_load_3d(buf + BUF_W, &tW, 0, wrow, 0, bar);
-        tma_load_3d(buf + BUF_W + 8192, &tW, 64, wrow, 0, bar);
-        tma_load_3d(buf + BUF_K, &tK, 0, p, tok, bar);
-        tma_load_3d(buf + BUF_K + 8192, &tK, 64, p, tok, bar);
-        if (mode != kModeHomog) tma_load_3d(buf + BUF_U, &tU, 0, h, tok, bar);
+        mbar_arrive_expect_tx(&bar_w, 16384u);
+        tma_load_3d(sm + OFF_W, &tW, 0, wrow, 0, &bar_w);
+        tma_load_3d(sm + OFF_W + 8192, &tW, 64, wrow, 0, &bar_w);
     };
-    int tma_issued = 0;  // thread 0: events whose tiles were requested
+    auto load_u = [&](int k) {
+        mbar_arrive_expect_tx(&bar_u, 16384u);
+        tma_load_3d(sm + OFF_U, &tU, 0, h, b * a.T_ + ev_c[k] * kChunk, &bar_u);
+    };
+    auto load_k = [&](int k) {
+        const int tok = b * a.T_ + ev_c[k] * kChunk;
+        mbar_arrive_expect_tx(&bar_k, 16384u);
+        tma_load_3d(sm + OFF_K, &tK, 0, p, tok, &bar_k);
+        tma_load_3d(sm + OFF_K + 8192, &tK, 64, p, tok, &bar_k);
+    };
+    // thread 0: events whose tiles were requested, and completed waits it observed (for the drain)
+    int loads_w = 0, loads_u = 0, loads_k = 0, seen_w = 0, seen_k = 0, seen_u = 0;
     if (tid == 0) {
-        issue_tma(0);
-        tma_issued = 1;
-    }
-
-    float S[32];
-    if (mode == kModeHomog) {
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] = (cs + jj == row) ? 1.f : 0.f;
-    } else if (mode == kModeInhom) {
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] = 0.f;
-    } else {
-        const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase) + 8 * seg * 128 + row;
-#pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 x = src[v4 * 128];
-            S[4 * v4] = x.x; S[4 * v4 + 1] = x.y; S[4 * v4 + 2] = x.z; S[4 * v4 + 3] = x.w;
+        load_w(0);
+        load_k(0);
+        loads_w = loads_k = 1;
+        if (with_u) {
+            load_u(0);
+            loads_u = 1;
         }
     }
-    __syncthreads();  // dec[] complete
+    {   // the entering state, into TMEM
+        float S[32];
+        if (mode == kModeHomog) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) S[jj] = (cs + jj == row) ? 1.f : 0.f;
+        } else if (mode == kModeInhom) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) S[jj] = 0.f;
+        } else {
+            const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase) + 8 * seg * 128 + row;
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+                const float4 x = src[v4 * 128];
+                S[4 * v4] = x.x; S[4 * v4 + 1] = x.y; S[4 * v4 + 2] = x.z; S[4 * v4 + 3] = x.w;
+            }
+        }
+        tmem_st32(t_s, S);
+        tmem_st_wait();
+    }
+    __syncthreads();  // dec[] and gamk[] complete
+    auto snapshot = [&](int slot, const float (&S)[32]) {  // row `row` of S^T, columns cs .. cs+31
+        if (slot >= 0 && slot < a.snap_cap) {
+            uint4 *sn = reinterpret_cast<uint4 *>(a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim) + row * kDim + cs);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                __nv_bfloat162 p2[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) p2[u] = __floats2bfloat162_rn(S[8 * q + 2 * u], S[8 * q + 2 * u + 1]);
+                sn[q] = *reinterpret_cast<uint4 *>(p2);
+            }
+        }
+    };
 
     const uint32_t id1 = idesc_bf16(128, 64, false, false);
     const uint32_t id2 = idesc_bf16(128, 128, false, true);
@@ -185,116 +219,138 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     int k = 0;
     for (; k < n_ev; ++k) {
         const int c = ev_c[k];
-        uint8_t *buf = sm + OFF_BUF + (k & 1) * BUF_BYTES;
-        const float gap = ex2((float)(Pl[c - c_lo] - Pl[cur - c_lo]));
+        if (tid == 0 && k > 0 && k < n_ev) {  // K buffer free: MMA2 of the previous event completed
+            load_k(k);
+            loads_k = k + 1;
+        }
+        {   // the state entering chunk c
+            float S[32];
+            tmem_ld32(t_s, S);
+            tmem_ld_wait();
+            if (mode == kModeFixup && k > 0) snapshot(ev_slot[k - 1], S);  // the state after event k-1
+            const float gap = ex2((float)(Pl[c - c_lo] - Pl[cur - c_lo]));
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] *= gap;
+            for (int jj = 0; jj < 32; ++jj) S[jj] *= gap;
 #pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(A1 + slab * kSlab, row, cin + k0, &S[k0]);
+            for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(A1 + slab * kSlab, row, cin + k0, &S[k0]);
+            const float dg = ex2(gamk[k]);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) S[jj] *= dg;
+            tmem_st32(t_s, S);  // 2^gamma S_c: MMA2 accumulates the write onto it
+            tmem_st_wait();
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (abort_s) break;
         if (tid == 0) {
-            if (!mbar_wait(&bar_tma[k & 1], (k >> 1) & 1)) {
+            if (!mbar_wait(&bar_w, k & 1)) {
                 fail(a, &abort_s);
             } else {
+                seen_w = k + 1;
                 tc_fence_after();
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(A1), ks, kSlab),
-                             kmajor_desc(smem_addr(buf + BUF_W), ks, 8192), id1, ks > 0);
+                             kmajor_desc(smem_addr(sm + OFF_W), ks, 8192), id1, ks > 0);
                 mma_commit(&bar_mma1);
-                if (k + 1 < n_ev) {
-                    if (mode == kModeFixup) bulk_wait_read();  // U' of event k-1 left that buffer
-                    issue_tma(k + 1);
-                    tma_issued = k + 2;
-                }
             }
         }
-        __syncthreads();
-        if (abort_s) break;
         if (!mbar_wait(&bar_mma1, k & 1)) fail(a, &abort_s);
-        tc_fence_after();
-        float acc[16];
-        tmem_ld16(tmem_addr(tbase, quarter * 32, TM_U + 16 * seg), acc);
-        tmem_ld_wait();
-        __nv_bfloat16 *Ut = reinterpret_cast<__nv_bfloat16 *>(buf + BUF_U);
-        const float gam = gamk[k];
-        float up[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            const int tt = 16 * seg + t;
-            const float u = mode == kModeHomog ? 0.f : __bfloat162float(Ut[tt * kDim + row]);
-            const float v = u - acc[t];
-            if (mode == kModeFixup) Ut[tt * kDim + row] = __float2bfloat16_rn(v);  // U' replaces U in the tile
-            up[t] = v * dec[k][tt];
+        if (with_u) {
+            if (!mbar_wait(&bar_u, k & 1)) fail(a, &abort_s);
+            else if (tid == 0) seen_u = k + 1;
         }
+        tc_fence_after();
+        {
+            float acc[16];
+            tmem_ld16(tmem_addr(tbase, quarter * 32, TM_U + 16 * seg), acc);
+            tmem_ld_wait();
+            __nv_bfloat16 *Ut = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_U);
+            float up[16];
 #pragma unroll
-        for (int t0 = 0; t0 < 16; t0 += 8) st_sw128_8(A2, row, 16 * seg + t0, &up[t0]);
+            for (int t = 0; t < 16; ++t) {
+                const int tt = 16 * seg + t;
+                const float u = with_u ? __bfloat162float(Ut[tt * kDim + row]) : 0.f;
+                const float v = u - acc[t];
+                if (mode == kModeFixup) Ut[tt * kDim + row] = __float2bfloat16_rn(v);  // U' replaces U in the tile
+                up[t] = v * dec[k][tt];
+            }
+#pragma unroll
+            for (int t0 = 0; t0 < 16; t0 += 8) st_sw128_8(A2, row, 16 * seg + t0, &up[t0]);
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (abort_s) break;
         if (tid == 0) {
             tc_fence_after();
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tbase + TM_S, kmajor_desc(smem_addr(A2), ks, kSlab),
-                         mnmajor_desc(smem_addr(buf + BUF_K), ks, 8192), id2, ks > 0);
-            mma_commit(&bar_mma2);
-            if (mode == kModeFixup) {  // U' of this event back to the U buffer, in place
-                tma_store_3d(&tU, 0, h, b * a.T_ + c * kChunk, buf + BUF_U);
-                bulk_commit();
+            if (!mbar_wait(&bar_k, k & 1)) {
+                fail(a, &abort_s);
+            } else {
+                seen_k = k + 1;
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tbase + TM_S, kmajor_desc(smem_addr(A2), ks, kSlab),
+                             mnmajor_desc(smem_addr(sm + OFF_K), ks, 8192), id2, 1);
+                mma_commit(&bar_mma2);
+                if (mode == kModeFixup) {  // U' of this event back over U
+                    tma_store_3d(&tU, 0, h, b * a.T_ + c * kChunk, sm + OFF_U);
+                    bulk_commit();
+                }
+                if (k + 1 < n_ev) {
+                    load_w(k + 1);  // MMA1 is done with the W buffer
+                    loads_w = k + 2;
+                    if (with_u) {
+                        if (mode == kModeFixup) bulk_wait_read();  // the U' store has left the U buffer
+                        load_u(k + 1);
+                        loads_u = k + 2;
+                    }
+                }
             }
         }
         if (!mbar_wait(&bar_mma2, k & 1)) fail(a, &abort_s);
         tc_fence_after();
-        float d0[32];
-        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_S + cs), d0);
-        tmem_ld_wait();
-        const float dg = ex2(gam);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] = dg * S[jj] + d0[jj];
-        if (mode == kModeFixup) {
-            const int slot = ev_slot[k];
-            if (slot >= 0 && slot < a.snap_cap) {
-                __nv_bfloat16 *sn = a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) sn[(cs + jj) * kDim + row] = __float2bfloat16_rn(S[jj]);
-            }
-        }
         cur = c + 1;
-        tc_fence_before();
-        __syncthreads();
-        if (abort_s) break;
     }
-    if (!abort_s && mode != kModeFixup) {
-        const float fin = ex2((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] *= fin;
-        if (mode == kModeHomog) {
-            // A_r^T rows staged as the chain's MN-major operand image, then one TMA store
-#pragma unroll
-            for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(A1 + slab * kSlab, row, cin + k0, &S[k0]);
-            fence_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                const int yrow = (int)((((int64_t)i * 2 + hh) * a.NR + rho) * kDim);
-                tma_store_3d(&tA, 0, yrow, 0, A1);
-                tma_store_3d(&tA, 64, yrow, 0, A1 + kSlab);
-                bulk_commit();
-            }
+    __syncthreads();
+    if (!abort_s) {
+        float S[32];
+        tmem_ld32(t_s, S);
+        tmem_ld_wait();
+        if (mode == kModeFixup) {
+            snapshot(ev_slot[n_ev - 1], S);
         } else {
-            float4 *dst = reinterpret_cast<float4 *>(a.bmap + ubase) + 8 * seg * 128 + row;
+            const float fin = ex2((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-                dst[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+            for (int jj = 0; jj < 32; ++jj) S[jj] *= fin;
+            if (mode == kModeHomog) {
+                // A_r^T rows staged as the chain's MN-major operand image, then one TMA store
+#pragma unroll
+                for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(A1 + slab * kSlab, row, cin + k0, &S[k0]);
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    const int yrow = (int)((((int64_t)i * 2 + hh) * a.NR + rho) * kDim);
+                    tma_store_3d(&tA, 0, yrow, 0, A1);
+                    tma_store_3d(&tA, 64, yrow, 0, A1 + kSlab);
+                    bulk_commit();
+                }
+            } else {
+                float4 *dst = reinterpret_cast<float4 *>(a.bmap + ubase) + 8 * seg * 128 + row;
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4)
+                    dst[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+            }
         }
     }
     if (tid == 0) bulk_wait_read();  // the stores only need their shared-memory sources before exit
     if (abort_s && tid == 0) {
-        // drain: tiles still in flight into shared memory, and the MMAs issued so far
-        for (int kk = k + 1; kk < tma_issued; ++kk) mbar_wait(&bar_tma[kk & 1], (kk >> 1) & 1);
-        mma_commit(&bar_mma2);
-        mbar_wait(&bar_mma2, (k + 1) & 1);
+        // drain: tiles still in flight into shared memory (phases this thread has not seen
+        // complete), then every MMA issued so far (a commit arrives after all of them)
+        for (int kk = seen_w; kk < loads_w; ++kk) mbar_wait(&bar_w, kk & 1);
+        for (int kk = seen_k; kk < loads_k; ++kk) mbar_wait(&bar_k, kk & 1);
+        for (int kk = seen_u; kk < loads_u; ++kk) mbar_wait(&bar_u, kk & 1);
+        mma_commit(&bar_drain);
+        mbar_wait(&bar_drain, 0);
     }
     tc_fence_before();
     __syncthreads();
