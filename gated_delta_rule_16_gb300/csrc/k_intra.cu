@@ -170,30 +170,44 @@ intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__re
 // {snapshot slot or -1, state kind, 2^(P_2r - P_(e+1)) of both heads} where e is
 // the group's predecessor event (kind 1), or {-1, 2, 2^P_2r} when the group
 // starts from h0 (kind 2), or kind 0 (zero state).
-__global__ void prefix_kernel(const float *__restrict__ g, int T_, int Nv, int C, int P_, int G,
-                              const int32_t *__restrict__ grp_pred, const int32_t *__restrict__ snap_slot,
-                              const int32_t *__restrict__ ev_chunk, int64_t ev_cap, int64_t snap_cap, int has_h0,
-                              double *__restrict__ P, int4 *__restrict__ grp_info) {
+__global__ void __launch_bounds__(256)
+prefix_kernel(const float *__restrict__ g, int T_, int Nv, int C, int P_, int G,
+              const int32_t *__restrict__ grp_pred, const int32_t *__restrict__ snap_slot,
+              const int32_t *__restrict__ ev_chunk, int64_t ev_cap, int64_t snap_cap, int has_h0,
+              double *__restrict__ P, int4 *__restrict__ grp_info, int p_in_smem) {
+    extern __shared__ double Ps[];  // [2][C + 1]: P of both heads, for the group table (when it fits)
     const int bp = blockIdx.x, b = bp / P_, p = bp % P_;
-    const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = 2 * p + hh;
-    double *Pu = P + ((int64_t)b * Nv + h) * (C + 1);
-    if (lane == 0) Pu[0] = 0.0;
-    double carry = 0.0;
-    for (int c0 = 0; c0 < C; c0 += 32) {
-        const int c = c0 + lane;
-        double x = c < C ? (double)g[((int64_t)b * T_ + (int64_t)c * kChunk + kChunk - 1) * Nv + h] : 0.0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < 2) {  // warp hh scans head 2p + hh: the gate tails of 32 chunks per step, loads issued ahead
+        const int h = 2 * p + warp;
+        double *Pu = P + ((int64_t)b * Nv + h) * (C + 1);
+        double *Pl = p_in_smem ? Ps + warp * (C + 1) : Pu;
+        if (lane == 0) { Pu[0] = 0.0; Pl[0] = 0.0; }
+        double carry = 0.0;
+        for (int c0 = 0; c0 < C; c0 += 256) {
+            double x[8];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            for (int q = 0; q < 8; ++q) {
+                const int c = c0 + 32 * q + lane;
+                x[q] = c < C ? (double)g[((int64_t)b * T_ + (int64_t)c * kChunk + kChunk - 1) * Nv + h] : 0.0;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                double v = x[q];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += y;
+                }
+                const int c = c0 + 32 * q + lane;
+                if (c < C) { Pu[c + 1] = carry + v; Pl[c + 1] = carry + v; }
+                carry += __shfl_sync(0xffffffffu, v, 31);
+            }
         }
-        if (c < C) Pu[c + 1] = carry + x;
-        carry += __shfl_sync(0xffffffffu, x, 31);
     }
     if (!grp_info) return;
-    __syncthreads();  // P of both heads written by this CTA
-    const double *P0 = P + ((int64_t)b * Nv + 2 * p) * (C + 1);
+    __syncthreads();  // P of both heads written (shared memory, or global memory by this CTA)
+    const double *P0 = p_in_smem ? Ps : P + ((int64_t)b * Nv + 2 * p) * (C + 1);
     const double *P1 = P0 + (C + 1);
     for (int r = threadIdx.x; r < G; r += blockDim.x) {
         const int pred = grp_pred[(int64_t)bp * G + r];
@@ -236,9 +250,16 @@ cudaError_t launch_intra(const Problem &pb, const Workspace &ws) {
 
 cudaError_t launch_prefix(const Problem &pb, const Workspace &ws) {
     if (pb.R == 0) return cudaSuccess;
-    prefix_kernel<<<pb.R, 64, 0, pb.stream>>>(pb.g, pb.T, pb.Nv, pb.C, pb.P, pb.G, ws.grp_pred, ws.snap_slot,
-                                              ws.ev_chunk, ws.ev_cap, ws.snap_cap, pb.h0 != nullptr, ws.P,
-                                              (int4 *)ws.grp_info);
+    const size_t want = 2 * (size_t)(pb.C + 1) * sizeof(double);
+    const int in_smem = want <= 96 * 1024;  // else the group table reads P from global memory
+    const size_t smem = in_smem ? want : 0;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    prefix_kernel<<<pb.R, 256, smem, pb.stream>>>(pb.g, pb.T, pb.Nv, pb.C, pb.P, pb.G, ws.grp_pred, ws.snap_slot,
+                                                  ws.ev_chunk, ws.ev_cap, ws.snap_cap, pb.h0 != nullptr, ws.P,
+                                                  (int4 *)ws.grp_info, in_smem);
     return cudaGetLastError();
 }
 

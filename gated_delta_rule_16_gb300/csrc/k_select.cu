@@ -53,8 +53,27 @@ __device__ void block_exclusive_scan(const int *a, int *out, int n, int *warp_to
     __syncthreads();
 }
 
-__device__ __forceinline__ bool is_set(const uint8_t *mask, int64_t row, int C, int c) {
-    return mask == nullptr ? true : mask[row * C + c] != 0;
+// One warp stages the 0/1 bits of mask row `row` as 32-chunk words: the loads of
+// 512 chunks are issued together before the ballots (mask == NULL: all chunks set).
+__device__ __forceinline__ void stage_row(const uint8_t *__restrict__ mask, int64_t row, int C, int NW,
+                                          unsigned *wrow) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t *mr = mask ? mask + row * C : nullptr;
+    for (int c0 = 0; c0 < C; c0 += 512) {
+        bool v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int c = c0 + 32 * q + lane;
+            v[q] = c < C && (mr == nullptr || mr[c] != 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const unsigned bits = __ballot_sync(0xffffffffu, v[q]);
+            const int w = (c0 >> 5) + q;
+            if (lane == 0 && w < NW) wrow[w] = bits;
+        }
+    }
+    __syncwarp();
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -80,7 +99,13 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     // 1. events per row
     for (int i = warp; i < R; i += kWarps) {
         int n = 0;
-        for (int c = lane; c < C; c += 32) n += is_set(mask, i, C, c);
+        if (mask) {
+            const uint8_t *mr = mask + (int64_t)i * C;
+#pragma unroll 8
+            for (int c = lane; c < C; c += 32) n += mr[c] != 0;
+        } else {
+            n = C > lane ? (C - lane + 31) / 32 : 0;
+        }
 #pragma unroll
         for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
         if (lane == 0) cnt[i] = n;
@@ -108,12 +133,7 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     for (int j = warp; j < R; j += kWarps) {
         const int i = order[j];
         const int base = ptr[j];
-        for (int w = 0; w < NW; ++w) {
-            const int c = 32 * w + lane;
-            const unsigned bits = __ballot_sync(0xffffffffu, c < C && is_set(mask, i, C, c));
-            if (lane == 0) wrow[w] = bits;
-        }
-        __syncwarp();
+        stage_row(mask, i, C, NW, wrow);
         int run = 0, nref = 0;
         for (int w = 0; w < NW; ++w) {
             const int c = 32 * w + lane;
@@ -162,12 +182,7 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     for (int j = warp; j < R; j += kWarps) {
         const int i = order[j];
         const int base = ptr[j];
-        for (int w = 0; w < NW; ++w) {
-            const int c = 32 * w + lane;
-            const unsigned bits = __ballot_sync(0xffffffffu, c < C && is_set(mask, i, C, c));
-            if (lane == 0) wrow[w] = bits;
-        }
-        __syncwarp();
+        stage_row(mask, i, C, NW, wrow);
         int run = 0, rrun = refb[j];
         for (int w = 0; w < NW; ++w) {
             const int c = 32 * w + lane;
