@@ -62,6 +62,8 @@ def _load():
             lib.gdn_oracle_events.restype = ctypes.c_int
             lib.gdn_oracle_events.argtypes = [ctypes.c_int] * 3 + [U8, ctypes.c_int] + [I] * 7
             F = ctypes.POINTER(ctypes.c_float)
+            lib.gdn_oracle_decode.restype = ctypes.c_int
+            lib.gdn_oracle_decode.argtypes = [ctypes.c_int] * 5 + [D] * 7
             lib.gdn_oracle_select.restype = ctypes.c_int
             lib.gdn_oracle_select.argtypes = [ctypes.c_int] * 3 + [F, F, F, U8, I, I]
             _lib = lib
@@ -164,3 +166,22 @@ def select(score, gamma, eta=None):
     if rc != 0:
         raise ValueError("gdn_oracle_select rejected its arguments (needs 16 head pairs)")
     return {"mask": mask, "tier": tier, "k": tuple(int(v) for v in k)}
+
+
+def decode(q, k, v, beta, a, S):
+    """One decode step (Eqs. 1-4 with a one-token chunk; see gdn_oracle.c).
+
+    q, k [B, Nq, d]; v [B, Nv, dv]; beta, a [B, Nv] (a: the token's log2
+    retention); S [B, Nv, d, dv].  Returns dict o [B, Nv, dv], s [B, Nv, d, dv].
+    """
+    lib = _load()
+    q, k, v, beta, a = map(_f64, (q, k, v, beta, a))
+    S = np.array(S, dtype=np.float64, order="C")
+    B, Nq, d = q.shape
+    Nv, dv = v.shape[1], v.shape[2]
+    o = np.zeros((B, Nv, dv))
+    rc = lib.gdn_oracle_decode(B, Nq, Nv, d, dv, _dptr(q), _dptr(k), _dptr(v), _dptr(beta), _dptr(a), _dptr(S),
+                               _dptr(o))
+    if rc != 0:
+        raise ValueError("gdn_oracle_decode rejected its arguments")
+    return {"o": o, "s": S}

@@ -40,7 +40,14 @@
  *   - the state entering a group is the directly propagated state (the
  *     prefix-gap recovery of Eq. 21 is not used here, so it can be tested).
  *
- * Exported entry points: gdn_oracle_prefill(), gdn_oracle_events().
+ * Single-token decode (the state S_C returned for later autoregressive
+ * decoding, Sec. 2.6): Eqs. 1-4 for a chunk of one token with log2 retention
+ * a (so g = gamma = a, A_Delta is empty, M = 1):
+ *   U = beta v,  W = beta 2^a k,  U' = U - W S,  S+ = 2^a S + k U'^T,
+ *   o = [2^a (q^T S) + <q,k> U'] / sqrt(d).
+ *
+ * Exported entry points: gdn_oracle_prefill(), gdn_oracle_events(),
+ * gdn_oracle_select(), gdn_oracle_decode().
  */
 #include <math.h>
 #include <pthread.h>
@@ -589,5 +596,45 @@ int gdn_oracle_select(int B, int Nv, int C, const float *score, const float *gam
     }
     free(rk);
     free(rank);
+    return 0;
+}
+
+/* One decode step for B sequences (Eqs. 1-4 with L = 1; see the header).
+ * q, k [B, Nq, d]; v [B, Nv, dv]; beta, a [B, Nv]; S [B, Nv, d, dv] updated in
+ * place; o [B, Nv, dv].  Value head h reads query/key head h / 2. */
+int gdn_oracle_decode(int B, int Nq, int Nv, int d, int dv, const double *q, const double *k, const double *v,
+                      const double *beta, const double *a, double *S, double *o)
+{
+    if (B < 0 || Nq <= 0 || Nv != 2 * Nq || d <= 0 || dv <= 0) return -1;
+    double *wS = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *up = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *qS = (double *)malloc(sizeof(double) * (size_t)dv);
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Nv; ++h) {
+            const int p = h / 2;
+            const double *qt = q + ((size_t)b * Nq + p) * d, *kt = k + ((size_t)b * Nq + p) * d;
+            const double *vt = v + ((size_t)b * Nv + h) * dv;
+            const double bt = beta[(size_t)b * Nv + h], at = a[(size_t)b * Nv + h];
+            double *Sh = S + ((size_t)b * Nv + h) * d * dv;
+            const double decay = pow(2.0, at), qk = dot(qt, kt, d);
+            for (int j = 0; j < dv; ++j) {          /* W S = beta 2^a (k^T S), and q^T S */
+                double ks = 0.0, qs = 0.0;
+                for (int i = 0; i < d; ++i) {
+                    ks += kt[i] * Sh[(size_t)i * dv + j];
+                    qs += qt[i] * Sh[(size_t)i * dv + j];
+                }
+                wS[j] = bt * decay * ks;
+                qS[j] = qs;
+            }
+            for (int j = 0; j < dv; ++j) up[j] = bt * vt[j] - wS[j];   /* U' = U - W S */
+            for (int i = 0; i < d; ++i)                                /* S+ = 2^a S + k U'^T */
+                for (int j = 0; j < dv; ++j)
+                    Sh[(size_t)i * dv + j] = decay * Sh[(size_t)i * dv + j] + kt[i] * up[j];
+            for (int j = 0; j < dv; ++j)
+                o[((size_t)b * Nv + h) * dv + j] = (decay * qS[j] + qk * up[j]) / sqrt((double)d);
+        }
+    free(wS);
+    free(up);
+    free(qS);
     return 0;
 }
