@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     GdnShape,
     STAGES,
     Workspace,
+    gdn_decode_step,
     gdn_events_status,
     gdn_prefill_dense,
     gdn_prefill_host,

@@ -25,7 +25,7 @@ EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
            "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout",
            "gdn_prefill_sparse_online", "gdn_select_events_scored", "gdn_select_scored_workspace_bytes",
-           "gdn_prefill_host", "gdn_prefill_host_workspace_bytes")
+           "gdn_prefill_host", "gdn_prefill_host_workspace_bytes", "gdn_decode_step")
 STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output", "selector")
 
 
@@ -79,6 +79,8 @@ def load(path: str | None = None):
             lib.gdn_select_events_scored.restype = i32
             lib.gdn_select_scored_workspace_bytes.argtypes = [shp]
             lib.gdn_select_scored_workspace_bytes.restype = sz
+            lib.gdn_decode_step.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.gdn_decode_step.restype = i32
             lib.gdn_prefill_host.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
             lib.gdn_prefill_host.restype = i32
             lib.gdn_prefill_host_workspace_bytes.argtypes = [shp, i32, i32]
@@ -364,6 +366,27 @@ def gdn_prefill_host(q, k, v, beta, g, mask=None, *, h0=None, solver="block_adj"
             ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(mask),
             SOLVERS[solver], _ptr(o), _ptr(s_final), _ptr(ws), ws.numel(), _stream(stream)))
     return o, s_final
+
+
+def gdn_decode_step(q, k, v, beta, a, state, *, o=None, stream=None):
+    """One decode step: q, k [B,Nq,d], v [B,Nv,dv], beta and a [B,Nv] fp32, state [B,Nv,d,dv] fp32
+    (updated in place).  Returns o [B,Nv,dv] in q's dtype."""
+    B, Nq, d = q.shape
+    Nv, dv = v.shape[1], v.shape[2]
+    _need(q, "q", shape=(B, Nq, d))
+    _need(k, "k", dtype=q.dtype, shape=(B, Nq, d))
+    _need(v, "v", dtype=q.dtype, shape=(B, Nv, dv))
+    _need(beta, "beta", torch.float32, (B, Nv))
+    _need(a, "a", torch.float32, (B, Nv))
+    _need(state, "state", torch.float32, (B, Nv, d, dv))
+    if o is None:
+        o = torch.empty((B, Nv, dv), dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype, (B, Nv, dv))
+    shape = GdnShape(B, 1, Nq, Nv, d, dv, _dtype_code(q))
+    with torch.cuda.device(q.device):
+        _check("gdn_decode_step", load().gdn_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                                         _ptr(a), _ptr(state), _ptr(o), _stream(stream)))
+    return o
 
 
 def gdn_select_events(mask: torch.Tensor, Nq: int | None = None, capacity: int | None = None, stream=None):

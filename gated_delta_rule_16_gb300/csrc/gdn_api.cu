@@ -352,6 +352,23 @@ gdn_status gdn_prefill_host(const gdn_shape *shape, const void *q, const void *k
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *beta,
+                           const float *a, float *state, void *o, void *stream) {
+    if (!shape) return GDN_ERR_NULL;
+    if (shape->dtype != GDN_BF16 && shape->dtype != GDN_F32) return GDN_ERR_DTYPE;
+    if (shape->B < 0 || shape->T != 1 || shape->Nq <= 0 || shape->Nv != 2 * shape->Nq) return GDN_ERR_SHAPE;
+    if (shape->d != kDim || shape->dv != kDim) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)shape->B * shape->Nv >= (int64_t)1 << 31) return GDN_ERR_SHAPE;
+    if (shape->B == 0) return GDN_OK;
+    if (!q || !k || !v || !beta || !a || !state || !o) return GDN_ERR_NULL;
+    const void *ptrs[] = {q, k, v, beta, a, state, o};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_ALIGN;
+    if (!device_ok()) return GDN_ERR_DEVICE;
+    return launch_decode(*shape, q, k, v, beta, a, state, o, (cudaStream_t)stream) == cudaSuccess ? GDN_OK
+                                                                                                  : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_prefill_sparse_online(const gdn_shape *shape, const void *q, const void *k, const void *v,
                                      const float *beta, const float *g, const float *h0, const float *eta,
                                      gdn_solver solver, void *o, float *s_final, float *score, uint8_t *mask_out,

@@ -100,6 +100,9 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws);
 // write_cbar: store the compact C-bar blocks (W is built later, after online selection)
 cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_cbar);
 // online selection: mask [B,16,C] (and tiers [B,16], may be NULL) from scores [B,Nv,C]
+// Single-token decode step from a state (see include/gdn.h, gdn_decode_step).
+cudaError_t launch_decode(const gdn_shape &s, const void *q, const void *k, const void *v, const float *beta,
+                          const float *a, float *state, void *o, cudaStream_t stream);
 // Deferred W on tensor cores for the selected events, from the compact bf16 C-bar
 // blocks that launch_intra_tc(..., write_cbar = true) stored (bf16 storage only).
 cudaError_t launch_wbuild_tc(const Problem &pb, const Workspace &ws);

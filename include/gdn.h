@@ -176,6 +176,20 @@ GDN_API gdn_status gdn_prefill_sparse_online(const gdn_shape *shape,
                                      int32_t *tier_out, void *workspace, size_t workspace_bytes,
                                      void *stream);
 
+/* One autoregressive decode step from a state, e.g. the S_final of a prefill
+ * (the pages return S_C for the decoding that follows; Sec. 2.6).  It is
+ * Eqs. 1-4 for a chunk of a single token whose log2 retention is a:
+ *   U' = beta v - beta 2^a S^T k,   S <- 2^a S + k U'^T,
+ *   o  = [2^a S^T q + <q,k> U'] / sqrt(d)   (= S_new^T q / sqrt(d)).
+ * shape: B sequences, T == 1, Nq, Nv = 2 Nq, d = dv = 128, dtype of q, k, v, o.
+ * q, k [B,Nq,d]; v [B,Nv,dv]; beta [B,Nv] fp32; a [B,Nv] fp32: this token's
+ * log2 retention (the increment of g; g of a prefill is its within-chunk
+ * running sum); state [B,Nv,d,dv] fp32, updated in place; o [B,Nv,dv] out.
+ * Value head h reads query/key head h/2.  All device pointers, 16-byte aligned.
+ * Enqueues one kernel on `stream`; no workspace. */
+GDN_API gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                                   const float *beta, const float *a, float *state, void *o, void *stream);
+
 /* Prefill with HOST inputs and outputs: the same computation as
  * gdn_prefill_sparse (mask != NULL) or gdn_prefill_dense (mask == NULL), with
  * q, k, v, beta, g, h0 (may be NULL), mask and the outputs o, s_final in host

@@ -159,3 +159,17 @@ def test_host_prefill_validation(lib):
     assert host(shape(), ws_bytes=dev_bytes) == 5     # the staging does not fit
     assert host(shape(), q=0) == 1
     assert host(shape(B=0), ws=0, q=0) == 0
+
+
+def test_decode_validation(lib):
+    f = ctypes.c_void_p(FAKE)
+
+    def dec(sh, q=FAKE, st=FAKE):
+        return lib.gdn_decode_step(ctypes.byref(sh), ctypes.c_void_p(q), f, f, f, f, ctypes.c_void_p(st), f, None)
+
+    assert dec(shape(T=4096)) == 2                    # SHAPE: one token per sequence
+    assert dec(shape(T=1, d=64, dv=64)) == 6          # UNSUPPORTED
+    assert dec(shape(T=1, Nv=3)) == 2
+    assert dec(shape(T=1), q=0) == 1
+    assert dec(shape(T=1), st=FAKE + 8) == 4
+    assert dec(shape(B=0, T=1), q=0, st=0) == 0
