@@ -314,3 +314,29 @@ def test_csr_capacity_overflow_is_reported():
     m = np.ones((1, 2, 4), np.uint8)
     r = oracle.events(m, capacity=7)
     assert r["overflow"] and r["n_events"] == 8
+
+
+# ------------------------------------------------ partial last chunk (ragged T) ---
+
+@pytest.mark.parametrize("T", [65, 100, 127, 300])
+def test_sparse_ragged_tail_equals_token_rule(T):
+    # C = ceil(T / 64) chunks, the last one partial; random masks, two pairs, two sequences, h0
+    x = gdn_synth.make_inputs(2, T, 2, 4, d=32, dv=32, dtype="f32", seed=T, mask="ones", with_h0=True)
+    C = (T + CH - 1) // CH
+    rng = np.random.default_rng(T)
+    for _ in range(3):
+        m = (rng.random((2, 2, C)) < 0.6).astype(np.uint8)
+        r = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=m, h0=x.h0, solver=oracle.SOLVER_EXACT)
+        ref = brute_prefill(x.q, x.k, x.v, x.beta, x.g, mask=m, h0=x.h0)
+        assert rel_fro(r["o"], ref["o"]) < 1e-10
+        assert rel_fro(r["s_final"], ref["s_final"]) < 1e-10
+
+
+def test_ragged_tail_is_a_prefix_of_the_full_chunk():
+    # a partial chunk of n tokens gives the first n outputs of the same chunk with more tokens
+    # (causality), and the state after it is that of the n-token prefix
+    x = gdn_synth.make_inputs(1, 192, 1, 2, d=32, dv=32, dtype="f32", seed=71, mask="ones")
+    full = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, solver=oracle.SOLVER_BLOCK_ADJ)
+    cut = oracle.prefill(x.q[:, :150], x.k[:, :150], x.v[:, :150], x.beta[:, :150], x.g[:, :150],
+                         solver=oracle.SOLVER_BLOCK_ADJ)
+    assert rel_fro(cut["o"], full["o"][:, :150]) < 1e-12
