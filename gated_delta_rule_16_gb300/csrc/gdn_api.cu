@@ -54,10 +54,10 @@ gdn_status check_shape(const gdn_shape *s) {
     if (s->dtype != GDN_BF16 && s->dtype != GDN_F32) return GDN_ERR_DTYPE;
     if (s->B < 0 || s->T < 0 || s->Nq <= 0 || s->Nv != 2 * s->Nq) return GDN_ERR_SHAPE;
     if (s->d != kDim || s->dv != kDim) return GDN_ERR_UNSUPPORTED;
-    if (s->T % kChunk != 0) return GDN_ERR_UNSUPPORTED;
-    if (s->T / kChunk > 16384) return GDN_ERR_UNSUPPORTED;  // compaction stages a row's mask bits in shared memory
+    // C = ceil(T / 64) chunks; a partial last chunk holds the remaining T - 64 (C - 1) tokens
+    const int64_t C = ((int64_t)s->T + kChunk - 1) / kChunk;
+    if (C > 16384) return GDN_ERR_UNSUPPORTED;  // compaction stages a row's mask bits in shared memory
     // index arithmetic uses int32 for chunk/row/event counts
-    const int64_t C = s->T / kChunk;
     // event tiles are addressed by int32 TMA row coordinates: events x 128 rows < 2^31
     if ((int64_t)s->B * s->Nq * C >= (int64_t)1 << 24) return GDN_ERR_SHAPE;
     if ((int64_t)s->B * s->T >= (int64_t)1 << 31) return GDN_ERR_SHAPE;
@@ -68,7 +68,7 @@ gdn_status check_shape(const gdn_shape *s) {
 void fill_problem(const gdn_shape *s, gdn_solver solver, Problem *pb) {
     std::memset(pb, 0, sizeof(*pb));
     pb->B = s->B; pb->T = s->T; pb->Nq = s->Nq; pb->Nv = s->Nv; pb->d = s->d; pb->dv = s->dv;
-    pb->C = s->T / kChunk;
+    pb->C = (s->T + kChunk - 1) / kChunk;
     pb->G = (pb->C + 1) / 2;
     pb->P = s->Nq;
     pb->R = s->B * s->Nq;
@@ -234,7 +234,7 @@ HostStaging host_staging(const gdn_shape *sh) {
     const size_t es = elem_size(sh->dtype), BT = (size_t)sh->B * sh->T;
     const size_t qk = BT * sh->Nq * sh->d * es, vo = BT * sh->Nv * sh->dv * es, bg = BT * sh->Nv * sizeof(float);
     const size_t st = (size_t)sh->B * sh->Nv * sh->d * sh->dv * sizeof(float);
-    const size_t mk = (size_t)sh->B * sh->Nq * (sh->T / kChunk);
+    const size_t mk = (size_t)sh->B * sh->Nq * ((sh->T + kChunk - 1) / kChunk);
     HostStaging h;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
@@ -331,7 +331,7 @@ gdn_status gdn_prefill_host(const gdn_shape *shape, const void *q, const void *k
     const size_t qk = BT * shape->Nq * shape->d * es, vo = BT * shape->Nv * shape->dv * es;
     const size_t bg = BT * shape->Nv * sizeof(float);
     const size_t stb = (size_t)shape->B * shape->Nv * shape->d * shape->dv * sizeof(float);
-    const size_t mk = (size_t)shape->B * shape->Nq * (shape->T / kChunk);
+    const size_t mk = (size_t)shape->B * shape->Nq * ((shape->T + kChunk - 1) / kChunk);
     cudaError_t e = cudaSuccess;
     auto h2d = [&](size_t off, const void *src, size_t n) {
         if (e == cudaSuccess && n) e = cudaMemcpyAsync(stg + off, src, n, cudaMemcpyHostToDevice, cs);
@@ -401,7 +401,7 @@ gdn_status gdn_select_events_scored(const gdn_shape *shape, const float *score, 
 
 size_t gdn_select_scored_workspace_bytes(const gdn_shape *shape) {
     if (check_shape(shape) != GDN_OK || shape->Nv != 32) return 0;
-    return align_up(selector_workspace_bytes(shape->B, (int)(shape->T / kChunk)) + 1);
+    return align_up(selector_workspace_bytes(shape->B, (int)((shape->T + kChunk - 1) / kChunk)) + 1);
 }
 
 gdn_status gdn_workspace_status(const void *workspace, void *stream) {

@@ -39,10 +39,11 @@ intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__re
     float *red = gg + kChunk;  // [8]
     const int c = blockIdx.x, p = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
     const int64_t tok0 = (int64_t)b * T_ + (int64_t)c * kChunk;
+    const int n = min(kChunk, T_ - c * kChunk);  // valid tokens (a partial last chunk has fewer)
 
     for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
         const int t = idx / kDim, m = idx % kDim;
-        Ks[t * (kDim + 1) + m] = io<T>::ld(K + ((tok0 + t) * Nq + p) * kDim + m);
+        Ks[t * (kDim + 1) + m] = t < n ? io<T>::ld(K + ((tok0 + t) * Nq + p) * kDim + m) : 0.f;
     }
     __syncthreads();
     {   // Gram matrix: thread owns row t, columns s = tid%4 + 4j
@@ -62,9 +63,9 @@ intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__re
 
     for (int hh = 0; hh < 2; ++hh) {
         const int h = 2 * p + hh;
-        if (tid < kChunk) {
-            bet[tid] = beta[(tok0 + tid) * Nv + h];
-            gg[tid] = g[(tok0 + tid) * Nv + h];
+        if (tid < kChunk) {  // past the sequence's end: beta = 0 and a finite g
+            bet[tid] = tid < n ? beta[(tok0 + tid) * Nv + h] : 0.f;
+            gg[tid] = g[(tok0 + min(tid, n - 1)) * Nv + h];
         }
         __syncthreads();
         for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
@@ -119,7 +120,7 @@ intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__re
         }
         for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
             const int t = idx / kDim, m = idx % kDim;
-            Vs[idx] = io<T>::ld(V + ((tok0 + t) * Nv + h) * kDim + m) * bet[t];
+            Vs[idx] = t < n ? io<T>::ld(V + ((tok0 + t) * Nv + h) * kDim + m) * bet[t] : 0.f;
         }
         __syncthreads();
         // U = C (diag(beta) V): thread rows ty*8+i, columns tx+32j
@@ -147,8 +148,8 @@ intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__re
             const int t = ty * 8 + i;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                io<T>::st(U + ((tok0 + t) * Nv + h) * kDim + tx + 32 * j, acc[i][j]);
-                if (t >= kChunk - kBlk) sq += acc[i][j] * acc[i][j];
+                if (t < n) io<T>::st(U + ((tok0 + t) * Nv + h) * kDim + tx + 32 * j, acc[i][j]);
+                if (t >= n - kBlk && t < n) sq += acc[i][j] * acc[i][j];  // Tail-16: the last 16 valid rows
             }
         }
 #pragma unroll
@@ -189,7 +190,8 @@ prefix_kernel(const float *__restrict__ g, int T_, int Nv, int C, int P_, int G,
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int c = c0 + 32 * q + lane;
-                x[q] = c < C ? (double)g[((int64_t)b * T_ + (int64_t)c * kChunk + kChunk - 1) * Nv + h] : 0.0;
+                // gamma_c: g at the chunk's last token (a partial last chunk ends at T - 1)
+                x[q] = c < C ? (double)g[((int64_t)b * T_ + min((int64_t)c * kChunk + kChunk, (int64_t)T_) - 1) * Nv + h] : 0.0;
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {

@@ -110,8 +110,7 @@ __device__ __forceinline__ void offdiag_blocks(const float *Ms, float *Cs, float
 
 __global__ void __launch_bounds__(kThreads, 1)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
-                const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tU64,
-                const __grid_constant__ CUtensorMap tW, IntraParams a) {
+                const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tW, IntraParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     __shared__ uint64_t bar_ld, bar_g, bar_u, bar_drain;
@@ -133,7 +132,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     const int r = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
     const int c0 = 2 * r;
     const int nch = c0 + 1 < a.C ? 2 : 1;
-    const int tok0 = b * a.T_ + c0 * kChunk;
+    const int t0 = c0 * kChunk;                        // first token of the group inside its sequence
+    const int nvalid = min(2 * kChunk, a.T_ - t0);     // tokens of the group (a partial last chunk has fewer)
+    const int64_t tok0 = (int64_t)b * a.T_ + t0;
+    // Tail-16 window of this thread's row: the last 16 valid rows of its chunk (rows past the
+    // sequence's end need no exclusion: beta = 0 there makes their U rows exactly zero)
+    const int nrow = min(kChunk, nvalid - kChunk * ct);
+    const bool in_tail = tl >= nrow - kBlk;
 
     if (tid == 0) {  // barriers, then the tiles: the loads overlap the set-up below
         mbar_init(&bar_ld, 1);
@@ -143,21 +148,22 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         fence_mbar_init();
         abort_s = 0;
         mbar_arrive_expect_tx(&bar_ld, 6 * kSlab);
-        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_ld);
-        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_ld);
+        tma_load_4d(sm + OFF_K, &tK, 0, p, t0, b, &bar_ld);  // rows past the sequence's end read zeros
+        tma_load_4d(sm + OFF_K + kSlab, &tK, 64, p, t0, b, &bar_ld);
         for (int hh = 0; hh < 2; ++hh) {
             uint8_t *vd = sm + OFF_V + hh * 2 * kSlab;
-            tma_load_3d(vd, &tV, 0, 2 * p + hh, tok0, &bar_ld);
-            tma_load_3d(vd + kSlab, &tV, 64, 2 * p + hh, tok0, &bar_ld);
+            tma_load_4d(vd, &tV, 0, 2 * p + hh, t0, b, &bar_ld);
+            tma_load_4d(vd + kSlab, &tV, 64, 2 * p + hh, t0, b, &bar_ld);
         }
     }
     if (tid < 2) ev_s[tid] = (a.ev_of && tid < nch) ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
     if (tid < 256) {  // beta and g of both heads, fetched once while the tiles load
+        // tokens past the sequence's end: beta = 0 (no write, no correction) and a finite g
         const int hh = tid >> 7, t = tid & 127;
-        const bool valid = (t >> 6) < nch;
-        const int64_t gi = ((int64_t)tok0 + t) * a.Nv + 2 * p + hh;
+        const bool valid = t < nvalid;
+        const int64_t gi = (tok0 + min(t, nvalid - 1)) * a.Nv + 2 * p + hh;
         bet2[tid] = valid ? a.beta[gi] : 0.f;
-        gg2[tid] = valid ? a.g[gi] : 0.f;
+        gg2[tid] = a.g[gi];
     }
     if (warp == 0) tmem_alloc<512>(&tmem_base);
     tc_fence_before();
@@ -309,7 +315,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 tmem_ld_wait();
 #pragma unroll
                 for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(ustage, row, c0s + 8 * v8, &u[8 * v8]);
-                if (tl >= kChunk - kBlk) {
+                if (in_tail) {
 #pragma unroll
                     for (int q2 = 0; q2 < 32; ++q2) sq += u[q2] * u[q2];
                 }
@@ -331,9 +337,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         __syncthreads();
         if (tid == 0) {
             uint8_t *ust = sm + OFF_V + hh * 2 * kSlab;
-            const CUtensorMap *m = nch == 2 ? &tU : &tU64;  // a final single-chunk group writes 64 rows only
-            tma_store_3d(m, 0, h, tok0, ust);
-            tma_store_3d(m, 64, h, tok0, ust + kSlab);
+            tma_store_4d(&tU, 0, h, t0, b, ust);  // rows past the sequence's end are clipped
+            tma_store_4d(&tU, 64, h, t0, b, ust + kSlab);
             for (int cc = 0; cc < nch; ++cc) {
                 const int ev = ev_s[cc];
                 if (ev < 0) continue;
@@ -363,13 +368,11 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 
 cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_cbar) {
     if (pb.B == 0 || pb.C == 0) return cudaSuccess;
-    CUtensorMap tK, tV, tU, tU64, tW;
-    const uint64_t BT = (uint64_t)pb.B * pb.T;
+    CUtensorMap tK, tV, tU, tW;
     const uint64_t wrows = (uint64_t)ws.ev_cap * 2 * kChunk;
-    if (!make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tV, pb.v, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tU, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tU64, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 64) ||
+    if (!make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 128) ||
+        !make_tmap_tokens(&tV, pb.v, pb.Nv, pb.T, pb.B, 64, 128) ||
+        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 128) ||
         !make_tmap_bf16_3d(&tW, ws.W, kDim, wrows, 1, kDim * 2, wrows * kDim * 2, 64, 64, 1))
         return cudaErrorInvalidValue;
     IntraParams a;
@@ -380,7 +383,7 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;
     a.exact = pb.solver == GDN_SOLVER_EXACT;
     cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraTcSmem);
-    intra_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream>>>(tK, tV, tU, tU64, tW, a);
+    intra_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream>>>(tK, tV, tU, tW, a);
     return cudaGetLastError();
 }
 

@@ -65,12 +65,13 @@ output_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restr
         for (int part = 0; part < nparts; ++part) {
             const int cq = c0 + part;
             const int64_t tq0 = (int64_t)b * T_ + (int64_t)cq * kChunk;
+            const int nq = min(kChunk, T_ - cq * kChunk);  // valid query tokens (a partial last chunk has fewer)
             __syncthreads();
             for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
                 const int t = idx / kDim, m = idx % kDim;
-                Qs[t * QS_ + m] = io<T>::ld(Q + ((tq0 + t) * Nq + p) * kDim + m);
+                Qs[t * QS_ + m] = t < nq ? io<T>::ld(Q + ((tq0 + t) * Nq + p) * kDim + m) : 0.f;
             }
-            if (tid < kChunk) gq[tid] = g[(tq0 + tid) * Nv + h];
+            if (tid < kChunk) gq[tid] = g[(tq0 + min(tid, nq - 1)) * Nv + h];
             __syncthreads();
             const float shift = part ? g[((int64_t)b * T_ + (int64_t)c0 * kChunk + kChunk - 1) * Nv + h] : 0.f;
             float acc[8][4];
@@ -100,13 +101,14 @@ output_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restr
                 const int ck = c0 + term;
                 const bool cross = part == 1 && term == 0;
                 const int64_t tk0 = (int64_t)b * T_ + (int64_t)ck * kChunk;
+                const int nk = min(kChunk, T_ - ck * kChunk);
                 __syncthreads();
                 for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
                     const int t = idx / kDim, m = idx % kDim;
-                    Ks[t * QS_ + m] = io<T>::ld(K + ((tk0 + t) * Nq + p) * kDim + m);
-                    Us[idx] = io<T>::ld(U + ((tk0 + t) * Nv + h) * kDim + m);
+                    Ks[t * QS_ + m] = t < nk ? io<T>::ld(K + ((tk0 + t) * Nq + p) * kDim + m) : 0.f;
+                    Us[idx] = t < nk ? io<T>::ld(U + ((tk0 + t) * Nv + h) * kDim + m) : 0.f;
                 }
-                if (tid < kChunk) gk[tid] = g[(tk0 + tid) * Nv + h];
+                if (tid < kChunk) gk[tid] = g[(tk0 + min(tid, nk - 1)) * Nv + h];
                 __syncthreads();
                 {   // A tile: row t = tid/4, columns s = tid%4 + 4j
                     const int t = tid >> 2;
@@ -146,7 +148,8 @@ output_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restr
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    io<T>::st(O + ((tq0 + ty * 8 + i) * Nv + h) * kDim + tx + 32 * j, acc[i][j] * inv_sqrt_d);
+                    if (ty * 8 + i < nq)
+                        io<T>::st(O + ((tq0 + ty * 8 + i) * Nv + h) * kDim + tx + 32 * j, acc[i][j] * inv_sqrt_d);
         }
     }
 }

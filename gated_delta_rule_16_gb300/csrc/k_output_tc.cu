@@ -47,7 +47,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 __global__ void __launch_bounds__(kThreads, 1)
 output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tK,
                  const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tS,
-                 const __grid_constant__ CUtensorMap tO, const __grid_constant__ CUtensorMap tO64, OutParams a) {
+                 const __grid_constant__ CUtensorMap tO, OutParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     __shared__ uint64_t bar_qk_ld, bar_h_ld[2], bar_s[2], bar_qk_mma, bar_h_mma, bar_drain;
@@ -63,7 +63,9 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     const int r = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
     const int c0 = 2 * r;
     const bool two = c0 + 1 < a.C;
-    const int tok0 = b * a.T_ + c0 * kChunk;
+    const int t0 = c0 * kChunk;                     // first token of the group inside its sequence
+    const int nvalid = min(2 * kChunk, a.T_ - t0);  // tokens of the group (a partial last chunk has fewer)
+    const int64_t tok0 = (int64_t)b * a.T_ + t0;
 
     if (tid == 0) {  // the tiles that do not depend on the predecessor lookup go first
         mbar_init(&bar_qk_ld, 1);
@@ -77,15 +79,15 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         fence_mbar_init();
         abort_s = 0;
         mbar_arrive_expect_tx(&bar_qk_ld, 4 * kSlab);
-        tma_load_3d(sm + OFF_Q, &tQ, 0, p, tok0, &bar_qk_ld);
-        tma_load_3d(sm + OFF_Q + kSlab, &tQ, 64, p, tok0, &bar_qk_ld);
-        tma_load_3d(sm + OFF_K, &tK, 0, p, tok0, &bar_qk_ld);
-        tma_load_3d(sm + OFF_K + kSlab, &tK, 64, p, tok0, &bar_qk_ld);
+        tma_load_4d(sm + OFF_Q, &tQ, 0, p, t0, b, &bar_qk_ld);  // rows past the sequence's end read zeros
+        tma_load_4d(sm + OFF_Q + kSlab, &tQ, 64, p, t0, b, &bar_qk_ld);
+        tma_load_4d(sm + OFF_K, &tK, 0, p, t0, b, &bar_qk_ld);
+        tma_load_4d(sm + OFF_K + kSlab, &tK, 64, p, t0, b, &bar_qk_ld);
         for (int hh = 0; hh < 2; ++hh) {
             uint8_t *ud = sm + (hh ? OFF_U1 : OFF_U0);
             mbar_arrive_expect_tx(&bar_h_ld[hh], 2 * kSlab);
-            tma_load_3d(ud, &tU, 0, 2 * p + hh, tok0, &bar_h_ld[hh]);
-            tma_load_3d(ud + kSlab, &tU, 64, 2 * p + hh, tok0, &bar_h_ld[hh]);
+            tma_load_4d(ud, &tU, 0, 2 * p + hh, t0, b, &bar_h_ld[hh]);
+            tma_load_4d(ud + kSlab, &tU, 64, 2 * p + hh, t0, b, &bar_h_ld[hh]);
         }
     }
     if (tid < 2) {  // entry state of the group: one table load (kind 1 snapshot, 2 h0, 0 zero)
@@ -95,10 +97,9 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         slot_s[hh] = info.x;
         fscale[hh] = __int_as_float(hh ? info.w : info.z);
     }
-    for (int idx = tid; idx < 256; idx += kThreads) {
+    for (int idx = tid; idx < 256; idx += kThreads) {  // tokens past the sequence's end: a finite g
         const int hh = idx >> 7, t = idx & 127;
-        const bool valid = t < 64 || two;
-        gs[hh][t] = valid ? a.g[((int64_t)tok0 + t) * a.Nv + 2 * p + hh] : 0.f;
+        gs[hh][t] = a.g[(tok0 + min(t, nvalid - 1)) * a.Nv + 2 * p + hh];
     }
     if (warp == 0) tmem_alloc<512>(&tmem_base);
     tc_fence_before();
@@ -232,9 +233,8 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         __syncthreads();
         if (tid == 0) {
             uint8_t *stage = sm + (hh ? OFF_U1 : OFF_U0);
-            const CUtensorMap *m = two ? &tO : &tO64;  // a final single-chunk group writes 64 rows only
-            tma_store_3d(m, 0, 2 * p + hh, tok0, stage);
-            tma_store_3d(m, 64, 2 * p + hh, tok0, stage + kSlab);
+            tma_store_4d(&tO, 0, 2 * p + hh, t0, b, stage);  // rows past the sequence's end are clipped
+            tma_store_4d(&tO, 64, 2 * p + hh, t0, b, stage + kSlab);
             bulk_commit();
         }
     }
@@ -258,22 +258,20 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
 
 cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
     if (pb.B == 0 || pb.C == 0) return cudaSuccess;
-    CUtensorMap tQ, tK, tU, tS, tO, tO64;
-    const uint64_t BT = (uint64_t)pb.B * pb.T;
+    CUtensorMap tQ, tK, tU, tS, tO;
     const uint64_t snap_rows = (uint64_t)(ws.snap_cap > 0 ? ws.snap_cap : 1) * 2 * kDim;
-    if (!make_tmap_bf16_3d(&tQ, pb.q, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tU, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
+    if (!make_tmap_tokens(&tQ, pb.q, pb.Nq, pb.T, pb.B, 64, 128) ||
+        !make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 128) ||
+        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 128) ||
         !make_tmap_bf16_3d(&tS, ws.snap, kDim, snap_rows, 1, kDim * 2, snap_rows * kDim * 2, 64, 128, 1) ||
-        !make_tmap_bf16_3d(&tO, pb.o, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 128) ||
-        !make_tmap_bf16_3d(&tO64, pb.o, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 64, 1, 64))
+        !make_tmap_tokens(&tO, pb.o, pb.Nv, pb.T, pb.B, 64, 128))
         return cudaErrorInvalidValue;
     OutParams a;
     a.g = pb.g; a.h0 = pb.h0; a.grp_info = (const int4 *)ws.grp_info;
     a.O = (__nv_bfloat16 *)pb.o; a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.G = pb.G;
     cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
-    output_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream>>>(tQ, tK, tU, tS, tO, tO64, a);
+    output_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream>>>(tQ, tK, tU, tS, tO, a);
     return cudaGetLastError();
 }
 

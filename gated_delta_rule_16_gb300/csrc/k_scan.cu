@@ -47,10 +47,11 @@ wbuild_kernel(const T *__restrict__ K, const float *__restrict__ cbar, const int
         const int j = find_row(row_ptr, R, (int)e);
         const int i = row_pair[j], b = i / P, p = i % P, c = ev_chunk[e];
         const int64_t tok0 = (int64_t)b * T_ + (int64_t)c * kChunk;
+        const int n = min(kChunk, T_ - c * kChunk);  // valid tokens (a partial last chunk has fewer)
         __syncthreads();
         for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
             const int t = idx / kDim, m = idx % kDim;
-            Ks[idx] = io<T>::ld(K + ((tok0 + t) * Nq + p) * kDim + m);
+            Ks[idx] = t < n ? io<T>::ld(K + ((tok0 + t) * Nq + p) * kDim + m) : 0.f;
         }
         for (int hh = 0; hh < 2; ++hh) {
             const int h = 2 * p + hh;
@@ -118,18 +119,19 @@ scan_kernel(const T *__restrict__ K, const T *__restrict__ W, T *__restrict__ U,
     for (int64_t e = e_beg; e < e_end; ++e) {
         const int c = ev_chunk[e];
         const int64_t tok0 = (int64_t)b * T_ + (int64_t)c * kChunk;
+        const int n = min(kChunk, T_ - c * kChunk);  // valid tokens (a partial last chunk has fewer)
         __syncthreads();
         const T *w = W + (e * 2 + hh) * kChunk * kDim;
         for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
             const int t = idx / kDim, m = idx % kDim;
             Ws[t * (kDim + 4) + m] = io<T>::ld(w + idx);
-            Ks[idx] = io<T>::ld(K + ((tok0 + t) * Nq + p) * kDim + m);
+            Ks[idx] = t < n ? io<T>::ld(K + ((tok0 + t) * Nq + p) * kDim + m) : 0.f;
         }
         for (int idx = tid; idx < kChunk * kSlice; idx += kThreads) {
             const int t = idx / kSlice, v = idx % kSlice;
-            Us[t * (kSlice + 1) + v] = io<T>::ld(U + ((tok0 + t) * Nv + h) * kDim + v0 + v);
+            Us[t * (kSlice + 1) + v] = t < n ? io<T>::ld(U + ((tok0 + t) * Nv + h) * kDim + v0 + v) : 0.f;
         }
-        if (tid < kChunk) gg[tid] = g[(tok0 + tid) * Nv + h];
+        if (tid < kChunk) gg[tid] = g[(tok0 + min(tid, n - 1)) * Nv + h];  // gg[63]: g at the last token
         const float gap = exp2f((float)(Pu[c] - Pu[cur]));
         for (int q = 0; q < 16; ++q) Ss[sm_row * kSlice + sm_col + q] *= gap;
         __syncthreads();
@@ -149,7 +151,7 @@ scan_kernel(const T *__restrict__ K, const T *__restrict__ W, T *__restrict__ U,
             for (int q = 0; q < 8; ++q) {
                 const int v = (tid & 3) + 4 * q;
                 const float up = Us[t * (kSlice + 1) + v] - acc[q];
-                io<T>::st(U + ((tok0 + t) * Nv + h) * kDim + v0 + v, up);
+                if (t < n) io<T>::st(U + ((tok0 + t) * Nv + h) * kDim + v0 + v, up);
                 Us[t * (kSlice + 1) + v] = up * dec;
             }
         }

@@ -143,8 +143,9 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     for (int idx = tid; idx < n_ev * kChunk; idx += kThreads) {
         const int k = idx >> 6, t = idx & 63;
         const int64_t tk = (int64_t)b * a.T_ + (int64_t)ev_c[k] * kChunk;
-        const float gam = a.g[(tk + kChunk - 1) * a.Nv + h];
-        dec[k][t] = ex2(gam - a.g[(tk + t) * a.Nv + h]);
+        const int n = min(kChunk, a.T_ - ev_c[k] * kChunk);  // valid tokens (a partial last chunk has fewer)
+        const float gam = a.g[(tk + n - 1) * a.Nv + h];       // gamma: g at the chunk's last token
+        dec[k][t] = ex2(gam - a.g[(tk + min(t, n - 1)) * a.Nv + h]);
         if (t == 0) gamk[k] = gam;
     }
     const uint32_t tbase = tmem_base;
@@ -161,13 +162,13 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     };
     auto load_u = [&](int k) {
         mbar_arrive_expect_tx(&bar_u, 16384u);
-        tma_load_3d(sm + OFF_U, &tU, 0, h, b * a.T_ + ev_c[k] * kChunk, &bar_u);
+        tma_load_4d(sm + OFF_U, &tU, 0, h, ev_c[k] * kChunk, b, &bar_u);
     };
     auto load_k = [&](int k) {
-        const int tok = b * a.T_ + ev_c[k] * kChunk;
+        const int tok = ev_c[k] * kChunk;
         mbar_arrive_expect_tx(&bar_k, 16384u);
-        tma_load_3d(sm + OFF_K, &tK, 0, p, tok, &bar_k);
-        tma_load_3d(sm + OFF_K + 8192, &tK, 64, p, tok, &bar_k);
+        tma_load_4d(sm + OFF_K, &tK, 0, p, tok, b, &bar_k);  // rows past the sequence's end read zeros
+        tma_load_4d(sm + OFF_K + 8192, &tK, 64, p, tok, b, &bar_k);
     };
     // thread 0: events whose tiles were requested, and completed waits it observed (for the drain)
     int loads_w = 0, loads_u = 0, loads_k = 0, seen_w = 0, seen_k = 0, seen_u = 0;
@@ -293,7 +294,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                              mnmajor_desc(smem_addr(sm + OFF_K), ks, 8192), id2, 1);
                 mma_commit(&bar_mma2);
                 if (mode == kModeFixup) {  // U' of this event back over U
-                    tma_store_3d(&tU, 0, h, b * a.T_ + c * kChunk, sm + OFF_U);
+                    tma_store_4d(&tU, 0, h, c * kChunk, b, sm + OFF_U);  // clipped at the sequence's end
                     bulk_commit();
                 }
                 if (k + 1 < n_ev) {
@@ -544,11 +545,10 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
     }
     if (NR == 0 || pb.C == 0) return cudaSuccess;
     CUtensorMap tW, tK, tU;
-    const uint64_t BT = (uint64_t)pb.B * pb.T;
     if (!make_tmap_bf16_3d(&tW, ws.W, kDim, (uint64_t)ws.ev_cap * 2 * kChunk, 1, kDim * 2,
                            (uint64_t)ws.ev_cap * 2 * kChunk * kDim * 2, 64, 64, 1, true) ||
-        !make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 64, true) ||
-        !make_tmap_bf16_3d(&tU, ws.U, kDim, pb.Nv, BT, kDim * 2, (uint64_t)pb.Nv * kDim * 2, 128, 1, 64, false))
+        !make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 64, true) ||
+        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 128, 64, false))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(scan_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmem);
     const int fixup = part == 2;

@@ -107,7 +107,8 @@ selector_pair_kernel(const float *__restrict__ score, const float *__restrict__ 
     // r_h: mean of 2^gamma over the last min(16, C) chunks
     const int c0 = C > 16 ? C - 16 : 0;
     double e2 = 0.0;
-    if (ht < C - c0) e2 = exp2((double)g[((int64_t)b * T_ + (int64_t)(c0 + ht) * kChunk + kChunk - 1) * Nv + h]);
+    if (ht < C - c0)  // gamma of chunk c0 + ht: g at its last token (a partial last chunk ends at T - 1)
+        e2 = exp2((double)g[((int64_t)b * T_ + min((int64_t)(c0 + ht + 1) * kChunk, (int64_t)T_) - 1) * Nv + h]);
     // both half-sums at once: lanes reduce within the warp, warps of a half combine in shared memory
 #pragma unroll
     for (int o = 16; o; o >>= 1) {

@@ -100,9 +100,9 @@ wbuild_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__
         if (tid == 0) {
             mbar_arrive_expect_tx(&bar_ld, (two ? 2 : 1) * 2 * 8192);
             for (int j = 0; j < (two ? 2 : 1); ++j) {
-                const int tok0 = ev_b[j] * a.T_ + ev_c[j] * kChunk;
-                tma_load_3d(sm + OFF_K + j * 8192, &tK, 0, ev_p[j], tok0, &bar_ld);
-                tma_load_3d(sm + OFF_K + kSlab + j * 8192, &tK, 64, ev_p[j], tok0, &bar_ld);
+                const int t0 = ev_c[j] * kChunk;  // rows past the sequence's end read zeros
+                tma_load_4d(sm + OFF_K + j * 8192, &tK, 0, ev_p[j], t0, ev_b[j], &bar_ld);
+                tma_load_4d(sm + OFF_K + kSlab + j * 8192, &tK, 64, ev_p[j], t0, ev_b[j], &bar_ld);
             }
         }
         if (!two) {  // the absent event's token rows meet zero coefficients: make them finite zeros
@@ -208,9 +208,8 @@ wbuild_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__
 cudaError_t launch_wbuild_tc(const Problem &pb, const Workspace &ws) {
     if (pb.B == 0 || pb.C == 0) return cudaSuccess;
     CUtensorMap tK, tW;
-    const uint64_t BT = (uint64_t)pb.B * pb.T;
     const uint64_t wrows = (uint64_t)ws.ev_cap * 2 * kChunk;
-    if (!make_tmap_bf16_3d(&tK, pb.k, kDim, pb.Nq, BT, kDim * 2, (uint64_t)pb.Nq * kDim * 2, 64, 1, 64) ||
+    if (!make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 64) ||
         !make_tmap_bf16_3d(&tW, ws.W, kDim, wrows, 1, kDim * 2, wrows * kDim * 2, 64, 64, 1))
         return cudaErrorInvalidValue;
     WbuildParams a;

@@ -44,4 +44,22 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, u
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Token-indexed bf16 tensor [B, T, heads, 128] as a 4-D map (128, heads, T, B): a box
+// that runs past a sequence's last token reads zeros and a store there is clipped,
+// so a partial last chunk never touches the next sequence.
+inline bool make_tmap_tokens(CUtensorMap *map, const void *base, uint64_t heads, uint64_t T, uint64_t B,
+                             uint32_t box_x, uint32_t box_rows, bool swizzle128 = true) {
+    if (reinterpret_cast<uintptr_t>(base) & 15u) return false;
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    const uint64_t row = 128 * 2;
+    cuuint64_t dims[4] = {128, heads, T, B};
+    cuuint64_t strides[3] = {row, heads * row, T * heads * row};
+    cuuint32_t box[4] = {box_x, 1, box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gdn

@@ -52,7 +52,8 @@ def test_workspace_bytes(lib):
     # U alone is B*T*Nv*dv*2 bytes for bf16; the workspace holds at least that
     assert n_ba > 1 * 4096 * 32 * 128 * 2
     assert gdn.gdn_workspace_bytes(shape(d=64, dv=64)) == 0
-    assert gdn.gdn_workspace_bytes(shape(T=100)) == 0
+    # a partial last chunk is allowed: C = ceil(T / 64)
+    assert 0 < gdn.gdn_workspace_bytes(shape(T=100)) < gdn.gdn_workspace_bytes(shape(T=128))
     assert gdn.gdn_workspace_bytes(shape(Nv=31)) == 0
     assert gdn.gdn_workspace_bytes(shape(T=0)) > 0
     # grows linearly with the batch
@@ -72,7 +73,8 @@ def call_dense(lib, s, ptrs=None, ws=FAKE, ws_bytes=1 << 40, solver=1):
 
 def test_host_validation(lib):
     assert call_dense(lib, shape(d=64, dv=64)) == 6          # UNSUPPORTED
-    assert call_dense(lib, shape(T=100)) == 6                 # UNSUPPORTED: T % 64
+    assert call_dense(lib, shape(T=100)) == 8                 # a partial last chunk passes validation (no GPU here)
+    assert call_dense(lib, shape(T=64 * 16385)) == 6          # UNSUPPORTED: more than 16384 chunks
     assert call_dense(lib, shape(Nv=31)) == 2                 # SHAPE
     assert call_dense(lib, shape(dtype=7)) == 3               # DTYPE
     assert call_dense(lib, shape(), solver=5) == 3            # DTYPE (solver)
@@ -153,7 +155,7 @@ def test_host_prefill_validation(lib):
         return lib.gdn_prefill_host(ctypes.byref(sh), ctypes.c_void_p(q), f, f, f, f, None, f, 1, f, f,
                                     ctypes.c_void_p(ws), ws_bytes, None)
 
-    assert host(shape(T=100)) == 6
+    assert host(shape(d=64, dv=64)) == 6
     assert host(shape(), ws=0) == 1
     assert host(shape(), ws=FAKE + 16) == 4
     assert host(shape(), ws_bytes=dev_bytes) == 5     # the staging does not fit

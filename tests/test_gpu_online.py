@@ -32,8 +32,10 @@ def _built():
 
 
 def chunk_gamma(g, C):
-    """gamma[b,h,c] = g at the last token of chunk c."""
-    return np.ascontiguousarray(np.moveaxis(g[:, 63::64, :][:, :C], 1, 2))
+    """gamma[b,h,c] = g at the last token of chunk c (of a partial last chunk: token T - 1)."""
+    T = g.shape[1]
+    idx = np.minimum(np.arange(C) * 64 + 63, T - 1)
+    return np.ascontiguousarray(np.moveaxis(g[:, idx, :], 1, 2))
 
 
 def gpu_select(score, g, eta=None):
@@ -147,3 +149,12 @@ def test_online_matches_given_mask_path_bitwise(solver):
     o2, s2 = gdn.gdn_prefill_sparse(t["q"], t["k"], t["v"], t["beta"], t["g"], mask.clone(), solver=solver)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+def test_online_prefill_ragged_T():
+    # 23 full chunks and a 5-token partial chunk
+    x = gdn_synth.make_inputs(1, 23 * 64 + 5, 16, 32, dtype="bf16", seed=44, mask="ones")
+    res = run_online(x)
+    check_selection(x, res)
+    ref = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=res["mask"], solver=oracle.SOLVER_BLOCK_ADJ)
+    assert_close(res, ref, "bf16", "online ragged T")

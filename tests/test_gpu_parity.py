@@ -215,3 +215,32 @@ def test_host_buffer_prefill_equals_device_path(dtype, sparse):
     stream.synchronize()
     assert np.array_equal(o.float().numpy().astype(np.float64), res["o"])
     assert np.array_equal(s.numpy().astype(np.float64), res["s_final"])
+
+
+# ------------------------------------------------- partial last chunk (ragged T) ---
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [100, 150, 337])
+def test_ragged_T_partial_last_chunk(dtype, T):
+    # two sequences (the partial chunk of the first must not touch the second), 3 pairs, h0,
+    # random masks; C = ceil(T / 64)
+    x = gdn_synth.make_inputs(2, T, 3, 6, dtype=dtype, seed=27 + T, mask="bernoulli", retention=0.6,
+                              with_h0=True)
+    for solver in ("exact", "block_adj"):
+        for sparse in (True, False):
+            res = run_gpu(x, solver=solver, sparse=sparse, score=True)
+            ref = oracle_run(x, solver, sparse, debug=True)
+            assert_close(res, ref, dtype, f"T={T} {dtype} {solver} sparse={sparse}")
+            rel = np.abs(res["score"] - ref["score"]) / np.maximum(ref["score"], 1e-30)
+            assert rel.max() <= TOL[dtype]
+
+
+def test_ragged_T_qwen_layer_sampled_pairs():
+    # one Qwen3.5-4B-shaped layer with a ragged tail, two sequences, 29% events
+    x = gdn_synth.make_inputs(2, 4096 + 37, 16, 32, dtype="bf16", seed=28, mask="beta")
+    res = run_gpu(x, solver="block_adj")
+    for b, p in ((0, 5), (1, 12)):
+        y = slice_pairs(x, b, [p])
+        ref = oracle_run(y, "block_adj")
+        got = {"o": res["o"][b:b + 1, :, 2 * p:2 * p + 2], "s_final": res["s_final"][b:b + 1, 2 * p:2 * p + 2]}
+        assert_close(got, ref, "bf16", f"ragged layer seq {b} pair {p}")
