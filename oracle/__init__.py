@@ -57,6 +57,9 @@ def _load():
             D = ctypes.POINTER(ctypes.c_double)
             I = ctypes.POINTER(ctypes.c_int)
             U8 = ctypes.POINTER(ctypes.c_uint8)
+            lib.gdn_oracle_prefill_tail.restype = ctypes.c_int
+            lib.gdn_oracle_prefill_tail.argtypes = ([ctypes.c_int] * 6 + [D] * 6 + [U8, ctypes.c_int, ctypes.c_int] +
+                                                    [D] * 9 + [ctypes.c_int])
             lib.gdn_oracle_prefill.restype = ctypes.c_int
             lib.gdn_oracle_prefill.argtypes = [ctypes.c_int] * 6 + [D] * 6 + [U8, ctypes.c_int, ctypes.c_int] + [D] * 9
             lib.gdn_oracle_events.restype = ctypes.c_int
@@ -81,14 +84,14 @@ def _f64(a):
 
 
 def prefill(q, k, v, beta, g, mask=None, h0=None, solver=SOLVER_BLOCK_ADJ,
-            nthreads=None, debug=False):
+            nthreads=None, debug=False, tail=16):
     """Run the oracle on one batch of inputs.
 
     q, k [B,T,Nq,d]; v [B,T,Nv,dv]; beta, g [B,T,Nv]; mask [B,Nv/2,C] (uint8) or
     None for the dense path (every chunk selected); h0 [B,Nv,d,dv] or None.
     Returns a dict with ``o`` [B,T,Nv,dv] and ``s_final`` [B,Nv,d,dv]; with
     ``debug`` also ``o_chunk``, ``u``, ``u_prime``, ``w``, ``s_in``
-    [B,Nv,C,d,dv], ``score`` [B,Nv,C] and ``cinv`` [B,Nv,C,64,64].
+    [B,Nv,C,d,dv], ``score`` [B,Nv,C] (Tail-``tail`` window) and ``cinv`` [B,Nv,C,64,64].
     """
     lib = _load()
     q, k, v, beta, g, h0 = map(_f64, (q, k, v, beta, g, h0))
@@ -111,10 +114,10 @@ def prefill(q, k, v, beta, g, mask=None, h0=None, solver=SOLVER_BLOCK_ADJ,
         if m.shape != (B, Nv // 2, C):
             raise ValueError(f"mask shape {m.shape} != {(B, Nv // 2, C)}")
     nthreads = nthreads or os.cpu_count() or 1
-    rc = lib.gdn_oracle_prefill(
+    rc = lib.gdn_oracle_prefill_tail(
         B, T, Nq, Nv, d, dv, _dptr(q), _dptr(k), _dptr(v), _dptr(beta), _dptr(g), _dptr(h0),
         None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
-        int(solver), int(nthreads), _dptr(o), _dptr(s_final), *[_dptr(x) for x in dbg])
+        int(solver), int(nthreads), _dptr(o), _dptr(s_final), *[_dptr(x) for x in dbg], int(tail))
     if rc != 0:
         raise ValueError(f"gdn_oracle_prefill rejected its arguments (rc={rc})")
     return out

@@ -26,7 +26,8 @@
  *   chunk form (Eqs. 3-4): O_c = [2^g_c * (Q_c S_c) + A_cc U'_c] / sqrt(d) for every c.
  *   block-adjacent solver (Eq. 7): C_ii = M_ii^-1, C_i,i-1 = -C_ii M_i,i-1 C_i-1,i-1,
  *     every other 16x16 block zero; exact ("Full64") solver: C = M^-1.
- *   tail score (Eq. 9): s_c = ||U[48:64, :]||_F.
+ *   tail score (Eq. 9): s_c = ||U[48:64, :]||_F (Tail-16; the window W of Tail-W, W in
+ *   {8, 16, 32, 64}, is the ablation axis of Sec. 3 / Fig. 10: the last W rows).
  *
  * Readings where the pages leave a step open (each is also listed in the
  * design notes):
@@ -67,6 +68,7 @@ typedef struct {
     /* optional diagnostics (NULL to skip) */
     double *o_chunk, *u, *u_prime, *w, *s_in, *score, *cinv;
     int nthreads;
+    int tail;                  /* rows of the tail-score window (16 by default) */
 } job_t;
 
 /* ---- small dense helpers (row-major, explicit sizes) --------------------- */
@@ -269,7 +271,7 @@ static void run_unit(const job_t *J, int b, int h, scratch_t *X)
         intra(J, n, X);
         if (J->score) {
             double acc = 0.0;
-            int t0 = n > BLK ? n - BLK : 0;
+            int t0 = n > J->tail ? n - J->tail : 0;
             for (int t = t0; t < n; ++t)
                 for (int j = 0; j < dv; ++j) acc += X->U[(size_t)t * dv + j] * X->U[(size_t)t * dv + j];
             J->score[((size_t)b * J->Nv + h) * C + c] = sqrt(acc);
@@ -342,19 +344,20 @@ static void *worker(void *arg)
  * s_in [B,Nv,C,d,dv] (state entering each chunk), score [B,Nv,C],
  * cinv [B,Nv,C,64,64] (the solver's C).
  * Returns 0, or -1 on a bad argument. */
-int gdn_oracle_prefill(int B, int T, int Nq, int Nv, int d, int dv,
-                       const double *q, const double *k, const double *v,
-                       const double *beta, const double *g, const double *h0,
-                       const unsigned char *mask, int solver, int nthreads,
-                       double *o, double *s_final,
-                       double *o_chunk, double *u, double *u_prime, double *w,
-                       double *s_in, double *score, double *cinv)
+int gdn_oracle_prefill_tail(int B, int T, int Nq, int Nv, int d, int dv,
+                            const double *q, const double *k, const double *v,
+                            const double *beta, const double *g, const double *h0,
+                            const unsigned char *mask, int solver, int nthreads,
+                            double *o, double *s_final,
+                            double *o_chunk, double *u, double *u_prime, double *w,
+                            double *s_in, double *score, double *cinv, int tail)
 {
     if (B < 0 || T < 0 || Nq <= 0 || Nv != 2 * Nq || d <= 0 || dv <= 0) return -1;
     if (solver != SOLVER_EXACT && solver != SOLVER_BLOCK_ADJ) return -1;
+    if (tail < 1 || tail > LCH) return -1;
     if (!s_final || (T > 0 && (!q || !k || !v || !beta || !g || !o))) return -1;
     job_t J = {B, T, Nq, Nv, d, dv, solver, q, k, v, beta, g, h0, mask, o, s_final,
-               o_chunk, u, u_prime, w, s_in, score, cinv, nthreads < 1 ? 1 : nthreads};
+               o_chunk, u, u_prime, w, s_in, score, cinv, nthreads < 1 ? 1 : nthreads, tail};
     int units = B * Nv;
     if (J.nthreads > units) J.nthreads = units > 0 ? units : 1;
     pthread_t th[1024];
@@ -366,6 +369,19 @@ int gdn_oracle_prefill(int B, int T, int Nq, int Nv, int d, int dv,
     }
     for (int t = 0; t < J.nthreads; ++t) pthread_join(th[t], NULL);
     return 0;
+}
+
+/* The prefill with the default Tail-16 score window. */
+int gdn_oracle_prefill(int B, int T, int Nq, int Nv, int d, int dv,
+                       const double *q, const double *k, const double *v,
+                       const double *beta, const double *g, const double *h0,
+                       const unsigned char *mask, int solver, int nthreads,
+                       double *o, double *s_final,
+                       double *o_chunk, double *u, double *u_prime, double *w,
+                       double *s_in, double *score, double *cinv)
+{
+    return gdn_oracle_prefill_tail(B, T, Nq, Nv, d, dv, q, k, v, beta, g, h0, mask, solver, nthreads, o, s_final,
+                                   o_chunk, u, u_prime, w, s_in, score, cinv, BLK);
 }
 
 /* ---- event compaction (Sec. 2.5 CSR layout) ------------------------------

@@ -340,3 +340,29 @@ def test_ragged_tail_is_a_prefix_of_the_full_chunk():
     cut = oracle.prefill(x.q[:, :150], x.k[:, :150], x.v[:, :150], x.beta[:, :150], x.g[:, :150],
                          solver=oracle.SOLVER_BLOCK_ADJ)
     assert rel_fro(cut["o"], full["o"][:, :150]) < 1e-12
+
+
+# ------------------------------------------------------- Tail-W score windows ---
+
+def test_tail_windows_are_nested_norms():
+    # Tail-W = Frobenius norm of the last W rows of U (Eq. 9; W in {8, 16, 32, 64}, Fig. 10):
+    # nested windows are monotone, their squares differ by the rows in between, and on a full
+    # chunk Tail-64 is the norm of the whole U; a partial chunk shorter than W uses all its rows
+    x = gdn_synth.make_inputs(1, 64 * 3 + 20, 1, 2, d=32, dv=32, dtype="f32", seed=81, mask="ones")
+    s = {w: oracle.prefill(x.q, x.k, x.v, x.beta, x.g, debug=True, tail=w) for w in (8, 16, 32, 64)}
+    u = s[16]["u"]                                           # [B,T,Nv,dv], independent of the window
+    for h in range(2):
+        for c in range(4):
+            n = min(64, 212 - 64 * c)
+            rows = u[0, 64 * c:64 * c + n, h]
+            sq = {w: s[w]["score"][0, h, c] ** 2 for w in s}
+            assert sq[8] <= sq[16] <= sq[32] <= sq[64]
+            for w in (16, 32, 64):
+                lo, hi = max(0, n - w), max(0, n - w // 2)
+                assert abs(sq[w] - sq[w // 2] - np.sum(rows[lo:hi] ** 2)) <= 1e-12 * max(sq[w], 1e-300)
+            if n == 64:
+                assert abs(sq[64] - np.sum(rows ** 2)) <= 1e-12 * sq[64]
+            else:  # 20 rows: every window of 32 or more covers them all
+                assert sq[32] == sq[64]
+    # the window only changes the score
+    assert np.array_equal(s[8]["o"], s[64]["o"]) and np.array_equal(s[8]["s_final"], s[64]["s_final"])
