@@ -231,6 +231,26 @@ def run_reference(args):
 
 # ------------------------------------------------------------ our CUDA path ---
 
+def timed_variant(gdn, call, x, steps, world, dev, stream):
+    """Time `call()` (one prefill) over `steps` after 3 warm-ups: ms per step, tokens/s, stages, kernels."""
+    import torch
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    gdn.gdn_profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stage_ms, nrec, n_launch = gdn.gdn_profile_read(with_launches=True)
+    gdn.gdn_profile_enable(False)
+    ms = reduce_step_ms(e0.elapsed_time(e1) / steps, world, dev)
+    return {"ms_per_step": ms, "value": job_throughput(x.B * x.T, world, ms), "unit": UNIT, "gpu_launches": n_launch,
+            "stages_ms": {k: round(v / max(nrec, 1), 4) for k, v in stage_ms.items()}}
+
+
 def online_variant(gdn, d_in, x, ws, stream, steps, world, dev):
     """The same step with the events chosen on the GPU from the Tail-16 scores
     (SparseGDN Sec. 2.4) instead of the given mask: time, stages and retention."""
@@ -360,6 +380,13 @@ def run_ours(args):
         raise RuntimeError("host-buffer prefill disagrees with the device-buffer prefill")
 
     online = online_variant(gdn, d_in, x, ws, stream, args.steps, world, dev)
+    # the pages' ablation axes on the same inputs (gdn_prefill_ex): W deferred to its own kernel
+    # (bit-identical result) and the exact Full64 solver with the same mask
+    def ex_call(**kw):
+        return lambda: gdn.gdn_prefill_ex(d_in["q"], d_in["k"], d_in["v"], d_in["beta"], d_in["g"], mode="sparse",
+                                          mask=d_in["mask"], o=o, s_final=s_final, workspace=ws, stream=stream, **kw)
+    w_deferred = timed_variant(gdn, ex_call(solver="block_adj", w_deferred=True), x, args.steps, world, dev, stream)
+    exact = timed_variant(gdn, ex_call(solver="exact"), x, args.steps, world, dev, stream)
 
     peak, peak_kind = peaks()
     per_stage = {k: v / max(nrec, 1) for k, v in stage_ms.items()}
@@ -390,7 +417,7 @@ def run_ours(args):
                      "note": f"achieved = compulsory bytes of one {dom_kernel} launch / its mean CUDA-event time; "
                              f"frac of {peak_kind} HBM copy bandwidth"},
         "stages_ms": {k: round(v, 4) for k, v in per_stage.items()},
-        "variants": {"online_selection": online},
+        "variants": {"online_selection": online, "w_deferred": w_deferred, "solver_exact": exact},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x)

@@ -7,12 +7,14 @@ from ._binding import (  # noqa: F401
     EXPORTS,
     GdnError,
     GdnEvents,
+    GdnOptions,
     GdnShape,
     STAGES,
     Workspace,
     gdn_decode_step,
     gdn_events_status,
     gdn_prefill_dense,
+    gdn_prefill_ex,
     gdn_prefill_host,
     gdn_prefill_sparse,
     gdn_prefill_sparse_noalloc,

@@ -25,7 +25,7 @@ EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
            "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout",
            "gdn_prefill_sparse_online", "gdn_select_events_scored", "gdn_select_scored_workspace_bytes",
-           "gdn_prefill_host", "gdn_prefill_host_workspace_bytes", "gdn_decode_step")
+           "gdn_prefill_host", "gdn_prefill_host_workspace_bytes", "gdn_decode_step", "gdn_prefill_ex")
 STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output", "selector")
 
 
@@ -38,6 +38,13 @@ class GdnError(RuntimeError):
 class GdnShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Nq", ctypes.c_int32), ("Nv", ctypes.c_int32),
                 ("d", ctypes.c_int32), ("dv", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class GdnOptions(ctypes.Structure):
+    _fields_ = [("tail_window", ctypes.c_int32), ("w_deferred", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6)]
+
+
+MODES = {"dense": 0, "sparse": 1, "online": 2}
 
 
 class GdnEvents(ctypes.Structure):
@@ -79,6 +86,9 @@ def load(path: str | None = None):
             lib.gdn_select_events_scored.restype = i32
             lib.gdn_select_scored_workspace_bytes.argtypes = [shp]
             lib.gdn_select_scored_workspace_bytes.restype = sz
+            lib.gdn_prefill_ex.argtypes = [shp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.POINTER(GdnOptions),
+                                           vp, vp, vp, vp, vp, vp, sz, vp]
+            lib.gdn_prefill_ex.restype = i32
             lib.gdn_decode_step.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.gdn_decode_step.restype = i32
             lib.gdn_prefill_host.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
@@ -366,6 +376,43 @@ def gdn_prefill_host(q, k, v, beta, g, mask=None, *, h0=None, solver="block_adj"
             ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(mask),
             SOLVERS[solver], _ptr(o), _ptr(s_final), _ptr(ws), ws.numel(), _stream(stream)))
     return o, s_final
+
+
+def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=None, solver="block_adj",
+                   tail_window=0, w_deferred=False, o=None, s_final=None, score=None, mask_out=None,
+                   tier_out=None, workspace=None, stream=None):
+    """The general prefill with execution variants; returns (o, s_final, mask_out, tier_out)."""
+    B, T, Nq, d = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    C = (T + 63) // 64
+    _need(q, "q", shape=(B, T, Nq, d))
+    _need(k, "k", dtype=q.dtype, shape=(B, T, Nq, d))
+    _need(v, "v", dtype=q.dtype, shape=(B, T, Nv, dv))
+    _need(beta, "beta", torch.float32, (B, T, Nv))
+    _need(g, "g", torch.float32, (B, T, Nv))
+    _need(h0, "h0", torch.float32, (B, Nv, d, dv))
+    _need(mask, "mask", torch.uint8, (B, Nq, C))
+    _need(eta, "eta", torch.float32, (B, Nv))
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, T, Nv, dv), dtype=q.dtype, device=dev)
+    if s_final is None:
+        s_final = torch.empty((B, Nv, d, dv), dtype=torch.float32, device=dev)
+    if mode == "online":
+        if mask_out is None:
+            mask_out = torch.empty((B, Nq, C), dtype=torch.uint8, device=dev)
+        if tier_out is None:
+            tier_out = torch.empty((B, Nq), dtype=torch.int32, device=dev)
+    _need(score, "score", torch.float32, (B, Nv, C))
+    shape = shape_of(q, v)
+    opt = GdnOptions(int(tail_window), int(bool(w_deferred)))
+    ws = _workspace(workspace, gdn_workspace_bytes(shape, solver, MODES[mode]), dev)
+    with torch.cuda.device(dev):
+        _check("gdn_prefill_ex", load().gdn_prefill_ex(
+            ctypes.byref(shape), MODES[mode], _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(mask),
+            _ptr(eta), SOLVERS[solver], ctypes.byref(opt), _ptr(o), _ptr(s_final), _ptr(score), _ptr(mask_out),
+            _ptr(tier_out), _ptr(ws), ws.numel(), _stream(stream)))
+    return o, s_final, mask_out, tier_out
 
 
 def gdn_decode_step(q, k, v, beta, a, state, *, o=None, stream=None):

@@ -75,6 +75,7 @@ void fill_problem(const gdn_shape *s, gdn_solver solver, Problem *pb) {
     pb->dtype = s->dtype;
     pb->solver = solver;
     pb->nblk = solver == GDN_SOLVER_EXACT ? kBlkFull : kBlkAdj;
+    pb->tail = kBlk;
 }
 
 size_t elem_size(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
@@ -142,12 +143,24 @@ namespace {
 
 enum PrefillMode { kDense = 0, kSparse = 1, kOnline = 2 };
 
+gdn_status check_options(const gdn_options *opt) {
+    if (!opt) return GDN_OK;
+    const int tw = opt->tail_window;
+    if (tw != 0 && tw != 8 && tw != 16 && tw != 32 && tw != 64) return GDN_ERR_UNSUPPORTED;
+    if (opt->w_deferred != 0 && opt->w_deferred != 1) return GDN_ERR_UNSUPPORTED;
+    for (int i = 0; i < 6; ++i)
+        if (opt->reserved[i] != 0) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
 gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *beta,
                        const float *g, const float *h0, const uint8_t *mask, const float *eta, PrefillMode mode,
                        gdn_solver solver, void *o, float *s_final, float *score, uint8_t *mask_out,
-                       int32_t *tier_out, void *workspace, size_t workspace_bytes, void *stream) {
+                       int32_t *tier_out, void *workspace, size_t workspace_bytes, void *stream,
+                       const gdn_options *opt = nullptr) {
     gdn_status st = check_shape(shape);
     if (st != GDN_OK) return st;
+    if ((st = check_options(opt)) != GDN_OK) return st;
     if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return GDN_ERR_DTYPE;
     if (mode == kOnline && shape->Nv != 32) return GDN_ERR_UNSUPPORTED;  // the tier table is for 16 pairs
     const bool has_tokens = shape->B > 0 && shape->T > 0;
@@ -161,6 +174,8 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     Problem pb;
     fill_problem(shape, solver, &pb);
     pb.online = mode == kOnline;
+    if (opt && opt->tail_window) pb.tail = opt->tail_window;
+    const bool w_deferred = opt && opt->w_deferred;
     if (shape->B == 0) return GDN_OK;
     const size_t need = workspace_layout(pb, nullptr, nullptr);
     if (workspace_bytes < need) return GDN_ERR_WORKSPACE;
@@ -205,8 +220,10 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     } else {
         stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
-        stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, false) : launch_intra(pb, ws); });
-        stage(3, tc ? 0 : 1, [&] { return tc ? none() : launch_wbuild(pb, ws); });  // bf16: W is built inside intra
+        stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, w_deferred) : launch_intra(pb, ws); });
+        // bf16: W is built inside intra for the event chunks, or after it from C-bar (w_deferred)
+        stage(3, !tc || w_deferred ? 1 : 0,
+              [&] { return !tc ? launch_wbuild(pb, ws) : (w_deferred ? launch_wbuild_tc(pb, ws) : none()); });
         stage(8, 0, none);
     }
     stage(4, tc ? 1 : 0, [&] { return tc ? launch_scan_tc(pb, ws, 0) : none(); });
@@ -367,6 +384,18 @@ gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
     if (!device_ok()) return GDN_ERR_DEVICE;
     return launch_decode(*shape, q, k, v, beta, a, state, o, (cudaStream_t)stream) == cudaSuccess ? GDN_OK
                                                                                                   : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_prefill_ex(const gdn_shape *shape, gdn_mode mode, const void *q, const void *k, const void *v,
+                          const float *beta, const float *g, const float *h0, const uint8_t *mask, const float *eta,
+                          gdn_solver solver, const gdn_options *opt, void *o, float *s_final, float *score,
+                          uint8_t *mask_out, int32_t *tier_out, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    if (mode != GDN_MODE_DENSE && mode != GDN_MODE_SPARSE && mode != GDN_MODE_ONLINE) return GDN_ERR_UNSUPPORTED;
+    if (mode == GDN_MODE_SPARSE && shape && shape->B > 0 && shape->T > 0 && !mask) return GDN_ERR_NULL;
+    const PrefillMode m = mode == GDN_MODE_DENSE ? kDense : (mode == GDN_MODE_SPARSE ? kSparse : kOnline);
+    return run_prefill(shape, q, k, v, beta, g, h0, m == kSparse ? mask : nullptr, eta, m, solver, o, s_final, score,
+                       mask_out, tier_out, workspace, workspace_bytes, stream, opt);
 }
 
 gdn_status gdn_prefill_sparse_online(const gdn_shape *shape, const void *q, const void *k, const void *v,

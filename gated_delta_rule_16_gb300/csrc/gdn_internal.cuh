@@ -50,6 +50,7 @@ struct Problem {
     gdn_solver solver;
     int nblk;                  // 7 (block-adjacent) or 10 (exact)
     int online;                // workspace also holds the online-selection buffers
+    int tail;                  // rows of the Tail-W score window (16 by default)
     const void *q, *k, *v;
     const float *beta, *g, *h0;
     const uint8_t *mask;       // NULL: every chunk is an event

@@ -25,7 +25,7 @@ constexpr size_t kIntraSmem = sizeof(float) * (KS + 3 * MS + VS + 3 * 256 + 2 * 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__restrict__ beta,
-             const float *__restrict__ g, int T_, int Nq, int Nv, int C, int nblk, int exact,
+             const float *__restrict__ g, int T_, int Nq, int Nv, int C, int nblk, int exact, int tail,
              T *__restrict__ U, float *__restrict__ cbar, float *__restrict__ score) {
     extern __shared__ float sm[];
     float *Ks = sm;            // [64][129]
@@ -149,7 +149,7 @@ intra_kernel(const T *__restrict__ K, const T *__restrict__ V, const float *__re
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (t < n) io<T>::st(U + ((tok0 + t) * Nv + h) * kDim + tx + 32 * j, acc[i][j]);
-                if (t >= n - kBlk && t < n) sq += acc[i][j] * acc[i][j];  // Tail-16: the last 16 valid rows
+                if (t >= n - tail && t < n) sq += acc[i][j] * acc[i][j];  // Tail-W: the last W valid rows
             }
         }
 #pragma unroll
@@ -239,12 +239,12 @@ cudaError_t launch_intra(const Problem &pb, const Workspace &ws) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraSmem);
         kern<<<grid, kThreads, kIntraSmem, pb.stream>>>(
             (const __nv_bfloat16 *)pb.k, (const __nv_bfloat16 *)pb.v, pb.beta, pb.g, pb.T, pb.Nq, pb.Nv, pb.C,
-            pb.nblk, exact, (__nv_bfloat16 *)ws.U, ws.cbar, pb.score);
+            pb.nblk, exact, pb.tail, (__nv_bfloat16 *)ws.U, ws.cbar, pb.score);
     } else {
         auto kern = intra_kernel<float>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraSmem);
         kern<<<grid, kThreads, kIntraSmem, pb.stream>>>(
-            (const float *)pb.k, (const float *)pb.v, pb.beta, pb.g, pb.T, pb.Nq, pb.Nv, pb.C, pb.nblk, exact,
+            (const float *)pb.k, (const float *)pb.v, pb.beta, pb.g, pb.T, pb.Nq, pb.Nv, pb.C, pb.nblk, exact, pb.tail,
             (float *)ws.U, ws.cbar, pb.score);
     }
     return cudaGetLastError();

@@ -50,7 +50,7 @@ struct IntraParams {
     __nv_bfloat16 *cbar;    // non-NULL: write the compact C-bar blocks [B,Nv,C,nblk,16,16] (bf16)
     float *score;
     int32_t *status;
-    int P_, T_, Nv, C, nblk, exact;
+    int P_, T_, Nv, C, nblk, exact, tail;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -135,10 +135,10 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     const int t0 = c0 * kChunk;                        // first token of the group inside its sequence
     const int nvalid = min(2 * kChunk, a.T_ - t0);     // tokens of the group (a partial last chunk has fewer)
     const int64_t tok0 = (int64_t)b * a.T_ + t0;
-    // Tail-16 window of this thread's row: the last 16 valid rows of its chunk (rows past the
+    // Tail-W window of this thread's row: the last W valid rows of its chunk (rows past the
     // sequence's end need no exclusion: beta = 0 there makes their U rows exactly zero)
     const int nrow = min(kChunk, nvalid - kChunk * ct);
-    const bool in_tail = tl >= nrow - kBlk;
+    const bool in_tail = tl >= nrow - a.tail;
 
     if (tid == 0) {  // barriers, then the tiles: the loads overlap the set-up below
         mbar_init(&bar_ld, 1);
@@ -382,6 +382,7 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
     a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;
     a.exact = pb.solver == GDN_SOLVER_EXACT;
+    a.tail = pb.tail;
     cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraTcSmem);
     intra_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream>>>(tK, tV, tU, tW, a);
     return cudaGetLastError();

@@ -107,6 +107,28 @@ typedef struct {
     int32_t capacity;   /* entries available in ev_chunk and snap_slot */
 } gdn_events;
 
+/* What gdn_prefill_ex computes: every chunk an event, a caller mask, or events
+ * chosen on the GPU from the Tail-W scores (Sec. 2.4). */
+typedef enum { GDN_MODE_DENSE = 0, GDN_MODE_SPARSE = 1, GDN_MODE_ONLINE = 2 } gdn_mode;
+
+/* Execution variants (the pages' ablation axes; Secs. 3.4-3.5).  Zero-initialise:
+ * every field's zero value is the default.
+ *   tail_window  rows of the Tail-W write-score window, the last W rows of a
+ *                chunk's U: 0 (= 16), 8, 16, 32 or 64 (Fig. 10).  Changes only
+ *                the scores, and through them an online selection.
+ *   w_deferred   0: with a mask known up front, W = C-bar K is built inside the
+ *                intra step for the event chunks;  1: the intra step stores the
+ *                compact C-bar blocks and a separate tensor-core kernel builds W
+ *                for the events after compaction (the order online selection
+ *                needs).  The results are identical bit for bit (bf16 storage;
+ *                fp32 storage always builds W separately).
+ *   reserved     must be zero. */
+typedef struct {
+    int32_t tail_window;
+    int32_t w_deferred;
+    int32_t reserved[6];
+} gdn_options;
+
 /* Bytes of workspace the prefill entry points need for `shape`: sparse = 0
  * gdn_prefill_dense, 1 gdn_prefill_sparse, 2 gdn_prefill_sparse_online.
  * 0 for invalid shapes. */
@@ -175,6 +197,20 @@ GDN_API gdn_status gdn_prefill_sparse_online(const gdn_shape *shape,
                                      void *o, float *s_final, float *score, uint8_t *mask_out,
                                      int32_t *tier_out, void *workspace, size_t workspace_bytes,
                                      void *stream);
+
+/* The general prefill: `mode` selects dense (mask ignored), sparse (mask
+ * required) or online selection (eta, mask_out and tier_out as in
+ * gdn_prefill_sparse_online, 16 head pairs); `opt` (NULL = defaults) selects
+ * execution variants.  Arguments otherwise as gdn_prefill_sparse; workspace
+ * gdn_workspace_bytes(shape, solver, mode).  Unknown option values return
+ * GDN_ERR_UNSUPPORTED before anything is enqueued. */
+GDN_API gdn_status gdn_prefill_ex(const gdn_shape *shape, gdn_mode mode,
+                          const void *q, const void *k, const void *v,
+                          const float *beta, const float *g, const float *h0,
+                          const uint8_t *mask, const float *eta, gdn_solver solver,
+                          const gdn_options *opt, void *o, float *s_final, float *score,
+                          uint8_t *mask_out, int32_t *tier_out, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /* One autoregressive decode step from a state, e.g. the S_final of a prefill
  * (the pages return S_C for the decoding that follows; Sec. 2.6).  It is

@@ -175,3 +175,21 @@ def test_decode_validation(lib):
     assert dec(shape(T=1), q=0) == 1
     assert dec(shape(T=1), st=FAKE + 8) == 4
     assert dec(shape(B=0, T=1), q=0, st=0) == 0
+
+
+def test_prefill_ex_option_validation(lib):
+    f = ctypes.c_void_p(FAKE)
+
+    def ex(mode=1, opt=None, mask=FAKE):
+        o = opt or bnd.GdnOptions()
+        return lib.gdn_prefill_ex(ctypes.byref(shape()), mode, f, f, f, f, f, None, ctypes.c_void_p(mask), None, 1,
+                                  ctypes.byref(o), f, f, None, None, None, f, 1 << 40, None)
+
+    assert ex(opt=bnd.GdnOptions(12)) == 6                 # tail window must be 8, 16, 32 or 64
+    assert ex(opt=bnd.GdnOptions(16, 2)) == 6              # w_deferred is 0 or 1
+    r = bnd.GdnOptions(16, 0)
+    r.reserved[3] = 1
+    assert ex(opt=r) == 6                                  # reserved fields must be zero
+    assert ex(mode=7) == 6
+    assert ex(mask=0) == 1                                 # sparse mode needs a mask
+    assert ex(opt=bnd.GdnOptions(64, 1)) == 8              # valid: stops at the device check here

@@ -1,0 +1,79 @@
+"""Execution variants (gdn_prefill_ex): the pages' ablation axes, through the C ABI.
+
+  * W built inside the intra step vs. deferred to its own kernel after compaction
+    must give identical bits (bf16 storage; both solvers, sparse and dense);
+  * the Tail-W score window (W = 8, 16, 32, 64) changes only the scores, which
+    match the oracle's Tail-W scores; the outputs stay bit-identical;
+  * online selection on Tail-32 scores selects exactly what the oracle's
+    selector selects on the same scores.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdn_synth
+import oracle
+from gpu_helpers import TOL, assert_close, dev, to_dev
+
+import gated_delta_rule_16_gb300 as gdn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from gated_delta_rule_16_gb300 import build
+    build.build()
+    gdn.load()
+
+
+def run(t, **kw):
+    o, s, m, tier = gdn.gdn_prefill_ex(t["q"], t["k"], t["v"], t["beta"], t["g"], h0=t["h0"], **kw)
+    torch.cuda.synchronize()
+    return o, s, m, tier
+
+
+@pytest.mark.parametrize("solver", ["exact", "block_adj"])
+@pytest.mark.parametrize("mode", ["sparse", "dense"])
+def test_w_deferred_is_bit_identical(solver, mode):
+    x = gdn_synth.make_inputs(2, 1000, 16, 32, dtype="bf16", seed=91, mask="beta", with_h0=True)
+    t = to_dev(x)
+    mask = t["mask"] if mode == "sparse" else None
+    o1, s1, _, _ = run(t, mode=mode, mask=mask, solver=solver)
+    o2, s2, _, _ = run(t, mode=mode, mask=mask, solver=solver, w_deferred=True)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tail_windows_match_oracle_and_change_only_scores(dtype):
+    x = gdn_synth.make_inputs(1, 64 * 5 + 24, 2, 4, dtype=dtype, seed=92, mask="bernoulli", retention=0.6)
+    t = to_dev(x)
+    base = None
+    for w in (8, 16, 32, 64):
+        sc = torch.full((x.B, x.Nv, x.C), -1.0, device=dev())
+        o, s, _, _ = run(t, mode="sparse", mask=t["mask"], tail_window=w, score=sc)
+        ref = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=x.mask, debug=True, tail=w)
+        got = sc.cpu().numpy()
+        rel = np.abs(got - ref["score"]) / np.maximum(ref["score"], 1e-30)
+        assert rel.max() <= TOL[dtype], (w, rel.max())
+        if base is None:
+            base = (o, s)
+        else:
+            assert torch.equal(o, base[0]) and torch.equal(s, base[1])
+
+
+def test_online_selection_on_tail32_scores():
+    x = gdn_synth.make_inputs(1, 40 * 64, 16, 32, dtype="bf16", seed=93, mask="ones")
+    t = to_dev(x)
+    sc = torch.zeros((x.B, x.Nv, x.C), device=dev())
+    o, s, m, tier = run(t, mode="online", tail_window=32, score=sc)
+    gamma = np.ascontiguousarray(np.moveaxis(x.g[:, 63::64, :], 1, 2))
+    sel = oracle.select(sc.cpu().numpy(), gamma)
+    assert np.array_equal(m.cpu().numpy(), sel["mask"]) and np.array_equal(tier.cpu().numpy(), sel["tier"])
+    ref = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=m.cpu().numpy(), debug=True, tail=32)
+    rel = np.abs(sc.cpu().numpy() - ref["score"]) / np.maximum(ref["score"], 1e-30)
+    assert rel.max() <= TOL["bf16"]
+    assert_close({"o": o.float().cpu().numpy().astype(np.float64), "s_final": s.cpu().numpy().astype(np.float64)},
+                 ref, "bf16", "online Tail-32")
