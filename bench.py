@@ -37,6 +37,15 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 
 
+# DRAM bytes (read + write) of one launch, measured with ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum) on the current version of the kernel and workload; an entry must be
+# removed whenever its kernel changes (the roofline's traffic is then reported as null).
+PROFILED_TRAFFIC = {
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 737.24e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 918.41e6,
+}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,7 +421,8 @@ def run_ours(args):
                 "pipelining": "2 streams x 2 workspaces", "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": n_launch,
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                     "frac": achieved / peak, "traffic": PROFILED_TRAFFIC.get((args.workload, dom_kernel)),
+                     "peak_source": peak_kind,
                      "step_frac": step_gbs / peak,
                      "note": f"achieved = compulsory bytes of one {dom_kernel} launch / its mean CUDA-event time; "
                              f"frac of {peak_kind} HBM copy bandwidth"},
