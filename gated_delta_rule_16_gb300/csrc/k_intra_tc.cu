@@ -278,7 +278,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 const int rw = blk_row(blk) * kBlk + rr, cl = blk_col(blk) * kBlk + col0;
                 const float *cr = Cs + (cc * kChunk + rw) * MS + cl;
                 const float *bg = bgs + 64 * cc + cl;
-                __nv_bfloat162 p2[4];
+                alignas(16) __nv_bfloat162 p2[4];
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2)
                     p2[q2] = __floats2bfloat162_rn(cr[2 * q2] * bg[2 * q2], cr[2 * q2 + 1] * bg[2 * q2 + 1]);

@@ -54,6 +54,9 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
     __shared__ float gs[2][128];
+    __shared__ __align__(16) float colf[2][128];  // 2^(c_h - G_j): column factors of the group's decay mask
+    __shared__ float cref[2], gmax_w[2][4], gmin_w[2][4];
+    __shared__ int fact[2];          // 1: the mask factorises (the group's log-decay range is moderate)
     __shared__ float fscale[2];
     __shared__ int has_s[2], slot_s[2];
 
@@ -107,6 +110,36 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tbase = tmem_base;
 
+    // Decay mask of the group.  With G_t the log2 decay accumulated from the group's start
+    // (chunk c: g_t; chunk c+1: gamma_c + g_t), every kept entry (j <= i, same chunk or the
+    // cross block) is 2^(G_i - G_j).  When the group's range of G is moderate the mask is a
+    // product of a row factor 2^(G_i - c) and a column factor 2^(c - G_j), c the middle of the
+    // range, so the A tile needs no per-element exp2; otherwise it falls back to one exp2 each.
+    auto gcum = [&](int hh, int t) { return t < 64 ? gs[hh][t] : gs[hh][63] + gs[hh][t]; };
+    if (tid < 256) {
+        const int hh = tid >> 7, t = tid & 127, wi = (tid >> 5) & 3;
+        const bool used = t < (two ? 128 : 64);
+        float mx = used ? gcum(hh, t) : -INFINITY, mn = used ? gcum(hh, t) : INFINITY;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
+        if (lane == 0) { gmax_w[hh][wi] = mx; gmin_w[hh][wi] = mn; }
+    }
+    __syncthreads();
+    if (tid < 256) {
+        const int hh = tid >> 7, t = tid & 127;
+        const float mx = fmaxf(fmaxf(gmax_w[hh][0], gmax_w[hh][1]), fmaxf(gmax_w[hh][2], gmax_w[hh][3]));
+        const float mn = fminf(fminf(gmin_w[hh][0], gmin_w[hh][1]), fminf(gmin_w[hh][2], gmin_w[hh][3]));
+        const float c = 0.5f * (mx + mn);
+        colf[hh][t] = ex2(c - gcum(hh, t));
+        if (t == 0) {
+            cref[hh] = c;
+            fact[hh] = (mx - mn) <= 200.f;  // both factors stay within 2^(+-100)
+        }
+    }
+
     // initial-state path (no predecessor event, h0 given): S^T = h0^T in bf16, K-major slabs
     auto fill_h0 = [&](int hh, uint8_t *dst) {
         const float *src = a.h0 + ((int64_t)b * a.Nv + 2 * p + hh) * (kDim * kDim);
@@ -151,28 +184,35 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         if (!mbar_wait(hh == 0 ? &bar_qk_mma : &bar_h_mma, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
         tc_fence_after();
         {
-            const float *g = gs[hh];
             const int ci = row >> 6;
-            const float gi = g[row];
-            const float gam0 = g[63];
-            {
-                float qk[32];
-                const int j0 = 32 * seg;
-                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QK + j0), qk);
-                tmem_ld_wait();
-                float w[32];
+            const float Gi = gcum(hh, row);
+            const bool zero_row = ci == 1 && !two;  // a final single-chunk group has no second chunk
+            float qk[32];
+            const int j0 = 32 * seg;
+            tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QK + j0), qk);
+            tmem_ld_wait();
+            float w[32];
+            if (fact[hh]) {
+                const float ef = ex2(Gi - cref[hh]);
+                const float4 *cf = reinterpret_cast<const float4 *>(colf[hh] + j0);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const int jj = j0 + t, cj = jj >> 6;
-                    float m = 0.f;
-                    if (ci == cj) m = jj <= row ? ex2(gi - g[jj]) : 0.f;
-                    else if (ci == 1) m = ex2(gi + gam0 - g[jj]);
-                    w[t] = (ci == 1 && !two) ? 0.f : qk[t] * m;
+                for (int t4 = 0; t4 < 8; ++t4) {
+                    const float4 f = cf[t4];
+                    const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = 4 * t4 + u;
+                        w[t] = (j0 + t <= row && !zero_row) ? qk[t] * ef * fv[u] : 0.f;
+                    }
                 }
+            } else {
 #pragma unroll
-                for (int t0 = 0; t0 < 32; t0 += 8)
-                    st_sw128_8(sm + OFF_A + (seg >> 1) * kSlab, row, 32 * (seg & 1) + t0, &w[t0]);
+                for (int t = 0; t < 32; ++t)
+                    w[t] = (j0 + t <= row && !zero_row) ? qk[t] * ex2(Gi - gcum(hh, j0 + t)) : 0.f;
             }
+#pragma unroll
+            for (int t0 = 0; t0 < 32; t0 += 8)
+                st_sw128_8(sm + OFF_A + (seg >> 1) * kSlab, row, 32 * (seg & 1) + t0, &w[t0]);
         }
         if (hh == 1 && has_s[1] == 2) fill_h0(1, sm + OFF_K);
         fence_async_smem();

@@ -206,7 +206,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
             uint4 *sn = reinterpret_cast<uint4 *>(a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim) + row * kDim + cs);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                __nv_bfloat162 p2[4];
+                alignas(16) __nv_bfloat162 p2[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) p2[u] = __floats2bfloat162_rn(S[8 * q + 2 * u], S[8 * q + 2 * u + 1]);
                 sn[q] = *reinterpret_cast<uint4 *>(p2);
