@@ -113,7 +113,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tW, IntraParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
-    __shared__ uint64_t bar_ld, bar_g, bar_u, bar_drain;
+    __shared__ uint64_t bar_ld, bar_g, bar_u, bar_w, bar_drain;
     __shared__ int ev_s[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
@@ -144,6 +144,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_g, 1);
         mbar_init(&bar_u, 1);
+        mbar_init(&bar_w, 1);
         mbar_init(&bar_drain, 1);
         fence_mbar_init();
         abort_s = 0;
@@ -190,7 +191,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         const int h = 2 * p + hh;
         const float *bet = bet2 + 128 * hh;
         const float *gg = gg2 + 128 * hh;
-        if (tid == 0) bulk_wait_read();  // the W store of the previous head has left the A tile
         if (tid < 128) bgs[tid] = bet[tid] * ex2(gg[tid]);
         if (tid < 2) ssum[tid] = 0.f;
         __syncthreads();
@@ -237,6 +237,9 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             for (int i2 = 0; i2 < kBlk; ++i2) Cb[i2 * MS] = x[i2];
         }
         __syncthreads();
+        // the previous head's W store must have left the A tile before step 3 rewrites it (the
+        // barriers inside the off-diagonal step order this wait before those writes)
+        if (tid == 0) bulk_wait_read();
         offdiag_blocks<1>(Ms, Cs, Tb, tid);
         if (max_off == 3) {
             offdiag_blocks<2>(Ms, Cs, Tb, tid);
@@ -297,11 +300,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
                          mnmajor_desc(smem_addr(vt), ks, kSlab), id, ks > 0);
-            if (any_event)
+            mma_commit(&bar_u);
+            if (any_event) {  // W on its own barrier: the U epilogue below overlaps it
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tbase + TM_W, kmajor_desc(smem_addr(Ms), ks, kSlab),
                              mnmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id, ks > 0);
-            mma_commit(&bar_u);
+                mma_commit(&bar_w);
+            }
         }
         if (!mbar_wait(&bar_u, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
         tc_fence_after();
@@ -323,6 +328,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 #pragma unroll
             for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
             if (lane == 0 && sq != 0.f) atomicAdd(&ssum[ct], sq);
+            if (any_event && !mbar_wait(&bar_w, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+            tc_fence_after();
             if (ev_s[ct] >= 0) {
                 uint8_t *wstage = sm + OFF_A + slab * kSlab;
                 float w[32];
