@@ -30,7 +30,7 @@ constexpr uint32_t OFF_U0 = 6 * kSlab;     // U' of head 0: 2 MN-stacks [128 tok
 constexpr uint32_t OFF_U1 = 8 * kSlab;     // U' of head 1
 constexpr uint32_t OFF_A = 10 * kSlab;     // decayed masked A: 2 K-slabs [128 q][64 k]
 constexpr uint32_t kOutSmem = 1024 + 12 * kSlab;
-constexpr uint32_t TM_QK = 0, TM_QS = 128, TM_AU = 256;
+constexpr uint32_t TM_QK = 0, TM_QS = 128, TM_AU = 256, TM_QS1 = 384;  // QS of head 0 / head 1
 
 struct OutParams {
     const float *g, *h0;
@@ -183,6 +183,28 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         // 1. A_h from QK (waits for the QK MMA; for head 1 also for head 0's AU MMA to free the A tile)
         if (!mbar_wait(hh == 0 ? &bar_qk_mma : &bar_h_mma, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
         tc_fence_after();
+        if (tid == 0 && !abort_s) {
+            if (hh == 0 && has_s[1] == 1) {  // the K tile is free once QK is done: head 1's snapshot goes there
+                mbar_arrive_expect_tx(&bar_s[1], 2 * kSlab);
+                tma_load_3d(sm + OFF_K, &tS, 0, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s[1]);
+                tma_load_3d(sm + OFF_K + kSlab, &tS, 64, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s[1]);
+                s1_issued = true;
+            }
+            // QS of this head needs only Q and its entry state (head 1 from h0: written with its A
+            // tile, so issued with AU below): issue it now, while the A tile is built
+            const bool qs_now = has_s[hh] == 1 || (hh == 0 && has_s[0] == 2);
+            if (qs_now) {
+                if (has_s[hh] == 1 && !mbar_wait(&bar_s[hh], 0)) {
+                    abort_s = 1;
+                    atomicOr(a.status, kStatusTimeout);
+                } else {
+                    uint8_t *st = sm + (hh ? OFF_K : OFF_S0);
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16(tbase + (hh ? TM_QS1 : TM_QS), kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                                 kmajor_desc(smem_addr(st), ks, kSlab), id_kk, ks > 0);
+                }
+            }
+        }
         {
             const int ci = row >> 6;
             const float Gi = gcum(hh, row);
@@ -227,12 +249,11 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
                 atomicOr(a.status, kStatusTimeout);
             } else {
                 tc_fence_after();
-                uint8_t *st = sm + (hh ? OFF_K : OFF_S0);
                 uint8_t *ut = sm + (hh ? OFF_U1 : OFF_U0);
-                if (has_s[hh])
+                if (hh == 1 && has_s[1] == 2)  // head 1 from h0: its state was written with the A tile
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16(tbase + TM_QS, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
-                                 kmajor_desc(smem_addr(st), ks, kSlab), id_kk, ks > 0);
+                        mma_bf16(tbase + TM_QS1, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                                 kmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id_kk, ks > 0);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tbase + TM_AU, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
                              mnmajor_desc(smem_addr(ut), ks, kSlab), id_km, ks > 0);
@@ -243,13 +264,6 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         if (abort_s) break;
         if (!mbar_wait(&bar_h_mma, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
         tc_fence_after();
-        // the K tile is free once QK is done: fetch head 1's snapshot into it
-        if (hh == 0 && tid == 0 && has_s[1] == 1) {
-            mbar_arrive_expect_tx(&bar_s[1], 2 * kSlab);
-            tma_load_3d(sm + OFF_K, &tS, 0, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s[1]);
-            tma_load_3d(sm + OFF_K + kSlab, &tS, 64, (slot_s[1] * 2 + 1) * kDim, 0, &bar_s[1]);
-            s1_issued = true;
-        }
         // 3. epilogue of head hh: O rows staged (bf16, 128B-swizzled) in the U' tile
         //    this head no longer needs, then written by one TMA store
         {
@@ -260,7 +274,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
                 float qs[32], au[32];
                 const int col = 32 * seg;
                 tmem_ld32(tmem_addr(tbase, quarter * 32, TM_AU + col), au);
-                if (has) tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QS + col), qs);
+                if (has) tmem_ld32(tmem_addr(tbase, quarter * 32, (hh ? TM_QS1 : TM_QS) + col), qs);
                 tmem_ld_wait();
 #pragma unroll
                 for (int t = 0; t < 32; ++t) au[t] = ((has ? f * qs[t] : 0.f) + au[t]) * inv_sqrt_d;
