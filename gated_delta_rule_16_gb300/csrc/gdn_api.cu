@@ -202,11 +202,18 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     auto mark = [&](int i) { if (prof) cudaEventRecord(prof[i], pb.stream); };
     const bool tc = pb.dtype == GDN_BF16;   // tensor-core path for bf16 storage
     cudaError_t e = cudaSuccess;
+    // Tensor-core path: every kernel after the prefill's first is a programmatic dependent of
+    // the one before (it may start while that one drains).  Not while profiling: the stage
+    // events between launches serialise them anyway.
+    pb.pdl_ok = tc && !prof;
+    bool launched = false;
     // kernels: how many kernels the stage's launcher issues (0 for an empty stage)
     auto stage = [&](int id, int kernels, auto &&launch) {
         mark(2 * id);
+        pb.pdl = pb.pdl_ok && launched;
         if (e == cudaSuccess) e = launch();
         mark(2 * id + 1);
+        if (kernels > 0) launched = true;
         if (prof) g_prof.launches += kernels;
     };
     auto none = [] { return cudaSuccess; };

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/gdn.h"
 
 namespace gdn {
@@ -43,6 +45,33 @@ template <> struct io<__nv_bfloat16> {
     static __device__ __forceinline__ void st(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 };
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel of the stream is still running (its CTAs fill the SMs the
+// previous kernel's last wave leaves idle).  Every such kernel calls pdl_wait()
+// in every CTA before it touches anything an earlier kernel wrote (and before any
+// early exit, so that a kernel's completion still implies its predecessors'), and
+// pdl_trigger() to let its own successor launch early.  Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---- problem description shared by the launchers -------------------------
 struct Problem {
     int B, T, Nq, Nv, d, dv, C, G, P, R;
@@ -51,6 +80,8 @@ struct Problem {
     int nblk;                  // 7 (block-adjacent) or 10 (exact)
     int online;                // workspace also holds the online-selection buffers
     int tail;                  // rows of the Tail-W score window (16 by default)
+    int pdl;                   // launch the stage's first kernel as a programmatic dependent of the previous one
+    int pdl_ok;                // programmatic dependent launch allowed in this prefill (later kernels of a stage)
     const void *q, *k, *v;
     const float *beta, *g, *h0;
     const uint8_t *mask;       // NULL: every chunk is an event

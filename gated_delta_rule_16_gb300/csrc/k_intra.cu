@@ -179,7 +179,8 @@ prefix_kernel(const float *__restrict__ g, int T_, int Nv, int C, int P_, int G,
     extern __shared__ double Ps[];  // [2][C + 1]: P of both heads, for the group table (when it fits)
     const int bp = blockIdx.x, b = bp / P_, p = bp % P_;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < 2) {  // warp hh scans head 2p + hh: the gate tails of 32 chunks per step, loads issued ahead
+    pdl_trigger();
+    if (warp < 2) {  // P needs only the gates: it overlaps the kernel before  // warp hh scans head 2p + hh: the gate tails of 32 chunks per step, loads issued ahead
         const int h = 2 * p + warp;
         double *Pu = P + ((int64_t)b * Nv + h) * (C + 1);
         double *Pl = p_in_smem ? Ps + warp * (C + 1) : Pu;
@@ -207,6 +208,7 @@ prefix_kernel(const float *__restrict__ g, int T_, int Nv, int C, int P_, int G,
             }
         }
     }
+    pdl_wait();  // the group table reads the compaction's output
     if (!grp_info) return;
     __syncthreads();  // P of both heads written (shared memory, or global memory by this CTA)
     const double *P0 = p_in_smem ? Ps : P + ((int64_t)b * Nv + 2 * p) * (C + 1);
@@ -259,10 +261,9 @@ cudaError_t launch_prefix(const Problem &pb, const Workspace &ws) {
         cudaError_t e = cudaFuncSetAttribute(prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    prefix_kernel<<<pb.R, 256, smem, pb.stream>>>(pb.g, pb.T, pb.Nv, pb.C, pb.P, pb.G, ws.grp_pred, ws.snap_slot,
-                                                  ws.ev_chunk, ws.ev_cap, ws.snap_cap, pb.h0 != nullptr, ws.P,
-                                                  (int4 *)ws.grp_info, in_smem);
-    return cudaGetLastError();
+    return launch_kernel(pb.pdl, prefix_kernel, pb.R, 256, smem, pb.stream, pb.g, pb.T, pb.Nv, pb.C, pb.P, pb.G,
+                         (const int32_t *)ws.grp_pred, (const int32_t *)ws.snap_slot, (const int32_t *)ws.ev_chunk,
+                         ws.ev_cap, ws.snap_cap, (int)(pb.h0 != nullptr), ws.P, (int4 *)ws.grp_info, in_smem);
 }
 
 }  // namespace gdn

@@ -140,6 +140,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     const int nrow = min(kChunk, nvalid - kChunk * ct);
     const bool in_tail = tl >= nrow - a.tail;
 
+    pdl_trigger();
     if (tid == 0) {  // barriers, then the tiles: the loads overlap the set-up below
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_g, 1);
@@ -157,7 +158,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             tma_load_4d(vd + kSlab, &tV, 64, 2 * p + hh, t0, b, &bar_ld);
         }
     }
-    if (tid < 2) ev_s[tid] = (a.ev_of && tid < nch) ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
     if (tid < 256) {  // beta and g of both heads, fetched once while the tiles load
         // tokens past the sequence's end: beta = 0 (no write, no correction) and a finite g
         const int hh = tid >> 7, t = tid & 127;
@@ -171,7 +171,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
-    const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;
     if (tid == 0) {
         if (!mbar_wait(&bar_ld, 0)) {
             abort_s = 1;
@@ -240,11 +239,16 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         // the previous head's W store must have left the A tile before step 3 rewrites it (the
         // barriers inside the off-diagonal step order this wait before those writes)
         if (tid == 0) bulk_wait_read();
+        if (hh == 0) {  // the event index of the group's chunks: the compaction's output
+            pdl_wait();
+            if (tid < 2) ev_s[tid] = (a.ev_of && tid < nch) ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
+        }
         offdiag_blocks<1>(Ms, Cs, Tb, tid);
         if (max_off == 3) {
             offdiag_blocks<2>(Ms, Cs, Tb, tid);
             offdiag_blocks<3>(Ms, Cs, Tb, tid);
         }
+        const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;  // published by the barriers above
         // 3. A tiles: C diag(beta) for U, and C diag(beta 2^g) for W (built in the
         //    fp32 M area, free once the solve is done); both bf16, block-diagonal
         {
@@ -366,6 +370,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         mma_commit(&bar_drain);
         mbar_wait(&bar_drain, 0);
     }
+    pdl_wait();  // also on an early exit: this grid's completion implies its predecessors'
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc<512>(tbase);
@@ -391,8 +396,8 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
     a.exact = pb.solver == GDN_SOLVER_EXACT;
     a.tail = pb.tail;
     cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraTcSmem);
-    intra_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream>>>(tK, tV, tU, tW, a);
-    return cudaGetLastError();
+    return launch_kernel(pb.pdl, intra_tc_kernel, dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream, tK, tV,
+                         tU, tW, a);
 }
 
 }  // namespace gdn

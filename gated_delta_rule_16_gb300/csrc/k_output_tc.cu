@@ -70,7 +70,8 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     const int nvalid = min(2 * kChunk, a.T_ - t0);  // tokens of the group (a partial last chunk has fewer)
     const int64_t tok0 = (int64_t)b * a.T_ + t0;
 
-    if (tid == 0) {  // the tiles that do not depend on the predecessor lookup go first
+    pdl_trigger();
+    if (tid == 0) {  // the caller's Q and K go first: they do not depend on the kernels before
         mbar_init(&bar_qk_ld, 1);
         mbar_init(&bar_h_ld[0], 1);
         mbar_init(&bar_h_ld[1], 1);
@@ -86,6 +87,14 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         tma_load_4d(sm + OFF_Q + kSlab, &tQ, 64, p, t0, b, &bar_qk_ld);
         tma_load_4d(sm + OFF_K, &tK, 0, p, t0, b, &bar_qk_ld);
         tma_load_4d(sm + OFF_K + kSlab, &tK, 64, p, t0, b, &bar_qk_ld);
+    }
+    for (int idx = tid; idx < 256; idx += kThreads) {  // tokens past the sequence's end: a finite g
+        const int hh = idx >> 7, t = idx & 127;
+        gs[hh][t] = a.g[(tok0 + min(t, nvalid - 1)) * a.Nv + 2 * p + hh];
+    }
+    if (warp == 0) tmem_alloc<512>(&tmem_base);
+    pdl_wait();  // U', the entry-state table and the snapshots come from the kernels before
+    if (tid == 0) {
         for (int hh = 0; hh < 2; ++hh) {
             uint8_t *ud = sm + (hh ? OFF_U1 : OFF_U0);
             mbar_arrive_expect_tx(&bar_h_ld[hh], 2 * kSlab);
@@ -100,11 +109,6 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         slot_s[hh] = info.x;
         fscale[hh] = __int_as_float(hh ? info.w : info.z);
     }
-    for (int idx = tid; idx < 256; idx += kThreads) {  // tokens past the sequence's end: a finite g
-        const int hh = idx >> 7, t = idx & 127;
-        gs[hh][t] = a.g[(tok0 + min(t, nvalid - 1)) * a.Nv + 2 * p + hh];
-    }
-    if (warp == 0) tmem_alloc<512>(&tmem_base);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -325,8 +329,8 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
     a.O = (__nv_bfloat16 *)pb.o; a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.G = pb.G;
     cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
-    output_tc_kernel<<<dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream>>>(tQ, tK, tU, tS, tO, a);
-    return cudaGetLastError();
+    return launch_kernel(pb.pdl, output_tc_kernel, dim3(pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream, tQ, tK, tU,
+                         tS, tO, a);
 }
 
 }  // namespace gdn

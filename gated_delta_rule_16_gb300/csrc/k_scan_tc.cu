@@ -106,8 +106,10 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     const int rho = blockIdx.x, j = blockIdx.z;
     const int hh = fixup ? (int)blockIdx.y : (int)(blockIdx.y >> 1);
     const int mode = fixup ? kModeFixup : (int)(blockIdx.y & 1);
-    const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
     const int c_lo = rho * kRun, c_hi = min(a.C, c_lo + kRun);
+    pdl_wait();  // everything below reads what the kernels before wrote
+    pdl_trigger();
+    const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
 
     if (tid == 0) {
         const int64_t f = min((int64_t)a.run_first[(int64_t)j * (a.NR + 1) + rho], a.ev_cap);
@@ -372,6 +374,8 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     const int row = quarter * 32 + lane;
     const int cs = 32 * seg, slab = seg >> 1, cin = 32 * (seg & 1);
     const int hh = blockIdx.x, j = blockIdx.y;
+    pdl_wait();  // the run maps of the kernel before
+    pdl_trigger();
     const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
     const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
     const int64_t sbase = ((int64_t)b * a.Nv + h) * (kDim * kDim);
@@ -540,8 +544,7 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
         return cudaErrorInvalidValue;
     if (part == 1) {  // chain
         cudaFuncSetAttribute(scan_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
-        scan_chain_kernel<<<dim3(2, pb.R), kThreads, kChainSmem, pb.stream>>>(tA, a);
-        return cudaGetLastError();
+        return launch_kernel(pb.pdl, scan_chain_kernel, dim3(2, pb.R), kThreads, kChainSmem, pb.stream, tA, a);
     }
     if (NR == 0 || pb.C == 0) return cudaSuccess;
     CUtensorMap tW, tK, tU;
@@ -552,8 +555,8 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(scan_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmem);
     const int fixup = part == 2;
-    scan_run_kernel<<<dim3(NR, fixup ? 2 : 4, pb.R), kThreads, kRunSmem, pb.stream>>>(tW, tK, tU, tA, a, fixup);
-    return cudaGetLastError();
+    return launch_kernel(pb.pdl, scan_run_kernel, dim3(NR, fixup ? 2 : 4, pb.R), kThreads, kRunSmem, pb.stream, tW,
+                         tK, tU, tA, a, fixup);
 }
 
 }  // namespace gdn

@@ -94,6 +94,8 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     unsigned *words = reinterpret_cast<unsigned *>(refb + R + 1);  // [kWarps][NW] one row's mask bits
     __shared__ int warp_tot[33];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();  // an online selection writes the mask just before
+    pdl_trigger();
     unsigned *wrow = words + warp * NW;
 
     // 1. events per row
@@ -232,11 +234,9 @@ cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_
         cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    select_kernel<<<1, kThreads, smem, pb.stream>>>(pb.mask, pb.R, pb.C, pb.G, ev.row_pair, ev.row_ptr,
-                                                    ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts,
-                                                    ev_of, run_first, (pb.C + kRunChunks - 1) / kRunChunks,
-                                                    (int64_t)ev.capacity, snap_cap);
-    return cudaGetLastError();
+    return launch_kernel(pb.pdl, select_kernel, 1, kThreads, smem, pb.stream, pb.mask, pb.R, pb.C, pb.G, ev.row_pair,
+                         ev.row_ptr, ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts, ev_of, run_first,
+                         (pb.C + kRunChunks - 1) / kRunChunks, (int64_t)ev.capacity, snap_cap);
 }
 
 }  // namespace gdn

@@ -93,6 +93,8 @@ selector_pair_kernel(const float *__restrict__ score, const float *__restrict__ 
     __shared__ float norm[2];
     __shared__ double L[2], G[2], rr[2], red[kThreads / 32], red2[kThreads / 32];
     const int p = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    pdl_wait();  // the intra step's scores
+    pdl_trigger();
     const int h0 = 2 * p;
     const float *s0 = score + ((int64_t)b * Nv + h0) * C;
     const float *s1 = s0 + C;
@@ -215,6 +217,8 @@ selector_tier_kernel(int C, const int32_t *__restrict__ rank_ws, const double *_
     __shared__ double gLM[kPairs], gMH[kPairs], xM[kPairs], xH[kPairs], xs[kPairs], sep[kPairs];
     __shared__ int ids[kPairs], rest[kPairs], tier[kPairs], kk[3], nH_s, nr_s;
     const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();  // the pair kernel's ranks and gains
+    pdl_trigger();
     if (tid < kPairs) {
         gLM[tid] = gains[((int64_t)b * kPairs + tid) * 2];
         gMH[tid] = gains[((int64_t)b * kPairs + tid) * 2 + 1];
@@ -307,12 +311,11 @@ cudaError_t launch_selector(const Problem &pb, const float *score, const float *
     if (e != cudaSuccess) return e;
     double *gains = (double *)ws;                                    // [B,16,2]
     int32_t *rank = (int32_t *)(gains + (size_t)pb.B * kPairs * 2);  // [B,16,C]
-    selector_pair_kernel<<<dim3(kPairs, pb.B), kThreads, smem, pb.stream>>>(score, pb.g, eta, pb.T, pb.Nv, pb.C,
-                                                                            npow2, rank, gains);
-    e = cudaGetLastError();
+    e = launch_kernel(pb.pdl, selector_pair_kernel, dim3(kPairs, pb.B), kThreads, smem, pb.stream, score, pb.g, eta,
+                      pb.T, pb.Nv, pb.C, npow2, rank, gains);
     if (e != cudaSuccess) return e;
-    selector_tier_kernel<<<pb.B, 256, 0, pb.stream>>>(pb.C, rank, gains, mask, tier_out);
-    return cudaGetLastError();
+    return launch_kernel(pb.pdl_ok, selector_tier_kernel, pb.B, 256, 0, pb.stream, pb.C, (const int32_t *)rank,
+                         (const double *)gains, mask, tier_out);
 }
 
 }  // namespace gdn

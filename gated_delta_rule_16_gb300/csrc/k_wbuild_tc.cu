@@ -64,6 +64,8 @@ wbuild_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__
     __shared__ uint32_t tmem_base;
     __shared__ int ev_b[2], ev_p[2], ev_c[2], abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();  // C-bar and the event lists of the kernels before
+    pdl_trigger();
     const int64_t E = min((int64_t)a.counts[0], a.ev_cap);
     const int64_t npairs = (E + 1) / 2;
     if (blockIdx.x >= npairs) return;
@@ -221,8 +223,7 @@ cudaError_t launch_wbuild_tc(const Problem &pb, const Workspace &ws) {
     const int64_t pairs = (ws.ev_cap + 1) / 2;
     const int grid = (int)(pairs < kMaxGrid ? pairs : kMaxGrid);
     cudaFuncSetAttribute(wbuild_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWbuildSmem);
-    wbuild_tc_kernel<<<grid, kThreads, kWbuildSmem, pb.stream>>>(tK, tW, a);
-    return cudaGetLastError();
+    return launch_kernel(pb.pdl, wbuild_tc_kernel, grid, kThreads, kWbuildSmem, pb.stream, tK, tW, a);
 }
 
 }  // namespace gdn
