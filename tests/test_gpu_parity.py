@@ -244,3 +244,13 @@ def test_ragged_T_qwen_layer_sampled_pairs():
         ref = oracle_run(y, "block_adj")
         got = {"o": res["o"][b:b + 1, :, 2 * p:2 * p + 2], "s_final": res["s_final"][b:b + 1, 2 * p:2 * p + 2]}
         assert_close(got, ref, "bf16", f"ragged layer seq {b} pair {p}")
+
+
+def test_maximum_chunk_count_one_pair():
+    # the largest sequence the boundary accepts: C = 16384 chunks (T = 1,048,576), one head pair,
+    # 29% events and an initial state: 1024 scan runs per row (the chain's limit), the compaction's
+    # largest mask staging; compared with the oracle on every token and the final state
+    x = gdn_synth.make_inputs(1, 64 * 16384, 1, 2, dtype="bf16", seed=29, mask="beta", with_h0=True)
+    res = run_gpu(x, solver="block_adj")
+    ref = oracle_run(x, "block_adj")
+    assert_close(res, ref, "bf16", "C=16384")
