@@ -106,8 +106,10 @@ def test_all_ones_sparse_equals_dense_bitwise():
 
 @pytest.mark.parametrize("shape,p", [((1, 1, 4), 0.5), ((2, 3, 7), 0.4), ((3, 16, 33), 0.29),
                                      ((1, 16, 512), 0.29), ((8, 16, 512), 0.29), ((2, 3, 6), 1.0),
-                                     ((2, 3, 6), 0.0), ((1, 16, 2048), 0.1), ((4, 5, 1), 0.5)])
+                                     ((2, 3, 6), 0.0), ((1, 16, 2048), 0.1), ((4, 5, 1), 0.5),
+                                     ((1, 16, 16384), 0.002), ((2, 16, 10000), 0.05), ((64, 16, 1024), 0.29)])
 def test_csr_bit_exact(shape, p):
+    # the last case is too large for the word-parallel compaction and takes the row-per-warp kernel
     rng = np.random.default_rng(sum(shape))
     m = (rng.random(shape) < p).astype(np.uint8)
     ev = gdn.gdn_select_events(torch.from_numpy(m).to(dev()))
