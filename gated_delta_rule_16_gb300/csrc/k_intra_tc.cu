@@ -1,19 +1,29 @@
 // k_intra_tc.cu -- intra-chunk step (SparseGDN Sec. 2.3, Eqs. 5-9) on tcgen05
 // tensor cores, for bf16 storage.
 //
-// One CTA per (group of two chunks, head pair, sequence): 128 tokens.
-//   Gram  G = K K^T [128 x 128]        (A = B = the K tile, K-major, by TMA), shared by the pair
-// per value head:
+// One CTA per (group of two chunks, value head, sequence): 128 tokens, 256 threads,
+// ~107 KB of shared memory and 256 TMEM columns, so two CTAs share an SM and one
+// CTA's loads, barriers and MMA round trips overlap the other's work.  The two heads
+// of a pair are adjacent CTAs (the second read of their K tile comes from L2).
+//   Gram  G = K K^T [128 x 128]        (A = B = the K tile, K-major, by TMA)
 //   A_Delta[t,s] = beta_t G[t,s] 2^(g_t - g_s), s < t in the same chunk; M = I + A_Delta
-//   C = M^-1 (exact) or the block-adjacent approximation (Eq. 7), fp32 on CUDA cores:
-//       C_ii = M_ii^-1 (forward substitution), C_ij = -C_ii sum_{k=j}^{i-1} M_ik C_kj
+//   C = M^-1 (exact) or the block-adjacent approximation (Eq. 7), fp32 on CUDA cores
+//       over compact 16x16 blocks: C_ii = M_ii^-1 (forward substitution),
+//       C_ij = -C_ii sum_{k=j}^{i-1} M_ik C_kj
 //   U = C diag(beta) V                  (A: C diag(beta) bf16, block-diagonal over the
 //                                        two chunks, K-major; B: V [tok][dv] MN-major by TMA)
 //   s = ||U[48:64,:]||_F (Tail-16 write score)
 //   W = C diag(beta 2^g) K for the chunks that are events (Eq. 15): A = C-bar bf16,
-//       block-diagonal, K-major; B = the K tile read as MN-major (token rows, d
-//       columns: the same bytes as the K-major Gram operand).  W is written at the
-//       event's index, so it is never built for skipped chunks.
+//       block-diagonal, K-major, built in the V tile once the U product has read it;
+//       B = the K tile read as MN-major (token rows, d columns: the same bytes as the
+//       K-major Gram operand).  W is written at the event's index, so it is never
+//       built for skipped chunks.
+// Shared memory over the CTA's life:
+//   [0, 32K)     K tile (Gram, then the W product)
+//   [32K, 64K)   V tile -> C-bar operand -> W staging
+//   [64K, 104K)  solver blocks (fp32) -> C diag(beta) operand (first 32K) -> U staging
+// Each thread keeps its row's 32 coefficients of C in registers between the solve and
+// the two operand builds, which is what lets the operands overwrite the solver blocks.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -23,25 +33,22 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 512;  // 16 warps: 4 per TMEM lane quarter, 32 columns each
+constexpr int kThreads = 256;  // 8 warps: 2 per TMEM lane quarter, 64 columns each
 constexpr uint32_t kSlab = 16384;
 constexpr uint32_t OFF_K = 0;            // K tile: 2 K-slabs [128 tok][64 d]
-constexpr uint32_t OFF_V = 2 * kSlab;    // V tiles of the two heads: 2 MN-stacks [128 tok][64 dv] each
-constexpr uint32_t OFF_A = 6 * kSlab;    // C diag(beta) bf16: 2 K-slabs [128 t][64 s]
-constexpr uint32_t OFF_F = 8 * kSlab;    // fp32 work area
-// Row stride of the fp32 64x64 tiles: 68 floats keeps rows 16-byte aligned, and a
-// 16-byte access by eight threads owning eight consecutive rows (one shared-memory
-// wavefront) touches 8 x 4 distinct banks.
-constexpr int MS = kChunk + 4;
-constexpr uint32_t F_M = 0;                              // [2][64][68] M
-constexpr uint32_t F_C = F_M + 2 * kChunk * MS * 4;      // [2][64][68] C
-constexpr uint32_t F_T = F_C + 2 * kChunk * MS * 4;      // [2][3][256] block products
-constexpr uint32_t F_B = F_T + 2 * 3 * 256 * 4;          // [2 heads][128] beta
-constexpr uint32_t F_G = F_B + 2 * 128 * 4;              // [2 heads][128] g
-constexpr uint32_t F_BG = F_G + 2 * 128 * 4;             // [128] beta 2^g of the current head
-constexpr uint32_t F_S = F_BG + 128 * 4;                 // [2] score partial sums
-constexpr uint32_t kIntraTcSmem = 1024 + OFF_F + F_S + 64;
-constexpr uint32_t TM_G = 0, TM_U = 128, TM_W = 256;
+constexpr uint32_t OFF_V = 2 * kSlab;    // V tile of the head: 2 MN-stacks [128 tok][64 dv]
+constexpr uint32_t OFF_A = 4 * kSlab;    // solver blocks, then C diag(beta) bf16: 2 K-slabs [128 t][64 s]
+// Solver blocks: 16x16 fp32 with a row stride of 20 floats (16-byte rows; eight rows read
+// at the same column quad fall in distinct banks).  Per chunk: the 4 diagonal blocks (M_ii,
+// then C_ii in place), the 6 below-diagonal blocks of M and the 6 of C.
+constexpr int BS = 20;
+constexpr int kBlkFloats = kBlk * BS;
+constexpr int kSlots = 16;
+constexpr uint32_t kSolveBytes = 2 * kSlots * kBlkFloats * 4;
+constexpr uint32_t OFF_SMALL = OFF_A + kSolveBytes;  // beta, g, beta 2^g of the 128 tokens
+constexpr uint32_t kIntraTcSmem = 1024 + OFF_SMALL + 3 * 128 * 4;
+static_assert(kSolveBytes >= 2 * kSlab, "the U operand and staging reuse the solver blocks");
+constexpr uint32_t TM_G = 0, TM_U = 128;  // W reuses the Gram columns
 
 struct IntraParams {
     const float *beta, *g;
@@ -65,71 +72,126 @@ __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
     acc.w += a * b.w;
 }
 
-// Off-diagonal 16x16 blocks at distance OFF of both chunks' C (Eq. 7 generalised):
-// C_ij = -C_ii (sum_{k=j}^{i-1} M_ik C_kj), i = j + OFF, once every block closer to
-// the diagonal is known.  Thread (chunk, block, row, column quad): 4 outputs from
-// 16-byte shared-memory loads (a row of M or C_ii, a quad of a row of C or T).
+// Solver block addresses inside the fp32 area F (chunk cc, block row ib, block column jb).
+__device__ __forceinline__ int below(int ib, int jb) { return ib * (ib - 1) / 2 + jb; }
+__device__ __forceinline__ float *blk_diag(float *F, int cc, int ib) { return F + (cc * kSlots + ib) * kBlkFloats; }
+__device__ __forceinline__ float *blk_m(float *F, int cc, int ib, int jb) {
+    return F + (cc * kSlots + 4 + below(ib, jb)) * kBlkFloats;
+}
+__device__ __forceinline__ float *blk_c(float *F, int cc, int ib, int jb) {
+    return F + (cc * kSlots + 10 + below(ib, jb)) * kBlkFloats;
+}
+__device__ __forceinline__ float *blk_cc(float *F, int cc, int ib, int jb) {
+    return ib == jb ? blk_diag(F, cc, ib) : blk_c(F, cc, ib, jb);
+}
+// Index of block (ib, jb) in the compact C-bar order (diagonal, sub-diagonal, far).
+__device__ __forceinline__ int cbar_index(int ib, int jb) {
+    return ib == jb ? ib : (jb + 1 == ib ? 3 + ib : (ib == 2 ? 7 : (jb == 1 ? 8 : 9)));
+}
+
+// Below-diagonal blocks at distance OFF of both chunks' C (Eq. 7 generalised), once every
+// block closer to the diagonal is known: T = sum_{k=jb}^{ib-1} M_{ib,k} C_{k,jb} is written
+// into C's block, then replaced by C_{ib,jb} = -C_{ib,ib} T.  Task (chunk, block, row,
+// column quad): 4 outputs from 16-byte shared-memory loads.
 template <int OFF>
-__device__ __forceinline__ void offdiag_blocks(const float *Ms, float *Cs, float *Tb, int tid) {
+__device__ __forceinline__ void offdiag_level(float *F, int tid) {
     constexpr int NB = 4 - OFF;
-    const bool act = tid < 2 * NB * 64;
-    const int cc = tid / (NB * 64), rem = tid % (NB * 64);
-    const int bi = rem >> 6, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
-    const int ib = bi + OFF, jb = bi;
-    if (act) {  // T = sum_k M_{ib,k} C_{k,jb}: row rr, columns q4 .. q4+3
-        const float *Mr = Ms + (cc * kChunk + ib * kBlk + rr) * MS + jb * kBlk;
-        const float *Cc = Cs + (cc * kChunk + jb * kBlk) * MS + jb * kBlk + q4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int NT = 2 * NB * 64;
+    constexpr int NU = (NT + kThreads - 1) / kThreads;
+    float4 acc[NU];
 #pragma unroll
-        for (int k4 = 0; k4 < kBlk * OFF; k4 += 4) {
-            const float4 m = ld4(Mr + k4);
-            fma4(acc, m.x, ld4(Cc + (k4 + 0) * MS));
-            fma4(acc, m.y, ld4(Cc + (k4 + 1) * MS));
-            fma4(acc, m.z, ld4(Cc + (k4 + 2) * MS));
-            fma4(acc, m.w, ld4(Cc + (k4 + 3) * MS));
+    for (int u = 0; u < NU; ++u) {
+        const int task = tid + u * kThreads;
+        if (task < NT) {
+            const int cc = task / (NB * 64), rem = task % (NB * 64);
+            const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kb = 0; kb < OFF; ++kb) {
+                const float *Mr = blk_m(F, cc, ib, jb + kb) + rr * BS;
+                const float *Cc = blk_cc(F, cc, jb + kb, jb) + q4;
+#pragma unroll
+                for (int k4 = 0; k4 < kBlk; k4 += 4) {
+                    const float4 m = ld4(Mr + k4);
+                    fma4(t, m.x, ld4(Cc + (k4 + 0) * BS));
+                    fma4(t, m.y, ld4(Cc + (k4 + 1) * BS));
+                    fma4(t, m.z, ld4(Cc + (k4 + 2) * BS));
+                    fma4(t, m.w, ld4(Cc + (k4 + 3) * BS));
+                }
+            }
+            *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) = t;
         }
-        *reinterpret_cast<float4 *>(Tb + (cc * NB + bi) * 256 + rr * 16 + q4) = acc;
     }
     __syncthreads();
-    if (act) {  // C_{ib,jb} = -C_{ib,ib} T
-        float *Cr = Cs + (cc * kChunk + ib * kBlk + rr) * MS;
-        const float *Tt = Tb + (cc * NB + bi) * 256 + q4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int m4 = 0; m4 < kBlk; m4 += 4) {
-            const float4 c = ld4(Cr + ib * kBlk + m4);
-            fma4(acc, c.x, ld4(Tt + (m4 + 0) * 16));
-            fma4(acc, c.y, ld4(Tt + (m4 + 1) * 16));
-            fma4(acc, c.z, ld4(Tt + (m4 + 2) * 16));
-            fma4(acc, c.w, ld4(Tt + (m4 + 3) * 16));
+    for (int u = 0; u < NU; ++u) {
+        const int task = tid + u * kThreads;
+        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (task < NT) {
+            const int cc = task / (NB * 64), rem = task % (NB * 64);
+            const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
+            const float *Cr = blk_diag(F, cc, ib) + rr * BS;
+            const float *Tt = blk_c(F, cc, ib, jb) + q4;
+#pragma unroll
+            for (int m4 = 0; m4 < kBlk; m4 += 4) {
+                const float4 c = ld4(Cr + m4);
+                fma4(acc[u], c.x, ld4(Tt + (m4 + 0) * BS));
+                fma4(acc[u], c.y, ld4(Tt + (m4 + 1) * BS));
+                fma4(acc[u], c.z, ld4(Tt + (m4 + 2) * BS));
+                fma4(acc[u], c.w, ld4(Tt + (m4 + 3) * BS));
+            }
         }
-        *reinterpret_cast<float4 *>(Cr + jb * kBlk + q4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const int task = tid + u * kThreads;
+        if (task < NT) {
+            const int cc = task / (NB * 64), rem = task % (NB * 64);
+            const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
+            *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) =
+                make_float4(-acc[u].x, -acc[u].y, -acc[u].z, -acc[u].w);
+        }
     }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// One row's 32 operand columns (this thread's half of its chunk) as bf16 into the
+// chunk's slab, and zeros into the other chunk's slab (the tile is block-diagonal).
+__device__ __forceinline__ void build_operand_row(uint8_t *tile, int row, int ct, int half, const float *creg,
+                                                  const float *fcol) {
+    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < 32; k0 += 8) {
+        const float4 f0 = ld4(fcol + k0), f1 = ld4(fcol + k0 + 4);
+        const float w[8] = {creg[k0] * f0.x,     creg[k0 + 1] * f0.y, creg[k0 + 2] * f0.z, creg[k0 + 3] * f0.w,
+                            creg[k0 + 4] * f1.x, creg[k0 + 5] * f1.y, creg[k0 + 6] * f1.z, creg[k0 + 7] * f1.w};
+        st_sw128_8(tile + ct * kSlab, row, 32 * half + k0, w);
+        st_sw128_8(tile + (1 - ct) * kSlab, row, 32 * half + k0, z);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tW, IntraParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     __shared__ uint64_t bar_ld, bar_g, bar_u, bar_w, bar_drain;
     __shared__ int ev_s[2];
+    __shared__ float ssum_w[kThreads / 32];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
-    float *Ms = reinterpret_cast<float *>(sm + OFF_F + F_M);
-    float *Cs = reinterpret_cast<float *>(sm + OFF_F + F_C);
-    float *Tb = reinterpret_cast<float *>(sm + OFF_F + F_T);
-    float *bet2 = reinterpret_cast<float *>(sm + OFF_F + F_B);
-    float *gg2 = reinterpret_cast<float *>(sm + OFF_F + F_G);
-    float *bgs = reinterpret_cast<float *>(sm + OFF_F + F_BG);
-    float *ssum = reinterpret_cast<float *>(sm + OFF_F + F_S);
+    float *F = reinterpret_cast<float *>(sm + OFF_A);
+    float *bet = reinterpret_cast<float *>(sm + OFF_SMALL);
+    float *gg = bet + 128;
+    float *bgs = gg + 128;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, seg = warp >> 2;  // TMEM lane quarter, 32-column segment
-    const int row = quarter * 32 + lane;            // token inside the group
-    const int ct = row >> 6, tl = row & 63;
-    const int r = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
+    const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; which 64 of 128 columns
+    const int row = quarter * 32 + lane;             // token inside the group
+    const int ct = row >> 6, tl = row & 63, ib = tl >> 4, rr = tl & 15;
+    const int hh = blockIdx.x & 1, r = blockIdx.x >> 1, p = blockIdx.y, b = blockIdx.z;
+    const int h = 2 * p + hh;
     const int c0 = 2 * r;
     const int nch = c0 + 1 < a.C ? 2 : 1;
     const int t0 = c0 * kChunk;                        // first token of the group inside its sequence
@@ -139,6 +201,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     // sequence's end need no exclusion: beta = 0 there makes their U rows exactly zero)
     const int nrow = min(kChunk, nvalid - kChunk * ct);
     const bool in_tail = tl >= nrow - a.tail;
+    const bool exact = a.exact != 0;
 
     pdl_trigger();
     if (tid == 0) {  // barriers, then the tiles: the loads overlap the set-up below
@@ -149,24 +212,20 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         mbar_init(&bar_drain, 1);
         fence_mbar_init();
         abort_s = 0;
-        mbar_arrive_expect_tx(&bar_ld, 6 * kSlab);
+        mbar_arrive_expect_tx(&bar_ld, 4 * kSlab);
         tma_load_4d(sm + OFF_K, &tK, 0, p, t0, b, &bar_ld);  // rows past the sequence's end read zeros
         tma_load_4d(sm + OFF_K + kSlab, &tK, 64, p, t0, b, &bar_ld);
-        for (int hh = 0; hh < 2; ++hh) {
-            uint8_t *vd = sm + OFF_V + hh * 2 * kSlab;
-            tma_load_4d(vd, &tV, 0, 2 * p + hh, t0, b, &bar_ld);
-            tma_load_4d(vd + kSlab, &tV, 64, 2 * p + hh, t0, b, &bar_ld);
-        }
+        tma_load_4d(sm + OFF_V, &tV, 0, h, t0, b, &bar_ld);
+        tma_load_4d(sm + OFF_V + kSlab, &tV, 64, h, t0, b, &bar_ld);
     }
-    if (tid < 256) {  // beta and g of both heads, fetched once while the tiles load
-        // tokens past the sequence's end: beta = 0 (no write, no correction) and a finite g
-        const int hh = tid >> 7, t = tid & 127;
-        const bool valid = t < nvalid;
-        const int64_t gi = (tok0 + min(t, nvalid - 1)) * a.Nv + 2 * p + hh;
-        bet2[tid] = valid ? a.beta[gi] : 0.f;
-        gg2[tid] = a.g[gi];
+    {   // beta and g of the head, fetched while the tiles load; tokens past the sequence's
+        // end: beta = 0 (no write, no correction) and a finite g
+        const int t = tid & 127;
+        const int64_t gi = (tok0 + min(t, nvalid - 1)) * a.Nv + h;
+        if (tid < 128) bet[t] = t < nvalid ? a.beta[gi] : 0.f;
+        else gg[t] = a.g[gi];
     }
-    if (warp == 0) tmem_alloc<512>(&tmem_base);
+    if (warp == 0) tmem_alloc<256>(&tmem_base);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -184,185 +243,198 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             mma_commit(&bar_g);
         }
     }
+    if (tid < 128) bgs[tid] = bet[tid] * ex2(gg[tid]);
+    // the event index of the group's chunks (the compaction's output), read by the last two
+    // threads while the others build M
+    int ev_mine = -1;
+    if (tid >= kThreads - 2) {
+        pdl_wait();
+        const int cc = tid - (kThreads - 2);
+        if (a.ev_of && cc < nch) ev_mine = a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + cc];
+    }
     __syncthreads();
-    const int max_off = a.exact ? 3 : 1;
-    for (int hh = 0; hh < 2 && !abort_s; ++hh) {
-        const int h = 2 * p + hh;
-        const float *bet = bet2 + 128 * hh;
-        const float *gg = gg2 + 128 * hh;
-        if (tid < 128) bgs[tid] = bet[tid] * ex2(gg[tid]);
-        if (tid < 2) ssum[tid] = 0.f;
-        __syncthreads();
-        // 1. M from the Gram block of the row's chunk: thread (row, half) covers 32 columns
-        if (hh == 0 && !mbar_wait(&bar_g, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+    if (!abort_s && !mbar_wait(&bar_g, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+    tc_fence_after();
+    // 1. M from the Gram block of the row's chunk: thread (row, half) covers blocks 2 half, 2 half + 1
+    {
+        float gv[32];
+        tmem_ld32(tmem_addr(tbase, quarter * 32, TM_G + 64 * ct + 32 * half), gv);
+        tmem_ld_wait();
+        const float bt = bet[row], gt = gg[row];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int jb = 2 * half + h2;
+            if (jb <= ib && (exact || jb + 1 >= ib)) {
+                float *dst = (jb == ib ? blk_diag(F, ct, ib) : blk_m(F, ct, ib, jb)) + rr * BS;
+                float v[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int s = 16 * jb + c;
+                    v[c] = s < tl ? bt * gv[16 * h2 + c] * ex2(gt - gg[64 * ct + s]) : (s == tl ? 1.f : 0.f);
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<float4 *>(dst + 4 * q4) =
+                        make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            }
+        }
+    }
+    if (tid >= kThreads - 2) ev_s[tid - (kThreads - 2)] = ev_mine;
+    tc_fence_before();
+    __syncthreads();
+    // 2. solve.  Diagonal 16x16 blocks by forward substitution, in place: warp w < 4 takes
+    //    blocks 2w and 2w+1 (8 blocks: 2 chunks x 4), one lane per column, the column of
+    //    C_ii in registers and the rows of M_ii broadcast from shared memory:
+    //    C_ii[i][j] = -sum_{s<i} M_ii[i][s] C_ii[s][j]   (C_ii[s][j] = 0 for s < j, 1 for s = j)
+    if (warp < 4) {
+        const int blk = 2 * warp + (lane >> 4), j = lane & 15;
+        float *Mb = blk_diag(F, blk >> 2, blk & 3);
+        float x[kBlk];
+#pragma unroll
+        for (int i2 = 0; i2 < kBlk; ++i2) x[i2] = i2 == j ? 1.f : 0.f;
+#pragma unroll
+        for (int i2 = 1; i2 < kBlk; ++i2) {
+            float acc = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < i2; ++s2) acc += Mb[i2 * BS + s2] * x[s2];
+            if (i2 > j) x[i2] = -acc;
+        }
+        __syncwarp();  // every lane has read M_ii before C_ii replaces it
+#pragma unroll
+        for (int i2 = 0; i2 < kBlk; ++i2) Mb[i2 * BS + j] = x[i2];
+    }
+    __syncthreads();
+    offdiag_level<1>(F, tid);
+    if (exact) {
+        offdiag_level<2>(F, tid);
+        offdiag_level<3>(F, tid);
+    }
+    const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;
+    // 3. this thread's 32 coefficients of C (blocks the solver does not keep are zero)
+    float creg[32];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+        const int jb = 2 * half + h2;
+        if (jb <= ib && (exact || jb + 1 >= ib)) {
+            const float *src = blk_cc(F, ct, ib, jb) + rr * BS;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 x = ld4(src + 4 * q4);
+                creg[16 * h2 + 4 * q4] = x.x;
+                creg[16 * h2 + 4 * q4 + 1] = x.y;
+                creg[16 * h2 + 4 * q4 + 2] = x.z;
+                creg[16 * h2 + 4 * q4 + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) creg[16 * h2 + c] = 0.f;
+        }
+    }
+    __syncthreads();  // the operand below overwrites the solver blocks
+    // 4. A = C diag(beta) for U; the compact C-bar blocks for a later W kernel (online selection)
+    build_operand_row(sm + OFF_A, row, ct, half, creg, bet + 64 * ct + 32 * half);
+    if (a.cbar && ct < nch) {  // C-bar = C diag(beta 2^g), bf16 as in the W operand
+        const float *gcol = bgs + 64 * ct + 32 * half;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int jb = 2 * half + h2;
+            if (jb <= ib && (exact || jb + 1 >= ib)) {
+                alignas(16) __nv_bfloat162 p2[8];
+#pragma unroll
+                for (int q2 = 0; q2 < 8; ++q2)
+                    p2[q2] = __floats2bfloat162_rn(creg[16 * h2 + 2 * q2] * gcol[16 * h2 + 2 * q2],
+                                                   creg[16 * h2 + 2 * q2 + 1] * gcol[16 * h2 + 2 * q2 + 1]);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.cbar + (((int64_t)b * a.Nv + h) * a.C + c0 + ct) * a.nblk * 256 +
+                                                       cbar_index(ib, jb) * 256 + rr * 16);
+                dst[0] = reinterpret_cast<const uint4 *>(p2)[0];
+                dst[1] = reinterpret_cast<const uint4 *>(p2)[1];
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // 5. U = (C diag(beta)) V
+    const uint32_t id = idesc_bf16(128, 128, false, true);
+    if (tid == 0 && !abort_s) {
         tc_fence_after();
-        if (seg < 2) {
-            const int hf = seg;
-            float gv[32];
-            tmem_ld32(tmem_addr(tbase, quarter * 32, TM_G + 64 * ct + 32 * hf), gv);
+        for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
+                     mnmajor_desc(smem_addr(sm + OFF_V), ks, kSlab), id, ks > 0);
+        mma_commit(&bar_u);
+    }
+    if (!abort_s && !mbar_wait(&bar_u, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+    tc_fence_after();
+    // 6. U rows staged over the A operand (read by now), the write score of the tail rows,
+    //    and, for events, the C-bar operand built over the V tile (also read by now)
+    {
+        float sq = 0.f;
+        uint8_t *ust = sm + OFF_A + half * kSlab;
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+            float u[32];
+            tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 64 * half + 32 * s2), u);
             tmem_ld_wait();
-            const float bt = bet[row], gt = gg[row];
-            float4 *mrow = reinterpret_cast<float4 *>(Ms + (ct * kChunk + tl) * MS + 32 * hf);
 #pragma unroll
-            for (int q2 = 0; q2 < 32; ++q2) {
-                const int s = 32 * hf + q2;
-                gv[q2] = s < tl ? bt * gv[q2] * ex2(gt - gg[64 * ct + s]) : (s == tl ? 1.f : 0.f);
-            }
+            for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(ust, row, 32 * s2 + 8 * v8, &u[8 * v8]);
+            if (in_tail) {
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                mrow[q4] = make_float4(gv[4 * q4], gv[4 * q4 + 1], gv[4 * q4 + 2], gv[4 * q4 + 3]);
-        }
-        __syncthreads();
-        // 2. solve.  Diagonal 16x16 blocks by forward substitution: warp w < 4 takes
-        //    blocks 2w and 2w+1 (8 blocks: 2 chunks x 4), one lane per column, the
-        //    column of C_ii in registers and the rows of M_ii broadcast from shared memory:
-        //    C_ii[i][j] = -sum_{s<i} M_ii[i][s] C_ii[s][j]   (C_ii[s][j] = 0 for s < j, 1 for s = j)
-        if (warp < 4) {
-            const int blk = 2 * warp + (lane >> 4), j = lane & 15;
-            const int cc = blk >> 2, r0 = (blk & 3) * kBlk;
-            const float *Mb = Ms + (cc * kChunk + r0) * MS + r0;
-            float x[kBlk];
-#pragma unroll
-            for (int i2 = 0; i2 < kBlk; ++i2) x[i2] = i2 == j ? 1.f : 0.f;
-#pragma unroll
-            for (int i2 = 1; i2 < kBlk; ++i2) {
-                float acc = 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < i2; ++s2) acc += Mb[i2 * MS + s2] * x[s2];
-                if (i2 > j) x[i2] = -acc;
-            }
-            float *Cb = Cs + (cc * kChunk + r0) * MS + r0 + j;
-#pragma unroll
-            for (int i2 = 0; i2 < kBlk; ++i2) Cb[i2 * MS] = x[i2];
-        }
-        __syncthreads();
-        // the previous head's W store must have left the A tile before step 3 rewrites it (the
-        // barriers inside the off-diagonal step order this wait before those writes)
-        if (tid == 0) bulk_wait_read();
-        if (hh == 0) {  // the event index of the group's chunks: the compaction's output
-            pdl_wait();
-            if (tid < 2) ev_s[tid] = (a.ev_of && tid < nch) ? a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + tid] : -1;
-        }
-        offdiag_blocks<1>(Ms, Cs, Tb, tid);
-        if (max_off == 3) {
-            offdiag_blocks<2>(Ms, Cs, Tb, tid);
-            offdiag_blocks<3>(Ms, Cs, Tb, tid);
-        }
-        const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;  // published by the barriers above
-        // 3. A tiles: C diag(beta) for U, and C diag(beta 2^g) for W (built in the
-        //    fp32 M area, free once the solve is done); both bf16, block-diagonal
-        {
-            const float *crow = Cs + (ct * kChunk + tl) * MS;
-            const int slab = seg >> 1, c0s = 32 * (seg & 1);  // this thread's 32 columns
-            for (int part = 0; part < (any_event ? 2 : 1); ++part) {
-                uint8_t *dst = (part == 0 ? sm + OFF_A : reinterpret_cast<uint8_t *>(Ms)) + slab * kSlab;
-                const float *f = (part == 0 ? bet : bgs) + 64 * ct;
-                if (slab == ct) {  // warp-uniform: these columns belong to the row's own chunk
-#pragma unroll
-                    for (int k0 = 0; k0 < 32; k0 += 8) {
-                        // blocks the solver does not keep (and those above the diagonal) are zero
-                        const int col = c0s + k0, jb = col >> 4, ib = tl >> 4;
-                        float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        if (jb <= ib && (max_off == 3 || jb + 1 >= ib)) {
-                            const float4 c0 = ld4(crow + col), c1 = ld4(crow + col + 4);
-                            const float4 f0 = ld4(f + col), f1 = ld4(f + col + 4);
-                            w[0] = c0.x * f0.x; w[1] = c0.y * f0.y; w[2] = c0.z * f0.z; w[3] = c0.w * f0.w;
-                            w[4] = c1.x * f1.x; w[5] = c1.y * f1.y; w[6] = c1.z * f1.z; w[7] = c1.w * f1.w;
-                        }
-                        st_sw128_8(dst, row, col, w);
-                    }
-                } else {
-                    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(dst, row, c0s + k0, z);
-                }
+                for (int q2 = 0; q2 < 32; ++q2) sq += u[q2] * u[q2];
             }
         }
-        if (a.cbar) {  // compact C-bar = C diag(beta 2^g), bf16 as in the W operand, for the W kernel after selection
-            for (int idx = tid; idx < nch * a.nblk * 32; idx += kThreads) {  // 8 coefficients (16 bytes) each
-                const int cc = idx / (a.nblk * 32), rem = idx % (a.nblk * 32);
-                const int blk = rem >> 5, rr = (rem >> 1) & 15, col0 = (rem & 1) * 8;
-                const int rw = blk_row(blk) * kBlk + rr, cl = blk_col(blk) * kBlk + col0;
-                const float *cr = Cs + (cc * kChunk + rw) * MS + cl;
-                const float *bg = bgs + 64 * cc + cl;
-                alignas(16) __nv_bfloat162 p2[4];
 #pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2)
-                    p2[q2] = __floats2bfloat162_rn(cr[2 * q2] * bg[2 * q2], cr[2 * q2 + 1] * bg[2 * q2 + 1]);
-                *reinterpret_cast<uint4 *>(a.cbar + (((int64_t)b * a.Nv + h) * a.C + c0 + cc) * a.nblk * 256 +
-                                           blk * 256 + rr * 16 + col0) = *reinterpret_cast<uint4 *>(p2);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // 4. U = (C diag(beta)) V and, for events, W = (C diag(beta 2^g)) K
-        if (tid == 0) {
+        for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (lane == 0) ssum_w[warp] = sq;
+    }
+    if (any_event) build_operand_row(sm + OFF_V, row, ct, half, creg, bgs + 64 * ct + 32 * half);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // 7. U out (rows past the sequence's end are clipped); W = (C diag(beta 2^g)) K for events
+    if (tid == 0 && !abort_s) {
+        tma_store_4d(&tU, 0, h, t0, b, sm + OFF_A);
+        tma_store_4d(&tU, 64, h, t0, b, sm + OFF_A + kSlab);
+        bulk_commit();
+        if (any_event) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 128, false, true);
-            uint8_t *vt = sm + OFF_V + hh * 2 * kSlab;
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
-                         mnmajor_desc(smem_addr(vt), ks, kSlab), id, ks > 0);
-            mma_commit(&bar_u);
-            if (any_event) {  // W on its own barrier: the U epilogue below overlaps it
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(tbase + TM_W, kmajor_desc(smem_addr(Ms), ks, kSlab),
-                             mnmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id, ks > 0);
-                mma_commit(&bar_w);
-            }
+                mma_bf16(tbase + TM_G, kmajor_desc(smem_addr(sm + OFF_V), ks, kSlab),
+                         mnmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id, ks > 0);
+            mma_commit(&bar_w);
         }
-        if (!mbar_wait(&bar_u, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+    }
+    if (tid < nch && a.score) {  // the chunk's four warps, summed in a fixed order
+        const int w0 = 2 * tid;
+        const float s = ssum_w[w0] + ssum_w[w0 + 1] + ssum_w[w0 + 4] + ssum_w[w0 + 5];
+        a.score[((int64_t)b * a.Nv + h) * a.C + c0 + tid] = sqrtf(s);
+    }
+    if (any_event) {
+        if (!abort_s && !mbar_wait(&bar_w, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
         tc_fence_after();
-        {   // U rows staged in this head's V tile (free once the MMAs are done), W rows in the A tile
-            float sq = 0.f;
-            const int slab = seg >> 1, c0s = 32 * (seg & 1);
-            uint8_t *ustage = sm + OFF_V + hh * 2 * kSlab + slab * kSlab;
-            {
-                float u[32];
-                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_U + 32 * seg), u);
-                tmem_ld_wait();
+        if (ev_s[ct] >= 0) {  // warp-uniform: W rows staged over the C-bar operand (read by now)
+            uint8_t *wst = sm + OFF_V + half * kSlab;
 #pragma unroll
-                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(ustage, row, c0s + 8 * v8, &u[8 * v8]);
-                if (in_tail) {
-#pragma unroll
-                    for (int q2 = 0; q2 < 32; ++q2) sq += u[q2] * u[q2];
-                }
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            if (lane == 0 && sq != 0.f) atomicAdd(&ssum[ct], sq);
-            if (any_event && !mbar_wait(&bar_w, hh)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
-            tc_fence_after();
-            if (ev_s[ct] >= 0) {
-                uint8_t *wstage = sm + OFF_A + slab * kSlab;
+            for (int s2 = 0; s2 < 2; ++s2) {
                 float w[32];
-                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_W + 32 * seg), w);
+                tmem_ld32(tmem_addr(tbase, quarter * 32, TM_G + 64 * half + 32 * s2), w);
                 tmem_ld_wait();
 #pragma unroll
-                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(wstage, row, c0s + 8 * v8, &w[8 * v8]);
+                for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(wst, row, 32 * s2 + 8 * v8, &w[8 * v8]);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
-            uint8_t *ust = sm + OFF_V + hh * 2 * kSlab;
-            tma_store_4d(&tU, 0, h, t0, b, ust);  // rows past the sequence's end are clipped
-            tma_store_4d(&tU, 64, h, t0, b, ust + kSlab);
+        if (tid == 0 && !abort_s) {
             for (int cc = 0; cc < nch; ++cc) {
                 const int ev = ev_s[cc];
                 if (ev < 0) continue;
                 const int wrow = (ev * 2 + hh) * kChunk;
-                tma_store_3d(&tW, 0, wrow, 0, sm + OFF_A + cc * 8192);
-                tma_store_3d(&tW, 64, wrow, 0, sm + OFF_A + kSlab + cc * 8192);
+                tma_store_3d(&tW, 0, wrow, 0, sm + OFF_V + cc * 8192);
+                tma_store_3d(&tW, 64, wrow, 0, sm + OFF_V + kSlab + cc * 8192);
             }
             bulk_commit();
         }
-        tc_fence_before();
-        __syncthreads();
-        if (tid < nch && a.score) a.score[((int64_t)b * a.Nv + h) * a.C + c0 + tid] = sqrtf(ssum[tid]);
-        __syncthreads();
     }
     if (tid == 0) bulk_wait_read();  // the stores only need their shared-memory sources before exit
     if (abort_s && tid == 0) {
@@ -373,7 +445,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     pdl_wait();  // also on an early exit: this grid's completion implies its predecessors'
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc<512>(tbase);
+    if (warp == 0) tmem_dealloc<256>(tbase);
 }
 
 }  // namespace
@@ -396,8 +468,8 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
     a.exact = pb.solver == GDN_SOLVER_EXACT;
     a.tail = pb.tail;
     cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraTcSmem);
-    return launch_kernel(pb.pdl, intra_tc_kernel, dim3(pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream, tK, tV,
-                         tU, tW, a);
+    return launch_kernel(pb.pdl, intra_tc_kernel, dim3(2 * pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream,
+                         tK, tV, tU, tW, a);
 }
 
 }  // namespace gdn
