@@ -100,7 +100,7 @@ struct Workspace {
     void *grp_info;            // [B, P, G] int4 {snapshot slot, kind, decay head 0, decay head 1}
     void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks (bf16 on the tensor-core path)
-    void *W;                   // [ev_cap, 2, 64, d] dtype, deferred W of events
+    void *W;                   // [ev_cap, 2, 64, d] dtype, W of events (bf16 storage: -W, for the scan's U' product)
     void *snap;                // post-event state snapshots: fp32 [snap_cap, 2, d, dv]; bf16 storage: S^T [snap_cap, 2, dv, d]
     // tensor-core scan (bf16 storage only; NR = ceil(C / kRunChunks))
     void *amap;                // [R, 2, NR, 128, 128] bf16: A_r^T of each run

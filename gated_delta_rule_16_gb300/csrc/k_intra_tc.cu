@@ -17,7 +17,7 @@
 //       block-diagonal, K-major, built in the V tile once the U product has read it;
 //       B = the K tile read as MN-major (token rows, d columns: the same bytes as the
 //       K-major Gram operand).  W is written at the event's index, so it is never
-//       built for skipped chunks.
+//       built for skipped chunks, and negated: the scan accumulates -S^T W^T onto U^T.
 // Shared memory over the CTA's life:
 //   [0, 32K)     K tile (Gram, then the W product)
 //   [32K, 64K)   V tile -> C-bar operand -> W staging
@@ -418,6 +418,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 float w[32];
                 tmem_ld32(tmem_addr(tbase, quarter * 32, TM_G + 64 * half + 32 * s2), w);
                 tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) w[q] = -w[q];  // the workspace holds -W
 #pragma unroll
                 for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(wst, row, 32 * s2 + 8 * v8, &w[8 * v8]);
             }

@@ -22,18 +22,22 @@
 // (row, segment) handles 32 of the row's 128 entries.  The state lives in TMEM
 // (fp32, 128 columns), which keeps the registers per thread low enough for two
 // CTAs per SM: one CTA's barriers and MMA round trips overlap the other's work.
-// Per event:
-//   S^T <- 2^(P_c - P_cur) S^T (gap decay): read from TMEM, written as the bf16
-//          operand of MMA1, and 2^gamma S^T written back to TMEM
-//   MMA1  U'^T_acc[128 x 64]  = S^T[128 x 128] . W^T      (A: S^T bf16 K-major; B: W [t][d] K-major)
-//   U'^T = U^T - U'^T_acc;  U''^T = U'^T * 2^(gamma - g_t)        (registers)
-//   MMA2  S^T += U''^T[128 x 64] . K                      (A: U''^T K-major; B: K [t][d] MN-major)
-// The W, K and U tiles are single-buffered; each buffer is refilled for the next
-// event as soon as its reader is done (W after MMA1, U after the U' pass, K after
-// MMA2), so every load has most of an event to land.  U' is written over U in the
-// U tile and TMA-stored.  Snapshots are stored in bf16 as S^T [dv][d] (each thread's
-// 32 state entries are 64 contiguous bytes), the K-major operand of the output
-// kernel's Q S product.
+// Scaled state.  TMEM holds S^T / sigma, sigma a CTA-uniform factor that absorbs
+// every decay of the run (sigma <- 2^(P_c - P_cur) 2^gamma sigma per event), so the
+// state is never rewritten for a decay; the write of an event is divided by the new
+// sigma instead.  When 1/sigma would pass 2^64 the event's decay is applied to TMEM
+// and sigma restarts at 1.  Per event:
+//   A1 = sigma 2^(P_c - P_cur) S_tmem^T, bf16 (the state entering chunk c)
+//   MMA  U'^T[128 x 64]  = U^T . I                         (A: U [t][dv] MN-major; B: identity)
+//   MMA1 U'^T          += A1[128 x 128] . (-W)^T           (B: -W [t][d] K-major, as stored)
+//   U''^T = U'^T * 2^(gamma - g_t) / sigma_new, bf16        (registers)
+//   MMA2 S_tmem^T      += U''^T[128 x 64] . K              (A: U''^T K-major; B: K [t][d] MN-major)
+// The W, K and U tiles are single-buffered; W and U are refilled for the next event
+// once MMA1 is done, K once MMA2 is done, so every load has most of an event to
+// land (the fix-up's U tile once its U' store has read it).  The fix-up writes U'
+// into the U tile and stores it over U by TMA.  Snapshots are stored in bf16 as
+// S^T [dv][d] (each thread's 32 state entries are 64 contiguous bytes), the
+// K-major operand of the output kernel's Q S product.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -50,8 +54,11 @@ constexpr uint32_t OFF_A1 = 0;           // S^T bf16, K-major, 2 slabs
 constexpr uint32_t OFF_A2 = 2 * kSlab;   // U''^T bf16, K-major, 1 slab
 constexpr uint32_t OFF_W = 3 * kSlab;    // W [64 t][128 d]: 2 K-slabs of [64][128 B], 8192 apart
 constexpr uint32_t OFF_K = 4 * kSlab;    // K MN-major: 2 stacks of [64 t][64 d], 8192 apart
-constexpr uint32_t OFF_U = 5 * kSlab;    // U [64 t][128 dv] bf16, unswizzled
-constexpr uint32_t kRunSmem = 1024 + 6 * kSlab;
+constexpr uint32_t OFF_U = 5 * kSlab;    // U MN-major: 2 stacks of [64 t][64 dv], 8192 apart
+constexpr uint32_t OFF_I = 6 * kSlab;    // identity [64 t'][64 t] bf16, K-major (8 KB)
+constexpr uint32_t kRunSmem = 1024 + 6 * kSlab + 8192;
+// The run kernel keeps 1/sigma below 2^64 (sigma: the state's scale in TMEM).
+constexpr float kMinLog2Scale = -64.f;
 constexpr uint32_t TM_U = 0;             // TMEM columns [0, 64): U'^T accumulator
 constexpr uint32_t TM_S = 128;           // TMEM columns [128, 256): the state S^T
 constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab;
@@ -97,7 +104,10 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     __shared__ int ev_c[kRun], ev_slot[kRun];
     __shared__ double Pl[kRun + 1];
     __shared__ float dec[kRun][kChunk];  // 2^(gamma - g_t) of each event chunk
-    __shared__ float gamk[kRun];         // gamma of each event chunk
+    __shared__ float gamk[kRun], dPk[kRun];  // gamma of each event chunk; log2 gap decay before it
+    // scaled state: TMEM holds S / sigma with sigma a CTA-uniform factor (see the header)
+    __shared__ float f_snap[kRun], f_op[kRun], f_ren[kRun], f_u[kRun], f_end;
+    __shared__ int ren[kRun];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, seg = warp >> 2;  // TMEM lane quarter, 32-column segment
@@ -148,7 +158,17 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         const int n = min(kChunk, a.T_ - ev_c[k] * kChunk);  // valid tokens (a partial last chunk has fewer)
         const float gam = a.g[(tk + n - 1) * a.Nv + h];       // gamma: g at the chunk's last token
         dec[k][t] = ex2(gam - a.g[(tk + min(t, n - 1)) * a.Nv + h]);
-        if (t == 0) gamk[k] = gam;
+        if (t == 0) {
+            gamk[k] = gam;
+            dPk[k] = (float)(Pl[ev_c[k] - c_lo] - Pl[(k ? ev_c[k - 1] + 1 : c_lo) - c_lo]);
+        }
+    }
+    {   // identity [64 t'][64 t], the K-major B operand that copies U^T into the U' accumulator
+        const int irow = tid >> 3, ich = tid & 7;
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 8 * ich + q == irow ? 1.f : 0.f;
+        st_sw128_8(sm + OFF_I, irow, 8 * ich, v);
     }
     const uint32_t tbase = tmem_base;
     const uint32_t t_s = tmem_addr(tbase, quarter * 32, TM_S + cs);
@@ -163,8 +183,10 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         tma_load_3d(sm + OFF_W + 8192, &tW, 64, wrow, 0, &bar_w);
     };
     auto load_u = [&](int k) {
+        const int tok = ev_c[k] * kChunk;
         mbar_arrive_expect_tx(&bar_u, 16384u);
-        tma_load_4d(sm + OFF_U, &tU, 0, h, ev_c[k] * kChunk, b, &bar_u);
+        tma_load_4d(sm + OFF_U, &tU, 0, h, tok, b, &bar_u);  // rows past the sequence's end read zeros
+        tma_load_4d(sm + OFF_U + 8192, &tU, 64, h, tok, b, &bar_u);
     };
     auto load_k = [&](int k) {
         const int tok = ev_c[k] * kChunk;
@@ -202,82 +224,114 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         tmem_st32(t_s, S);
         tmem_st_wait();
     }
-    __syncthreads();  // dec[] and gamk[] complete
-    auto snapshot = [&](int slot, const float (&S)[32]) {  // row `row` of S^T, columns cs .. cs+31
+    __syncthreads();  // dec[], gamk[], dPk[] complete
+    if (tid == 0) {   // the scale sigma = 2^ls through the run
+        float ls = 0.f;
+        for (int k = 0; k < n_ev; ++k) {
+            f_snap[k] = ex2(ls);            // the state left by event k-1
+            const float lop = ls + dPk[k];  // the state entering chunk c_k
+            f_op[k] = ex2(lop);
+            const float lnew = lop + gamk[k];
+            ren[k] = lnew < kMinLog2Scale;  // keep 1/sigma in range: apply this decay to TMEM instead
+            f_ren[k] = ex2(lnew);
+            ls = ren[k] ? 0.f : lnew;
+            f_u[k] = ex2(-ls);
+        }
+        const int cl = ev_c[n_ev - 1] + 1;
+        f_end = ex2(ls + (mode == kModeFixup ? 0.f : (float)(Pl[c_hi - c_lo] - Pl[cl - c_lo])));
+    }
+    __syncthreads();
+    auto snapshot = [&](int slot, const float (&S)[32], float f) {  // row `row` of f S^T, columns cs .. cs+31
         if (slot >= 0 && slot < a.snap_cap) {
             uint4 *sn = reinterpret_cast<uint4 *>(a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim) + row * kDim + cs);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 alignas(16) __nv_bfloat162 p2[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) p2[u] = __floats2bfloat162_rn(S[8 * q + 2 * u], S[8 * q + 2 * u + 1]);
+                for (int u = 0; u < 4; ++u) p2[u] = __floats2bfloat162_rn(f * S[8 * q + 2 * u], f * S[8 * q + 2 * u + 1]);
                 sn[q] = *reinterpret_cast<uint4 *>(p2);
             }
         }
     };
 
     const uint32_t id1 = idesc_bf16(128, 64, false, false);
+    const uint32_t idu = idesc_bf16(128, 64, true, false);
     const uint32_t id2 = idesc_bf16(128, 128, false, true);
-    int cur = c_lo;
-    int k = 0;
-    for (; k < n_ev; ++k) {
+    for (int k = 0; k < n_ev; ++k) {
         const int c = ev_c[k];
-        if (tid == 0 && k > 0 && k < n_ev) {  // K buffer free: MMA2 of the previous event completed
+        if (tid == 0 && k > 0) {  // K buffer free: MMA2 of the previous event completed
             load_k(k);
             loads_k = k + 1;
         }
-        {   // the state entering chunk c
+        {   // the state entering chunk c, sigma 2^(P_c - P_cur) S_tmem, as the bf16 operand of MMA1
             float S[32];
             tmem_ld32(t_s, S);
             tmem_ld_wait();
-            if (mode == kModeFixup && k > 0) snapshot(ev_slot[k - 1], S);  // the state after event k-1
-            const float gap = ex2((float)(Pl[c - c_lo] - Pl[cur - c_lo]));
+            if (mode == kModeFixup && k > 0) snapshot(ev_slot[k - 1], S, f_snap[k]);
+            const float fo = f_op[k];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] *= gap;
+            for (int k0 = 0; k0 < 32; k0 += 8) {
+                float w[8];
 #pragma unroll
-            for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(A1 + slab * kSlab, row, cin + k0, &S[k0]);
-            const float dg = ex2(gamk[k]);
+                for (int q = 0; q < 8; ++q) w[q] = S[k0 + q] * fo;
+                st_sw128_8(A1 + slab * kSlab, row, cin + k0, w);
+            }
+            if (ren[k]) {  // CTA-uniform
+                const float fr = f_ren[k];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] *= dg;
-            tmem_st32(t_s, S);  // 2^gamma S_c: MMA2 accumulates the write onto it
-            tmem_st_wait();
+                for (int jj = 0; jj < 32; ++jj) S[jj] *= fr;
+                tmem_st32(t_s, S);
+                tmem_st_wait();
+            }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (abort_s) break;
-        if (tid == 0) {
-            if (!mbar_wait(&bar_w, k & 1)) {
+        if (tid == 0) {  // U'^T = U^T I - S_c^T W^T (the workspace holds -W)
+            const bool landed_w = mbar_wait(&bar_w, k & 1);
+            const bool landed_u = landed_w && (!with_u || mbar_wait(&bar_u, k & 1));
+            if (!landed_u) {
                 fail(a, &abort_s);
             } else {
                 seen_w = k + 1;
+                if (with_u) seen_u = k + 1;
                 tc_fence_after();
+                if (with_u)
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tbase + TM_U, mnmajor_desc(smem_addr(sm + OFF_U), ks, 8192),
+                                 kmajor_desc(smem_addr(sm + OFF_I), ks, 8192), idu, ks > 0);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(A1), ks, kSlab),
-                             kmajor_desc(smem_addr(sm + OFF_W), ks, 8192), id1, ks > 0);
+                             kmajor_desc(smem_addr(sm + OFF_W), ks, 8192), id1, with_u || ks > 0);
                 mma_commit(&bar_mma1);
             }
         }
         if (!mbar_wait(&bar_mma1, k & 1)) fail(a, &abort_s);
-        if (with_u) {
-            if (!mbar_wait(&bar_u, k & 1)) fail(a, &abort_s);
-            else if (tid == 0) seen_u = k + 1;
+        if (tid == 0 && k + 1 < n_ev && !abort_s) {  // the products just done have read W and U
+            load_w(k + 1);
+            loads_w = k + 2;
+            if (mode == kModeInhom) {  // (the fix-up writes U' into the U tile first)
+                load_u(k + 1);
+                loads_u = k + 2;
+            }
         }
         tc_fence_after();
         {
             float acc[16];
             tmem_ld16(tmem_addr(tbase, quarter * 32, TM_U + 16 * seg), acc);
             tmem_ld_wait();
-            __nv_bfloat16 *Ut = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_U);
+            if (mode == kModeFixup) {  // U' over U in the tile (read by now), stored below
+                uint8_t *ut = sm + OFF_U + (row >> 6) * 8192;
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    *reinterpret_cast<__nv_bfloat16 *>(ut + sw128_offset(16 * seg + t, row & 63)) =
+                        __float2bfloat16_rn(acc[t]);
+            }
+            const float fs = f_u[k];
             float up[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int tt = 16 * seg + t;
-                const float u = with_u ? __bfloat162float(Ut[tt * kDim + row]) : 0.f;
-                const float v = u - acc[t];
-                if (mode == kModeFixup) Ut[tt * kDim + row] = __float2bfloat16_rn(v);  // U' replaces U in the tile
-                up[t] = v * dec[k][tt];
-            }
+            for (int t = 0; t < 16; ++t) up[t] = acc[t] * dec[k][16 * seg + t] * fs;
 #pragma unroll
             for (int t0 = 0; t0 < 16; t0 += 8) st_sw128_8(A2, row, 16 * seg + t0, &up[t0]);
         }
@@ -295,15 +349,12 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                     mma_bf16(tbase + TM_S, kmajor_desc(smem_addr(A2), ks, kSlab),
                              mnmajor_desc(smem_addr(sm + OFF_K), ks, 8192), id2, 1);
                 mma_commit(&bar_mma2);
-                if (mode == kModeFixup) {  // U' of this event back over U
-                    tma_store_4d(&tU, 0, h, c * kChunk, b, sm + OFF_U);  // clipped at the sequence's end
+                if (mode == kModeFixup) {  // U' of this event back over U (clipped at the sequence's end)
+                    tma_store_4d(&tU, 0, h, c * kChunk, b, sm + OFF_U);
+                    tma_store_4d(&tU, 64, h, c * kChunk, b, sm + OFF_U + 8192);
                     bulk_commit();
-                }
-                if (k + 1 < n_ev) {
-                    load_w(k + 1);  // MMA1 is done with the W buffer
-                    loads_w = k + 2;
-                    if (with_u) {
-                        if (mode == kModeFixup) bulk_wait_read();  // the U' store has left the U buffer
+                    if (k + 1 < n_ev) {
+                        bulk_wait_read();  // the store has left the U tile
                         load_u(k + 1);
                         loads_u = k + 2;
                     }
@@ -312,7 +363,6 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         }
         if (!mbar_wait(&bar_mma2, k & 1)) fail(a, &abort_s);
         tc_fence_after();
-        cur = c + 1;
     }
     __syncthreads();
     if (!abort_s) {
@@ -320,9 +370,9 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         tmem_ld32(t_s, S);
         tmem_ld_wait();
         if (mode == kModeFixup) {
-            snapshot(ev_slot[n_ev - 1], S);
+            snapshot(ev_slot[n_ev - 1], S, f_end);
         } else {
-            const float fin = ex2((float)(Pl[c_hi - c_lo] - Pl[cur - c_lo]));
+            const float fin = f_end;  // sigma and the decay of the run's chunks after its last event
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) S[jj] *= fin;
             if (mode == kModeHomog) {
@@ -551,7 +601,7 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
     if (!make_tmap_bf16_3d(&tW, ws.W, kDim, (uint64_t)ws.ev_cap * 2 * kChunk, 1, kDim * 2,
                            (uint64_t)ws.ev_cap * 2 * kChunk * kDim * 2, 64, 64, 1, true) ||
         !make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 64, true) ||
-        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 128, 64, false))
+        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 64, true))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(scan_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmem);
     const int fixup = part == 2;

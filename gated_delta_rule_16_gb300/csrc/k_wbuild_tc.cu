@@ -10,8 +10,9 @@
 //         assembled in shared memory from the compact blocks
 //   B   = the two events' K tiles                  [128 tokens x 128 d] bf16, MN-major, by TMA
 //   D_h = A_h B                                     fp32 in TMEM, columns 128 h .. 128 h + 127
-// and writes D_h rounded to bf16 at W rows (2 e + h) * 64 by TMA.  The event
-// count is read on the device; the grid strides over event pairs.
+// and writes -D_h rounded to bf16 at W rows (2 e + h) * 64 by TMA (the workspace
+// holds -W, which the scan's U' product accumulates onto U).  The event count is
+// read on the device; the grid strides over event pairs.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -173,6 +174,8 @@ wbuild_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__
                     float w[32];
                     tmem_ld32(tmem_addr(tbase, quarter * 32, 128 * hh + 64 * dh + 32 * c32), w);
                     tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) w[q] = -w[q];  // stored negated (see the header)
 #pragma unroll
                     for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(stage, row, 32 * c32 + 8 * v8, &w[8 * v8]);
                 }
