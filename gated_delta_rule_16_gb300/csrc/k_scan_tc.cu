@@ -63,6 +63,11 @@ constexpr uint32_t TM_U = 0;             // TMEM columns [0, 64): U'^T accumulat
 constexpr uint32_t TM_S = 128;           // TMEM columns [128, 256): the state S^T
 constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab;
 constexpr int kMaxRuns = 1024;  // C <= 16384 chunks
+// The chain of one (row, head) is split over kChainSplit CTAs, each owning kChainRows rows
+// of S^T (the rows evolve independently); its MMAs keep M = 128 with the other rows zero.
+constexpr int kChainSplit = 4;
+constexpr int kChainRows = kDim / kChainSplit;
+static_assert(kChainRows == 32, "the active rows are TMEM lanes 0..31: one warp per column segment");
 
 enum { kModeHomog = 0, kModeInhom = 1, kModeFixup = 2 };
 
@@ -410,7 +415,7 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     if (warp == 0) tmem_dealloc<256>(tbase);
 }
 
-// grid: (2 heads, CSR rows R).  S_{r+1}^T = S_r^T A_r^T + B_r^T over the runs.
+// grid: (2 heads x kChainSplit row blocks, CSR rows R).  S_{r+1}^T = S_r^T A_r^T + B_r^T over the runs.
 __global__ void __launch_bounds__(kThreads, 1)
 scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     extern __shared__ uint8_t smraw[];
@@ -423,7 +428,9 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     const int quarter = warp & 3, seg = warp >> 2;
     const int row = quarter * 32 + lane;
     const int cs = 32 * seg, slab = seg >> 1, cin = 32 * (seg & 1);
-    const int hh = blockIdx.x, j = blockIdx.y;
+    const int hh = blockIdx.x / kChainSplit, part = blockIdx.x % kChainSplit, j = blockIdx.y;
+    const bool active = row < kChainRows;         // warp-uniform: TMEM lanes 0 .. 31
+    const int dv = part * kChainRows + row;       // this thread's row of S^T
     pdl_wait();  // the run maps of the kernel before
     pdl_trigger();
     const int i = a.row_pair[j], b = i / a.P_, p = i % a.P_, h = 2 * p + hh;
@@ -469,7 +476,11 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
 
     float S[32];
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) S[jj] = a.h0 ? a.h0[sbase + (int64_t)(cs + jj) * kDim + row] : 0.f;
+    for (int jj = 0; jj < 32; ++jj) S[jj] = a.h0 && active ? a.h0[sbase + (int64_t)(cs + jj) * kDim + dv] : 0.f;
+    {   // rows of the operand other than this CTA's stay zero
+        uint4 *z = reinterpret_cast<uint4 *>(Atile);
+        for (int q = tid; q < 2 * (int)kSlab / 16; q += kThreads) z[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
 
     auto next_run = [&](int r) -> int { return r < a.NR ? nxt[r] : a.NR; };
     int n_loads = 0, n_mma = 0;
@@ -487,8 +498,8 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     float Bm[32];  // B^T row segment of the next run with events
     {
         const int r0 = next_run(0);
-        if (r0 < a.NR) {
-            const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r0) * (kDim * kDim)) + 8 * seg * 128 + row;
+        if (r0 < a.NR && active) {
+            const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r0) * (kDim * kDim)) + 8 * seg * 128 + dv;
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4) {
                 const float4 x = bsrc[v4 * 128];
@@ -498,9 +509,11 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     }
     for (int r = 0; r < a.NR; ++r) {
         const int c_lo = r * kRun, c_hi = min(a.C, c_lo + kRun);
-        float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim)) + 8 * seg * 128 + row;
+        if (active) {
+            float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim)) + 8 * seg * 128 + dv;
 #pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4) ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+            for (int v4 = 0; v4 < 8; ++v4) ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+        }
         const bool has = nxt[r] == r;
         if (!has) {
             const float f = ex2((float)(Pu[c_hi] - Pu[c_lo]));
@@ -508,8 +521,10 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
             for (int jj = 0; jj < 32; ++jj) S[jj] *= f;
             continue;
         }
+        if (active) {
 #pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(Atile + slab * kSlab, row, cin + k0, &S[k0]);
+            for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(Atile + slab * kSlab, row, cin + k0, &S[k0]);
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -541,16 +556,17 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         ++n_mma;
         ++used;
         tc_fence_after();
-        float d0[32];
-        tmem_ld32(tmem_addr(tbase, quarter * 32, cs), d0);
-        tmem_ld_wait();
+        if (active) {
+            float d0[32];
+            tmem_ld32(tmem_addr(tbase, quarter * 32, cs), d0);
+            tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] = d0[jj] + Bm[jj];
-        {   // refill with the next run's B^T row; the loads land during the next step
+            for (int jj = 0; jj < 32; ++jj) S[jj] = d0[jj] + Bm[jj];
+            // refill with the next run's B^T row; the loads land during the next step
             const int rn2 = next_run(r + 1);
             if (rn2 < a.NR) {
                 const float4 *bsrc =
-                    reinterpret_cast<const float4 *>(a.bmap + (rbase + rn2) * (kDim * kDim)) + 8 * seg * 128 + row;
+                    reinterpret_cast<const float4 *>(a.bmap + (rbase + rn2) * (kDim * kDim)) + 8 * seg * 128 + dv;
 #pragma unroll
                 for (int v4 = 0; v4 < 8; ++v4) {
                     const float4 x = bsrc[v4 * 128];
@@ -563,8 +579,10 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         if (abort_s) break;
     }
     if (!abort_s) {
+        if (active) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) a.s_final[sbase + (int64_t)(cs + jj) * kDim + row] = S[jj];
+            for (int jj = 0; jj < 32; ++jj) a.s_final[sbase + (int64_t)(cs + jj) * kDim + dv] = S[jj];
+        }
     } else if (tid == 0) {
         for (int u = used + 1; u < n_loads; ++u) mbar_wait(&bar_tma[u & 1], (u >> 1) & 1);
         mma_commit(&bar_mma);
@@ -594,7 +612,8 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
         return cudaErrorInvalidValue;
     if (part == 1) {  // chain
         cudaFuncSetAttribute(scan_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
-        return launch_kernel(pb.pdl, scan_chain_kernel, dim3(2, pb.R), kThreads, kChainSmem, pb.stream, tA, a);
+        return launch_kernel(pb.pdl, scan_chain_kernel, dim3(2 * kChainSplit, pb.R), kThreads, kChainSmem, pb.stream,
+                             tA, a);
     }
     if (NR == 0 || pb.C == 0) return cudaSuccess;
     CUtensorMap tW, tK, tU;
