@@ -95,7 +95,6 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_ev_chunk = take(ev_cap * sizeof(int32_t));
     const size_t o_grp_pred = take(R * G * sizeof(int32_t));
     const size_t o_snap_slot = take(ev_cap * sizeof(int32_t));
-    const size_t o_ev_of = take(R * C * sizeof(int32_t));
     const size_t o_run_first = take(R * ((C + kRunChunks - 1) / kRunChunks + 1) * sizeof(int32_t));
     const size_t o_P = take((size_t)pb.B * pb.Nv * (C + 1) * sizeof(double));
     const size_t o_grp_info = take((size_t)R * G * 16);
@@ -119,7 +118,6 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
         ws->ev_chunk = (int32_t *)(b + o_ev_chunk);
         ws->grp_pred = (int32_t *)(b + o_grp_pred);
         ws->snap_slot = (int32_t *)(b + o_snap_slot);
-        ws->ev_of = (int32_t *)(b + o_ev_of);
         ws->run_first = (int32_t *)(b + o_run_first);
         ws->P = (double *)(b + o_P);
         ws->grp_info = b + o_grp_info;
@@ -217,15 +215,20 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
         if (prof) g_prof.launches += kernels;
     };
     auto none = [] { return cudaSuccess; };
+    // the status word collects every kernel's bits (timeouts, capacity overflows) for this prefill
+    if (cudaMemsetAsync(ws.counts + 2, 0, sizeof(int32_t), pb.stream) != cudaSuccess) return GDN_ERR_CUDA;
     if (mode == kOnline) {
         // intra first (its Tail-16 scores drive the selection), then the rest of the pipeline
         stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
         stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
-        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, ws.run_first, true, true); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
         stage(3, 1, [&] { return tc ? launch_wbuild_tc(pb, ws) : launch_wbuild(pb, ws); });
     } else {
-        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.ev_of, ws.run_first); });
+        // intra needs only the caller's mask (W goes to slot row * C + chunk), so it does not wait
+        // for the compaction and the prefix: their few CTAs run beside intra's first waves, and
+        // intra waits for them only before it exits
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, ws.run_first, false, true); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
         stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, w_deferred) : launch_intra(pb, ws); });
         // bf16: W is built inside intra for the event chunks, or after it from C-bar (w_deferred)
@@ -304,7 +307,7 @@ gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask, gdn_ev
     pb.mask = mask;
     pb.stream = (cudaStream_t)stream;
     // the snapshot numbering needs no capacity of its own: it never exceeds E
-    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity, nullptr, nullptr);
+    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity, nullptr, nullptr, true, false);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

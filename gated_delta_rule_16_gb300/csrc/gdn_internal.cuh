@@ -94,7 +94,6 @@ struct Problem {
 struct Workspace {
     int32_t *counts;           // [4]: E, n_snap, status, reserved
     int32_t *row_pair, *row_ptr, *ev_chunk, *grp_pred, *snap_slot;
-    int32_t *ev_of;            // [R, C] event index of each (physical row, chunk), or -1
     int32_t *run_first;        // [R, NR+1] first event of each run, per CSR row
     double *P;                 // [B, Nv, C+1] log2 decay prefix (Eq. 19)
     void *grp_info;            // [B, P, G] int4 {snapshot slot, kind, decay head 0, decay head 1}
@@ -119,8 +118,10 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws);
 // ev_of (may be NULL): [R, C] event index of each (physical row, chunk), -1 when not selected.
 // run_first (may be NULL): [R, NR+1] per CSR row, index of the first event of each run of
 // kRunChunks chunks (entry NR: the row's end).  Both need kRunChunks = 16 (two runs per mask word).
+// wait_first: the mask comes from the kernel before (else the kernel waits for it only before
+// exiting); or_status: OR the status bits into counts[2] instead of overwriting it.
 cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of,
-                          int32_t *run_first);
+                          int32_t *run_first, bool wait_first, bool or_status);
 cudaError_t launch_prefix(const Problem &pb, const Workspace &ws);
 cudaError_t launch_intra(const Problem &pb, const Workspace &ws);
 cudaError_t launch_wbuild(const Problem &pb, const Workspace &ws);

@@ -2,7 +2,7 @@
 // tensor cores, for bf16 storage.
 //
 // One CTA per (group of two chunks, value head, sequence): 128 tokens, 256 threads,
-// ~107 KB of shared memory and 256 TMEM columns, so two CTAs share an SM and one
+// ~109 KB of shared memory and 256 TMEM columns, so two CTAs share an SM and one
 // CTA's loads, barriers and MMA round trips overlap the other's work.  The two heads
 // of a pair are adjacent CTAs (the second read of their K tile comes from L2).
 //   Gram  G = K K^T [128 x 128]        (A = B = the K tile, K-major, by TMA)
@@ -18,10 +18,12 @@
 //       B = the K tile read as MN-major (token rows, d columns: the same bytes as the
 //       K-major Gram operand).  W is written at the event's index, so it is never
 //       built for skipped chunks, and negated: the scan accumulates -S^T W^T onto U^T.
+//       W of (row i = b P + p, chunk c) lives at slot i C + c, so this kernel needs only
+//       the caller's mask and runs before the compaction.
 // Shared memory over the CTA's life:
 //   [0, 32K)     K tile (Gram, then the W product)
 //   [32K, 64K)   V tile -> C-bar operand -> W staging
-//   [64K, 104K)  solver blocks (fp32) -> C diag(beta) operand (first 32K) -> U staging
+//   [64K, 106K)  solver blocks (fp32) -> C diag(beta) operand (first 32K) -> U staging
 // Each thread keeps its row's 32 coefficients of C in registers between the solve and
 // the two operand builds, which is what lets the operands overwrite the solver blocks.
 #include "gdn_internal.cuh"
@@ -39,20 +41,24 @@ constexpr uint32_t OFF_K = 0;            // K tile: 2 K-slabs [128 tok][64 d]
 constexpr uint32_t OFF_V = 2 * kSlab;    // V tile of the head: 2 MN-stacks [128 tok][64 dv]
 constexpr uint32_t OFF_A = 4 * kSlab;    // solver blocks, then C diag(beta) bf16: 2 K-slabs [128 t][64 s]
 // Solver blocks: 16x16 fp32 with a row stride of 20 floats (16-byte rows; eight rows read
-// at the same column quad fall in distinct banks).  Per chunk: the 4 diagonal blocks (M_ii,
-// then C_ii in place), the 6 below-diagonal blocks of M and the 6 of C.
+// at the same column quad fall in distinct banks), slots 16 floats apart beyond that so
+// that neighbouring blocks start 16 banks apart (the two half-warps of the diagonal solve
+// read two blocks at once).  Per chunk: the 4 diagonal blocks (M_ii, then C_ii in place),
+// the 6 below-diagonal blocks of M and the 6 of C.
 constexpr int BS = 20;
-constexpr int kBlkFloats = kBlk * BS;
+constexpr int kBlkFloats = kBlk * BS + 16;
 constexpr int kSlots = 16;
 constexpr uint32_t kSolveBytes = 2 * kSlots * kBlkFloats * 4;
 constexpr uint32_t OFF_SMALL = OFF_A + kSolveBytes;  // beta, g, beta 2^g of the 128 tokens
 constexpr uint32_t kIntraTcSmem = 1024 + OFF_SMALL + 3 * 128 * 4;
 static_assert(kSolveBytes >= 2 * kSlab, "the U operand and staging reuse the solver blocks");
+static_assert(kIntraTcSmem + 1024 <= 114 * 1024, "two CTAs per SM");
 constexpr uint32_t TM_G = 0, TM_U = 128;  // W reuses the Gram columns
 
 struct IntraParams {
     const float *beta, *g;
-    const int32_t *ev_of;   // NULL: no W here (online selection builds W later from C-bar)
+    const uint8_t *mask;    // [B,P,C] event mask, NULL: every chunk is an event
+    int build_w;            // 0: no W here (it is built later from C-bar)
     __nv_bfloat16 *U, *W;
     __nv_bfloat16 *cbar;    // non-NULL: write the compact C-bar blocks [B,Nv,C,nblk,16,16] (bf16)
     float *score;
@@ -218,6 +224,11 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         tma_load_4d(sm + OFF_V, &tV, 0, h, t0, b, &bar_ld);
         tma_load_4d(sm + OFF_V + kSlab, &tV, 64, h, t0, b, &bar_ld);
     }
+    if (tid >= kThreads - 2) {  // the W slot of each event chunk of the group, else -1
+        const int cc = tid - (kThreads - 2);
+        const int64_t slot = ((int64_t)b * a.P_ + p) * a.C + c0 + cc;
+        ev_s[cc] = a.build_w && cc < nch && (!a.mask || a.mask[slot]) ? (int)slot : -1;
+    }
     {   // beta and g of the head, fetched while the tiles load; tokens past the sequence's
         // end: beta = 0 (no write, no correction) and a finite g
         const int t = tid & 127;
@@ -244,14 +255,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         }
     }
     if (tid < 128) bgs[tid] = bet[tid] * ex2(gg[tid]);
-    // the event index of the group's chunks (the compaction's output), read by the last two
-    // threads while the others build M
-    int ev_mine = -1;
-    if (tid >= kThreads - 2) {
-        pdl_wait();
-        const int cc = tid - (kThreads - 2);
-        if (a.ev_of && cc < nch) ev_mine = a.ev_of[((int64_t)b * a.P_ + p) * a.C + c0 + cc];
-    }
     __syncthreads();
     if (!abort_s && !mbar_wait(&bar_g, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
     tc_fence_after();
@@ -279,7 +282,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
             }
         }
     }
-    if (tid >= kThreads - 2) ev_s[tid - (kThreads - 2)] = ev_mine;
     tc_fence_before();
     __syncthreads();
     // 2. solve.  Diagonal 16x16 blocks by forward substitution, in place: warp w < 4 takes
@@ -462,7 +464,7 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
         !make_tmap_bf16_3d(&tW, ws.W, kDim, wrows, 1, kDim * 2, wrows * kDim * 2, 64, 64, 1))
         return cudaErrorInvalidValue;
     IntraParams a;
-    a.beta = pb.beta; a.g = pb.g; a.ev_of = write_cbar ? nullptr : ws.ev_of;
+    a.beta = pb.beta; a.g = pb.g; a.mask = pb.mask; a.build_w = !write_cbar;
     a.cbar = write_cbar ? reinterpret_cast<__nv_bfloat16 *>(ws.cbar) : nullptr;
     a.U = (__nv_bfloat16 *)ws.U; a.W = (__nv_bfloat16 *)ws.W; a.score = pb.score;
     a.status = ws.counts + 2;

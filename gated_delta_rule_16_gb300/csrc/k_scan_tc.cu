@@ -181,8 +181,8 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     uint8_t *A2 = sm + OFF_A2;
     const bool with_u = mode != kModeHomog;
     // loads of event k (thread 0), each once its buffer is free
-    auto load_w = [&](int k) {
-        const int wrow = ((e_first + k) * 2 + hh) * kChunk;
+    auto load_w = [&](int k) {  // W of (row i, chunk c) at slot i C + c
+        const int wrow = (int)((((int64_t)i * a.C + ev_c[k]) * 2 + hh) * kChunk);
         mbar_arrive_expect_tx(&bar_w, 16384u);
         tma_load_3d(sm + OFF_W, &tW, 0, wrow, 0, &bar_w);
         tma_load_3d(sm + OFF_W + 8192, &tW, 64, wrow, 0, &bar_w);

@@ -86,7 +86,7 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
               int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
               int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
               int32_t *__restrict__ ev_of, int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
-              int64_t snap_cap) {
+              int64_t snap_cap, int wait_first, int or_status) {
     extern __shared__ int sm[];
     const int NW = (C + 31) >> 5;   // 32-chunk mask words per row
     int *cnt = sm;               // [R]   events per physical row
@@ -98,7 +98,9 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     unsigned *words = reinterpret_cast<unsigned *>(refb + R + 1);  // [kWarps][NW] one row's mask bits
     __shared__ int warp_tot[33];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    pdl_wait();  // an online selection writes the mask just before
+    // An online selection writes the mask just before: wait for it.  A caller's mask needs no
+    // wait, so the compaction overlaps the kernel before and waits only before it exits.
+    if (wait_first) pdl_wait();
     pdl_trigger();
     unsigned *wrow = words + warp * NW;
 
@@ -224,9 +226,11 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
         if (ns > snap_cap) st |= kStatusSnapOverflow;
         counts[0] = (int)E;
         counts[1] = ns;
-        counts[2] = st;
+        if (or_status) atomicOr(&counts[2], st);  // other kernels of the prefill latch theirs there too
+        else counts[2] = st;
         counts[3] = 0;
     }
+    if (!wait_first) pdl_wait();  // this grid's completion implies its predecessors'
 }
 
 // Word-parallel variant, used when the whole mask fits in shared memory as
@@ -246,7 +250,7 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
                     int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
                     int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
                     int32_t *__restrict__ ev_of, int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
-                    int64_t snap_cap) {
+                    int64_t snap_cap, int wait_first, int or_status) {
     extern __shared__ int sm[];
     const int NW = (C + 31) >> 5;
     const int NF = R * NW;
@@ -260,7 +264,9 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     __shared__ int warp_tot[33];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const unsigned below = (1u << lane) - 1u;
-    pdl_wait();  // an online selection writes the mask just before
+    // An online selection writes the mask just before: wait for it.  A caller's mask needs no
+    // wait, so the compaction overlaps the kernel before and waits only before it exits.
+    if (wait_first) pdl_wait();
     pdl_trigger();
     // 1. stage the mask: one warp per (row, 256 chunks), eight coalesced loads in flight
     const int NB = (NW + 7) >> 3;
@@ -383,15 +389,17 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
         if (ns > snap_cap) st |= kStatusSnapOverflow;
         counts[0] = E;
         counts[1] = ns;
-        counts[2] = st;
+        if (or_status) atomicOr(&counts[2], st);  // other kernels of the prefill latch theirs there too
+        else counts[2] = st;
         counts[3] = 0;
     }
+    if (!wait_first) pdl_wait();  // this grid's completion implies its predecessors'
 }
 
 }  // namespace
 
 cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of,
-                          int32_t *run_first) {
+                          int32_t *run_first, bool wait_first, bool or_status) {
     const int NW = (pb.C + 31) / 32, NR = (pb.C + kRunChunks - 1) / kRunChunks;
     const size_t fast = words_smem_bytes(pb.R, pb.R * NW);
     const bool use_words = fast <= kWordsSmemLimit;
@@ -403,7 +411,7 @@ cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_
     }
     return launch_kernel(pb.pdl, kernel, 1, kThreads, smem, pb.stream, pb.mask, pb.R, pb.C, pb.G, ev.row_pair,
                          ev.row_ptr, ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts, ev_of, run_first, NR,
-                         (int64_t)ev.capacity, snap_cap);
+                         (int64_t)ev.capacity, snap_cap, (int)wait_first, (int)or_status);
 }
 
 }  // namespace gdn

@@ -10,8 +10,9 @@
 //         assembled in shared memory from the compact blocks
 //   B   = the two events' K tiles                  [128 tokens x 128 d] bf16, MN-major, by TMA
 //   D_h = A_h B                                     fp32 in TMEM, columns 128 h .. 128 h + 127
-// and writes -D_h rounded to bf16 at W rows (2 e + h) * 64 by TMA (the workspace
-// holds -W, which the scan's U' product accumulates onto U).  The event count is
+// and writes -D_h rounded to bf16 at W rows (2 (i C + c) + h) * 64 by TMA, i the event's
+// row and c its chunk (the workspace holds -W, which the scan's U' product accumulates
+// onto U).  The event count is
 // read on the device; the grid strides over event pairs.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
@@ -63,7 +64,7 @@ wbuild_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t bar_ld, bar_mma, bar_drain;
     __shared__ uint32_t tmem_base;
-    __shared__ int ev_b[2], ev_p[2], ev_c[2], abort_s;
+    __shared__ int ev_b[2], ev_p[2], ev_c[2], ev_i[2], abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_wait();  // C-bar and the event lists of the kernels before
     pdl_trigger();
@@ -92,6 +93,7 @@ wbuild_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__
                 const int i = a.row_pair[j];
                 ev_b[tid] = i / a.P_;
                 ev_p[tid] = i % a.P_;
+                ev_i[tid] = i;
                 ev_c[tid] = a.ev_chunk[e];
             } else {
                 ev_b[tid] = -1;
@@ -186,9 +188,9 @@ wbuild_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__
         __syncthreads();
         if (tid == 0) {
             for (int j = 0; j < (two ? 2 : 1); ++j) {
-                const int64_t e = 2 * pi + j;
+                const int64_t slot = (int64_t)ev_i[j] * a.C + ev_c[j];  // W of (row i, chunk c)
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int wrow = (int)((e * 2 + hh) * kChunk);
+                    const int wrow = (int)((slot * 2 + hh) * kChunk);
                     uint8_t *stage = sm + OFF_A + hh * 2 * kSlab + j * 8192;
                     tma_store_3d(&tW, 0, wrow, 0, stage);
                     tma_store_3d(&tW, 64, wrow, 0, stage + kSlab);
