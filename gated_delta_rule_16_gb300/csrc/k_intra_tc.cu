@@ -97,14 +97,16 @@ __device__ __forceinline__ int cbar_index(int ib, int jb) {
 
 // Below-diagonal blocks at distance OFF of both chunks' C (Eq. 7 generalised), once every
 // block closer to the diagonal is known: T = sum_{k=jb}^{ib-1} M_{ib,k} C_{k,jb} is written
-// into C's block, then replaced by C_{ib,jb} = -C_{ib,ib} T.  Task (chunk, block, row,
-// column quad): 4 outputs from 16-byte shared-memory loads.
-template <int OFF>
+// into C's block (or, when no later level reads M, over M's own block, which saves a
+// barrier), then C_{ib,jb} = -C_{ib,ib} T.  Task (chunk, block, row, column quad): 4
+// outputs from 16-byte shared-memory loads.
+template <int OFF, bool T_OVER_M>
 __device__ __forceinline__ void offdiag_level(float *F, int tid) {
     constexpr int NB = 4 - OFF;
     constexpr int NT = 2 * NB * 64;
     constexpr int NU = (NT + kThreads - 1) / kThreads;
     float4 acc[NU];
+    float4 tv[NU];
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
         const int task = tid + u * kThreads;
@@ -125,7 +127,20 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
                     fma4(t, m.w, ld4(Cc + (k4 + 3) * BS));
                 }
             }
-            *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) = t;
+            if (T_OVER_M) tv[u] = t;
+            else *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) = t;
+        }
+    }
+    if (T_OVER_M) {  // a row of M's block is read only by the four lanes of its row's tasks (one warp)
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const int task = tid + u * kThreads;
+            if (task < NT) {
+                const int cc = task / (NB * 64), rem = task % (NB * 64);
+                const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
+                *reinterpret_cast<float4 *>(blk_m(F, cc, ib, jb) + rr * BS + q4) = tv[u];
+            }
         }
     }
     __syncthreads();
@@ -137,7 +152,7 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
             const int cc = task / (NB * 64), rem = task % (NB * 64);
             const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
             const float *Cr = blk_diag(F, cc, ib) + rr * BS;
-            const float *Tt = blk_c(F, cc, ib, jb) + q4;
+            const float *Tt = (T_OVER_M ? blk_m(F, cc, ib, jb) : blk_c(F, cc, ib, jb)) + q4;
 #pragma unroll
             for (int m4 = 0; m4 < kBlk; m4 += 4) {
                 const float4 c = ld4(Cr + m4);
@@ -148,7 +163,7 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
             }
         }
     }
-    __syncthreads();
+    if (!T_OVER_M) __syncthreads();  // T was in C's block: every reader is done before C replaces it
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
         const int task = tid + u * kThreads;
@@ -296,9 +311,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         for (int i2 = 0; i2 < kBlk; ++i2) x[i2] = i2 == j ? 1.f : 0.f;
 #pragma unroll
         for (int i2 = 1; i2 < kBlk; ++i2) {
+            float mr[kBlk];  // row i2 of M_ii, 16-byte loads (broadcast across the half-warp)
+#pragma unroll
+            for (int q4 = 0; q4 < (i2 + 3) / 4; ++q4) {
+                const float4 m4 = ld4(Mb + i2 * BS + 4 * q4);
+                mr[4 * q4] = m4.x; mr[4 * q4 + 1] = m4.y; mr[4 * q4 + 2] = m4.z; mr[4 * q4 + 3] = m4.w;
+            }
             float acc = 0.f;
 #pragma unroll
-            for (int s2 = 0; s2 < i2; ++s2) acc += Mb[i2 * BS + s2] * x[s2];
+            for (int s2 = 0; s2 < i2; ++s2) acc += mr[s2] * x[s2];
             if (i2 > j) x[i2] = -acc;
         }
         __syncwarp();  // every lane has read M_ii before C_ii replaces it
@@ -306,10 +327,12 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         for (int i2 = 0; i2 < kBlk; ++i2) Mb[i2 * BS + j] = x[i2];
     }
     __syncthreads();
-    offdiag_level<1>(F, tid);
-    if (exact) {
-        offdiag_level<2>(F, tid);
-        offdiag_level<3>(F, tid);
+    if (exact) {  // the far levels read M's distance-1 blocks: T goes to C's block
+        offdiag_level<1, false>(F, tid);
+        offdiag_level<2, false>(F, tid);
+        offdiag_level<3, false>(F, tid);
+    } else {
+        offdiag_level<1, true>(F, tid);
     }
     const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;
     // 3. this thread's 32 coefficients of C (blocks the solver does not keep are zero)

@@ -246,6 +246,8 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
         f_end = ex2(ls + (mode == kModeFixup ? 0.f : (float)(Pl[c_hi - c_lo] - Pl[cl - c_lo])));
     }
     __syncthreads();
+    for (int idx = tid; idx < n_ev * kChunk; idx += kThreads) dec[idx >> 6][idx & 63] *= f_u[idx >> 6];
+    __syncthreads();  // dec[k][t] = 2^(gamma - g_t) / sigma after event k
     auto snapshot = [&](int slot, const float (&S)[32], float f) {  // row `row` of f S^T, columns cs .. cs+31
         if (slot >= 0 && slot < a.snap_cap) {
             uint4 *sn = reinterpret_cast<uint4 *>(a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim) + row * kDim + cs);
@@ -333,10 +335,9 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                     *reinterpret_cast<__nv_bfloat16 *>(ut + sw128_offset(16 * seg + t, row & 63)) =
                         __float2bfloat16_rn(acc[t]);
             }
-            const float fs = f_u[k];
             float up[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) up[t] = acc[t] * dec[k][16 * seg + t] * fs;
+            for (int t = 0; t < 16; ++t) up[t] = acc[t] * dec[k][16 * seg + t];
 #pragma unroll
             for (int t0 = 0; t0 < 16; t0 += 8) st_sw128_8(A2, row, 16 * seg + t0, &up[t0]);
         }
