@@ -61,7 +61,8 @@ constexpr uint32_t kRunSmem = 1024 + 6 * kSlab + 8192;
 constexpr float kMinLog2Scale = -64.f;
 constexpr uint32_t TM_U = 0;             // TMEM columns [0, 64): U'^T accumulator
 constexpr uint32_t TM_S = 128;           // TMEM columns [128, 256): the state S^T
-constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab;
+constexpr uint32_t kBlockQuads = 32 * 4 * 32 * 4;  // one row block's 32 rows of a column-quad fp32 tile (16 KB)
+constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab + 3 * kBlockQuads;
 constexpr int kMaxRuns = 1024;  // C <= 16384 chunks
 // The chain of one (row, head) is split over kChainSplit CTAs, each owning kChainRows rows
 // of S^T (the rows evolve independently); its MMAs keep M = 128 with the other rows zero.
@@ -418,7 +419,8 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
 
 // grid: (2 heads x kChainSplit row blocks, CSR rows R).  S_{r+1}^T = S_r^T A_r^T + B_r^T over the runs.
 __global__ void __launch_bounds__(kThreads, 1)
-scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
+scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                  const __grid_constant__ CUtensorMap tE, ScanParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     __shared__ uint64_t bar_tma[2], bar_mma;
@@ -472,8 +474,11 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
-    uint8_t *Atile = sm;
-    uint8_t *Mbuf = sm + 2 * kSlab;
+    uint8_t *Atile = sm;                  // S^T bf16, K-major (rows of other blocks stay zero)
+    uint8_t *Mbuf = sm + 2 * kSlab;       // A_r^T, two buffers
+    uint8_t *Bbuf = sm + 6 * kSlab;       // this block's rows of B_r^T (fp32, column quads), two buffers
+    uint8_t *Estage = sm + 8 * kSlab;     // this block's rows of the entry state, for one TMA store
+    const int qrow = row * 16;            // byte offset of this thread's row inside a column quad
 
     float S[32];
 #pragma unroll
@@ -484,45 +489,43 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
     }
 
     auto next_run = [&](int r) -> int { return r < a.NR ? nxt[r] : a.NR; };
+    // thread 0: A_r^T and this block's B_r^T rows of run rn into buffer nb
+    auto load_run = [&](int rn, int nb) {
+        mbar_arrive_expect_tx(&bar_tma[nb], 2 * kSlab + kBlockQuads);
+        tma_load_3d(Mbuf + nb * 2 * kSlab, &tA, 0, (int)((rbase + rn) * kDim), 0, &bar_tma[nb]);
+        tma_load_3d(Mbuf + nb * 2 * kSlab + kSlab, &tA, 64, (int)((rbase + rn) * kDim), 0, &bar_tma[nb]);
+        tma_load_2d(Bbuf + nb * kBlockQuads, &tB, part * 4 * kChainRows, (int)((rbase + rn) * 32), &bar_tma[nb]);
+    };
     int n_loads = 0, n_mma = 0;
     if (tid == 0) {
         const int r0 = next_run(0);
         if (r0 < a.NR) {
-            mbar_arrive_expect_tx(&bar_tma[0], 2 * kSlab);
-            tma_load_3d(Mbuf, &tA, 0, (int)((rbase + r0) * kDim), 0, &bar_tma[0]);
-            tma_load_3d(Mbuf + kSlab, &tA, 64, (int)((rbase + r0) * kDim), 0, &bar_tma[0]);
+            load_run(r0, 0);
             n_loads = 1;
         }
     }
     const uint32_t idesc = idesc_bf16(128, 128, false, true);
     int used = 0;  // map tiles consumed
-    float Bm[32];  // B^T row segment of the next run with events
-    {
-        const int r0 = next_run(0);
-        if (r0 < a.NR && active) {
-            const float4 *bsrc = reinterpret_cast<const float4 *>(a.bmap + (rbase + r0) * (kDim * kDim)) + 8 * seg * 128 + dv;
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) {
-                const float4 x = bsrc[v4 * 128];
-                Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
-            }
-        }
-    }
     for (int r = 0; r < a.NR; ++r) {
         const int c_lo = r * kRun, c_hi = min(a.C, c_lo + kRun);
-        if (active) {
-            float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim)) + 8 * seg * 128 + dv;
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
-        }
         const bool has = nxt[r] == r;
-        if (!has) {
+        if (!has) {  // no events: the state only decays (the entry state goes out directly)
+            if (active) {
+                float4 *ent = reinterpret_cast<float4 *>(a.entry + (rbase + r) * (kDim * kDim)) + 8 * seg * 128 + dv;
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4)
+                    ent[v4 * 128] = make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
+            }
             const float f = ex2((float)(Pu[c_hi] - Pu[c_lo]));
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) S[jj] *= f;
             continue;
         }
-        if (active) {
+        if (active) {  // the entering state: fp32 for the entry table, bf16 as the MMA operand
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+                *reinterpret_cast<float4 *>(Estage + (cs / 4 + v4) * 512 + qrow) =
+                    make_float4(S[4 * v4], S[4 * v4 + 1], S[4 * v4 + 2], S[4 * v4 + 3]);
 #pragma unroll
             for (int k0 = 0; k0 < 32; k0 += 8) st_sw128_8(Atile + slab * kSlab, row, cin + k0, &S[k0]);
         }
@@ -531,6 +534,8 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         __syncthreads();
         const int bufi = used & 1;
         if (tid == 0) {
+            tma_store_2d(&tE, part * 4 * kChainRows, (int)((rbase + r) * 32), Estage);
+            bulk_commit();
             if (!mbar_wait(&bar_tma[bufi], (used >> 1) & 1)) {
                 fail(a, &abort_s);
             } else {
@@ -541,12 +546,8 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
                              idesc, ks > 0);
                 mma_commit(&bar_mma);
                 const int rn = next_run(r + 1);
-                if (rn < a.NR) {
-                    const int nb = (used + 1) & 1;
-                    uint8_t *dst = Mbuf + nb * 2 * kSlab;
-                    mbar_arrive_expect_tx(&bar_tma[nb], 2 * kSlab);
-                    tma_load_3d(dst, &tA, 0, (int)((rbase + rn) * kDim), 0, &bar_tma[nb]);
-                    tma_load_3d(dst + kSlab, &tA, 64, (int)((rbase + rn) * kDim), 0, &bar_tma[nb]);
+                if (rn < a.NR) {  // the other buffer was read by the previous step (its MMA and B rows)
+                    load_run(rn, (used + 1) & 1);
                     ++n_loads;
                 }
             }
@@ -555,26 +556,24 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         if (abort_s) break;
         if (!mbar_wait(&bar_mma, n_mma & 1)) fail(a, &abort_s);
         ++n_mma;
-        ++used;
         tc_fence_after();
         if (active) {
+            if (tid != 0 && !mbar_wait(&bar_tma[bufi], (used >> 1) & 1)) fail(a, &abort_s);  // B rows visible
             float d0[32];
             tmem_ld32(tmem_addr(tbase, quarter * 32, cs), d0);
             tmem_ld_wait();
+            const uint8_t *bsrc = Bbuf + bufi * kBlockQuads + qrow;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] = d0[jj] + Bm[jj];
-            // refill with the next run's B^T row; the loads land during the next step
-            const int rn2 = next_run(r + 1);
-            if (rn2 < a.NR) {
-                const float4 *bsrc =
-                    reinterpret_cast<const float4 *>(a.bmap + (rbase + rn2) * (kDim * kDim)) + 8 * seg * 128 + dv;
-#pragma unroll
-                for (int v4 = 0; v4 < 8; ++v4) {
-                    const float4 x = bsrc[v4 * 128];
-                    Bm[4 * v4] = x.x; Bm[4 * v4 + 1] = x.y; Bm[4 * v4 + 2] = x.z; Bm[4 * v4 + 3] = x.w;
-                }
+            for (int v4 = 0; v4 < 8; ++v4) {
+                const float4 x = *reinterpret_cast<const float4 *>(bsrc + (cs / 4 + v4) * 512);
+                S[4 * v4] = d0[4 * v4] + x.x;
+                S[4 * v4 + 1] = d0[4 * v4 + 1] + x.y;
+                S[4 * v4 + 2] = d0[4 * v4 + 2] + x.z;
+                S[4 * v4 + 3] = d0[4 * v4 + 3] + x.w;
             }
         }
+        ++used;
+        if (tid == 0) bulk_wait_read();  // the entry store has read the staging tile
         tc_fence_before();
         __syncthreads();
         if (abort_s) break;
@@ -589,6 +588,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, ScanParams a) {
         mma_commit(&bar_mma);
         mbar_wait(&bar_mma, n_mma & 1);
     }
+    if (tid == 0) bulk_wait_read();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc<128>(tbase);
@@ -613,8 +613,14 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
         return cudaErrorInvalidValue;
     if (part == 1) {  // chain
         cudaFuncSetAttribute(scan_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
+        // B_r^T and entry tiles as [quads][512 floats]: a box of 128 floats x 32 quads is one row block
+        CUtensorMap tB, tE;
+        const uint64_t quads = (uint64_t)pb.R * 2 * (NR > 0 ? NR : 1) * 32;
+        if (!make_tmap_f32_2d(&tB, ws.bmap, 512, quads, 2048, 4 * kChainRows, 32) ||
+            !make_tmap_f32_2d(&tE, ws.entry, 512, quads, 2048, 4 * kChainRows, 32))
+            return cudaErrorInvalidValue;
         return launch_kernel(pb.pdl, scan_chain_kernel, dim3(2 * kChainSplit, pb.R), kThreads, kChainSmem, pb.stream,
-                             tA, a);
+                             tA, tB, tE, a);
     }
     if (NR == 0 || pb.C == 0) return cudaSuccess;
     CUtensorMap tW, tK, tU;

@@ -62,4 +62,20 @@ inline bool make_tmap_tokens(CUtensorMap *map, const void *base, uint64_t heads,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A rank-2 fp32 tensor: dims[0] contiguous (elements), rows stride1_bytes apart (a multiple
+// of 16), box {box0, box1}, no swizzle.  Returns false if encoding fails.
+inline bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t stride1_bytes,
+                             uint32_t box0, uint32_t box1) {
+    if (reinterpret_cast<uintptr_t>(base) & 15u) return false;
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {d0, d1};
+    cuuint64_t strides[1] = {stride1_bytes};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gdn
