@@ -363,16 +363,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
             const int jb = 2 * half + h2;
-            if (jb <= ib && (exact || jb + 1 >= ib)) {
-                alignas(16) __nv_bfloat162 p2[8];
+            if (jb <= ib && (exact || jb + 1 >= ib)) {  // one block row: 32 bytes, a whole sector
+                uint32_t w[8];
 #pragma unroll
                 for (int q2 = 0; q2 < 8; ++q2)
-                    p2[q2] = __floats2bfloat162_rn(creg[16 * h2 + 2 * q2] * gcol[16 * h2 + 2 * q2],
-                                                   creg[16 * h2 + 2 * q2 + 1] * gcol[16 * h2 + 2 * q2 + 1]);
-                uint4 *dst = reinterpret_cast<uint4 *>(a.cbar + (((int64_t)b * a.Nv + h) * a.C + c0 + ct) * a.nblk * 256 +
-                                                       cbar_index(ib, jb) * 256 + rr * 16);
-                dst[0] = reinterpret_cast<const uint4 *>(p2)[0];
-                dst[1] = reinterpret_cast<const uint4 *>(p2)[1];
+                    w[q2] = pack_bf16x2(creg[16 * h2 + 2 * q2] * gcol[16 * h2 + 2 * q2],
+                                        creg[16 * h2 + 2 * q2 + 1] * gcol[16 * h2 + 2 * q2 + 1]);
+                st_global_v8(a.cbar + (((int64_t)b * a.Nv + h) * a.C + c0 + ct) * a.nblk * 256 +
+                                 cbar_index(ib, jb) * 256 + rr * 16,
+                             w);
             }
         }
     }

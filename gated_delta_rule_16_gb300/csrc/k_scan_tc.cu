@@ -251,13 +251,13 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     __syncthreads();  // dec[k][t] = 2^(gamma - g_t) / sigma after event k
     auto snapshot = [&](int slot, const float (&S)[32], float f) {  // row `row` of f S^T, columns cs .. cs+31
         if (slot >= 0 && slot < a.snap_cap) {
-            uint4 *sn = reinterpret_cast<uint4 *>(a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim) + row * kDim + cs);
+            __nv_bfloat16 *sn = a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim) + row * kDim + cs;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                alignas(16) __nv_bfloat162 p2[4];
+            for (int q = 0; q < 2; ++q) {  // 32 bytes per lane and store: whole sectors (half-sector
+                uint32_t w[8];             // 16-byte stores made this the fix-up's slowest part)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) p2[u] = __floats2bfloat162_rn(f * S[8 * q + 2 * u], f * S[8 * q + 2 * u + 1]);
-                sn[q] = *reinterpret_cast<uint4 *>(p2);
+                for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(f * S[16 * q + 2 * u], f * S[16 * q + 2 * u + 1]);
+                st_global_v8(sn + 16 * q, w);
             }
         }
     };

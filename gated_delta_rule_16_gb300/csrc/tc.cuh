@@ -269,6 +269,19 @@ __host__ __device__ __forceinline__ uint32_t quad_index(uint32_t row, uint32_t c
     return (col >> 2) * 512u + row * 4u + (col & 3u);
 }
 
+// Two floats as a packed bf16 pair (round to nearest even).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// 32-byte global store of eight 32-bit words (address 32-byte aligned): a whole L2 sector.
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // Stores 8 consecutive K values (k0 % 8 == 0) of one row as one 16-byte chunk.
 __device__ __forceinline__ void st_sw128_8(uint8_t *slab, uint32_t row, uint32_t k0, const float *v) {
     __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
