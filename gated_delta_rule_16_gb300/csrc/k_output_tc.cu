@@ -17,8 +17,9 @@
 //   [0, 32K)    Q (QK and QS) -> the A tile
 //   [32K, 64K)  K (QK) -> U' (loaded once QK is done) -> O staging
 //   [64K, 96K)  the entry state S^T
-// The A values wait in registers (packed bf16) until QS has read Q; AU accumulates
-// into QK's TMEM columns.
+// The A values wait in registers (packed bf16) until QS has read Q; QS is issued after
+// they are built, so the snapshot's load does not delay them; AU accumulates into QK's
+// TMEM columns.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -160,7 +161,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     const float inv_sqrt_d = rsqrtf((float)kDim);
     const int kind = has_s;
     bool s_wait_ok = true;  // thread 0
-    if (tid == 0) {  // QK, then QS (its state is loaded or written by now)
+    if (tid == 0) {  // QK (QS follows the A values: its state may still be landing)
         if (!mbar_wait(&bar_qk_ld, 0)) {
             abort_s = 1;
             atomicOr(a.status, kStatusTimeout);
@@ -170,18 +171,6 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
                 mma_bf16(tbase + TM_QK, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
                          kmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id_kk, ks > 0);
             mma_commit(&bar_qk);
-            if (kind != 0) {
-                if (kind == 1 && !mbar_wait(&bar_s, 0)) {
-                    s_wait_ok = false;
-                    abort_s = 1;
-                    atomicOr(a.status, kStatusTimeout);
-                } else {
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16(tbase + TM_QS, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
-                                 kmajor_desc(smem_addr(sm + OFF_S), ks, kSlab), id_kk, ks > 0);
-                }
-            }
-            mma_commit(&bar_qs);  // also without QS: arrives once QK is done
         }
     }
     __syncthreads();  // publishes abort_s and the mask factors
@@ -224,11 +213,24 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     }
     tc_fence_before();
     __syncthreads();
-    // 2. K has been read: U' takes its place
+    // 2. K has been read: U' takes its place; QS once its state has landed
     if (tid == 0 && !abort_s) {
         mbar_arrive_expect_tx(&bar_u_ld, 2 * kSlab);
         tma_load_4d(sm + OFF_K, &tU, 0, h, t0, b, &bar_u_ld);
         tma_load_4d(sm + OFF_K + kSlab, &tU, 64, h, t0, b, &bar_u_ld);
+        if (kind != 0) {
+            if (kind == 1 && !mbar_wait(&bar_s, 0)) {
+                s_wait_ok = false;
+                abort_s = 1;
+                atomicOr(a.status, kStatusTimeout);
+            } else {
+                tc_fence_after();
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tbase + TM_QS, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                             kmajor_desc(smem_addr(sm + OFF_S), ks, kSlab), id_kk, ks > 0);
+            }
+        }
+        mma_commit(&bar_qs);  // also without QS: arrives at once (QK is done)
     }
     // 3. once QS has read Q, the A tile goes there
     if (!abort_s && !mbar_wait(&bar_qs, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
