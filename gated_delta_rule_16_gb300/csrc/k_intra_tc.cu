@@ -197,7 +197,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
                 const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tW, IntraParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
-    __shared__ uint64_t bar_ld, bar_g, bar_u, bar_w, bar_drain;
+    __shared__ uint64_t bar_ld, bar_v, bar_g, bar_u, bar_w, bar_drain;
     __shared__ int ev_s[2];
     __shared__ float ssum_w[kThreads / 32];
     __shared__ uint32_t tmem_base;
@@ -227,17 +227,19 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     pdl_trigger();
     if (tid == 0) {  // barriers, then the tiles: the loads overlap the set-up below
         mbar_init(&bar_ld, 1);
+        mbar_init(&bar_v, 1);
         mbar_init(&bar_g, 1);
         mbar_init(&bar_u, 1);
         mbar_init(&bar_w, 1);
         mbar_init(&bar_drain, 1);
         fence_mbar_init();
         abort_s = 0;
-        mbar_arrive_expect_tx(&bar_ld, 4 * kSlab);
+        mbar_arrive_expect_tx(&bar_ld, 2 * kSlab);  // K: the Gram product starts once it lands
         tma_load_4d(sm + OFF_K, &tK, 0, p, t0, b, &bar_ld);  // rows past the sequence's end read zeros
         tma_load_4d(sm + OFF_K + kSlab, &tK, 64, p, t0, b, &bar_ld);
-        tma_load_4d(sm + OFF_V, &tV, 0, h, t0, b, &bar_ld);
-        tma_load_4d(sm + OFF_V + kSlab, &tV, 64, h, t0, b, &bar_ld);
+        mbar_arrive_expect_tx(&bar_v, 2 * kSlab);   // V: needed only by the U product
+        tma_load_4d(sm + OFF_V, &tV, 0, h, t0, b, &bar_v);
+        tma_load_4d(sm + OFF_V + kSlab, &tV, 64, h, t0, b, &bar_v);
     }
     if (tid >= kThreads - 2) {  // the W slot of each event chunk of the group, else -1
         const int cc = tid - (kThreads - 2);
@@ -381,11 +383,16 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     // 5. U = (C diag(beta)) V
     const uint32_t id = idesc_bf16(128, 128, false, true);
     if (tid == 0 && !abort_s) {
-        tc_fence_after();
-        for (int ks = 0; ks < 8; ++ks)
-            mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
-                     mnmajor_desc(smem_addr(sm + OFF_V), ks, kSlab), id, ks > 0);
-        mma_commit(&bar_u);
+        if (!mbar_wait(&bar_v, 0)) {
+            abort_s = 1;
+            atomicOr(a.status, kStatusTimeout);
+        } else {
+            tc_fence_after();
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tbase + TM_U, kmajor_desc(smem_addr(sm + OFF_A), ks, kSlab),
+                         mnmajor_desc(smem_addr(sm + OFF_V), ks, kSlab), id, ks > 0);
+            mma_commit(&bar_u);
+        }
     }
     if (!abort_s && !mbar_wait(&bar_u, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
     tc_fence_after();
@@ -465,6 +472,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     if (tid == 0) bulk_wait_read();  // the stores only need their shared-memory sources before exit
     if (abort_s && tid == 0) {
         mbar_wait(&bar_ld, 0);
+        mbar_wait(&bar_v, 0);
         mma_commit(&bar_drain);
         mbar_wait(&bar_drain, 0);
     }
