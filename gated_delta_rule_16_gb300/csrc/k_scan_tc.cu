@@ -62,7 +62,8 @@ constexpr float kMinLog2Scale = -64.f;
 constexpr uint32_t TM_U = 0;             // TMEM columns [0, 64): U'^T accumulator
 constexpr uint32_t TM_S = 128;           // TMEM columns [128, 256): the state S^T
 constexpr uint32_t kBlockQuads = 32 * 4 * 32 * 4;  // one row block's 32 rows of a column-quad fp32 tile (16 KB)
-constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + 2 * 2 * kSlab + 3 * kBlockQuads;
+constexpr int kChainBufs = 3;  // A_r / B_r buffers: runs are prefetched two steps ahead
+constexpr uint32_t kChainSmem = 1024 + 2 * kSlab + kChainBufs * (2 * kSlab + kBlockQuads) + kBlockQuads;
 constexpr int kMaxRuns = 1024;  // C <= 16384 chunks
 // The chain of one (row, head) is split over kChainSplit CTAs, each owning kChainRows rows
 // of S^T (the rows evolve independently); its MMAs keep M = 128 with the other rows zero.
@@ -423,7 +424,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
                   const __grid_constant__ CUtensorMap tE, ScanParams a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
-    __shared__ uint64_t bar_tma[2], bar_mma;
+    __shared__ uint64_t bar_tma[kChainBufs], bar_mma;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
     __shared__ int nxt[kMaxRuns + 1];  // nxt[r]: first run >= r holding events of this row (NR if none)
@@ -442,8 +443,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
     const int64_t rbase = ((int64_t)i * 2 + hh) * a.NR;
 
     if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
+        for (int q = 0; q < kChainBufs; ++q) mbar_init(&bar_tma[q], 1);
         mbar_init(&bar_mma, 1);
         fence_mbar_init();
         abort_s = 0;
@@ -475,9 +475,9 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
     tc_fence_after();
     const uint32_t tbase = tmem_base;
     uint8_t *Atile = sm;                  // S^T bf16, K-major (rows of other blocks stay zero)
-    uint8_t *Mbuf = sm + 2 * kSlab;       // A_r^T, two buffers
-    uint8_t *Bbuf = sm + 6 * kSlab;       // this block's rows of B_r^T (fp32, column quads), two buffers
-    uint8_t *Estage = sm + 8 * kSlab;     // this block's rows of the entry state, for one TMA store
+    uint8_t *Mbuf = sm + 2 * kSlab;                              // A_r^T, kChainBufs buffers
+    uint8_t *Bbuf = Mbuf + kChainBufs * 2 * kSlab;               // this block's rows of B_r^T (fp32, column quads)
+    uint8_t *Estage = Bbuf + kChainBufs * kBlockQuads;           // this block's rows of the entry state
     const int qrow = row * 16;            // byte offset of this thread's row inside a column quad
 
     float S[32];
@@ -496,12 +496,14 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
         tma_load_3d(Mbuf + nb * 2 * kSlab + kSlab, &tA, 64, (int)((rbase + rn) * kDim), 0, &bar_tma[nb]);
         tma_load_2d(Bbuf + nb * kBlockQuads, &tB, part * 4 * kChainRows, (int)((rbase + rn) * 32), &bar_tma[nb]);
     };
-    int n_loads = 0, n_mma = 0;
+    int n_loads = 0, n_mma = 0, last = -1;  // thread 0: tiles requested, the last run requested
     if (tid == 0) {
-        const int r0 = next_run(0);
-        if (r0 < a.NR) {
-            load_run(r0, 0);
-            n_loads = 1;
+        for (int q = 0; q < kChainBufs - 1; ++q) {
+            const int rn = next_run(last + 1);
+            if (rn >= a.NR) break;
+            load_run(rn, q);
+            last = rn;
+            ++n_loads;
         }
     }
     const uint32_t idesc = idesc_bf16(128, 128, false, true);
@@ -532,11 +534,12 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        const int bufi = used & 1;
+        const int bufi = used % kChainBufs;
+        const uint32_t par = (uint32_t)(used / kChainBufs) & 1u;
         if (tid == 0) {
             tma_store_2d(&tE, part * 4 * kChainRows, (int)((rbase + r) * 32), Estage);
             bulk_commit();
-            if (!mbar_wait(&bar_tma[bufi], (used >> 1) & 1)) {
+            if (!mbar_wait(&bar_tma[bufi], par)) {
                 fail(a, &abort_s);
             } else {
                 tc_fence_after();
@@ -545,9 +548,10 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
                     mma_bf16(tbase, kmajor_desc(smem_addr(Atile), ks, kSlab), mnmajor_desc(smem_addr(mt), ks, kSlab),
                              idesc, ks > 0);
                 mma_commit(&bar_mma);
-                const int rn = next_run(r + 1);
-                if (rn < a.NR) {  // the other buffer was read by the previous step (its MMA and B rows)
-                    load_run(rn, (used + 1) & 1);
+                const int rn = next_run(last + 1);
+                if (rn < a.NR) {  // the buffer the previous step read (its MMA and B rows are done)
+                    load_run(rn, (used + kChainBufs - 1) % kChainBufs);
+                    last = rn;
                     ++n_loads;
                 }
             }
@@ -558,7 +562,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
         ++n_mma;
         tc_fence_after();
         if (active) {
-            if (tid != 0 && !mbar_wait(&bar_tma[bufi], (used >> 1) & 1)) fail(a, &abort_s);  // B rows visible
+            if (tid != 0 && !mbar_wait(&bar_tma[bufi], par)) fail(a, &abort_s);  // B rows visible
             float d0[32];
             tmem_ld32(tmem_addr(tbase, quarter * 32, cs), d0);
             tmem_ld_wait();
@@ -584,7 +588,7 @@ scan_chain_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant_
             for (int jj = 0; jj < 32; ++jj) a.s_final[sbase + (int64_t)(cs + jj) * kDim + dv] = S[jj];
         }
     } else if (tid == 0) {
-        for (int u = used + 1; u < n_loads; ++u) mbar_wait(&bar_tma[u & 1], (u >> 1) & 1);
+        for (int u = used + 1; u < n_loads; ++u) mbar_wait(&bar_tma[u % kChainBufs], (u / kChainBufs) & 1);
         mma_commit(&bar_mma);
         mbar_wait(&bar_mma, n_mma & 1);
     }
