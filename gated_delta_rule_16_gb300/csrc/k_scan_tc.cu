@@ -146,6 +146,18 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     }
     const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
     if (tid <= c_hi - c_lo) Pl[tid] = Pu[c_lo + tid];
+    float S0[32];  // the entering state (fix-up: the chain's entry table), loaded with the lists above
+    if (mode == kModeFixup) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase) + 8 * seg * 128 + row;
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 x = src[v4 * 128];
+            S0[4 * v4] = x.x; S0[4 * v4 + 1] = x.y; S0[4 * v4 + 2] = x.z; S0[4 * v4 + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) S0[jj] = mode == kModeHomog && cs + jj == row ? 1.f : 0.f;
+    }
     if (tid == 0) {
         mbar_init(&bar_w, 1);
         mbar_init(&bar_k, 1);
@@ -212,40 +224,46 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
             loads_u = 1;
         }
     }
-    {   // the entering state, into TMEM
-        float S[32];
-        if (mode == kModeHomog) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] = (cs + jj == row) ? 1.f : 0.f;
-        } else if (mode == kModeInhom) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] = 0.f;
-        } else {
-            const float4 *src = reinterpret_cast<const float4 *>(a.entry + ubase) + 8 * seg * 128 + row;
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) {
-                const float4 x = src[v4 * 128];
-                S[4 * v4] = x.x; S[4 * v4 + 1] = x.y; S[4 * v4 + 2] = x.z; S[4 * v4 + 3] = x.w;
-            }
-        }
-        tmem_st32(t_s, S);
-        tmem_st_wait();
-    }
+    tmem_st32(t_s, S0);  // the entering state: identity (A_r), zero (B_r) or the true entry (fix-up)
+    tmem_st_wait();
     __syncthreads();  // dec[], gamk[], dPk[] complete
-    if (tid == 0) {   // the scale sigma = 2^ls through the run
-        float ls = 0.f;
-        for (int k = 0; k < n_ev; ++k) {
-            f_snap[k] = ex2(ls);            // the state left by event k-1
-            const float lop = ls + dPk[k];  // the state entering chunk c_k
-            f_op[k] = ex2(lop);
-            const float lnew = lop + gamk[k];
-            ren[k] = lnew < kMinLog2Scale;  // keep 1/sigma in range: apply this decay to TMEM instead
-            f_ren[k] = ex2(lnew);
-            ls = ren[k] ? 0.f : lnew;
-            f_u[k] = ex2(-ls);
+    if (warp == 0) {  // the scale sigma = 2^ls through the run: ls is a prefix sum of (dP_k + gamma_k)
+        const float x = lane < n_ev ? dPk[lane] + gamk[lane] : 0.f;
+        float incl = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
-        const int cl = ev_c[n_ev - 1] + 1;
-        f_end = ex2(ls + (mode == kModeFixup ? 0.f : (float)(Pl[c_hi - c_lo] - Pl[cl - c_lo])));
+        const bool low = __any_sync(0xffffffffu, lane < n_ev && incl < kMinLog2Scale);
+        if (!low) {  // 1/sigma stays in range over the whole run
+            const float excl = incl - x;
+            if (lane < n_ev) {
+                f_snap[lane] = ex2(excl);
+                f_op[lane] = ex2(excl + dPk[lane]);
+                ren[lane] = 0;
+                f_ren[lane] = 1.f;
+                f_u[lane] = ex2(-incl);
+            }
+            if (lane == n_ev - 1) {
+                const int cl = ev_c[n_ev - 1] + 1;
+                f_end = ex2(incl + (mode == kModeFixup ? 0.f : (float)(Pl[c_hi - c_lo] - Pl[cl - c_lo])));
+            }
+        } else if (lane == 0) {  // a renormalisation is due somewhere: the serial rule
+            float ls = 0.f;
+            for (int k = 0; k < n_ev; ++k) {
+                f_snap[k] = ex2(ls);            // the state left by event k-1
+                const float lop = ls + dPk[k];  // the state entering chunk c_k
+                f_op[k] = ex2(lop);
+                const float lnew = lop + gamk[k];
+                ren[k] = lnew < kMinLog2Scale;  // keep 1/sigma in range: apply this decay to TMEM instead
+                f_ren[k] = ex2(lnew);
+                ls = ren[k] ? 0.f : lnew;
+                f_u[k] = ex2(-ls);
+            }
+            const int cl = ev_c[n_ev - 1] + 1;
+            f_end = ex2(ls + (mode == kModeFixup ? 0.f : (float)(Pl[c_hi - c_lo] - Pl[cl - c_lo])));
+        }
     }
     __syncthreads();
     for (int idx = tid; idx < n_ev * kChunk; idx += kThreads) dec[idx >> 6][idx & 63] *= f_u[idx >> 6];
