@@ -102,6 +102,20 @@ def test_all_ones_sparse_equals_dense_bitwise():
         assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["s_final"], b["s_final"])
 
 
+@pytest.mark.parametrize("scale", [20.0, 100.0])
+def test_strong_decay(scale):
+    # Gates scaled so that the decay over a run of chunks passes 2^-64: the tensor-core scan then
+    # applies decays to its TMEM state and restarts the state's scale inside runs (scale 20: about
+    # every second event chunk; scale 100: every event).  Scale 100 (about -160 log2 decay per chunk)
+    # also sends the output's decay mask to its per-element path (a two-chunk range above 200).
+    x = gdn_synth.make_inputs(1, 4096, 2, 4, dtype="bf16", seed=73, mask="bernoulli", retention=0.5,
+                              with_h0=True)
+    x.g = (x.g.astype(np.float64) * scale).astype(np.float32)
+    for solver in ("block_adj", "exact"):
+        res = run_gpu(x, solver=solver)
+        assert_close(res, oracle_run(x, solver), "bf16", f"gates x{scale} {solver}")
+
+
 # ----------------------------------------------------------------- CSR ---
 
 @pytest.mark.parametrize("shape,p", [((1, 1, 4), 0.5), ((2, 3, 7), 0.4), ((3, 16, 33), 0.29),
