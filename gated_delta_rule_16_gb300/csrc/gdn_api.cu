@@ -221,14 +221,14 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
         // intra first (its Tail-16 scores drive the selection), then the rest of the pipeline
         stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
         stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
-        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, ws.run_first, true, true); });
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.run_first, true, true); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
         stage(3, 1, [&] { return tc ? launch_wbuild_tc(pb, ws) : launch_wbuild(pb, ws); });
     } else {
         // intra needs only the caller's mask (W goes to slot row * C + chunk), so it does not wait
         // for the compaction and the prefix: their few CTAs run beside intra's first waves, and
         // intra waits for them only before it exits
-        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, ws.run_first, false, true); });
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.run_first, false, true); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
         stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, w_deferred) : launch_intra(pb, ws); });
         // bf16: W is built inside intra for the event chunks, or after it from C-bar (w_deferred)
@@ -307,7 +307,7 @@ gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask, gdn_ev
     pb.mask = mask;
     pb.stream = (cudaStream_t)stream;
     // the snapshot numbering needs no capacity of its own: it never exceeds E
-    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity, nullptr, nullptr, true, false);
+    const cudaError_t e = launch_select(pb, *events, (int64_t)events->capacity, nullptr, true, false);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

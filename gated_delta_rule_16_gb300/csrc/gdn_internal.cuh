@@ -115,13 +115,12 @@ struct Workspace {
 size_t workspace_layout(const Problem &pb, void *base, Workspace *ws);
 
 // ---- launchers (each returns cudaGetLastError()) --------------------------
-// ev_of (may be NULL): [R, C] event index of each (physical row, chunk), -1 when not selected.
 // run_first (may be NULL): [R, NR+1] per CSR row, index of the first event of each run of
-// kRunChunks chunks (entry NR: the row's end).  Both need kRunChunks = 16 (two runs per mask word).
+// kRunChunks chunks (entry NR: the row's end); needs kRunChunks = 16 (two runs per mask word).
 // wait_first: the mask comes from the kernel before (else the kernel waits for it only before
 // exiting); or_status: OR the status bits into counts[2] instead of overwriting it.
-cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of,
-                          int32_t *run_first, bool wait_first, bool or_status);
+cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *run_first,
+                          bool wait_first, bool or_status);
 cudaError_t launch_prefix(const Problem &pb, const Workspace &ws);
 cudaError_t launch_intra(const Problem &pb, const Workspace &ws);
 cudaError_t launch_wbuild(const Problem &pb, const Workspace &ws);

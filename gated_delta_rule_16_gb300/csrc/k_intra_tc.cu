@@ -16,10 +16,9 @@
 //   W = C diag(beta 2^g) K for the chunks that are events (Eq. 15): A = C-bar bf16,
 //       block-diagonal, K-major, built in the V tile once the U product has read it;
 //       B = the K tile read as MN-major (token rows, d columns: the same bytes as the
-//       K-major Gram operand).  W is written at the event's index, so it is never
-//       built for skipped chunks, and negated: the scan accumulates -S^T W^T onto U^T.
-//       W of (row i = b P + p, chunk c) lives at slot i C + c, so this kernel needs only
-//       the caller's mask and runs before the compaction.
+//       K-major Gram operand).  W is built only for event chunks and stored negated
+//       (the scan accumulates -S^T W^T onto U^T).  W of (row i = b P + p, chunk c) lives
+//       at slot i C + c, so this kernel needs only the caller's mask, not the compaction.
 // Shared memory over the CTA's life:
 //   [0, 32K)     K tile (Gram, then the W product)
 //   [32K, 64K)   V tile -> C-bar operand -> W staging

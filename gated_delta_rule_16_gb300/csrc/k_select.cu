@@ -85,7 +85,7 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
               int32_t *__restrict__ row_pair, int32_t *__restrict__ row_ptr,
               int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
               int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
-              int32_t *__restrict__ ev_of, int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
+              int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
               int64_t snap_cap, int wait_first, int or_status) {
     extern __shared__ int sm[];
     const int NW = (C + 31) >> 5;   // 32-chunk mask words per row
@@ -134,8 +134,8 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     // 3. row offsets
     block_exclusive_scan(sorted_cnt, ptr, R, warp_tot);
     const int64_t E = ptr[R];
-    // 4. per row (one warp): stage the mask bits, write event chunks, the chunk -> event
-    //    map, each group's predecessor, and count the events some group references
+    // 4. per row (one warp): stage the mask bits, write event chunks, run starts, each
+    //    group's predecessor, and count the events some group references
     //    (event at chunk c, next event of the row at cn or none: referenced iff the
     //    smallest even chunk index m > c satisfies m <= cn and m <= 2(G-1)).
     for (int j = warp; j < R; j += kWarps) {
@@ -150,7 +150,6 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
             const int before = __popc(bits & ((1u << lane) - 1u));
             const int e = base + run + before;
             if (s && (int64_t)e < ev_cap) ev_chunk[e] = c;
-            if (ev_of && c < C) ev_of[(int64_t)i * C + c] = s ? e : -1;
             if (run_first && lane < 2) {  // runs of 16 chunks starting inside this word
                 const int rr = 2 * w + lane;
                 if (rr < NR) run_first[(int64_t)j * (NR + 1) + rr] = base + run + (lane ? __popc(bits & 0xFFFFu) : 0);
@@ -249,7 +248,7 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
                     int32_t *__restrict__ row_pair, int32_t *__restrict__ row_ptr,
                     int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
                     int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
-                    int32_t *__restrict__ ev_of, int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
+                    int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
                     int64_t snap_cap, int wait_first, int or_status) {
     extern __shared__ int sm[];
     const int NW = (C + 31) >> 5;
@@ -327,8 +326,8 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     }
     __syncthreads();
     block_exclusive_scan(evb, evb, NF, warp_tot);
-    // 5. one warp per (sorted row j, word w): event chunks, the chunk -> event map, run
-    //    starts, group predecessors, and which events some group references (event at
+    // 5. one warp per (sorted row j, word w): event chunks, run starts, group
+    //    predecessors, and which events some group references (event at
     //    chunk c, next event of the row at cn or none: referenced iff the smallest even
     //    chunk index m > c satisfies m <= cn and m <= 2(G-1))
     for (int f = warp; f < NF; f += kWarps) {
@@ -340,7 +339,6 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
         const bool s = (bits >> lane) & 1u;
         const int e = e0 + __popc(bits & below);
         if (s && (int64_t)e < ev_cap) ev_chunk[e] = c;
-        if (ev_of && c < C) ev_of[(int64_t)i * C + c] = s ? e : -1;
         if (run_first && lane < 2) {  // runs of 16 chunks starting inside this word
             const int rr = 2 * w + lane;
             if (rr < NR) run_first[(int64_t)j * (NR + 1) + rr] = e0 + (lane ? __popc(bits & 0xFFFFu) : 0);
@@ -398,8 +396,8 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
 
 }  // namespace
 
-cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *ev_of,
-                          int32_t *run_first, bool wait_first, bool or_status) {
+cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *run_first,
+                          bool wait_first, bool or_status) {
     const int NW = (pb.C + 31) / 32, NR = (pb.C + kRunChunks - 1) / kRunChunks;
     const size_t fast = words_smem_bytes(pb.R, pb.R * NW);
     const bool use_words = fast <= kWordsSmemLimit;
@@ -410,7 +408,7 @@ cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_
         if (e != cudaSuccess) return e;
     }
     return launch_kernel(pb.pdl, kernel, 1, kThreads, smem, pb.stream, pb.mask, pb.R, pb.C, pb.G, ev.row_pair,
-                         ev.row_ptr, ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts, ev_of, run_first, NR,
+                         ev.row_ptr, ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts, run_first, NR,
                          (int64_t)ev.capacity, snap_cap, (int)wait_first, (int)or_status);
 }
 
