@@ -10,8 +10,9 @@
 //   1. scan_run_kernel, "map" mode, all runs in parallel: the run's events
 //      applied to the identity with U = 0 give A_r (homogeneous part), applied
 //      to 0 with the true U give B_r (inhomogeneous part);
-//   2. scan_chain_kernel, per (row, head): S_{r+1} = A_r S_r + B_r, one
-//      128x128x128 MMA per run; writes every run's entry state and S_final;
+//   2. scan_chain_kernel, per (row, head) and block of 32 state rows:
+//      S_{r+1} = A_r S_r + B_r, one 128x128x128 MMA per run; writes every
+//      run's entry state and S_final;
 //   3. scan_run_kernel, "fix-up" mode, all runs in parallel: the run's events
 //      from the true entry state, writing U' = U - W S in place of U and the
 //      post-event snapshots that output groups read.
@@ -36,8 +37,8 @@
 // once MMA1 is done, K once MMA2 is done, so every load has most of an event to
 // land (the fix-up's U tile once its U' store has read it).  The fix-up writes U'
 // into the U tile and stores it over U by TMA.  Snapshots are stored in bf16 as
-// S^T [dv][d] (each thread's 32 state entries are 64 contiguous bytes), the
-// K-major operand of the output kernel's Q S product.
+// S^T [dv][d] (each thread's 32 state entries are 64 contiguous bytes, written as
+// two whole 32-byte sectors), the K-major operand of the output kernel's Q S product.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
