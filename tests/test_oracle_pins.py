@@ -88,6 +88,20 @@ def test_sparse_odd_chunk_count_random_masks():
         assert rel_fro(r["o"], ref["o"]) < 1e-10
 
 
+@pytest.mark.parametrize("scale", [20.0, 100.0])
+def test_strong_decay_sparse_equals_token_rule(scale):
+    # the stress gates of the GPU parity test (about -33 and -163 log2 decay per chunk): the oracle's
+    # chunkwise form still equals the token recurrence, so it can serve as the reference there
+    x = inputs(320, seed=9, Nq=2, mask="bernoulli", with_h0=True)
+    g = (np.asarray(x.g, np.float64) * scale).astype(np.float32)
+    rng = np.random.default_rng(2)
+    m = (rng.random((1, 2, 5)) < 0.5).astype(np.uint8)
+    r = oracle.prefill(x.q, x.k, x.v, x.beta, g, mask=m, h0=x.h0, solver=oracle.SOLVER_EXACT)
+    ref = brute_prefill(x.q, x.k, x.v, x.beta, g, mask=m, h0=x.h0)
+    assert rel_fro(r["o"], ref["o"]) < 1e-10
+    assert rel_fro(r["s_final"], ref["s_final"]) < 1e-10
+
+
 def test_all_ones_mask_is_dense_path():
     x = inputs(320, seed=8)
     for solver in (oracle.SOLVER_EXACT, oracle.SOLVER_BLOCK_ADJ):
