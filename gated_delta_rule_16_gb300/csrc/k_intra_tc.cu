@@ -94,18 +94,16 @@ __device__ __forceinline__ int cbar_index(int ib, int jb) {
     return ib == jb ? ib : (jb + 1 == ib ? 3 + ib : (ib == 2 ? 7 : (jb == 1 ? 8 : 9)));
 }
 
-// Below-diagonal blocks at distance OFF of both chunks' C (Eq. 7 generalised), once every
-// block closer to the diagonal is known: T = sum_{k=jb}^{ib-1} M_{ib,k} C_{k,jb} is written
-// into C's block (or, when no later level reads M, over M's own block, which saves a
-// barrier), then C_{ib,jb} = -C_{ib,ib} T.  Task (chunk, block, row, column quad): 4
-// outputs from 16-byte shared-memory loads.
-template <int OFF, bool T_OVER_M>
+// Exact solver: below-diagonal blocks at distance OFF of both chunks' C (Eq. 7 generalised),
+// once every block closer to the diagonal is known: T = sum_{k=jb}^{ib-1} M_{ib,k} C_{k,jb}
+// is written into C's block, then replaced by C_{ib,jb} = -C_{ib,ib} T.  Task (chunk, block,
+// row, column quad): 4 outputs from 16-byte shared-memory loads.
+template <int OFF>
 __device__ __forceinline__ void offdiag_level(float *F, int tid) {
     constexpr int NB = 4 - OFF;
     constexpr int NT = 2 * NB * 64;
     constexpr int NU = (NT + kThreads - 1) / kThreads;
     float4 acc[NU];
-    float4 tv[NU];
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
         const int task = tid + u * kThreads;
@@ -126,20 +124,7 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
                     fma4(t, m.w, ld4(Cc + (k4 + 3) * BS));
                 }
             }
-            if (T_OVER_M) tv[u] = t;
-            else *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) = t;
-        }
-    }
-    if (T_OVER_M) {  // a row of M's block is read only by the four lanes of its row's tasks (one warp)
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int task = tid + u * kThreads;
-            if (task < NT) {
-                const int cc = task / (NB * 64), rem = task % (NB * 64);
-                const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
-                *reinterpret_cast<float4 *>(blk_m(F, cc, ib, jb) + rr * BS + q4) = tv[u];
-            }
+            *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) = t;
         }
     }
     __syncthreads();
@@ -151,7 +136,7 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
             const int cc = task / (NB * 64), rem = task % (NB * 64);
             const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
             const float *Cr = blk_diag(F, cc, ib) + rr * BS;
-            const float *Tt = (T_OVER_M ? blk_m(F, cc, ib, jb) : blk_c(F, cc, ib, jb)) + q4;
+            const float *Tt = blk_c(F, cc, ib, jb) + q4;
 #pragma unroll
             for (int m4 = 0; m4 < kBlk; m4 += 4) {
                 const float4 c = ld4(Cr + m4);
@@ -162,7 +147,7 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
             }
         }
     }
-    if (!T_OVER_M) __syncthreads();  // T was in C's block: every reader is done before C replaces it
+    __syncthreads();  // T is in C's block: every reader is done before C replaces it
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
         const int task = tid + u * kThreads;
@@ -174,6 +159,48 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
         }
     }
     __syncthreads();
+}
+
+// Block-adjacent solver's below-diagonal blocks, one warp per block (warps 0..5: chunk w / 3,
+// block column jb = w % 3, row ib = jb + 1): T = M_{ib,jb} C_{jb,jb}, then C_{ib,jb} = -C_{ib,ib} T.
+// Lane (row rr = lane / 2, columns 8 (lane % 2) .. +7); T goes over M's block (each row of it is read
+// only by the two lanes of that row), so the warp needs no block-wide barrier between the products.
+// The sums run over k in the same order as offdiag_level's.
+__device__ __forceinline__ void offdiag_adjacent_warp(float *F, int warp, int lane) {
+    if (warp >= 6) return;
+    const int cc = warp / 3, jb = warp % 3, ib = jb + 1;
+    const int rr = lane >> 1, c8 = (lane & 1) * 8;
+    float *Mb = blk_m(F, cc, ib, jb);
+    const float *Cj = blk_diag(F, cc, jb), *Ci = blk_diag(F, cc, ib);
+    float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0;
+#pragma unroll
+    for (int k4 = 0; k4 < kBlk; k4 += 4) {
+        const float4 m = ld4(Mb + rr * BS + k4);
+        const float mv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            fma4(t0, mv[q], ld4(Cj + (k4 + q) * BS + c8));
+            fma4(t1, mv[q], ld4(Cj + (k4 + q) * BS + c8 + 4));
+        }
+    }
+    __syncwarp();  // every lane has read its M row
+    *reinterpret_cast<float4 *>(Mb + rr * BS + c8) = t0;
+    *reinterpret_cast<float4 *>(Mb + rr * BS + c8 + 4) = t1;
+    __syncwarp();  // T complete
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+    for (int m4 = 0; m4 < kBlk; m4 += 4) {
+        const float4 c = ld4(Ci + rr * BS + m4);
+        const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            fma4(a0, cv[q], ld4(Mb + (m4 + q) * BS + c8));
+            fma4(a1, cv[q], ld4(Mb + (m4 + q) * BS + c8 + 4));
+        }
+    }
+    float *Cb = blk_c(F, cc, ib, jb) + rr * BS + c8;
+    *reinterpret_cast<float4 *>(Cb) = make_float4(-a0.x, -a0.y, -a0.z, -a0.w);
+    *reinterpret_cast<float4 *>(Cb + 4) = make_float4(-a1.x, -a1.y, -a1.z, -a1.w);
 }
 
 // One row's 32 operand columns (this thread's half of its chunk) as bf16 into the
@@ -328,12 +355,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         for (int i2 = 0; i2 < kBlk; ++i2) Mb[i2 * BS + j] = x[i2];
     }
     __syncthreads();
-    if (exact) {  // the far levels read M's distance-1 blocks: T goes to C's block
-        offdiag_level<1, false>(F, tid);
-        offdiag_level<2, false>(F, tid);
-        offdiag_level<3, false>(F, tid);
+    if (exact) {
+        offdiag_level<1>(F, tid);
+        offdiag_level<2>(F, tid);
+        offdiag_level<3>(F, tid);
     } else {
-        offdiag_level<1, true>(F, tid);
+        offdiag_adjacent_warp(F, warp, lane);
+        __syncthreads();
     }
     const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;
     // 3. this thread's 32 coefficients of C (blocks the solver does not keep are zero)
