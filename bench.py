@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum) on the current version of the kernel and workload; an entry must be
 # removed whenever its kernel changes (the roofline's traffic is then reported as null).
 PROFILED_TRAFFIC = {
-    ("qwen35_4b_layer_T32768_sparse29", "intra"): 739.13e6,
-    ("qwen35_4b_layer_T32768_sparse29", "output"): 921.62e6,
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 739.37e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 921.59e6,
 }
 
 
