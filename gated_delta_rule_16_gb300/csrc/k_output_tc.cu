@@ -160,7 +160,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     const uint32_t id_km = idesc_bf16(128, 128, false, true);
     const float inv_sqrt_d = rsqrtf((float)kDim);
     const int kind = has_s;
-    bool s_wait_ok = true;  // thread 0
+    bool s_wait_ok = true, u_issued = false;  // thread 0
     if (tid == 0) {  // QK (QS follows the A values: its state may still be landing)
         if (!mbar_wait(&bar_qk_ld, 0)) {
             abort_s = 1;
@@ -218,6 +218,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         mbar_arrive_expect_tx(&bar_u_ld, 2 * kSlab);
         tma_load_4d(sm + OFF_K, &tU, 0, h, t0, b, &bar_u_ld);
         tma_load_4d(sm + OFF_K + kSlab, &tU, 64, h, t0, b, &bar_u_ld);
+        u_issued = true;
         if (kind != 0) {
             if (kind == 1 && !mbar_wait(&bar_s, 0)) {
                 s_wait_ok = false;
@@ -291,6 +292,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         // let every copy and MMA issued so far land before the CTA releases its memory
         mbar_wait(&bar_qk_ld, 0);
         if (kind == 1 && s_wait_ok) mbar_wait(&bar_s, 0);
+        if (u_issued) mbar_wait(&bar_u_ld, 0);
         mma_commit(&bar_drain);
         mbar_wait(&bar_drain, 0);
     }
