@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     Workspace,
     gdn_decode_step,
     gdn_events_status,
+    gdn_noalloc_status,
     gdn_prefill_dense,
     gdn_prefill_ex,
     gdn_prefill_host,

@@ -25,7 +25,8 @@ EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn
            "gdn_prefill_sparse", "gdn_workspace_status", "gdn_status_string", "gdn_version",
            "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout",
            "gdn_prefill_sparse_online", "gdn_select_events_scored", "gdn_select_scored_workspace_bytes",
-           "gdn_prefill_host", "gdn_prefill_host_workspace_bytes", "gdn_decode_step", "gdn_prefill_ex")
+           "gdn_prefill_host", "gdn_prefill_host_workspace_bytes", "gdn_decode_step", "gdn_prefill_ex",
+           "gdn_workspace_bytes_ex", "gdn_events_bytes", "gdn_events_carve", "gdn_noalloc_status")
 STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output", "selector")
 
 
@@ -41,7 +42,8 @@ class GdnShape(ctypes.Structure):
 
 
 class GdnOptions(ctypes.Structure):
-    _fields_ = [("tail_window", ctypes.c_int32), ("w_deferred", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6)]
+    _fields_ = [("tail_window", ctypes.c_int32), ("w_deferred", ctypes.c_int32), ("scan_runs", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 5)]
 
 
 MODES = {"dense": 0, "sparse": 1, "online": 2}
@@ -71,6 +73,12 @@ def load(path: str | None = None):
             evp = ctypes.POINTER(GdnEvents)
             lib.gdn_workspace_bytes.argtypes = [shp, i32, i32]
             lib.gdn_workspace_bytes.restype = sz
+            lib.gdn_workspace_bytes_ex.argtypes = [shp, i32, i32, ctypes.POINTER(GdnOptions)]
+            lib.gdn_workspace_bytes_ex.restype = sz
+            lib.gdn_events_bytes.argtypes = [shp, ctypes.c_int32]
+            lib.gdn_events_bytes.restype = sz
+            lib.gdn_events_carve.argtypes = [shp, ctypes.c_int32, vp, evp]
+            lib.gdn_events_carve.restype = i32
             lib.gdn_select_events.argtypes = [shp, vp, evp, vp]
             lib.gdn_select_events.restype = i32
             lib.gdn_events_status.argtypes = [evp, vp]
@@ -97,6 +105,8 @@ def load(path: str | None = None):
             lib.gdn_prefill_host_workspace_bytes.restype = sz
             lib.gdn_prefill_sparse_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
             lib.gdn_prefill_sparse_noalloc.restype = i32
+            lib.gdn_noalloc_status.argtypes = [vp]
+            lib.gdn_noalloc_status.restype = i32
             lib.gdn_selftest_wait_timeout.argtypes = [vp, i32, vp]
             lib.gdn_selftest_wait_timeout.restype = i32
             lib.gdn_workspace_status.argtypes = [vp, vp]
@@ -379,7 +389,8 @@ def gdn_prefill_host(q, k, v, beta, g, mask=None, *, h0=None, solver="block_adj"
 
 
 def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=None, solver="block_adj",
-                   tail_window=0, w_deferred=False, o=None, s_final=None, score=None, mask_out=None,
+                   tail_window=0, w_deferred=False, scan_runs=False, o=None, s_final=None, score=None,
+                   mask_out=None,
                    tier_out=None, workspace=None, stream=None):
     """The general prefill with execution variants; returns (o, s_final, mask_out, tier_out)."""
     B, T, Nq, d = q.shape
@@ -405,8 +416,11 @@ def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=N
             tier_out = torch.empty((B, Nq), dtype=torch.int32, device=dev)
     _need(score, "score", torch.float32, (B, Nv, C))
     shape = shape_of(q, v)
-    opt = GdnOptions(int(tail_window), int(bool(w_deferred)))
-    ws = _workspace(workspace, gdn_workspace_bytes(shape, solver, MODES[mode]), dev)
+    opt = GdnOptions(int(tail_window), int(bool(w_deferred)), int(bool(scan_runs)))
+    nbytes = int(load().gdn_workspace_bytes_ex(ctypes.byref(shape), SOLVERS[solver], MODES[mode], ctypes.byref(opt)))
+    if nbytes == 0:
+        raise GdnError("gdn_workspace_bytes_ex", 2, "invalid shape or options")
+    ws = _workspace(workspace, nbytes, dev)
     with torch.cuda.device(dev):
         _check("gdn_prefill_ex", load().gdn_prefill_ex(
             ctypes.byref(shape), MODES[mode], _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(mask),
@@ -437,22 +451,28 @@ def gdn_decode_step(q, k, v, beta, a, state, *, o=None, stream=None):
 
 
 def gdn_select_events(mask: torch.Tensor, Nq: int | None = None, capacity: int | None = None, stream=None):
-    """Mask [B,P,C] uint8 -> CSR event lists on the device (dict of int32 tensors)."""
+    """Mask [B,P,C] uint8 -> CSR event lists on the device (dict of int32 tensors, views of one
+    buffer sized by gdn_events_bytes and laid out by gdn_events_carve)."""
     _need(mask, "mask", torch.uint8)
     B, P, C = mask.shape
     G = (C + 1) // 2
     cap = B * P * C if capacity is None else int(capacity)
     dev = mask.device
-    out = {"row_pair": torch.empty(max(B * P, 1), dtype=torch.int32, device=dev),
-           "row_ptr": torch.empty(B * P + 1, dtype=torch.int32, device=dev),
-           "ev_chunk": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
-           "grp_pred": torch.empty(max(B * P * G, 1), dtype=torch.int32, device=dev),
-           "snap_slot": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
-           "counts": torch.zeros(4, dtype=torch.int32, device=dev)}
-    ev = GdnEvents(*(out[n].data_ptr() for n in ("row_pair", "row_ptr", "ev_chunk", "grp_pred", "snap_slot",
-                                                  "counts")), cap)
     shape = GdnShape(B, C * 64, P, 2 * P, 128, 128, GDN_BF16)
     lib = load()
+    nbytes = int(lib.gdn_events_bytes(ctypes.byref(shape), cap))
+    if nbytes == 0:
+        raise GdnError("gdn_events_bytes", 2, "invalid shape or capacity")
+    buf = torch.zeros(nbytes + 256, dtype=torch.uint8, device=dev)
+    base = buf.data_ptr()
+    pad = (-base) % 256
+    ev = GdnEvents()
+    _check("gdn_events_carve", lib.gdn_events_carve(ctypes.byref(shape), cap, ctypes.c_void_p(base + pad),
+                                                    ctypes.byref(ev)))
+    view = lambda ptr, n: buf[ptr - base:ptr - base + 4 * n].view(torch.int32)
+    out = {"row_pair": view(ev.row_pair, B * P), "row_ptr": view(ev.row_ptr, B * P + 1),
+           "ev_chunk": view(ev.ev_chunk, cap), "grp_pred": view(ev.grp_pred, B * P * G),
+           "snap_slot": view(ev.snap_slot, cap), "counts": view(ev.counts, 4), "_buf": buf}
     with torch.cuda.device(dev):
         _check("gdn_select_events", lib.gdn_select_events(ctypes.byref(shape), _ptr(mask), ctypes.byref(ev),
                                                           _stream(stream)))
@@ -462,6 +482,12 @@ def gdn_select_events(mask: torch.Tensor, Nq: int | None = None, capacity: int |
 
 def gdn_events_status(events: dict, stream=None) -> int:
     return int(load().gdn_events_status(ctypes.byref(events["_struct"]), _stream(stream)))
+
+
+def gdn_noalloc_status(device="cuda:0", stream=None) -> int:
+    """Status of the last allocation-free prefill on `device` (synchronises the stream)."""
+    with torch.cuda.device(torch.device(device)):
+        return int(load().gdn_noalloc_status(_stream(stream)))
 
 
 def gdn_workspace_status(workspace, stream=None) -> int:

@@ -80,6 +80,13 @@ void fill_problem(const gdn_shape *s, gdn_solver solver, Problem *pb) {
 
 size_t elem_size(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
 
+// Which optional workspace buffers a prefill of this mode and these options uses.
+void set_buffers(Problem *pb, bool online, const gdn_options *opt) {
+    pb->online = online;
+    pb->need_cbar = pb->dtype == GDN_F32 || online || (opt && opt->w_deferred);
+    pb->need_runs = pb->dtype == GDN_BF16 && opt && opt->scan_runs;
+}
+
 }  // namespace
 
 size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
@@ -99,13 +106,13 @@ size_t workspace_layout(const Problem &pb, void *base, Workspace *ws) {
     const size_t o_P = take((size_t)pb.B * pb.Nv * (C + 1) * sizeof(double));
     const size_t o_grp_info = take((size_t)R * G * 16);
     const size_t o_U = take((size_t)pb.B * pb.T * pb.Nv * pb.dv * es);
-    const size_t o_cbar = take((size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float));
+    const size_t o_cbar = take(pb.need_cbar ? (size_t)pb.B * pb.Nv * C * pb.nblk * 256 * sizeof(float) : 0);
     const size_t o_W = take((size_t)ev_cap * 2 * kChunk * pb.d * es);
     const size_t o_snap = take((size_t)snap_cap * 2 * pb.d * pb.dv * es);
     const size_t o_sel_ws = take(pb.online ? selector_workspace_bytes(pb.B, (int)C) : 0);
     const size_t o_sel_score = take(pb.online ? (size_t)pb.B * pb.Nv * C * sizeof(float) : 0);
     const size_t o_sel_mask = take(pb.online ? (size_t)R * C : 0);
-    const int64_t nr = pb.dtype == GDN_BF16 ? (C + kRunChunks - 1) / kRunChunks : 0;
+    const int64_t nr = pb.dtype == GDN_BF16 && pb.need_runs ? (C + kRunChunks - 1) / kRunChunks : 0;
     const size_t run_elems = (size_t)R * 2 * nr * kDim * kDim;
     const size_t o_amap = take(run_elems * 2);
     const size_t o_bmap = take(run_elems * sizeof(float));
@@ -146,7 +153,8 @@ gdn_status check_options(const gdn_options *opt) {
     const int tw = opt->tail_window;
     if (tw != 0 && tw != 8 && tw != 16 && tw != 32 && tw != 64) return GDN_ERR_UNSUPPORTED;
     if (opt->w_deferred != 0 && opt->w_deferred != 1) return GDN_ERR_UNSUPPORTED;
-    for (int i = 0; i < 6; ++i)
+    if (opt->scan_runs != 0 && opt->scan_runs != 1) return GDN_ERR_UNSUPPORTED;
+    for (int i = 0; i < 5; ++i)
         if (opt->reserved[i] != 0) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
@@ -171,7 +179,7 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     if (workspace && ((uintptr_t)workspace % kAlign) != 0) return GDN_ERR_ALIGN;
     Problem pb;
     fill_problem(shape, solver, &pb);
-    pb.online = mode == kOnline;
+    set_buffers(&pb, mode == kOnline, opt);
     if (opt && opt->tail_window) pb.tail = opt->tail_window;
     const bool w_deferred = opt && opt->w_deferred;
     if (shape->B == 0) return GDN_OK;
@@ -221,14 +229,14 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
         // intra first (its Tail-16 scores drive the selection), then the rest of the pipeline
         stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
         stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
-        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.run_first, true, true); });
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, pb.need_runs ? ws.run_first : nullptr, true, true); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
         stage(3, 1, [&] { return tc ? launch_wbuild_tc(pb, ws) : launch_wbuild(pb, ws); });
     } else {
         // intra needs only the caller's mask (W goes to slot row * C + chunk), so it does not wait
         // for the compaction and the prefix: their few CTAs run beside intra's first waves, and
         // intra waits for them only before it exits
-        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, ws.run_first, false, true); });
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, pb.need_runs ? ws.run_first : nullptr, false, true); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
         stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, w_deferred) : launch_intra(pb, ws); });
         // bf16: W is built inside intra for the event chunks, or after it from C-bar (w_deferred)
@@ -236,9 +244,13 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
               [&] { return !tc ? launch_wbuild(pb, ws) : (w_deferred ? launch_wbuild_tc(pb, ws) : none()); });
         stage(8, 0, none);
     }
-    stage(4, tc ? 1 : 0, [&] { return tc ? launch_scan_tc(pb, ws, 0) : none(); });
-    stage(5, tc ? 1 : 0, [&] { return tc ? launch_scan_tc(pb, ws, 1) : none(); });
-    stage(6, 1, [&] { return tc ? launch_scan_tc(pb, ws, 2) : launch_scan(pb, ws); });
+    // bf16 storage: one pass over each CSR row, or run maps + chain + fix-up (scan_runs)
+    const bool runs = pb.need_runs != 0;
+    stage(4, runs ? 1 : 0, [&] { return runs ? launch_scan_tc(pb, ws, 0) : none(); });
+    stage(5, runs ? 1 : 0, [&] { return runs ? launch_scan_tc(pb, ws, 1) : none(); });
+    stage(6, 1, [&] {
+        return !tc ? launch_scan(pb, ws) : (runs ? launch_scan_tc(pb, ws, 2) : launch_scan_warp(pb, ws));
+    });
     stage(7, 1, [&] { return tc ? launch_output_tc(pb, ws) : launch_output(pb, ws); });
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -281,12 +293,56 @@ extern "C" {
 size_t gdn_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse) {
     // dense and sparse share one layout (the dense path is the all-events case);
     // sparse == 2 (online selection) adds the selector's buffers
-    if (check_shape(shape) != GDN_OK) return 0;
+    return gdn_workspace_bytes_ex(shape, solver, sparse == 2 ? GDN_MODE_ONLINE : (gdn_mode)(sparse != 0), nullptr);
+}
+
+size_t gdn_workspace_bytes_ex(const gdn_shape *shape, gdn_solver solver, gdn_mode mode, const gdn_options *opt) {
+    if (check_shape(shape) != GDN_OK || check_options(opt) != GDN_OK) return 0;
     if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return 0;
+    if (mode != GDN_MODE_DENSE && mode != GDN_MODE_SPARSE && mode != GDN_MODE_ONLINE) return 0;
     Problem pb;
     fill_problem(shape, solver, &pb);
-    pb.online = sparse == 2;
+    set_buffers(&pb, mode == GDN_MODE_ONLINE, opt);
     return workspace_layout(pb, nullptr, nullptr);
+}
+
+namespace {
+struct EventsLayout {
+    size_t row_pair, row_ptr, ev_chunk, grp_pred, snap_slot, counts, total;
+};
+EventsLayout events_layout(const gdn_shape *s, int32_t capacity) {
+    const int64_t R = (int64_t)s->B * s->Nq, C = ((int64_t)s->T + kChunk - 1) / kChunk, G = (C + 1) / 2;
+    EventsLayout l;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+    l.row_pair = take(R * 4); l.row_ptr = take((R + 1) * 4); l.ev_chunk = take((size_t)capacity * 4);
+    l.grp_pred = take(R * G * 4); l.snap_slot = take((size_t)capacity * 4); l.counts = take(4 * 4);
+    l.total = off;
+    return l;
+}
+}  // namespace
+
+size_t gdn_events_bytes(const gdn_shape *shape, int32_t capacity) {
+    if (check_shape(shape) != GDN_OK || capacity < 0) return 0;
+    return events_layout(shape, capacity).total;
+}
+
+gdn_status gdn_events_carve(const gdn_shape *shape, int32_t capacity, void *buffer, gdn_events *events) {
+    gdn_status st = check_shape(shape);
+    if (st != GDN_OK) return st;
+    if (!buffer || !events) return GDN_ERR_NULL;
+    if (capacity < 0) return GDN_ERR_SHAPE;
+    if (((uintptr_t)buffer % kAlign) != 0) return GDN_ERR_ALIGN;
+    const EventsLayout l = events_layout(shape, capacity);
+    char *b = (char *)buffer;
+    events->row_pair = (int32_t *)(b + l.row_pair);
+    events->row_ptr = (int32_t *)(b + l.row_ptr);
+    events->ev_chunk = (int32_t *)(b + l.ev_chunk);
+    events->grp_pred = (int32_t *)(b + l.grp_pred);
+    events->snap_slot = (int32_t *)(b + l.snap_slot);
+    events->counts = (int32_t *)(b + l.counts);
+    events->capacity = capacity;
+    return GDN_OK;
 }
 
 gdn_status gdn_select_events(const gdn_shape *shape, const uint8_t *mask, gdn_events *events, void *stream) {
@@ -457,7 +513,7 @@ const char *gdn_status_string(gdn_status status) {
         case GDN_ERR_DTYPE: return "unknown dtype or solver";
         case GDN_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
         case GDN_ERR_WORKSPACE: return "workspace smaller than gdn_workspace_bytes()";
-        case GDN_ERR_UNSUPPORTED: return "request not implemented by this build (needs d == dv == 128, T % 64 == 0)";
+        case GDN_ERR_UNSUPPORTED: return "request not implemented by this build (needs d == dv == 128, ceil(T/64) <= 16384)";
         case GDN_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
         case GDN_ERR_DEVICE: return "current device is not a compute-capability 10.3 (GB300) GPU";
         case GDN_ERR_CAPACITY: return "device-side event or snapshot capacity exceeded";

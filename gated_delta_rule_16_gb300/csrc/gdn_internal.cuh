@@ -79,6 +79,8 @@ struct Problem {
     gdn_solver solver;
     int nblk;                  // 7 (block-adjacent) or 10 (exact)
     int online;                // workspace also holds the online-selection buffers
+    int need_cbar;             // workspace holds the compact C-bar blocks (fp32 storage, online, W deferred)
+    int need_runs;             // workspace holds the run maps of the run-map scan (bf16, scan_runs)
     int tail;                  // rows of the Tail-W score window (16 by default)
     int pdl;                   // launch the stage's first kernel as a programmatic dependent of the previous one
     int pdl_ok;                // programmatic dependent launch allowed in this prefill (later kernels of a stage)
@@ -129,6 +131,9 @@ cudaError_t launch_output(const Problem &pb, const Workspace &ws);
 // part 0: run maps, 1: chain over runs, 2: per-run fix-up (writes U' and snapshots)
 cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part);
 cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws);
+// The whole event scan in one launch: one warp per 16 state columns walks its CSR row
+// once (writes U', the snapshots and S_final; bf16 storage only).
+cudaError_t launch_scan_warp(const Problem &pb, const Workspace &ws);
 // write_cbar: store the compact C-bar blocks (W is built later, after online selection)
 cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_cbar);
 // online selection: mask [B,16,C] (and tiers [B,16], may be NULL) from scores [B,Nv,C]

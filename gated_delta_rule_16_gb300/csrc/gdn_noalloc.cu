@@ -6,8 +6,6 @@
 // gdn_prefill_sparse_noalloc() serves them: it runs the same kernels as
 // gdn_prefill_sparse(), with the workspace carved from one fixed array in the
 // library's own device memory instead of a caller buffer.
-#include <mutex>
-
 #include "gdn_internal.cuh"
 
 namespace {
@@ -15,24 +13,17 @@ namespace {
 // The scratch: every GPU that loads the library holds these bytes until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch per device ordinal.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device with cudaGetSymbolAddress (with that device current).
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mutex;
-
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress (with the device current) on every call: the lookup is a
+// host-side table read, allocates nothing, and stays right if the context is
+// reset or another context of the device is current (the module is then loaded
+// again, at a new address).  The first lookup in a context loads the module and
+// with it the array.
 gdn_status scratch_for_current_device(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_DEVICE;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+    *out = p;
     return GDN_OK;
 }
 
@@ -53,8 +44,16 @@ extern "C" gdn_status gdn_prefill_sparse_noalloc(const gdn_shape *shape, const v
     const gdn_status st = scratch_for_current_device(&scratch);
     if (st != GDN_OK) return st;
     // Nothing in the scratch needs to start at zero: every value the pipeline
-    // reads (CSR lists, counters, prefix, U, C-bar, W, snapshots) is written
-    // earlier in the same call, so the previous call's contents are harmless.
+    // reads (CSR lists, counters, prefix, U, W, snapshots) is written earlier in
+    // the same call, so the previous call's contents are harmless.
     return gdn_prefill_sparse(shape, q, k, v, beta, g, h0, mask, solver, o, s_final, score, scratch,
                               (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" gdn_status gdn_noalloc_status(void *stream) {
+    void *scratch = nullptr;
+    const gdn_status st = scratch_for_current_device(&scratch);
+    if (st != GDN_OK) return st;
+    // the status word sits where a caller workspace keeps it: the counters at offset 0
+    return gdn_workspace_status(scratch, stream);
 }

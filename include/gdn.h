@@ -14,9 +14,10 @@
  * ---------------------------------------
  * Shapes.  B sequences of T tokens; Nq query/key heads of width d; Nv = 2*Nq
  * value heads of width dv.  Value heads 2p and 2p+1 form head pair p and read
- * query/key head p.  C = T/64 chunks, G = ceil(C/2) output groups, P = Nq
- * pairs.  This version requires d == dv == 128 and T % 64 == 0 (T == 0 and
- * B == 0 are accepted).
+ * query/key head p.  C = ceil(T/64) chunks (a partial last chunk holds the
+ * remaining T - 64 (C-1) tokens), G = ceil(C/2) output groups, P = Nq pairs.
+ * This version requires d == dv == 128 and C <= 16384 (T == 0 and B == 0 are
+ * accepted).
  *
  * Layouts (row-major, contiguous, innermost last):
  *   q, k      [B, T, Nq, d]      dtype (bf16 or fp32)
@@ -122,17 +123,49 @@ typedef enum { GDN_MODE_DENSE = 0, GDN_MODE_SPARSE = 1, GDN_MODE_ONLINE = 2 } gd
  *                for the events after compaction (the order online selection
  *                needs).  The results are identical bit for bit (bf16 storage;
  *                fp32 storage always builds W separately).
+ *   scan_runs    bf16 storage only.  0: the event scan walks each CSR row once,
+ *                the state held on chip for the whole row (every event applied
+ *                once);  1: the row is cut into runs of 16 chunks whose affine
+ *                maps are built in parallel, chained, then replayed (three
+ *                launches; every event applied three times, on tcgen05 tensor
+ *                cores).  Both compute the same recurrence (Eqs. 1-2, 17-21);
+ *                their fp32 rounding orders differ, so the results agree to
+ *                rounding, not bit for bit.  scan_runs = 1 needs the larger
+ *                workspace that gdn_workspace_bytes_ex() reports for it.
  *   reserved     must be zero. */
 typedef struct {
     int32_t tail_window;
     int32_t w_deferred;
-    int32_t reserved[6];
+    int32_t scan_runs;
+    int32_t reserved[5];
 } gdn_options;
 
 /* Bytes of workspace the prefill entry points need for `shape`: sparse = 0
- * gdn_prefill_dense, 1 gdn_prefill_sparse, 2 gdn_prefill_sparse_online.
- * 0 for invalid shapes. */
+ * gdn_prefill_dense, 1 gdn_prefill_sparse, 2 gdn_prefill_sparse_online (all
+ * with default execution variants).  0 for invalid shapes. */
 GDN_API size_t gdn_workspace_bytes(const gdn_shape *shape, gdn_solver solver, int sparse);
+
+/* Bytes of workspace gdn_prefill_ex needs for `mode` and the options `opt`
+ * (NULL = defaults; equal to gdn_workspace_bytes for the same mode).  Some
+ * variants keep extra buffers: w_deferred the compact C-bar blocks, scan_runs
+ * the per-run affine maps.  0 for invalid shapes or options. */
+GDN_API size_t gdn_workspace_bytes_ex(const gdn_shape *shape, gdn_solver solver, gdn_mode mode,
+                                      const gdn_options *opt);
+
+/* Bytes of one device buffer that holds the arrays of a gdn_events for `shape`
+ * with room for `capacity` events: row_pair, row_ptr, ev_chunk, grp_pred,
+ * snap_slot and counts, in that order, each at a 256-byte aligned offset.
+ * 0 for an invalid shape or a negative capacity.  A capacity of B*P*C always
+ * suffices (every chunk of every pair an event); the pages' selector bounds E
+ * by 16 k_H per sequence (Sec. 2.5). */
+GDN_API size_t gdn_events_bytes(const gdn_shape *shape, int32_t capacity);
+
+/* Points the arrays of *events into `buffer` (device memory of at least
+ * gdn_events_bytes(shape, capacity) bytes, 256-byte aligned) in the layout
+ * gdn_events_bytes() describes, and sets events->capacity.  Host-only: nothing
+ * is enqueued and the buffer is not touched.  Returns GDN_ERR_NULL, _SHAPE or
+ * _ALIGN on bad arguments. */
+GDN_API gdn_status gdn_events_carve(const gdn_shape *shape, int32_t capacity, void *buffer, gdn_events *events);
 
 /* Event compaction (Sec. 2.5, Eq. 16): turn the [B,P,C] 0/1 mask into CSR
  * event lists, the per-group predecessor event and the snapshot numbering.
@@ -202,7 +235,7 @@ GDN_API gdn_status gdn_prefill_sparse_online(const gdn_shape *shape,
  * required) or online selection (eta, mask_out and tier_out as in
  * gdn_prefill_sparse_online, 16 head pairs); `opt` (NULL = defaults) selects
  * execution variants.  Arguments otherwise as gdn_prefill_sparse; workspace
- * gdn_workspace_bytes(shape, solver, mode).  Unknown option values return
+ * gdn_workspace_bytes_ex(shape, solver, mode, opt).  Unknown option values return
  * GDN_ERR_UNSUPPORTED before anything is enqueued. */
 GDN_API gdn_status gdn_prefill_ex(const gdn_shape *shape, gdn_mode mode,
                           const void *q, const void *k, const void *v,
@@ -257,23 +290,36 @@ GDN_API size_t gdn_prefill_host_workspace_bytes(const gdn_shape *shape, gdn_solv
  * exits.  The call allocates nothing and calls no allocating routine.
  *   - Size limit: shapes with gdn_workspace_bytes(shape, solver, 1) above
  *     64 MiB are rejected with GDN_ERR_WORKSPACE before anything is enqueued
- *     (with this version's workspace layout: B=1, Nq=16, bf16,
- *     block-adjacent up to T = 1984; one head pair in fp32 up to T = 20352).
- *   - Set-up: the first call on each device looks up the array's device
- *     address (cudaGetSymbolAddress, with that device current).  Make that
- *     first call before any stream capture.
+ *     (with this version's workspace layout: B=1, Nq=16, bf16 up to
+ *     T = 2688; one head pair in fp32 up to T = 20352).
+ *   - Set-up: the array belongs to the library's device code, which CUDA loads
+ *     lazily: the first call in each context (this entry point or
+ *     gdn_noalloc_status) loads it, claiming the 64 MiB then, and looks up its
+ *     address with that device current.  Make that first call at start-up,
+ *     before a host runtime reserves the rest of the device memory and before
+ *     any stream capture.  Every call looks the address up again (no cache), so
+ *     a reset context or another context of the same device is handled.
  *   - Sharing: every call uses the same array and it keeps the last call's
  *     contents.  Nothing in it must start at zero (each value read is written
  *     earlier in the same call), but calls that overlap on the GPU (other
  *     streams, other host threads) race on it: serialise them.
- *   - The device status word lives in that array: read it with
- *     gdn_workspace_status() only on a workspace you own, not here. */
+ *   - Failure detection: the device status word lives in that array; read it
+ *     with gdn_noalloc_status(), which reports the last call on the current
+ *     device. */
 #define GDN_NOALLOC_SCRATCH_BYTES (64ull << 20)
 GDN_API gdn_status gdn_prefill_sparse_noalloc(const gdn_shape *shape,
                                       const void *q, const void *k, const void *v,
                                       const float *beta, const float *g, const float *h0,
                                       const uint8_t *mask, gdn_solver solver,
                                       void *o, float *s_final, float *score, void *stream);
+
+/* Synchronises `stream` and reports the device-latched status (GDN_OK,
+ * GDN_ERR_CAPACITY or GDN_ERR_TIMEOUT) of the last gdn_prefill_sparse_noalloc()
+ * call on the current device, read from the library's scratch array.  Also
+ * loads that array when called first (see the set-up note above).  Allocates
+ * nothing.  No counterpart in the paper: part of the allocation-free entry
+ * point. */
+GDN_API gdn_status gdn_noalloc_status(void *stream);
 
 /* Self-test of failure detection: every wait inside the kernels is bounded in
  * time.  Launches one thread that waits on a barrier nothing arrives at, with

@@ -64,12 +64,33 @@ def max_rel_err(got, want, kind):
     return worst_rel, worst_abs
 
 
+def max_rel_err_chunks(got, want):
+    """O arrays [B,T,Nv,dv]: the largest relative Frobenius error over (sequence, value head,
+    64-token chunk), each chunk's error against that chunk's own reference norm (so an error
+    confined to one chunk is not diluted by the rest of the sequence).  Chunks whose reference
+    is exactly zero are measured by the absolute norm.  Returns (max rel, max abs where zero)."""
+    B, T, Nv, dv = want.shape
+    C = (T + 63) // 64
+    pad = C * 64 - T
+    g = np.pad(got, ((0, 0), (0, pad), (0, 0), (0, 0))).reshape(B, C, 64, Nv, dv)
+    w = np.pad(want, ((0, 0), (0, pad), (0, 0), (0, 0))).reshape(B, C, 64, Nv, dv)
+    num = np.sqrt(((g - w) ** 2).sum(axis=(2, 4)))
+    den = np.sqrt((w ** 2).sum(axis=(2, 4)))
+    zero = den == 0.0
+    rel = np.where(zero, 0.0, num / np.where(zero, 1.0, den))
+    return float(rel.max()), float(np.where(zero, num, 0.0).max())
+
+
 def assert_close(res, ref, dtype, what=""):
     tol = TOL[dtype]
     for key, kind in (("o", "o"), ("s_final", "s")):
         rel, ab = max_rel_err(res[key], ref[key], kind)
         assert rel <= tol, f"{what} {key}: max relative Frobenius error {rel:.3e} > {tol}"
         assert ab <= ABS_ZERO, f"{what} {key}: absolute error {ab:.3e} where the reference is zero"
+    # the same bound per 64-token chunk of O
+    rel, ab = max_rel_err_chunks(res["o"], ref["o"])
+    assert rel <= tol, f"{what} o: max relative Frobenius error of one chunk {rel:.3e} > {tol}"
+    assert ab <= ABS_ZERO, f"{what} o: absolute error {ab:.3e} in a chunk where the reference is zero"
 
 
 def slice_pairs(x, b, pairs):

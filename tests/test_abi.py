@@ -48,7 +48,9 @@ def test_workspace_bytes(lib):
     s = shape()
     n_ex = gdn.gdn_workspace_bytes(s, "exact")
     n_ba = gdn.gdn_workspace_bytes(s, "block_adj")
-    assert n_ex > n_ba > 0
+    assert n_ex == n_ba > 0   # bf16 defaults keep no solver blocks (W is built inside the intra step)
+    s32 = shape(dtype=bnd.GDN_F32)  # fp32 storage keeps C-bar: 10 blocks (exact) vs 7 per chunk and head
+    assert gdn.gdn_workspace_bytes(s32, "exact") - gdn.gdn_workspace_bytes(s32, "block_adj") == 4096 * 32 // 64 * 3 * 256 * 4
     # U alone is B*T*Nv*dv*2 bytes for bf16; the workspace holds at least that
     assert n_ba > 1 * 4096 * 32 * 128 * 2
     assert gdn.gdn_workspace_bytes(shape(d=64, dv=64)) == 0
@@ -193,3 +195,39 @@ def test_prefill_ex_option_validation(lib):
     assert ex(mode=7) == 6
     assert ex(mask=0) == 1                                 # sparse mode needs a mask
     assert ex(opt=bnd.GdnOptions(64, 1)) == 8              # valid: stops at the device check here
+
+
+def test_workspace_bytes_ex_matches_and_orders_variants(lib):
+    s = shape(T=32768)
+    opt = lambda **kw: bnd.GdnOptions(kw.get("tw", 0), kw.get("wd", 0), kw.get("runs", 0))
+    wsx = lambda mode, o=None: int(lib.gdn_workspace_bytes_ex(ctypes.byref(s), 1, mode,
+                                                               None if o is None else ctypes.byref(o)))
+    base = gdn.gdn_workspace_bytes(s, "block_adj", 1)
+    assert wsx(1) == base == wsx(1, opt()) == wsx(0)       # defaults: dense and sparse share one layout
+    assert wsx(2) == gdn.gdn_workspace_bytes(s, "block_adj", 2) > base
+    # the compact C-bar blocks (bf16: 7 blocks of 16x16 per chunk and head, fp32 slots)
+    assert wsx(1, opt(wd=1)) - base >= 32 * 512 * 7 * 256 * 4
+    # the run maps: A (bf16), B and the entry states (fp32), 128 x 128 per run, head and pair
+    assert wsx(1, opt(runs=1)) - base >= 16 * 2 * 32 * 128 * 128 * 10
+    assert wsx(1, opt(runs=2)) == 0 and wsx(1, opt(tw=5)) == 0 and wsx(3) == 0
+    # fp32 storage always keeps C-bar (its W is built after the intra step)
+    s32 = shape(T=1024, dtype=bnd.GDN_F32)
+    assert int(lib.gdn_workspace_bytes_ex(ctypes.byref(s32), 1, 1, None)) == gdn.gdn_workspace_bytes(s32)
+
+
+def test_events_bytes_and_carve(lib):
+    s = shape(B=2, T=1000, Nq=3, Nv=6)            # R = 6 rows, C = 16 chunks, G = 8 groups
+    up = lambda n: (n + 255) // 256 * 256
+    want = up(6 * 4) + up(7 * 4) + up(50 * 4) + up(6 * 8 * 4) + up(50 * 4) + up(16)
+    assert int(lib.gdn_events_bytes(ctypes.byref(s), 50)) == want
+    assert int(lib.gdn_events_bytes(ctypes.byref(s), -1)) == 0
+    assert int(lib.gdn_events_bytes(ctypes.byref(shape(Nv=31)), 8)) == 0
+    ev = bnd.GdnEvents()
+    base = 1 << 20                                # never dereferenced: carving only computes addresses
+    assert lib.gdn_events_carve(ctypes.byref(s), 50, ctypes.c_void_p(base), ctypes.byref(ev)) == 0
+    offs = [p - base for p in (ev.row_pair, ev.row_ptr, ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts)]
+    assert offs == [0, 256, 512, 768, 1024, 1280] and ev.capacity == 50
+    assert offs[-1] + 16 <= want
+    assert lib.gdn_events_carve(ctypes.byref(s), 50, ctypes.c_void_p(base + 16), ctypes.byref(ev)) == 4  # ALIGN
+    assert lib.gdn_events_carve(ctypes.byref(s), 50, None, ctypes.byref(ev)) == 1                        # NULL
+    assert lib.gdn_events_carve(ctypes.byref(s), -3, ctypes.c_void_p(base), ctypes.byref(ev)) == 2       # SHAPE

@@ -64,6 +64,20 @@ def test_selector_bit_exact(B, C, kind, with_eta):
     assert np.array_equal(mask, ref["mask"]), f"{np.count_nonzero(mask != ref['mask'])} mask bytes differ"
 
 
+@pytest.mark.parametrize("name", ["window", "sum_from_one", "closed_form"])
+def test_selector_memory_lifetime_cases(name):
+    # inputs whose tier split is decided by Eq. 11's memory lifetime (r_h over the last 16 chunks,
+    # L_h summed from j = 1): the GPU's tiers and mask equal the expected split and the oracle's
+    from selector_cases import CASES
+    score, gamma, tiers = CASES[name]()
+    C = score.shape[-1]
+    g = np.ascontiguousarray(np.repeat(np.moveaxis(gamma, 1, 2), 64, axis=1))  # [1, 64 C, 32]: g = gamma per chunk
+    mask, tier = gpu_select(score, g)
+    ref = oracle.select(score, chunk_gamma(g, C))
+    assert tier[0].tolist() == tiers.tolist()
+    assert np.array_equal(tier, ref["tier"]) and np.array_equal(mask, ref["mask"])
+
+
 def test_selector_all_zero_scores_and_eta():
     score = np.zeros((2, 32, 40), np.float32)
     g = gdn_synth.make_gates(2, 64 * 40, 32, 5)

@@ -2,7 +2,9 @@
 
 Element-by-element comparisons on seeded inputs at sizes the oracle finishes
 in seconds (several chunks, groups, pairs, sequences, and an odd chunk count),
-plus the full-size sparse layer (T = 32768) checked on sampled head pairs.
+plus the full-size sparse layer (T = 32768) and two layers of the 128K-token
+prefill on every head pair, and the eight-sequence batch on sampled pairs.
+Errors are bounded per (sequence, value head) and per 64-token chunk of O.
 CSR event lists are compared bit for bit.
 """
 import itertools
@@ -167,26 +169,41 @@ def test_dense_layer_T4096(solver):
     assert_close(res, oracle_run(x, solver, sparse=False), "bf16", f"T=4096 dense {solver}")
 
 
-def test_sparse_layer_T32768_sampled_pairs():
+def test_sparse_layer_T32768_all_pairs():
+    # the benchmark's layer, every head pair (all 32 value heads) against the oracle
     x = gdn_synth.make_workload("qwen35_4b_layer_T32768_sparse29")
     res = run_gpu(x, solver="block_adj")
+    assert_close(res, oracle_run(x, "block_adj"), "bf16", "T=32768 all pairs")
+
+
+@pytest.mark.parametrize("scan_runs", [False, True])
+def test_sparse_layer_T32768_scan_variants_sampled(scan_runs):
+    # both event-scan schedules (one pass per row / run maps + chain + fix-up) on the longest and
+    # the shortest row
+    x = gdn_synth.make_workload("qwen35_4b_layer_T32768_sparse29")
+    t = to_dev(x)
+    o, s, _, _ = gdn.gdn_prefill_ex(t["q"], t["k"], t["v"], t["beta"], t["g"], mode="sparse", mask=t["mask"],
+                                    solver="block_adj", scan_runs=scan_runs)
+    torch.cuda.synchronize()
     counts = x.mask[0].sum(-1)
-    pairs = [int(np.argmax(counts)), int(np.argmin(counts)), 7]
-    for p in pairs:
+    for p in (int(np.argmax(counts)), int(np.argmin(counts))):
         y = slice_pairs(x, 0, [p])
-        ref = oracle_run(y, "block_adj")
-        got = {"o": res["o"][:, :, 2 * p:2 * p + 2], "s_final": res["s_final"][:, 2 * p:2 * p + 2]}
-        assert_close(got, ref, "bf16", f"T=32768 pair {p} ({counts[p]} events)")
+        got = {"o": o[:, :, 2 * p:2 * p + 2].float().cpu().numpy().astype(np.float64),
+               "s_final": s[:, 2 * p:2 * p + 2].cpu().numpy().astype(np.float64)}
+        assert_close(got, oracle_run(y, "block_adj"), "bf16", f"scan_runs={scan_runs} pair {p}")
 
 
 def test_batch8_T32768_sampled_pairs():
+    # eight sequences with their own masks; two head pairs of every sequence
     x = gdn_synth.make_workload("qwen35_4b_layer_B8_T32768_sparse29")
     res = run_gpu(x, solver="block_adj")
-    for b, p in ((0, 3), (5, 11), (7, 0)):
-        y = slice_pairs(x, b, [p])
+    for b in range(8):
+        pairs = [(3 * b) % 16, (3 * b + 8) % 16]
+        y = slice_pairs(x, b, pairs)
         ref = oracle_run(y, "block_adj")
-        got = {"o": res["o"][b:b + 1, :, 2 * p:2 * p + 2], "s_final": res["s_final"][b:b + 1, 2 * p:2 * p + 2]}
-        assert_close(got, ref, "bf16", f"B=8 seq {b} pair {p}")
+        vi = [2 * p + j for p in pairs for j in (0, 1)]
+        got = {"o": res["o"][b:b + 1][:, :, vi], "s_final": res["s_final"][b:b + 1][:, vi]}
+        assert_close(got, ref, "bf16", f"B=8 seq {b} pairs {pairs}")
 
 
 def test_workspace_status_ok_after_prefill():
@@ -206,15 +223,40 @@ def test_bounded_wait_times_out_and_context_survives():
 
 
 @pytest.mark.parametrize("layer", [0, 23])
-def test_long_context_T131072_layer_sampled_pair(layer):
-    # one layer of the 24-layer, 128K-token prefill; its final state (and output) on a sampled pair
+def test_long_context_T131072_layer_all_pairs(layer):
+    # one layer of the 24-layer, 128K-token prefill: output and final state of every head pair
     x = gdn_synth.make_workload("qwen35_4b_24layers_T131072_sparse29", layer=layer)
     res = run_gpu(x, solver="block_adj")
-    p = (5 * layer + 2) % x.Nq
-    y = slice_pairs(x, 0, [p])
-    ref = oracle_run(y, "block_adj")
-    got = {"o": res["o"][:, :, 2 * p:2 * p + 2], "s_final": res["s_final"][:, 2 * p:2 * p + 2]}
-    assert_close(got, ref, "bf16", f"T=131072 layer {layer} pair {p}")
+    assert_close(res, oracle_run(x, "block_adj"), "bf16", f"T=131072 layer {layer}")
+
+
+@pytest.mark.parametrize("sparse", [True, False])
+@pytest.mark.parametrize("T1", [128, 1024 + 128])
+def test_chunked_prefill_resume(sparse, T1):
+    # prefill(T1) then prefill(rest, h0 = its S_final) equals prefill(T1 + rest): T1 a multiple of
+    # 128, so both halves keep the two-chunk groups of the whole (the pages return S_C for later use)
+    x = gdn_synth.make_inputs(2, 2048 + 37, 4, 8, dtype="bf16", seed=30 + T1, mask="beta", with_h0=True)
+    whole = run_gpu(x, solver="block_adj", sparse=sparse)
+    ref = oracle_run(x, "block_adj", sparse)
+    assert_close(whole, ref, "bf16", "whole")
+    C1 = T1 // 64
+    first, second = slice_tokens(x, 0, T1), slice_tokens(x, T1, x.T)
+    first.mask, second.mask = x.mask[:, :, :C1], x.mask[:, :, C1:]
+    r1 = run_gpu(first, solver="block_adj", sparse=sparse)
+    r2 = run_gpu(second, solver="block_adj", sparse=sparse, h0=r1["s_final"].astype(np.float32))
+    joined = {"o": np.concatenate([r1["o"], r2["o"]], axis=1), "s_final": r2["s_final"]}
+    assert_close(joined, ref, "bf16", f"resumed at T1={T1}")
+    assert_close(joined, whole, "bf16", f"resumed vs whole at T1={T1}")
+
+
+def slice_tokens(x, t0, t1):
+    """Inputs restricted to tokens [t0, t1) of every sequence (h0 kept)."""
+    import copy
+    y = copy.copy(x)
+    y.q, y.k, y.v = x.q[:, t0:t1], x.k[:, t0:t1], x.v[:, t0:t1]
+    y.beta, y.g = x.beta[:, t0:t1], x.g[:, t0:t1]
+    y.T = t1 - t0
+    return y
 
 
 @pytest.mark.parametrize("dtype,sparse", [("bf16", True), ("bf16", False), ("f32", True)])

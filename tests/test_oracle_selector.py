@@ -92,3 +92,15 @@ def test_zero_visibility_pair_is_never_high_tier():
     r0 = oracle.select(s, g, eta)
     assert r0["tier"][0][0] != 2
     assert np.array_equal(oracle.select(s, g)["mask"], oracle.select(s, g, np.ones((1, NV), np.float32))["mask"])
+
+
+# ---- Eq. 11: the memory lifetime r_h, L_h decides these splits (inputs in selector_cases.py) ----
+
+@pytest.mark.parametrize("name", ["window", "sum_from_one", "closed_form"])
+def test_memory_lifetime_decides_the_tiers(name):
+    from selector_cases import CASES
+    s, g, tiers = CASES[name]()
+    r = oracle.select(s, g)
+    assert r["tier"][0].tolist() == tiers.tolist()
+    k = r["k"]
+    assert r["mask"][0].sum(-1).tolist() == [k[t] for t in tiers]  # every pair keeps its tier's budget
