@@ -508,8 +508,9 @@ def gdn_version() -> int:
     return int(load().gdn_version())
 
 
-def gdn_profile_enable(enable: bool = True) -> None:
-    """Record per-stage CUDA events in the following prefills (see include/gdn.h)."""
+def gdn_profile_enable(enable=True) -> None:
+    """True / 1: record per-stage CUDA events in the following prefills (one-stream schedule);
+    2: only count the kernels they launch (their normal schedule); False / 0: off (include/gdn.h)."""
     _check("gdn_profile_enable", load().gdn_profile_enable(int(enable)))
 
 

@@ -3,6 +3,7 @@
 // prefill pipeline.  No allocation, no synchronisation (except the status
 // queries), no host copy of the event count.
 #include <cstring>
+#include <mutex>
 
 #include "gdn_internal.cuh"
 
@@ -21,16 +22,18 @@ inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 constexpr int kStages = 9;
 constexpr int kProfSlots = 256;
 struct Profiler {
-    bool on = false, created = false;
-    int used = 0;
-    int64_t launches = 0;                      // kernels launched by the recorded prefills
+    int mode = 0;                              // 0 off, 1 stage events (one stream), 2 count kernels only
+    bool created = false;
+    int used = 0;                              // prefills with stage events recorded
+    int64_t calls = 0;                         // prefills run while enabled
+    int64_t launches = 0;                      // kernels those prefills launched
     cudaEvent_t ev[kProfSlots][2 * kStages];  // start and end of every stage
 };
 Profiler g_prof;
 
-// Returns the event row of this prefill, or nullptr when not profiling.
+// Returns the event row of this prefill, or nullptr when not recording stage events.
 cudaEvent_t *prof_slot() {
-    if (!g_prof.on || g_prof.used >= kProfSlots) return nullptr;
+    if (g_prof.mode != 1 || g_prof.used >= kProfSlots) return nullptr;
     return g_prof.ev[g_prof.used++];
 }
 
@@ -148,6 +151,53 @@ namespace {
 
 enum PrefillMode { kDense = 0, kSparse = 1, kOnline = 2 };
 
+// ---- row classes on concurrent streams ----------------------------------------
+// CSR rows are sorted by event count, longest first, so the scan's critical path is
+// the first rows.  The bf16 prefill splits the rows into classes by CSR index (no
+// event count leaves the device): class c = rows [bound_c, bound_c+1) with bounds
+// 0, R/8, R/4, R/2, R.  Each class runs its intra step (given mask), scan and output
+// on its own stream, the longest class first and at the highest priority, so its
+// scan starts once its own intra step is done while the shorter classes' intra steps,
+// scans and outputs fill the GPU around it.  Streams and events are made once per
+// device; a mutex keeps one prefill's fork / join sequence together on the host.
+constexpr int kClasses = 4;
+struct ClassStreams {
+    bool tried = false, ok = false;
+    cudaStream_t s[kClasses - 1];  // classes 0 .. 2 (the last class runs on the caller's stream)
+    cudaEvent_t fork, join[kClasses - 1];
+};
+ClassStreams g_class_streams[64];
+std::mutex g_class_mutex;
+
+ClassStreams *class_streams() {  // under g_class_mutex; nullptr if they cannot be made
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    ClassStreams &cs = g_class_streams[dev];
+    if (!cs.tried) {
+        cs.tried = true;
+        int least = 0, greatest = 0;
+        cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        bool ok = cudaEventCreateWithFlags(&cs.fork, cudaEventDisableTiming) == cudaSuccess;
+        for (int c = 0; ok && c < kClasses - 1; ++c) {
+            const int prio = greatest + c < least ? greatest + c : least;  // class 0 first
+            ok = cudaStreamCreateWithPriority(&cs.s[c], cudaStreamNonBlocking, prio) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&cs.join[c], cudaEventDisableTiming) == cudaSuccess;
+        }
+        cs.ok = ok;
+    }
+    return cs.ok ? &cs : nullptr;
+}
+
+// Class bounds for R rows: returns the number of non-empty classes.
+int class_bounds(int R, int *bound) {
+    const int cand[kClasses + 1] = {0, (R + 7) / 8, (R + 3) / 4, (R + 1) / 2, R};
+    int n = 0;
+    bound[0] = 0;
+    for (int c = 1; c <= kClasses; ++c)
+        if (cand[c] > bound[n]) bound[++n] = cand[c];
+    return n;
+}
+
 gdn_status check_options(const gdn_options *opt) {
     if (!opt) return GDN_OK;
     const int tw = opt->tail_window;
@@ -163,7 +213,7 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
                        const float *g, const float *h0, const uint8_t *mask, const float *eta, PrefillMode mode,
                        gdn_solver solver, void *o, float *s_final, float *score, uint8_t *mask_out,
                        int32_t *tier_out, void *workspace, size_t workspace_bytes, void *stream,
-                       const gdn_options *opt = nullptr) {
+                       const gdn_options *opt = nullptr, bool single_stream = false) {
     gdn_status st = check_shape(shape);
     if (st != GDN_OK) return st;
     if ((st = check_options(opt)) != GDN_OK) return st;
@@ -214,17 +264,71 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     pb.pdl_ok = tc && !prof;
     bool launched = false;
     // kernels: how many kernels the stage's launcher issues (0 for an empty stage)
+    const bool counting = g_prof.mode != 0;
+    if (counting) ++g_prof.calls;
     auto stage = [&](int id, int kernels, auto &&launch) {
         mark(2 * id);
         pb.pdl = pb.pdl_ok && launched;
         if (e == cudaSuccess) e = launch();
         mark(2 * id + 1);
         if (kernels > 0) launched = true;
-        if (prof) g_prof.launches += kernels;
+        if (counting) g_prof.launches += kernels;
     };
     auto none = [] { return cudaSuccess; };
     // the status word collects every kernel's bits (timeouts, capacity overflows) for this prefill
     if (cudaMemsetAsync(ws.counts + 2, 0, sizeof(int32_t), pb.stream) != cudaSuccess) return GDN_ERR_CUDA;
+    const bool runs = pb.need_runs != 0;
+    // row classes on concurrent streams (bf16 one-pass scan; not while profiling, whose stage
+    // events need one stream, nor for a caller that asked for a single stream)
+    std::unique_lock<std::mutex> class_lock(g_class_mutex, std::defer_lock);
+    ClassStreams *cs = nullptr;
+    if (tc && !runs && !prof && !single_stream && pb.R > 1) {
+        class_lock.lock();
+        cs = class_streams();
+        if (!cs) class_lock.unlock();
+    }
+    if (cs) {
+        // the compaction and the prefix first (the classes need the CSR rows), then per class
+        // [intra (given mask) ->] scan -> output
+        const bool intra_split = mode != kOnline && !w_deferred;
+        if (mode == kOnline) {
+            stage(2, 1, [&] { return launch_intra_tc(pb, ws, true); });
+            stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
+            stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, true, true); });
+            stage(1, 1, [&] { return launch_prefix(pb, ws); });
+            stage(3, 1, [&] { return launch_wbuild_tc(pb, ws); });
+        } else {
+            stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, false, true); });
+            stage(1, 1, [&] { return launch_prefix(pb, ws); });
+            if (!intra_split) {
+                stage(2, 1, [&] { return launch_intra_tc(pb, ws, true); });
+                stage(3, 1, [&] { return launch_wbuild_tc(pb, ws); });
+            }
+        }
+        int bound[kClasses + 1];
+        const int ncls = class_bounds(pb.R, bound);
+        if (e == cudaSuccess) e = cudaEventRecord(cs->fork, pb.stream);
+        for (int c = 0; c < ncls && e == cudaSuccess; ++c) {
+            Problem q = pb;
+            q.row_pair = ws.row_pair;
+            q.row0 = bound[c];
+            q.nrows = bound[c + 1] - bound[c];
+            const bool last = c == ncls - 1;
+            q.stream = last ? pb.stream : cs->s[c];
+            if (!last) e = cudaStreamWaitEvent(q.stream, cs->fork, 0);
+            // No programmatic dependent launch inside a class: a dependent's CTAs would sit on SMs
+            // waiting for their predecessor (the output for the whole scan), which the other
+            // classes' kernels need.  (The first kernel of a class also reads the CSR rows.)
+            q.pdl = 0;
+            if (e == cudaSuccess && intra_split) e = launch_intra_tc(q, ws, false);
+            if (e == cudaSuccess) e = launch_scan_warp(q, ws);
+            if (e == cudaSuccess) e = launch_output_tc(q, ws);
+            if (counting) g_prof.launches += intra_split ? 3 : 2;
+            if (e == cudaSuccess && !last) e = cudaEventRecord(cs->join[c], q.stream);
+        }
+        for (int c = 0; c + 1 < ncls && e == cudaSuccess; ++c) e = cudaStreamWaitEvent(pb.stream, cs->join[c], 0);
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
     if (mode == kOnline) {
         // intra first (its Tail-16 scores drive the selection), then the rest of the pipeline
         stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
@@ -245,7 +349,6 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
         stage(8, 0, none);
     }
     // bf16 storage: one pass over each CSR row, or run maps + chain + fix-up (scan_runs)
-    const bool runs = pb.need_runs != 0;
     stage(4, runs ? 1 : 0, [&] { return runs ? launch_scan_tc(pb, ws, 0) : none(); });
     stage(5, runs ? 1 : 0, [&] { return runs ? launch_scan_tc(pb, ws, 1) : none(); });
     stage(6, 1, [&] {
@@ -284,6 +387,17 @@ HostStaging host_staging(const gdn_shape *sh) {
 }
 
 }  // namespace
+
+// gdn_prefill_sparse on the caller's stream alone (no library-owned streams or events, which the
+// allocation-free entry point must not create); same kernels, same results.
+gdn_status prefill_sparse_single_stream(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                                        const float *beta, const float *g, const float *h0, const uint8_t *mask,
+                                        gdn_solver solver, void *o, float *s_final, float *score, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+    return run_prefill(shape, q, k, v, beta, g, h0, mask, nullptr, kSparse, solver, o, s_final, score, nullptr,
+                       nullptr, workspace, workspace_bytes, stream, nullptr, true);
+}
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -525,15 +639,17 @@ const char *gdn_status_string(gdn_status status) {
 int32_t gdn_version(void) { return 100; }
 
 gdn_status gdn_profile_enable(int enable) {
-    if (enable && !g_prof.created) {
+    if (enable < 0 || enable > 2) return GDN_ERR_UNSUPPORTED;
+    if (enable == 1 && !g_prof.created) {
         if (!device_ok()) return GDN_ERR_DEVICE;
         for (int i = 0; i < kProfSlots; ++i)
             for (int j = 0; j < 2 * kStages; ++j)
                 if (cudaEventCreate(&g_prof.ev[i][j]) != cudaSuccess) return GDN_ERR_CUDA;
         g_prof.created = true;
     }
-    g_prof.on = enable != 0;
+    g_prof.mode = enable;
     g_prof.used = 0;
+    g_prof.calls = 0;
     g_prof.launches = 0;
     return GDN_OK;
 }
@@ -543,8 +659,9 @@ gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefil
     if (n_launches) *n_launches = g_prof.launches;
     if (n_stages < 0 || n_stages > kStages) return GDN_ERR_SHAPE;
     for (int j = 0; j < n_stages; ++j) stage_ms[j] = 0.f;
-    *n_prefills = g_prof.created ? g_prof.used : 0;
-    for (int i = 0; i < *n_prefills; ++i) {
+    const int recorded = g_prof.created ? g_prof.used : 0;
+    *n_prefills = g_prof.mode == 2 ? (int32_t)g_prof.calls : recorded;
+    for (int i = 0; i < recorded; ++i) {
         for (int j = 0; j < n_stages; ++j) {
             float ms = 0.f;
             if (cudaEventSynchronize(g_prof.ev[i][2 * j + 1]) != cudaSuccess) return GDN_ERR_CUDA;
@@ -554,6 +671,7 @@ gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefil
         }
     }
     g_prof.used = 0;
+    g_prof.calls = 0;
     g_prof.launches = 0;
     return GDN_OK;
 }

@@ -84,6 +84,11 @@ struct Problem {
     int tail;                  // rows of the Tail-W score window (16 by default)
     int pdl;                   // launch the stage's first kernel as a programmatic dependent of the previous one
     int pdl_ok;                // programmatic dependent launch allowed in this prefill (later kernels of a stage)
+    // Row range: when nrows > 0 the intra, scan and output launchers cover only the pairs of CSR
+    // rows [row0, row0 + nrows) (physical pair row_pair[j]; the compaction must have completed);
+    // nrows == 0: every pair, gridded by (pair, sequence).
+    const int32_t *row_pair;
+    int row0, nrows;
     const void *q, *k, *v;
     const float *beta, *g, *h0;
     const uint8_t *mask;       // NULL: every chunk is an event
@@ -115,6 +120,12 @@ struct Workspace {
 };
 
 size_t workspace_layout(const Problem &pb, void *base, Workspace *ws);
+
+// gdn_prefill_sparse with every kernel on the caller's stream (no library-owned streams).
+gdn_status prefill_sparse_single_stream(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                                        const float *beta, const float *g, const float *h0, const uint8_t *mask,
+                                        gdn_solver solver, void *o, float *s_final, float *score, void *workspace,
+                                        size_t workspace_bytes, void *stream);
 
 // ---- launchers (each returns cudaGetLastError()) --------------------------
 // run_first (may be NULL): [R, NR+1] per CSR row, index of the first event of each run of

@@ -46,8 +46,9 @@ extern "C" gdn_status gdn_prefill_sparse_noalloc(const gdn_shape *shape, const v
     // Nothing in the scratch needs to start at zero: every value the pipeline
     // reads (CSR lists, counters, prefix, U, W, snapshots) is written earlier in
     // the same call, so the previous call's contents are harmless.
-    return gdn_prefill_sparse(shape, q, k, v, beta, g, h0, mask, solver, o, s_final, score, scratch,
-                              (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);
+    // one stream: the library-owned streams of the multi-stream schedule are not made here
+    return gdn::prefill_sparse_single_stream(shape, q, k, v, beta, g, h0, mask, solver, o, s_final, score, scratch,
+                                             (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 extern "C" gdn_status gdn_noalloc_status(void *stream) {

@@ -62,6 +62,8 @@ struct IntraParams {
     __nv_bfloat16 *cbar;    // non-NULL: write the compact C-bar blocks [B,Nv,C,nblk,16,16] (bf16)
     float *score;
     int32_t *status;
+    const int32_t *row_pair;  // non-NULL: blockIdx.y is CSR row row0 + y (pair row_pair[row0 + y])
+    int row0;
     int P_, T_, Nv, C, nblk, exact, tail;
 };
 
@@ -237,7 +239,9 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; which 64 of 128 columns
     const int row = quarter * 32 + lane;             // token inside the group
     const int ct = row >> 6, tl = row & 63, ib = tl >> 4, rr = tl & 15;
-    const int hh = blockIdx.x & 1, r = blockIdx.x >> 1, p = blockIdx.y, b = blockIdx.z;
+    const int hh = blockIdx.x & 1, r = blockIdx.x >> 1;
+    const int pr = a.row_pair ? a.row_pair[a.row0 + blockIdx.y] : 0;
+    const int p = a.row_pair ? pr % a.P_ : (int)blockIdx.y, b = a.row_pair ? pr / a.P_ : (int)blockIdx.z;
     const int h = 2 * p + hh;
     const int c0 = 2 * r;
     const int nch = c0 + 1 < a.C ? 2 : 1;
@@ -528,9 +532,11 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.nblk = pb.nblk;
     a.exact = pb.solver == GDN_SOLVER_EXACT;
     a.tail = pb.tail;
+    a.row_pair = pb.nrows > 0 ? pb.row_pair : nullptr;
+    a.row0 = pb.row0;
     cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraTcSmem);
-    return launch_kernel(pb.pdl, intra_tc_kernel, dim3(2 * pb.G, pb.P, pb.B), kThreads, kIntraTcSmem, pb.stream,
-                         tK, tV, tU, tW, a);
+    const dim3 grid = pb.nrows > 0 ? dim3(2 * pb.G, pb.nrows, 1) : dim3(2 * pb.G, pb.P, pb.B);
+    return launch_kernel(pb.pdl, intra_tc_kernel, grid, kThreads, kIntraTcSmem, pb.stream, tK, tV, tU, tW, a);
 }
 
 }  // namespace gdn

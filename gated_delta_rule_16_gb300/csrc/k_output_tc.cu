@@ -42,6 +42,8 @@ struct OutParams {
     const int4 *grp_info;   // per group: {snapshot slot, kind, decay head 0, decay head 1}
     __nv_bfloat16 *O;
     int32_t *status;
+    const int32_t *row_pair;  // non-NULL: blockIdx.y is CSR row row0 + y (pair row_pair[row0 + y])
+    int row0;
     int P_, T_, Nv, C, G;
 };
 
@@ -73,7 +75,10 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; which 64 of 128 columns
     const int row = quarter * 32 + lane;             // query token inside the group
-    const int hh = blockIdx.x & 1, r = blockIdx.x >> 1, p = blockIdx.y, b = blockIdx.z;
+    const int hh = blockIdx.x & 1, r = blockIdx.x >> 1;
+    // (row_pair is complete before this kernel's stream forked from the compaction's)
+    const int pr = a.row_pair ? a.row_pair[a.row0 + blockIdx.y] : 0;
+    const int p = a.row_pair ? pr % a.P_ : (int)blockIdx.y, b = a.row_pair ? pr / a.P_ : (int)blockIdx.z;
     const int h = 2 * p + hh;
     const int c0 = 2 * r;
     const bool two = c0 + 1 < a.C;
@@ -317,9 +322,11 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
     a.g = pb.g; a.h0 = pb.h0; a.grp_info = (const int4 *)ws.grp_info;
     a.O = (__nv_bfloat16 *)pb.o; a.status = ws.counts + 2;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.G = pb.G;
+    a.row_pair = pb.nrows > 0 ? pb.row_pair : nullptr;
+    a.row0 = pb.row0;
     cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
-    return launch_kernel(pb.pdl, output_tc_kernel, dim3(2 * pb.G, pb.P, pb.B), kThreads, kOutSmem, pb.stream, tQ, tK,
-                         tU, tS, tO, a);
+    const dim3 grid = pb.nrows > 0 ? dim3(2 * pb.G, pb.nrows, 1) : dim3(2 * pb.G, pb.P, pb.B);
+    return launch_kernel(pb.pdl, output_tc_kernel, grid, kThreads, kOutSmem, pb.stream, tQ, tK, tU, tS, tO, a);
 }
 
 }  // namespace gdn

@@ -63,6 +63,7 @@ struct WarpScanParams {
     float *s_final;
     int32_t *status;
     int P_, T_, Nv, C;
+    int row0;               // first CSR row of this launch (blockIdx.z = row - row0)
     int64_t ev_cap, snap_cap;
 };
 
@@ -141,7 +142,7 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;           // fragment row group, column pair
     const uint32_t lrow = lane & 7, lmat = lane >> 3;  // ldmatrix / stmatrix: row in matrix, matrix id
-    const int hh = blockIdx.y, j = blockIdx.z;
+    const int hh = blockIdx.y, j = a.row0 + (int)blockIdx.z;
     const int dv0 = blockIdx.x * kSlice;               // the CTA's first state column
     const int t0w = 16 * warp, d0w = 32 * warp;        // this warp's tokens (MMA1) and d columns (MMA2)
     pdl_trigger();
@@ -427,8 +428,9 @@ cudaError_t launch_stages(const Problem &pb, const CUtensorMap &tW, const CUtens
                           const WarpScanParams &a) {
     constexpr uint32_t smem = Layout<STAGES>::smem;
     cudaFuncSetAttribute(scan_warp_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return launch_kernel(pb.pdl, scan_warp_kernel<STAGES>, dim3(kDim / kSlice, 2, pb.R), kThreads + 32, smem, pb.stream,
-                         tW, tK, tU, a);
+    const int nrows = pb.nrows > 0 ? pb.nrows : pb.R;
+    return launch_kernel(pb.pdl, scan_warp_kernel<STAGES>, dim3(kDim / kSlice, 2, nrows), kThreads + 32, smem,
+                         pb.stream, tW, tK, tU, a);
 }
 
 }  // namespace
@@ -449,12 +451,17 @@ cudaError_t launch_scan_warp(const Problem &pb, const Workspace &ws) {
     a.U = (__nv_bfloat16 *)ws.U; a.snap = (__nv_bfloat16 *)ws.snap;
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C;
     a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
-    // Up to two waves of CTAs: one CTA per SM with a deep ring (the longest row sets the time);
-    // more: a shallow ring and several CTAs per SM (throughput).
+    a.row0 = pb.nrows > 0 ? pb.row0 : 0;
+    const int nrows = pb.nrows > 0 ? pb.nrows : pb.R;
+    // The whole scan alone in up to two waves: a deep ring and the SM to itself (151 KB; a
+    // latency-bound loop runs slower beside another kernel's CTAs).  A row class beside the
+    // other classes' kernels: 111 KB, so an intra or output CTA fits beside it.  Many CTAs: a
+    // shallow ring and two scan CTAs per SM (throughput).
     int sms = 148, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t ctas = (int64_t)pb.R * 2 * (kDim / kSlice);
-    if (ctas <= 2 * (int64_t)sms) return launch_stages<4>(pb, tW, tK, tU, a);
+    const int64_t ctas = (int64_t)nrows * 2 * (kDim / kSlice);
+    if (pb.nrows == 0 && ctas <= 2 * (int64_t)sms) return launch_stages<4>(pb, tW, tK, tU, a);
+    if (ctas <= 2 * (int64_t)sms) return launch_stages<3>(pb, tW, tK, tU, a);
     return launch_stages<2>(pb, tW, tK, tU, a);
 }
 

@@ -34,11 +34,18 @@
  *
  * Memory and streams.  Every pointer is a caller-owned DEVICE pointer on the
  * current CUDA device, 16-byte aligned (the workspace: 256-byte aligned).  The
- * library never allocates, never frees and never synchronises, except
- * gdn_workspace_status().  Work is enqueued on `stream` (a cudaStream_t; NULL
- * = legacy default stream) and is complete only when that stream is.  The
- * event count E never leaves the device.  Calls on distinct workspaces are
- * independent; two calls that share a workspace must be stream-ordered.
+ * library never allocates device memory, never frees and never synchronises,
+ * except in the status queries.  Work is enqueued on `stream` (a cudaStream_t;
+ * NULL = legacy default stream) and is complete only when that stream is.  The
+ * bf16 prefills fork part of their kernels onto library-owned streams (made
+ * once per device, at higher priority) with an event recorded on `stream`,
+ * and join them back with events before returning, so `stream` alone orders
+ * the work; a stream capture of `stream` takes the forked kernels in.  Make
+ * the first prefill on a device outside a capture (it creates those streams).
+ * Calls on distinct workspaces are independent (concurrent calls share the
+ * library's streams, so their forked kernels run one call after the other);
+ * two calls that share a workspace must be stream-ordered.  The event count E
+ * never leaves the device.
  *
  * Errors.  Argument problems are detected on the host before anything is
  * enqueued and returned synchronously (GDN_ERR_NULL / SHAPE / DTYPE / ALIGN /
@@ -337,20 +344,24 @@ GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream);
 
 GDN_API const char *gdn_status_string(gdn_status status);
 
-/* Stage timing for benchmarks.  While enabled, each prefill records a CUDA
- * event before its first and after each pipeline stage on its own stream
+/* Stage timing for benchmarks.  enable = 1: each following prefill records a
+ * CUDA event before its first and after each pipeline stage on its own stream
  * (stages: 0 compaction, 1 log-decay prefix, 2 intra, 3 deferred W, 4 scan
- * run maps, 5 scan chain over runs, 6 scan (fix-up, or the whole scan for fp32
- * storage), 7 group output, 8 online selector; a stage a path does not run
- * reads 0), for up to 256 prefills.  Enabling (again) drops
- * earlier records.  Not thread-safe: one host thread drives the profiler.
- * The events are created on the first enable (no device memory). */
+ * run maps, 5 scan chain over runs, 6 scan (the one-pass scan, the run-map
+ * fix-up, or the fp32 scan), 7 group output, 8 online selector; a stage a path
+ * does not run reads 0), for up to 256 prefills; while recording, a prefill
+ * runs every kernel on the caller's stream, one after another.  enable = 2:
+ * nothing is recorded and the prefills keep their normal schedule; only the
+ * kernels they launch are counted.  0: off.  Enabling (again) drops earlier
+ * records.  Not thread-safe: one host thread drives the profiler.  The events
+ * are created on the first enable = 1 (no device memory). */
 GDN_API gdn_status gdn_profile_enable(int enable);
 
 /* Synchronises on the recorded events, writes the summed milliseconds of each
- * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 9),
- * the number of recorded prefills to *n_prefills, the number of kernels those
- * prefills launched to *n_launches (may be NULL), and clears the records. */
+ * stage over all recorded prefills to stage_ms[0..n_stages) (n_stages <= 9;
+ * zeros under enable = 2), the number of prefills run since enabling to
+ * *n_prefills, the number of kernels they launched to *n_launches (may be
+ * NULL), and clears the records. */
 GDN_API gdn_status gdn_profile_read(float *stage_ms, int32_t n_stages, int32_t *n_prefills,
                                     int64_t *n_launches);
 
