@@ -38,11 +38,15 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # DRAM bytes (read + write) of one launch, measured with ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum) on the current version of the kernel and workload; an entry must be
-# removed whenever its kernel changes (the roofline's traffic is then reported as null).
+# dram__bytes_write.sum) on the current version of each kernel and workload (all launches of
+# one prefill summed per kernel); an entry must be removed whenever its kernel changes (the
+# traffic is then reported as null).
 PROFILED_TRAFFIC = {
-    ("qwen35_4b_layer_T32768_sparse29", "intra"): 739.37e6,
-    ("qwen35_4b_layer_T32768_sparse29", "output"): 921.59e6,
+    ("qwen35_4b_layer_T32768_sparse29", "select"): 0.067e6,
+    ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.134e6,
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 633.4e6,
+    ("qwen35_4b_layer_T32768_sparse29", "scan"): 231.2e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 848.3e6,
 }
 
 
@@ -55,6 +59,7 @@ def parse():
     ap.add_argument("--workload", default="qwen35_4b_layer_T32768_sparse29")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' timings")
     return ap.parse_args()
 
 
@@ -93,6 +98,17 @@ def peaks():
 
 
 # ------------------------------------------------------------ accounting ---
+
+def compulsory_share(x, kernel: str) -> float:
+    """The part of the step's compulsory bytes each kernel moves (inputs read once,
+    outputs written once): intra k, v, beta, g; scan S_final; output q and o;
+    compaction the mask."""
+    es = 2 if x.dtype == "bf16" else 4
+    B, T, Nq, Nv, d, dv = x.B, x.T, x.Nq, x.Nv, x.d, x.dv
+    qk, vo, bg = B * T * Nq * d * es, B * T * Nv * dv * es, B * T * Nv * 4
+    return {"intra": qk + vo + 2 * bg, "scan": B * Nv * d * dv * 4, "output": qk + vo,
+            "select": x.mask.size, "prefix": 0}.get(kernel, 0)
+
 
 def algorithmic_bytes(x, kernel: str, n_snap: int = 0) -> float:
     """Compulsory bytes of one launch: inputs read once, outputs written once.
@@ -195,13 +211,26 @@ def oracle_sample(x, pairs, t_tokens, nthreads):
     return t_tokens * len(pairs) / x.Nq / dt, dt, min(nthreads, 2 * len(pairs))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), or 'unknown'."""
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in outp.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
 def cpu_baseline(x):
     cores = os.cpu_count() or 1
     npairs = max(1, min(x.Nq, cores))
     pairs = list(range(npairs))
     t_tokens = min(x.T, 16384)
     value, dt, used = oracle_sample(x, pairs, t_tokens, nthreads=min(2 * npairs, cores))
-    return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+    return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "cpu_model": cpu_model(),
+            "host_cores": cores,
             "sample": f"fp64 C oracle, head pairs 0..{npairs - 1} of {x.Nq}, tokens 0..{t_tokens - 1} of sequence 0 "
                       f"({dt:.1f} s wall, {used} threads); tokens/s scaled to the full layer by the head fraction"}
 
@@ -230,7 +259,7 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "B": x.B, "T": x.T, "Nq": x.Nq, "Nv": x.Nv, "d": x.d, "dv": x.dv,
                        "retention": round(x.retention(), 4), "solver": "block_adj"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "cpu_model": cpu_model(),
                              "sample": f"each step: {npairs} head pairs (cycling) x tokens 0..{t_tokens - 1} of "
                                        f"sequence 0; tokens/s scaled to the full layer by the head fraction"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -239,6 +268,96 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------ our CUDA path ---
+
+def count_launches(gdn, call, steps):
+    """Kernels that `steps` calls launch on their normal schedule (profile mode 2: counted, not timed)."""
+    import torch
+    gdn.gdn_profile_enable(2)
+    for _ in range(steps):
+        call()
+    torch.cuda.synchronize()
+    _, _, n_launch = gdn.gdn_profile_read(with_launches=True)
+    gdn.gdn_profile_enable(False)
+    return n_launch
+
+
+def time_plain(call, steps, world, dev, warmup=3):
+    """Mean ms of `call()` over `steps` after `warmup` calls (CUDA events on the current stream)."""
+    import torch
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    return reduce_step_ms(e0.elapsed_time(e1) / steps, world, dev)
+
+
+def other_configs(gdn, gdn_synth, args, world, dev, stream, rank):
+    """The other workloads of the study, timed on their own inputs (tokens/s per layer):
+    the T=4096 dense layer through gdn_prefill_dense with both solvers, the batch of
+    B = 2, 4, 8 sequences at T=32K (29% events), and the 24-layer, 128K-token prefill
+    timed end to end (24 independently seeded layers back to back in one stream)."""
+    import torch
+    out = {}
+    st = torch.bfloat16
+
+    def dev_inputs(x):
+        f = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(dt)
+        return {"q": f(x.q, st), "k": f(x.k, st), "v": f(x.v, st), "beta": f(x.beta, torch.float32),
+                "g": f(x.g, torch.float32), "mask": f(x.mask, torch.uint8)}
+
+    x = gdn_synth.make_workload("qwen35_4b_layer_T4096_dense", batch_index=rank_batch_index(rank))
+    t = dev_inputs(x)
+    ws = gdn.Workspace()
+    for solver in ("exact", "block_adj"):
+        call = lambda: gdn.gdn_prefill_dense(t["q"], t["k"], t["v"], t["beta"], t["g"], solver=solver, workspace=ws,
+                                             stream=stream)
+        ms = time_plain(call, args.steps, world, dev)
+        out[f"qwen35_4b_layer_T4096_dense_{solver}"] = {
+            "ms_per_step": ms, "value": job_throughput(x.B * x.T, world, ms), "unit": UNIT,
+            "api": "gdn_prefill_dense", "gpu_launches": count_launches(gdn, call, 1)}
+    del t, ws
+    for B in (2, 4, 8):
+        x = gdn_synth.make_workload("qwen35_4b_layer_B8_T32768_sparse29", B=B, batch_index=rank_batch_index(rank))
+        t = dev_inputs(x)
+        ws = gdn.Workspace()
+        call = lambda: gdn.gdn_prefill_sparse(t["q"], t["k"], t["v"], t["beta"], t["g"], t["mask"],
+                                              solver="block_adj", workspace=ws, stream=stream)
+        ms = time_plain(call, max(3, args.steps // 4), world, dev)
+        out[f"qwen35_4b_layer_B{B}_T32768_sparse29"] = {
+            "ms_per_step": ms, "value": job_throughput(x.B * x.T, world, ms), "unit": UNIT,
+            "retention": round(x.retention(), 4), "api": "gdn_prefill_sparse",
+            "gpu_launches": count_launches(gdn, call, 1)}
+        del t, ws
+        torch.cuda.empty_cache()
+    # 24 layers x T = 131072: inputs drawn on the GPU (the same recipe, a device generator)
+    name, L, T = "qwen35_4b_24layers_T131072_sparse29", 24, 131072
+    layers = [gdn_synth.make_layer_on_device(1, T, 16, 32, gdn_synth.seed_for(3, layer, rank_batch_index(rank)), dev)
+              for layer in range(L)]
+    o = torch.empty((1, T, 32, 128), dtype=st, device=dev)
+    finals = torch.empty((L, 1, 32, 128, 128), dtype=torch.float32, device=dev)
+    ws = gdn.Workspace()
+
+    def prefill_24():
+        for i, t in enumerate(layers):
+            gdn.gdn_prefill_sparse(t["q"], t["k"], t["v"], t["beta"], t["g"], t["mask"], solver="block_adj",
+                                   o=o, s_final=finals[i], workspace=ws, stream=stream)
+
+    ms = time_plain(prefill_24, 3, world, dev, warmup=1)
+    ok = bool(torch.isfinite(finals).all().item()) and gdn.gdn_workspace_status(ws) == 0
+    out[name] = {"ms_per_prefill": ms, "value": job_throughput(L * T, world, ms), "unit": "tokens/s per layer",
+                 "layers": L, "T": T, "timed": "24 layers back to back in one stream, end to end",
+                 "inputs": "seeded, drawn on the GPU (gdn_synth.make_layer_on_device)",
+                 "retention": round(float(sum(t["mask"].float().mean().item() for t in layers) / L), 4),
+                 "s_final_finite_and_status_ok": ok, "gpu_launches": count_launches(gdn, prefill_24, 1)}
+    del layers, o, finals, ws
+    torch.cuda.empty_cache()
+    return out
+
 
 def timed_variant(gdn, call, x, steps, world, dev, stream):
     """Time `call()` (one prefill) over `steps` after 3 warm-ups: ms per step, tokens/s, stages, kernels."""
@@ -256,8 +375,9 @@ def timed_variant(gdn, call, x, steps, world, dev, stream):
     for _ in range(steps):
         call()
     torch.cuda.synchronize()
-    stage_ms, nrec, n_launch = gdn.gdn_profile_read(with_launches=True)
+    stage_ms, nrec, _ = gdn.gdn_profile_read(with_launches=True)
     gdn.gdn_profile_enable(False)
+    n_launch = count_launches(gdn, call, steps)
     ms = reduce_step_ms(e0.elapsed_time(e1) / steps, world, dev)
     return {"ms_per_step": ms, "value": job_throughput(x.B * x.T, world, ms), "unit": UNIT, "gpu_launches": n_launch,
             "stages_ms": {k: round(v / max(nrec, 1), 4) for k, v in stage_ms.items()}}
@@ -340,8 +460,9 @@ def run_ours(args):
     for _ in range(args.steps):
         step()
     torch.cuda.synchronize()
-    stage_ms, nrec, n_launch = gdn.gdn_profile_read(with_launches=True)
+    stage_ms, nrec, _ = gdn.gdn_profile_read(with_launches=True)
     gdn.gdn_profile_enable(False)
+    n_launch = count_launches(gdn, step, args.steps)
     ms = reduce_step_ms(ev0.elapsed_time(ev1) / args.steps, world, dev)
     value = job_throughput(tok, world, ms)
 
@@ -385,20 +506,38 @@ def run_ours(args):
 
     online = online_variant(gdn, d_in, x, ws, stream, args.steps, world, dev)
     # the pages' ablation axes on the same inputs (gdn_prefill_ex): W deferred to its own kernel
-    # (bit-identical result) and the exact Full64 solver with the same mask
+    # (bit-identical result), the exact Full64 solver with the same mask, the run-map event scan
     def ex_call(**kw):
         return lambda: gdn.gdn_prefill_ex(d_in["q"], d_in["k"], d_in["v"], d_in["beta"], d_in["g"], mode="sparse",
                                           mask=d_in["mask"], o=o, s_final=s_final, workspace=ws, stream=stream, **kw)
     w_deferred = timed_variant(gdn, ex_call(solver="block_adj", w_deferred=True), x, args.steps, world, dev, stream)
     exact = timed_variant(gdn, ex_call(solver="exact"), x, args.steps, world, dev, stream)
+    scan_runs = timed_variant(gdn, ex_call(solver="block_adj", scan_runs=True), x, args.steps, world, dev, stream)
+    # this build's own dense path on the same layer (every chunk an event, gdn_prefill_dense)
+    dense = timed_variant(gdn, lambda: gdn.gdn_prefill_dense(
+        d_in["q"], d_in["k"], d_in["v"], d_in["beta"], d_in["g"], solver="block_adj", o=o, s_final=s_final,
+        workspace=ws, stream=stream), x, args.steps, world, dev, stream)
+    variants = {"online_selection": online, "w_deferred": w_deferred, "solver_exact": exact, "scan_runs": scan_runs,
+                "dense_same_layer": dense}
+    del o, s_final
+    ws = None
+    torch.cuda.empty_cache()
+    configs = {} if args.no_configs else other_configs(gdn, gdn_synth, args, world, dev, stream, rank)
 
     peak, peak_kind = peaks()
     per_stage = {k: v / max(nrec, 1) for k, v in stage_ms.items()}
-    dom = max(per_stage, key=per_stage.get)
-    dom_kernel = dom if dom in ("output", "intra") else "step"
-    dom_ms = per_stage[dom] if dom_kernel != "step" else ms
-    achieved = algorithmic_bytes(x, dom_kernel, n_snap) / (dom_ms / 1000.0) / 1e9
-    step_gbs = algorithmic_bytes(x, "step") / (ms / 1000.0) / 1e9
+    step_bytes = algorithmic_bytes(x, "step")
+    step_gbs = step_bytes / (ms / 1000.0) / 1e9
+    traffic = {k: PROFILED_TRAFFIC.get((args.workload, k)) for k in ("select", "prefix", "intra", "scan", "output")}
+    step_traffic = sum(traffic.values()) if all(v is not None for v in traffic.values()) else None
+    kernels = {}
+    for k in ("select", "prefix", "intra", "scan", "output"):
+        share = compulsory_share(x, k)
+        t = per_stage.get(k, 0.0)
+        kernels[k] = {"ms_one_stream": round(t, 4), "compulsory_bytes": share,
+                      "frac_of_peak": (share / (t / 1000.0) / 1e9 / peak) if t > 0 and share else None,
+                      "dram_bytes": traffic[k],
+                      "dram_over_compulsory": (traffic[k] / share) if traffic[k] and share else None}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -407,22 +546,23 @@ def run_ours(args):
         "config": {"workload": args.workload, "B": x.B, "T": x.T, "Nq": x.Nq, "Nv": x.Nv, "d": x.d, "dv": x.dv,
                    "retention": round(x.retention(), 4), "events": n_events, "snapshots": n_snap,
                    "solver": "block_adj",
-                   "l2": "inputs larger than L2 (%.0f MB compulsory bytes per step), no flush" %
-                         (algorithmic_bytes(x, "step") / 1e6),
+                   "l2": "inputs larger than L2 (%.0f MB compulsory bytes per step), no flush" % (step_bytes / 1e6),
                    "parallelism": "one independent sequence per GPU" if world > 1 else "single GPU"},
         "clocks": clk,
         "e2e": {"value": job_throughput(tok, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": "gdn_prefill_host (C ABI, host buffers)",
                 "pipelining": "2 streams x 2 workspaces", "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": n_launch,
-        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": PROFILED_TRAFFIC.get((args.workload, dom_kernel)),
-                     "peak_source": peak_kind,
-                     "step_frac": step_gbs / peak,
-                     "note": f"achieved = compulsory bytes of one {dom_kernel} launch / its mean CUDA-event time; "
-                             f"frac of {peak_kind} HBM copy bandwidth"},
-        "stages_ms": {k: round(v, 4) for k, v in per_stage.items()},
-        "variants": {"online_selection": online, "w_deferred": w_deferred, "solver_exact": exact},
+        "roofline": {"bound": "hbm", "kernel": "step (the whole hot path: compaction, prefix, intra, scan, output)",
+                     "achieved": step_gbs, "peak": peak, "unit": "GB/s", "frac": step_gbs / peak,
+                     "traffic": step_traffic, "peak_source": peak_kind,
+                     "note": f"achieved = the step's compulsory bytes ({step_bytes / 1e6:.1f} MB: q, k, v, beta, g, "
+                             f"mask read once; o, S_final written once) / ms_per_step; frac of {peak_kind} HBM copy "
+                             f"bandwidth; traffic = ncu DRAM bytes of one prefill summed over its kernels",
+                     "kernels": kernels},
+        "stages_ms_one_stream": {k: round(v, 4) for k, v in per_stage.items()},
+        "variants": variants,
+        "configs": configs,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x)

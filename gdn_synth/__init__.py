@@ -236,3 +236,34 @@ def make_workload(name: str, layer: int = 0, batch_index: int = 0, **override) -
     cfg = w.pop("config")
     return make_inputs(w.pop("B"), w.pop("T"), w.pop("Nq"), w.pop("Nv"),
                        seed=seed_for(cfg, layer, batch_index), **w)
+
+
+def make_layer_on_device(B: int, T: int, Nq: int, Nv: int, seed: int, device, d: int = 128, dv: int = 128,
+                         mask: str = "beta", retention: float = 0.29) -> dict:
+    """The same recipe as make_inputs (bf16 storage), drawn on the GPU with a seeded
+    torch generator, for workloads too large to draw on the host in a benchmark (the
+    24-layer, 128K-token prefill).  The bits differ from make_inputs' for the same
+    seed; the distributions are the same.  The mask is drawn on the host with
+    make_mask.  Returns device tensors q, k [B,T,Nq,d] bf16; v [B,T,Nv,dv] bf16;
+    beta, g [B,T,Nv] fp32; mask [B,Nv/2,C] uint8."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    f32 = torch.float32
+
+    def l2n(x):
+        return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+
+    q = l2n(torch.randn((B, T, Nq, d), generator=gen, device=device, dtype=f32)).to(torch.bfloat16)
+    k = l2n(torch.randn((B, T, Nq, d), generator=gen, device=device, dtype=f32)).to(torch.bfloat16)
+    v = torch.randn((B, T, Nv, dv), generator=gen, device=device, dtype=f32).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn((B, T, Nv), generator=gen, device=device, dtype=f32))
+    a = -(0.001 + 0.049 * torch.rand((B, T, Nv), generator=gen, device=device, dtype=f32))
+    C = (T + CHUNK - 1) // CHUNK
+    pad = C * CHUNK - T
+    ap = torch.nn.functional.pad(a, (0, 0, 0, pad)).view(B, C, CHUNK, Nv)
+    g = torch.cumsum(ap, dim=2).view(B, C * CHUNK, Nv)[:, :T].contiguous()
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0]))
+    m = torch.from_numpy(make_mask(rng, B, Nv // 2, C, mask, retention)).to(device)
+    return {"q": q, "k": k, "v": v, "beta": beta, "g": g, "mask": m}

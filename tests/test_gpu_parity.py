@@ -230,6 +230,31 @@ def test_long_context_T131072_layer_all_pairs(layer):
     assert_close(res, oracle_run(x, "block_adj"), "bf16", f"T=131072 layer {layer}")
 
 
+def test_long_context_24_layers_every_layer_sampled_pair():
+    # the 24-layer, 128K-token prefill as the benchmark runs it (inputs drawn on the GPU, layers
+    # back to back on one workspace): every layer's output and final state on one sampled head
+    # pair, against the oracle run on that pair's inputs (all 24 pairs as one batch of sequences)
+    L, T = 24, 131072
+    ws = gdn.Workspace()
+    qs, ks, vs, bs, gs, ms, os_, ss = [], [], [], [], [], [], [], []
+    for layer in range(L):
+        t = gdn_synth.make_layer_on_device(1, T, 16, 32, gdn_synth.seed_for(3, layer), dev())
+        o, s = gdn.gdn_prefill_sparse(t["q"], t["k"], t["v"], t["beta"], t["g"], t["mask"], solver="block_adj",
+                                      workspace=ws)
+        p = (7 * layer + 3) % 16
+        hv = [2 * p, 2 * p + 1]
+        f64 = lambda a: a.float().cpu().numpy().astype(np.float64)
+        qs.append(f64(t["q"][:, :, p:p + 1])); ks.append(f64(t["k"][:, :, p:p + 1]))
+        vs.append(f64(t["v"][:, :, hv])); bs.append(f64(t["beta"][:, :, hv])); gs.append(f64(t["g"][:, :, hv]))
+        ms.append(t["mask"][:, p:p + 1].cpu().numpy())
+        os_.append(f64(o[:, :, hv])); ss.append(s[:, hv].cpu().numpy().astype(np.float64))
+        del t, o, s
+    assert gdn.gdn_workspace_status(ws) == 0
+    cat = lambda a: np.concatenate(a, axis=0)
+    ref = oracle.prefill(cat(qs), cat(ks), cat(vs), cat(bs), cat(gs), mask=cat(ms), solver=oracle.SOLVER_BLOCK_ADJ)
+    assert_close({"o": cat(os_), "s_final": cat(ss)}, ref, "bf16", "24 layers x T=131072")
+
+
 @pytest.mark.parametrize("sparse", [True, False])
 @pytest.mark.parametrize("T1", [128, 1024 + 128])
 def test_chunked_prefill_resume(sparse, T1):
