@@ -513,12 +513,17 @@ def run_ours(args):
     w_deferred = timed_variant(gdn, ex_call(solver="block_adj", w_deferred=True), x, args.steps, world, dev, stream)
     exact = timed_variant(gdn, ex_call(solver="exact"), x, args.steps, world, dev, stream)
     scan_runs = timed_variant(gdn, ex_call(solver="block_adj", scan_runs=True), x, args.steps, world, dev, stream)
+    # the pages' reference paths (Table 6), bit-identical results: the masked full scan, and the
+    # dense group entry states read by group instead of compact snapshots through the group map
+    scan_full = timed_variant(gdn, ex_call(solver="block_adj", scan_full=True), x, args.steps, world, dev, stream)
+    expanded = timed_variant(gdn, ex_call(solver="block_adj", states_expanded=True), x, args.steps, world, dev,
+                             stream)
     # this build's own dense path on the same layer (every chunk an event, gdn_prefill_dense)
     dense = timed_variant(gdn, lambda: gdn.gdn_prefill_dense(
         d_in["q"], d_in["k"], d_in["v"], d_in["beta"], d_in["g"], solver="block_adj", o=o, s_final=s_final,
         workspace=ws, stream=stream), x, args.steps, world, dev, stream)
     variants = {"online_selection": online, "w_deferred": w_deferred, "solver_exact": exact, "scan_runs": scan_runs,
-                "dense_same_layer": dense}
+                "scan_full_masked": scan_full, "states_expanded_unmapped_o": expanded, "dense_same_layer": dense}
     del o, s_final
     ws = None
     torch.cuda.empty_cache()

@@ -43,7 +43,7 @@ class GdnShape(ctypes.Structure):
 
 class GdnOptions(ctypes.Structure):
     _fields_ = [("tail_window", ctypes.c_int32), ("w_deferred", ctypes.c_int32), ("scan_runs", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("scan_full", ctypes.c_int32), ("states_expanded", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 MODES = {"dense": 0, "sparse": 1, "online": 2}
@@ -389,8 +389,8 @@ def gdn_prefill_host(q, k, v, beta, g, mask=None, *, h0=None, solver="block_adj"
 
 
 def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=None, solver="block_adj",
-                   tail_window=0, w_deferred=False, scan_runs=False, o=None, s_final=None, score=None,
-                   mask_out=None,
+                   tail_window=0, w_deferred=False, scan_runs=False, scan_full=False, states_expanded=False,
+                   o=None, s_final=None, score=None, mask_out=None,
                    tier_out=None, workspace=None, stream=None):
     """The general prefill with execution variants; returns (o, s_final, mask_out, tier_out)."""
     B, T, Nq, d = q.shape
@@ -416,7 +416,8 @@ def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=N
             tier_out = torch.empty((B, Nq), dtype=torch.int32, device=dev)
     _need(score, "score", torch.float32, (B, Nv, C))
     shape = shape_of(q, v)
-    opt = GdnOptions(int(tail_window), int(bool(w_deferred)), int(bool(scan_runs)))
+    opt = GdnOptions(int(tail_window), int(bool(w_deferred)), int(bool(scan_runs)), int(bool(scan_full)),
+                     int(bool(states_expanded)))
     nbytes = int(load().gdn_workspace_bytes_ex(ctypes.byref(shape), SOLVERS[solver], MODES[mode], ctypes.byref(opt)))
     if nbytes == 0:
         raise GdnError("gdn_workspace_bytes_ex", 2, "invalid shape or options")

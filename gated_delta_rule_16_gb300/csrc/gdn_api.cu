@@ -204,7 +204,13 @@ gdn_status check_options(const gdn_options *opt) {
     if (tw != 0 && tw != 8 && tw != 16 && tw != 32 && tw != 64) return GDN_ERR_UNSUPPORTED;
     if (opt->w_deferred != 0 && opt->w_deferred != 1) return GDN_ERR_UNSUPPORTED;
     if (opt->scan_runs != 0 && opt->scan_runs != 1) return GDN_ERR_UNSUPPORTED;
-    for (int i = 0; i < 5; ++i)
+    if (opt->scan_full != 0 && opt->scan_full != 1) return GDN_ERR_UNSUPPORTED;
+    if (opt->states_expanded != 0 && opt->states_expanded != 1) return GDN_ERR_UNSUPPORTED;
+    // the masked full scan and the expanded states are variants of the one-pass scan
+    if ((opt->scan_full || opt->states_expanded) && opt->scan_runs) return GDN_ERR_UNSUPPORTED;
+    // the masked full scan reads W of every chunk, built in the intra step from a mask known up front
+    if (opt->scan_full && opt->w_deferred) return GDN_ERR_UNSUPPORTED;
+    for (int i = 0; i < 3; ++i)
         if (opt->reserved[i] != 0) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
@@ -219,6 +225,8 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     if ((st = check_options(opt)) != GDN_OK) return st;
     if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return GDN_ERR_DTYPE;
     if (mode == kOnline && shape->Nv != 32) return GDN_ERR_UNSUPPORTED;  // the tier table is for 16 pairs
+    if (opt && (opt->scan_full || opt->states_expanded) && shape->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    if (opt && opt->scan_full && mode == kOnline) return GDN_ERR_UNSUPPORTED;
     const bool has_tokens = shape->B > 0 && shape->T > 0;
     if (shape->B > 0 && !s_final) return GDN_ERR_NULL;
     if (has_tokens && (!q || !k || !v || !beta || !g || !o || (mode == kSparse && !mask))) return GDN_ERR_NULL;
@@ -231,6 +239,8 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     fill_problem(shape, solver, &pb);
     set_buffers(&pb, mode == kOnline, opt);
     if (opt && opt->tail_window) pb.tail = opt->tail_window;
+    pb.scan_full = opt && opt->scan_full;
+    pb.states_expanded = opt && opt->states_expanded;
     const bool w_deferred = opt && opt->w_deferred;
     if (shape->B == 0) return GDN_OK;
     const size_t need = workspace_layout(pb, nullptr, nullptr);

@@ -89,6 +89,8 @@ struct Problem {
     // nrows == 0: every pair, gridded by (pair, sequence).
     const int32_t *row_pair;
     int row0, nrows;
+    int scan_full;             // masked full scan: W built for every chunk, the scan visits every chunk
+    int states_expanded;       // one entry state per output group (slot i G + r), read by group
     const void *q, *k, *v;
     const float *beta, *g, *h0;
     const uint8_t *mask;       // NULL: every chunk is an event

@@ -525,7 +525,8 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
         !make_tmap_bf16_3d(&tW, ws.W, kDim, wrows, 1, kDim * 2, wrows * kDim * 2, 64, 64, 1))
         return cudaErrorInvalidValue;
     IntraParams a;
-    a.beta = pb.beta; a.g = pb.g; a.mask = pb.mask; a.build_w = !write_cbar;
+    // the masked full scan reads W of every chunk: build it for all of them
+    a.beta = pb.beta; a.g = pb.g; a.mask = pb.scan_full ? nullptr : pb.mask; a.build_w = !write_cbar;
     a.cbar = write_cbar ? reinterpret_cast<__nv_bfloat16 *>(ws.cbar) : nullptr;
     a.U = (__nv_bfloat16 *)ws.U; a.W = (__nv_bfloat16 *)ws.W; a.score = pb.score;
     a.status = ws.counts + 2;

@@ -44,6 +44,7 @@ struct OutParams {
     int32_t *status;
     const int32_t *row_pair;  // non-NULL: blockIdx.y is CSR row row0 + y (pair row_pair[row0 + y])
     int row0;
+    int expanded;             // entry states by group (slot (b P + p) G + r), not through the map
     int P_, T_, Nv, C, G;
 };
 
@@ -112,9 +113,10 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         has_s = kind;
         fscale = __int_as_float(hh ? info.w : info.z);
         if (kind == 1) {
+            const int slot = a.expanded ? (b * a.P_ + p) * a.G + r : info.x;
             mbar_arrive_expect_tx(&bar_s, 2 * kSlab);
-            tma_load_3d(sm + OFF_S, &tS, 0, (info.x * 2 + hh) * kDim, 0, &bar_s);
-            tma_load_3d(sm + OFF_S + kSlab, &tS, 64, (info.x * 2 + hh) * kDim, 0, &bar_s);
+            tma_load_3d(sm + OFF_S, &tS, 0, (slot * 2 + hh) * kDim, 0, &bar_s);
+            tma_load_3d(sm + OFF_S + kSlab, &tS, 64, (slot * 2 + hh) * kDim, 0, &bar_s);
         }
     }
     tc_fence_before();
@@ -324,6 +326,7 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C; a.G = pb.G;
     a.row_pair = pb.nrows > 0 ? pb.row_pair : nullptr;
     a.row0 = pb.row0;
+    a.expanded = pb.states_expanded;
     cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
     const dim3 grid = pb.nrows > 0 ? dim3(2 * pb.G, pb.nrows, 1) : dim3(2 * pb.G, pb.P, pb.B);
     return launch_kernel(pb.pdl, output_tc_kernel, grid, kThreads, kOutSmem, pb.stream, tQ, tK, tU, tS, tO, a);

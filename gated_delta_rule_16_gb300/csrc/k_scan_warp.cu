@@ -65,6 +65,12 @@ struct WarpScanParams {
     int P_, T_, Nv, C;
     int row0;               // first CSR row of this launch (blockIdx.z = row - row0)
     int64_t ev_cap, snap_cap;
+    // execution variants (bit-identical results): the masked full scan walks every chunk
+    // (mask [B,P,C], the products computed on every chunk and kept on the events only);
+    // expanded entry states: the state after an event goes to the slot of every output group
+    // it enters (physical row i, group r: slot i G + r) instead of its compact snapshot slot
+    const uint8_t *mask;
+    int expanded, G;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -129,7 +135,8 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, uint32_t r, uint32_t 
 }
 
 // grid: (dv slices 8, 2 heads, CSR rows R); block: 4 consumer warps + 1 producer warp.
-template <int STAGES>
+// FULL: the masked full scan (every chunk a step; see WarpScanParams).
+template <int STAGES, bool FULL>
 __global__ void __launch_bounds__(kThreads + 32, 1)
 scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tK,
                  const __grid_constant__ CUtensorMap tU, WarpScanParams a) {
@@ -162,11 +169,13 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
     const double *Pu = a.P + ((int64_t)b * a.Nv + h) * (a.C + 1);
     const int64_t gbase = (int64_t)b * a.T_;
     const uint32_t sb = smem_addr(sm + L::sb), upp = smem_addr(sm + L::upp);
+    const int n_steps = FULL ? a.C : n_ev;  // the masked full scan visits every chunk
+    const uint8_t *mrow = FULL ? a.mask + (int64_t)i * a.C : nullptr;
 
-    if (warp == kWarps) {  // ---- producer: the tiles of event k into stage k % STAGES ----
+    if (warp == kWarps) {  // ---- producer: the tiles of step k (event k / chunk k) into stage k % STAGES ----
         __syncthreads();
         int kk = 0;
-        for (; kk < n_ev; ++kk) {
+        for (; kk < n_steps; ++kk) {
             const int s = kk % STAGES;
             if (kk >= STAGES && !mbar_wait(&empty[s], ((kk / STAGES) - 1) & 1)) {
                 if (lane == 0) {
@@ -177,7 +186,7 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
             }
             if (*(volatile int *)&abort_s) break;
             if (lane == 0) {
-                const int c = a.ev_chunk[e_lo + kk];
+                const int c = FULL ? kk : a.ev_chunk[e_lo + kk];
                 uint8_t *st = sm + s * kStage;
                 const int wrow = (int)((((int64_t)i * a.C + c) * 2 + hh) * kChunk);  // W of (row i, chunk c): slot i C + c
                 mbar_arrive_expect_tx(&full[s], kStage);
@@ -294,13 +303,20 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
     }
     __syncthreads();  // barriers initialised, the bf16 state published
 
-    int k = 0;
-    for (; k < n_ev; ++k) {
-        const int s = k % STAGES;
-        const int c = c_k, slot = slot_k;
-        // a failed wait leaves garbage in this event's products (all accesses stay in shared
+    int k = 0;       // events applied
+    int zb = 0;      // masked full scan: lane l holds the mask bit of chunk 32 (st / 32) + l
+    int st = 0;      // steps (events, or chunks for the masked full scan)
+    for (; st < n_steps; ++st) {
+        const int s = st % STAGES;
+        bool is_ev = true;
+        if (FULL) {
+            if ((st & 31) == 0) zb = st + lane < a.C ? mrow[st + lane] != 0 : 0;
+            is_ev = __shfl_sync(0xffffffffu, zb, st & 31) != 0;
+        }
+        const int c = FULL ? st : c_k, slot = slot_k;
+        // a failed wait leaves garbage in this step's products (all accesses stay in shared
         // memory); the CTA then stops together at the next barrier
-        const int bad = !mbar_wait(&full[s], (k / STAGES) & 1) || *(volatile int *)&abort_s;
+        const int bad = !mbar_wait(&full[s], (st / STAGES) & 1) || *(volatile int *)&abort_s;
         const uint32_t wbase = smem_addr(sm + s * kStage), kbase = wbase + kTile, ubase = wbase + 2 * kTile;
 
         // MMA1 on this warp's 16 tokens: Pm = bf16(S^T) (-W)^T over all d (two accumulator sets
@@ -350,11 +366,13 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
             }
             break;
         }
-        // MMA2 on this warp's 32 d columns: S^T <- fsta S^T + U''^T K over all tokens
+        // MMA2 on this warp's 32 d columns: S^T <- fsta S^T + U''^T K over all tokens (the masked
+        // full scan computes it on every chunk and keeps it on the events)
+        float Sx[4][4];
 #pragma unroll
         for (int nd = 0; nd < 4; ++nd)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) S[nd][q] *= fsta;
+            for (int q = 0; q < 4; ++q) Sx[nd][q] = S[nd][q] * fsta;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             uint32_t af[4];
@@ -365,10 +383,21 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
                 const uint32_t t = 16 * ks + 8 * (lmat & 1) + lrow, d = d0w + 8 * (np + (lmat >> 1));
                 uint32_t b0, b1, b2, b3;
                 ldsm4t(sw_addr(kbase, t, d, 8192), b0, b1, b2, b3);
-                mma16816(S[np], af, b0, b1);
-                mma16816(S[np + 1], af, b2, b3);
+                mma16816(Sx[np], af, b0, b1);
+                mma16816(Sx[np + 1], af, b2, b3);
             }
         }
+        if (!is_ev) {  // masked full scan, a chunk that is no event: the state only decays (Eq. 18,
+            // applied at the next event through its gap factor); nothing is written
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            cta_bar(2);  // every warp has read U'' before the next step rewrites it
+            continue;
+        }
+#pragma unroll
+        for (int nd = 0; nd < 4; ++nd)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) S[nd][q] = Sx[nd][q];
         // U' out: this warp's 16 rows, bf16, through its staging: lane l writes half of row l / 2
         // (each 32-byte row segment of U is one whole sector)
         {
@@ -383,6 +412,8 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
             __syncwarp();
         }
         P_end = pe_k;
+        // chunk of the next event (expanded entry states: the groups this event enters end there)
+        const int c_next = k + 1 < n_ev ? chunk_of(k + 1, k) : 2 * a.G;
         // the next event's scalars while the products complete (its gates were loaded an event
         // ago); the gates of the event after it go in flight.  Past the row's end the values
         // are computed for a clamped event and never used.
@@ -397,8 +428,10 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
         if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
         publish_state();
         cta_bar(2);  // the new bf16 state is complete
-        if (slot >= 0 && slot < a.snap_cap) {  // snapshot S_(c+1): bf16 S^T rows dv0 .. dv0 + 15, 4 KB
-            __nv_bfloat16 *dst = a.snap + ((int64_t)slot * 2 + hh) * (kDim * kDim) + dv0 * kDim;
+        // snapshot S_(c+1): bf16 S^T rows dv0 .. dv0 + 15 (4 KB) into its compact slot, or
+        // (expanded entry states) into the slot of every group r with c < 2r <= c_next
+        auto put = [&](int64_t sl) {
+            __nv_bfloat16 *dst = a.snap + (sl * 2 + hh) * (kDim * kDim) + dv0 * kDim;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {  // 16-byte chunk (row r, columns 8 j ..): a warp writes two whole rows
                 const int idx = tid + q * kThreads, r = idx >> 4, jj = idx & 15;
@@ -406,7 +439,14 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
                                                                  sw128_offset(r, (jj & 7) * 8));
                 *reinterpret_cast<uint4 *>(dst + r * kDim + jj * 8) = v;
             }
+        };
+        if (a.expanded) {
+            const int r_hi = min(c_next / 2, a.G - 1);
+            for (int r = c / 2 + 1; r <= r_hi; ++r) put((int64_t)i * a.G + r);
+        } else if (slot >= 0 && slot < a.snap_cap) {
+            put(slot);
         }
+        ++k;
     }
 
     if (!*(volatile int *)&abort_s) {  // S_final = 2^(P_C - P_end) S, written as s_final[d][dv]
@@ -423,14 +463,20 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
     }
 }
 
-template <int STAGES>
+template <int STAGES, bool FULL>
 cudaError_t launch_stages(const Problem &pb, const CUtensorMap &tW, const CUtensorMap &tK, const CUtensorMap &tU,
                           const WarpScanParams &a) {
     constexpr uint32_t smem = Layout<STAGES>::smem;
-    cudaFuncSetAttribute(scan_warp_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(scan_warp_kernel<STAGES, FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const int nrows = pb.nrows > 0 ? pb.nrows : pb.R;
-    return launch_kernel(pb.pdl, scan_warp_kernel<STAGES>, dim3(kDim / kSlice, 2, nrows), kThreads + 32, smem,
+    return launch_kernel(pb.pdl, scan_warp_kernel<STAGES, FULL>, dim3(kDim / kSlice, 2, nrows), kThreads + 32, smem,
                          pb.stream, tW, tK, tU, a);
+}
+
+template <int STAGES>
+cudaError_t launch_mode(const Problem &pb, const CUtensorMap &tW, const CUtensorMap &tK, const CUtensorMap &tU,
+                        const WarpScanParams &a) {
+    return a.mask ? launch_stages<STAGES, true>(pb, tW, tK, tU, a) : launch_stages<STAGES, false>(pb, tW, tK, tU, a);
 }
 
 }  // namespace
@@ -452,6 +498,10 @@ cudaError_t launch_scan_warp(const Problem &pb, const Workspace &ws) {
     a.P_ = pb.P; a.T_ = pb.T; a.Nv = pb.Nv; a.C = pb.C;
     a.ev_cap = ws.ev_cap; a.snap_cap = ws.snap_cap;
     a.row0 = pb.nrows > 0 ? pb.row0 : 0;
+    // the masked full scan needs the mask (the dense path's full scan is its CSR scan)
+    a.mask = pb.scan_full && pb.mask ? pb.mask : nullptr;
+    a.expanded = pb.states_expanded;
+    a.G = pb.G;
     const int nrows = pb.nrows > 0 ? pb.nrows : pb.R;
     // The whole scan alone in up to two waves: a deep ring and the SM to itself (151 KB; a
     // latency-bound loop runs slower beside another kernel's CTAs).  A row class beside the
@@ -460,9 +510,9 @@ cudaError_t launch_scan_warp(const Problem &pb, const Workspace &ws) {
     int sms = 148, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t ctas = (int64_t)nrows * 2 * (kDim / kSlice);
-    if (pb.nrows == 0 && ctas <= 2 * (int64_t)sms) return launch_stages<4>(pb, tW, tK, tU, a);
-    if (ctas <= 2 * (int64_t)sms) return launch_stages<3>(pb, tW, tK, tU, a);
-    return launch_stages<2>(pb, tW, tK, tU, a);
+    if (pb.nrows == 0 && ctas <= 2 * (int64_t)sms) return launch_mode<4>(pb, tW, tK, tU, a);
+    if (ctas <= 2 * (int64_t)sms) return launch_mode<3>(pb, tW, tK, tU, a);
+    return launch_mode<2>(pb, tW, tK, tU, a);
 }
 
 }  // namespace gdn

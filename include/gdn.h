@@ -139,12 +139,28 @@ typedef enum { GDN_MODE_DENSE = 0, GDN_MODE_SPARSE = 1, GDN_MODE_ONLINE = 2 } gd
  *                their fp32 rounding orders differ, so the results agree to
  *                rounding, not bit for bit.  scan_runs = 1 needs the larger
  *                workspace that gdn_workspace_bytes_ex() reports for it.
+ *   scan_full    1: the masked full scan, the pages' reference for the CSR
+ *                scan (Table 6): the intra step builds W for every chunk and
+ *                the scan visits every chunk, computing both products on each
+ *                but keeping them on the mask's events only, with the same
+ *                decay arithmetic (the gap factors of Eq. 21).  Identical
+ *                results bit for bit; more work.  bf16, given mask or dense
+ *                (not online selection, not w_deferred, not scan_runs).
+ *   states_expanded  1: the pages' reference for compact states and mapped
+ *                output (Table 6): the scan writes the entry state of every
+ *                two-chunk output group to a slot of its own (dense group
+ *                states, B*P*G slots), and the output reads its group's slot
+ *                directly instead of the predecessor's compact snapshot
+ *                through the group map.  Identical results bit for bit.  bf16,
+ *                one-pass scan.
  *   reserved     must be zero. */
 typedef struct {
     int32_t tail_window;
     int32_t w_deferred;
     int32_t scan_runs;
-    int32_t reserved[5];
+    int32_t scan_full;
+    int32_t states_expanded;
+    int32_t reserved[3];
 } gdn_options;
 
 /* Bytes of workspace the prefill entry points need for `shape`: sparse = 0

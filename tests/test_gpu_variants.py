@@ -5,7 +5,10 @@
   * the Tail-W score window (W = 8, 16, 32, 64) changes only the scores, which
     match the oracle's Tail-W scores; the outputs stay bit-identical;
   * online selection on Tail-32 scores selects exactly what the oracle's
-    selector selects on the same scores.
+    selector selects on the same scores;
+  * the masked full scan (every chunk visited, products kept on events) and the
+    expanded group entry states (read by group, not through the map) give the
+    default path's bits.
 """
 import numpy as np
 import pytest
@@ -44,6 +47,23 @@ def test_w_deferred_is_bit_identical(solver, mode):
     o1, s1, _, _ = run(t, mode=mode, mask=mask, solver=solver)
     o2, s2, _, _ = run(t, mode=mode, mask=mask, solver=solver, w_deferred=True)
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("mode", ["sparse", "dense"])
+def test_full_scan_and_expanded_states_are_bit_identical(mode):
+    # the pages' reference paths for the CSR scan (masked full scan) and for compact states with
+    # mapped output (dense group entry states read by group): same results bit for bit, on a
+    # ragged, batched case with an initial state
+    x = gdn_synth.make_inputs(2, 1000 + 37, 16, 32, dtype="bf16", seed=94, mask="beta", with_h0=True)
+    t = to_dev(x)
+    mask = t["mask"] if mode == "sparse" else None
+    o0, s0, _, _ = run(t, mode=mode, mask=mask)
+    for kw in ({"scan_full": True}, {"states_expanded": True}, {"scan_full": True, "states_expanded": True}):
+        o1, s1, _, _ = run(t, mode=mode, mask=mask, **kw)
+        assert torch.equal(o0, o1) and torch.equal(s0, s1), kw
+    ref = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=x.mask if mode == "sparse" else None, h0=x.h0)
+    assert_close({"o": o0.float().cpu().numpy().astype(np.float64), "s_final": s0.cpu().numpy().astype(np.float64)},
+                 ref, "bf16", f"{mode} default")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
