@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' timings")
+    ap.add_argument("--shard", choices=["pairs", "sequences"], default="pairs",
+                    help="with several ranks: split the layer's head pairs over the ranks (tensor "
+                         "parallelism, strong scaling) or give each rank its own sequence (weak scaling)")
     return ap.parse_args()
 
 
@@ -414,13 +417,22 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    x = gdn_synth.make_workload(args.workload, batch_index=rank_batch_index(rank))
-    tok = x.B * x.T
+    pair_shard = world > 1 and args.shard == "pairs"
+    x = gdn_synth.make_workload(args.workload, batch_index=0 if pair_shard else rank_batch_index(rank))
+    tok = x.B * x.T  # tokens of this rank's layer (with pair sharding: the layer all ranks share)
+    if pair_shard:  # this rank's block of head pairs (gated_delta_rule_16_gb300.sharded.pair_block)
+        from gated_delta_rule_16_gb300.sharded import pair_block
+        p0, p1 = pair_block(rank, world, x.Nq)
+        x.q, x.k = x.q[:, :, p0:p1], x.k[:, :, p0:p1]
+        x.v, x.beta, x.g = x.v[:, :, 2 * p0:2 * p1], x.beta[:, :, 2 * p0:2 * p1], x.g[:, :, 2 * p0:2 * p1]
+        x.mask = x.mask[:, p0:p1]
+        x.Nq, x.Nv = p1 - p0, 2 * (p1 - p0)
     st = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+    c = np.ascontiguousarray
     host = {
-        "q": torch.from_numpy(x.q).to(st).pin_memory(), "k": torch.from_numpy(x.k).to(st).pin_memory(),
-        "v": torch.from_numpy(x.v).to(st).pin_memory(), "beta": torch.from_numpy(x.beta).pin_memory(),
-        "g": torch.from_numpy(x.g).pin_memory(), "mask": torch.from_numpy(x.mask).pin_memory(),
+        "q": torch.from_numpy(c(x.q)).to(st).pin_memory(), "k": torch.from_numpy(c(x.k)).to(st).pin_memory(),
+        "v": torch.from_numpy(c(x.v)).to(st).pin_memory(), "beta": torch.from_numpy(c(x.beta)).pin_memory(),
+        "g": torch.from_numpy(c(x.g)).pin_memory(), "mask": torch.from_numpy(c(x.mask)).pin_memory(),
     }
     d_in = {n: t.to(dev) for n, t in host.items()}
     o = torch.empty((x.B, x.T, x.Nv, x.dv), dtype=st, device=dev)
@@ -464,7 +476,9 @@ def run_ours(args):
     gdn.gdn_profile_enable(False)
     n_launch = count_launches(gdn, step, args.steps)
     ms = reduce_step_ms(ev0.elapsed_time(ev1) / args.steps, world, dev)
-    value = job_throughput(tok, world, ms)
+    # with pair sharding the ranks share one layer: its tokens over the slowest rank's time
+    ranks_tokens = 1 if pair_shard else world
+    value = job_throughput(tok, ranks_tokens, ms)
 
     # end to end through the C ABI with host buffers (gdn_prefill_host): each step copies its
     # inputs from pinned host memory, runs the prefill and copies O and S_final back.  Serial:
@@ -527,7 +541,7 @@ def run_ours(args):
     del o, s_final
     ws = None
     torch.cuda.empty_cache()
-    configs = {} if args.no_configs else other_configs(gdn, gdn_synth, args, world, dev, stream, rank)
+    configs = {} if args.no_configs or world > 1 else other_configs(gdn, gdn_synth, args, world, dev, stream, rank)
 
     peak, peak_kind = peaks()
     per_stage = {k: v / max(nrec, 1) for k, v in stage_ms.items()}
@@ -546,15 +560,18 @@ def run_ours(args):
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "strong" if pair_shard else "weak",
         "vs_baseline": None, "dtype": x.dtype, "data": "synthetic",
         "config": {"workload": args.workload, "B": x.B, "T": x.T, "Nq": x.Nq, "Nv": x.Nv, "d": x.d, "dv": x.dv,
                    "retention": round(x.retention(), 4), "events": n_events, "snapshots": n_snap,
                    "solver": "block_adj",
                    "l2": "inputs larger than L2 (%.0f MB compulsory bytes per step), no flush" % (step_bytes / 1e6),
-                   "parallelism": "one independent sequence per GPU" if world > 1 else "single GPU"},
+                   "parallelism": (f"head pairs split over {world} GPUs (tensor parallel, no collective with a "
+                                   f"given mask)" if pair_shard else
+                                   "one independent sequence per GPU" if world > 1 else "single GPU")},
         "clocks": clk,
-        "e2e": {"value": job_throughput(tok, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(tok, ranks_tokens, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": "gdn_prefill_host (C ABI, host buffers)",
                 "pipelining": "2 streams x 2 workspaces", "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": n_launch,

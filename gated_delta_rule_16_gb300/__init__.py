@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     gdn_profile_enable,
     gdn_profile_read,
     gdn_select_events,
+    gdn_select_events_gamma,
     gdn_select_events_scored,
     gdn_selftest_wait_timeout,
     gdn_version,

@@ -26,7 +26,8 @@ EXPORTS = ("gdn_workspace_bytes", "gdn_select_events", "gdn_events_status", "gdn
            "gdn_profile_enable", "gdn_profile_read", "gdn_prefill_sparse_noalloc", "gdn_selftest_wait_timeout",
            "gdn_prefill_sparse_online", "gdn_select_events_scored", "gdn_select_scored_workspace_bytes",
            "gdn_prefill_host", "gdn_prefill_host_workspace_bytes", "gdn_decode_step", "gdn_prefill_ex",
-           "gdn_workspace_bytes_ex", "gdn_events_bytes", "gdn_events_carve", "gdn_noalloc_status")
+           "gdn_workspace_bytes_ex", "gdn_events_bytes", "gdn_events_carve", "gdn_noalloc_status",
+           "gdn_select_events_gamma")
 STAGES = ("select", "prefix", "intra", "wbuild", "scan_runs", "scan_chain", "scan", "output", "selector")
 
 
@@ -43,7 +44,8 @@ class GdnShape(ctypes.Structure):
 
 class GdnOptions(ctypes.Structure):
     _fields_ = [("tail_window", ctypes.c_int32), ("w_deferred", ctypes.c_int32), ("scan_runs", ctypes.c_int32),
-                ("scan_full", ctypes.c_int32), ("states_expanded", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("scan_full", ctypes.c_int32), ("states_expanded", ctypes.c_int32), ("online_split", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 MODES = {"dense": 0, "sparse": 1, "online": 2}
@@ -92,6 +94,8 @@ def load(path: str | None = None):
             lib.gdn_prefill_sparse_online.restype = i32
             lib.gdn_select_events_scored.argtypes = [shp, vp, vp, vp, vp, vp, vp, sz, vp]
             lib.gdn_select_events_scored.restype = i32
+            lib.gdn_select_events_gamma.argtypes = [shp, vp, vp, vp, vp, vp, vp, sz, vp]
+            lib.gdn_select_events_gamma.restype = i32
             lib.gdn_select_scored_workspace_bytes.argtypes = [shp]
             lib.gdn_select_scored_workspace_bytes.restype = sz
             lib.gdn_prefill_ex.argtypes = [shp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.POINTER(GdnOptions),
@@ -340,6 +344,31 @@ def gdn_select_events_scored(score: torch.Tensor, g: torch.Tensor, eta=None, *, 
     return mask_out, tier_out
 
 
+def gdn_select_events_gamma(score: torch.Tensor, gamma: torch.Tensor, eta=None, *, mask_out=None, tier_out=None,
+                            workspace=None, stream=None):
+    """Online selection from Tail-16 scores [B,32,C] and chunk gate tails gamma [B,32,C]
+    (g at each chunk's last token); returns (mask, tier)."""
+    _need(score, "score", torch.float32)
+    B, Nv, C = score.shape
+    _need(gamma, "gamma", torch.float32, (B, Nv, C))
+    _need(eta, "eta", torch.float32, (B, Nv))
+    dev = score.device
+    if mask_out is None:
+        mask_out = torch.empty((B, Nv // 2, C), dtype=torch.uint8, device=dev)
+    if tier_out is None:
+        tier_out = torch.empty((B, Nv // 2), dtype=torch.int32, device=dev)
+    _need(mask_out, "mask_out", torch.uint8, (B, Nv // 2, C))
+    _need(tier_out, "tier_out", torch.int32, (B, Nv // 2))
+    shape = GdnShape(B, C * 64, Nv // 2, Nv, 128, 128, GDN_BF16)
+    lib = load()
+    ws = _workspace(workspace, int(lib.gdn_select_scored_workspace_bytes(ctypes.byref(shape))), dev)
+    with torch.cuda.device(dev):
+        _check("gdn_select_events_gamma", lib.gdn_select_events_gamma(
+            ctypes.byref(shape), _ptr(score), _ptr(gamma), _ptr(eta), _ptr(mask_out), _ptr(tier_out), _ptr(ws),
+            ws.numel(), _stream(stream)))
+    return mask_out, tier_out
+
+
 def _need_host(t, name, dtype=None, shape=None):
     if t is None:
         return
@@ -390,7 +419,7 @@ def gdn_prefill_host(q, k, v, beta, g, mask=None, *, h0=None, solver="block_adj"
 
 def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=None, solver="block_adj",
                    tail_window=0, w_deferred=False, scan_runs=False, scan_full=False, states_expanded=False,
-                   o=None, s_final=None, score=None, mask_out=None,
+                   online_split=0, o=None, s_final=None, score=None, mask_out=None,
                    tier_out=None, workspace=None, stream=None):
     """The general prefill with execution variants; returns (o, s_final, mask_out, tier_out)."""
     B, T, Nq, d = q.shape
@@ -409,7 +438,7 @@ def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=N
         o = torch.empty((B, T, Nv, dv), dtype=q.dtype, device=dev)
     if s_final is None:
         s_final = torch.empty((B, Nv, d, dv), dtype=torch.float32, device=dev)
-    if mode == "online":
+    if mode == "online" and not online_split:
         if mask_out is None:
             mask_out = torch.empty((B, Nq, C), dtype=torch.uint8, device=dev)
         if tier_out is None:
@@ -417,7 +446,7 @@ def gdn_prefill_ex(q, k, v, beta, g, *, mode="sparse", mask=None, h0=None, eta=N
     _need(score, "score", torch.float32, (B, Nv, C))
     shape = shape_of(q, v)
     opt = GdnOptions(int(tail_window), int(bool(w_deferred)), int(bool(scan_runs)), int(bool(scan_full)),
-                     int(bool(states_expanded)))
+                     int(bool(states_expanded)), int(online_split))
     nbytes = int(load().gdn_workspace_bytes_ex(ctypes.byref(shape), SOLVERS[solver], MODES[mode], ctypes.byref(opt)))
     if nbytes == 0:
         raise GdnError("gdn_workspace_bytes_ex", 2, "invalid shape or options")

@@ -206,11 +206,12 @@ gdn_status check_options(const gdn_options *opt) {
     if (opt->scan_runs != 0 && opt->scan_runs != 1) return GDN_ERR_UNSUPPORTED;
     if (opt->scan_full != 0 && opt->scan_full != 1) return GDN_ERR_UNSUPPORTED;
     if (opt->states_expanded != 0 && opt->states_expanded != 1) return GDN_ERR_UNSUPPORTED;
+    if (opt->online_split < 0 || opt->online_split > 2) return GDN_ERR_UNSUPPORTED;
     // the masked full scan and the expanded states are variants of the one-pass scan
     if ((opt->scan_full || opt->states_expanded) && opt->scan_runs) return GDN_ERR_UNSUPPORTED;
     // the masked full scan reads W of every chunk, built in the intra step from a mask known up front
     if (opt->scan_full && opt->w_deferred) return GDN_ERR_UNSUPPORTED;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 2; ++i)
         if (opt->reserved[i] != 0) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
@@ -224,7 +225,12 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     if (st != GDN_OK) return st;
     if ((st = check_options(opt)) != GDN_OK) return st;
     if (solver != GDN_SOLVER_EXACT && solver != GDN_SOLVER_BLOCK_ADJ) return GDN_ERR_DTYPE;
-    if (mode == kOnline && shape->Nv != 32) return GDN_ERR_UNSUPPORTED;  // the tier table is for 16 pairs
+    const int split = opt ? opt->online_split : 0;  // online selection in two calls (sharded head pairs)
+    if (split && mode != kOnline) return GDN_ERR_UNSUPPORTED;
+    // the tier table is for 16 pairs (a split call selects nothing itself)
+    if (mode == kOnline && !split && shape->Nv != 32) return GDN_ERR_UNSUPPORTED;
+    if (split == 1 && shape->B > 0 && shape->T > 0 && !score) return GDN_ERR_NULL;
+    if (split == 2 && shape->B > 0 && shape->T > 0 && !mask) return GDN_ERR_NULL;
     if (opt && (opt->scan_full || opt->states_expanded) && shape->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
     if (opt && opt->scan_full && mode == kOnline) return GDN_ERR_UNSUPPORTED;
     const bool has_tokens = shape->B > 0 && shape->T > 0;
@@ -252,7 +258,9 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     Workspace ws;
     workspace_layout(pb, workspace, &ws);
     pb.score = score;
-    if (mode == kOnline) {
+    if (mode == kOnline && split == 2) {
+        pb.mask = mask;  // the rank's rows of a selection over all ranks' pairs
+    } else if (mode == kOnline) {
         if (!pb.score) pb.score = ws.sel_score;
         if (!mask_out) mask_out = ws.sel_mask;
         pb.mask = mask_out;
@@ -286,7 +294,13 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     };
     auto none = [] { return cudaSuccess; };
     // the status word collects every kernel's bits (timeouts, capacity overflows) for this prefill
-    if (cudaMemsetAsync(ws.counts + 2, 0, sizeof(int32_t), pb.stream) != cudaSuccess) return GDN_ERR_CUDA;
+    // (a second online_split call adds its bits to the first one's)
+    if (split != 2 && cudaMemsetAsync(ws.counts + 2, 0, sizeof(int32_t), pb.stream) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (split == 1) {  // the intra step and its scores only
+        stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
     const bool runs = pb.need_runs != 0;
     // row classes on concurrent streams (bf16 one-pass scan; not while profiling, whose stage
     // events need one stream, nor for a caller that asked for a single stream)
@@ -302,9 +316,11 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
         // [intra (given mask) ->] scan -> output
         const bool intra_split = mode != kOnline && !w_deferred;
         if (mode == kOnline) {
-            stage(2, 1, [&] { return launch_intra_tc(pb, ws, true); });
-            stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
-            stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, true, true); });
+            if (!split) {
+                stage(2, 1, [&] { return launch_intra_tc(pb, ws, true); });
+                stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
+            }
+            stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, !split, true); });
             stage(1, 1, [&] { return launch_prefix(pb, ws); });
             stage(3, 1, [&] { return launch_wbuild_tc(pb, ws); });
         } else {
@@ -341,9 +357,12 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
     }
     if (mode == kOnline) {
         // intra first (its Tail-16 scores drive the selection), then the rest of the pipeline
-        stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
-        stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
-        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, pb.need_runs ? ws.run_first : nullptr, true, true); });
+        // (a second online_split call starts after both, with the caller's mask)
+        if (!split) {
+            stage(2, 1, [&] { return tc ? launch_intra_tc(pb, ws, true) : launch_intra(pb, ws); });
+            stage(8, 2, [&] { return launch_selector(pb, pb.score, eta, mask_out, tier_out, ws.sel_ws); });
+        }
+        stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, pb.need_runs ? ws.run_first : nullptr, !split, true); });
         stage(1, 1, [&] { return launch_prefix(pb, ws); });
         stage(3, 1, [&] { return tc ? launch_wbuild_tc(pb, ws) : launch_wbuild(pb, ws); });
     } else {
@@ -584,7 +603,8 @@ gdn_status gdn_prefill_ex(const gdn_shape *shape, gdn_mode mode, const void *q, 
     if (mode != GDN_MODE_DENSE && mode != GDN_MODE_SPARSE && mode != GDN_MODE_ONLINE) return GDN_ERR_UNSUPPORTED;
     if (mode == GDN_MODE_SPARSE && shape && shape->B > 0 && shape->T > 0 && !mask) return GDN_ERR_NULL;
     const PrefillMode m = mode == GDN_MODE_DENSE ? kDense : (mode == GDN_MODE_SPARSE ? kSparse : kOnline);
-    return run_prefill(shape, q, k, v, beta, g, h0, m == kSparse ? mask : nullptr, eta, m, solver, o, s_final, score,
+    const bool takes_mask = m == kSparse || (m == kOnline && opt && opt->online_split == 2);
+    return run_prefill(shape, q, k, v, beta, g, h0, takes_mask ? mask : nullptr, eta, m, solver, o, s_final, score,
                        mask_out, tier_out, workspace, workspace_bytes, stream, opt);
 }
 
@@ -596,17 +616,19 @@ gdn_status gdn_prefill_sparse_online(const gdn_shape *shape, const void *q, cons
                        tier_out, workspace, workspace_bytes, stream);
 }
 
-gdn_status gdn_select_events_scored(const gdn_shape *shape, const float *score, const float *g, const float *eta,
-                                    uint8_t *mask_out, int32_t *tier_out, void *workspace, size_t workspace_bytes,
-                                    void *stream) {
+namespace {
+// The online selection on its own: gates either per token (g) or per chunk (gamma).
+gdn_status select_scored(const gdn_shape *shape, const float *score, const float *g, const float *gamma,
+                         const float *eta, uint8_t *mask_out, int32_t *tier_out, void *workspace,
+                         size_t workspace_bytes, void *stream) {
     gdn_status st = check_shape(shape);
     if (st != GDN_OK) return st;
     if (shape->Nv != 32) return GDN_ERR_UNSUPPORTED;
     Problem pb;
     fill_problem(shape, GDN_SOLVER_BLOCK_ADJ, &pb);
     if (pb.B == 0 || pb.C == 0) return GDN_OK;
-    if (!score || !g || !mask_out || !workspace) return GDN_ERR_NULL;
-    const void *ptrs[] = {score, g, eta, tier_out};
+    if (!score || !(g || gamma) || !mask_out || !workspace) return GDN_ERR_NULL;
+    const void *ptrs[] = {score, g, gamma, eta, tier_out};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return GDN_ERR_ALIGN;
     if (((uintptr_t)workspace % kAlign) != 0) return GDN_ERR_ALIGN;
@@ -614,8 +636,23 @@ gdn_status gdn_select_events_scored(const gdn_shape *shape, const float *score, 
     if (!device_ok()) return GDN_ERR_DEVICE;
     pb.g = g;
     pb.stream = (cudaStream_t)stream;
-    const cudaError_t e = launch_selector(pb, score, eta, mask_out, tier_out, workspace);
+    const cudaError_t e = launch_selector(pb, score, eta, mask_out, tier_out, workspace, gamma);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+}  // namespace
+
+gdn_status gdn_select_events_scored(const gdn_shape *shape, const float *score, const float *g, const float *eta,
+                                    uint8_t *mask_out, int32_t *tier_out, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (!g && shape && shape->B > 0 && shape->T > 0) return GDN_ERR_NULL;
+    return select_scored(shape, score, g, nullptr, eta, mask_out, tier_out, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_select_events_gamma(const gdn_shape *shape, const float *score, const float *gamma, const float *eta,
+                                   uint8_t *mask_out, int32_t *tier_out, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    if (!gamma && shape && shape->B > 0 && shape->T > 0) return GDN_ERR_NULL;
+    return select_scored(shape, score, nullptr, gamma, eta, mask_out, tier_out, workspace, workspace_bytes, stream);
 }
 
 size_t gdn_select_scored_workspace_bytes(const gdn_shape *shape) {

@@ -159,7 +159,8 @@ cudaError_t launch_wbuild_tc(const Problem &pb, const Workspace &ws);
 // Online selection (Eqs. 10-14) for 16 head pairs: score [B,32,C] -> mask [B,16,C],
 // tier_out [B,16] (may be NULL); ws holds selector_workspace_bytes(B, C).
 size_t selector_workspace_bytes(int B, int C);
+// gamma [B,Nv,C] (may be NULL: read from pb.g at each chunk's last token)
 cudaError_t launch_selector(const Problem &pb, const float *score, const float *eta, uint8_t *mask,
-                            int32_t *tier_out, void *ws);
+                            int32_t *tier_out, void *ws, const float *gamma = nullptr);
 
 }  // namespace gdn

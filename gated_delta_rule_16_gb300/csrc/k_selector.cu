@@ -87,8 +87,9 @@ __device__ __forceinline__ int tier_size(int l, int C) {
 // sum the gains of the upgrades L -> M and M -> H.  Writes rank[c] (-1 for the
 // anchors) and gains[2] = {gain_LM, gain_MH}.
 __global__ void __launch_bounds__(kThreads)
-selector_pair_kernel(const float *__restrict__ score, const float *__restrict__ g, const float *__restrict__ eta,
-                     int T_, int Nv, int C, int npow2, int32_t *__restrict__ rank_ws, double *__restrict__ gains) {
+selector_pair_kernel(const float *__restrict__ score, const float *__restrict__ g, const float *__restrict__ gamma,
+                     const float *__restrict__ eta, int T_, int Nv, int C, int npow2, int32_t *__restrict__ rank_ws,
+                     double *__restrict__ gains) {
     extern __shared__ unsigned long long keys[];  // [npow2]
     __shared__ float norm[2];
     __shared__ double L[2], G[2], rr[2], red[kThreads / 32], red2[kThreads / 32];
@@ -109,8 +110,9 @@ selector_pair_kernel(const float *__restrict__ score, const float *__restrict__ 
     // r_h: mean of 2^gamma over the last min(16, C) chunks
     const int c0 = C > 16 ? C - 16 : 0;
     double e2 = 0.0;
-    if (ht < C - c0)  // gamma of chunk c0 + ht: g at its last token (a partial last chunk ends at T - 1)
-        e2 = exp2((double)g[((int64_t)b * T_ + min((int64_t)(c0 + ht + 1) * kChunk, (int64_t)T_) - 1) * Nv + h]);
+    if (ht < C - c0)  // gamma of chunk c0 + ht: given, or g at its last token (a partial last chunk ends at T - 1)
+        e2 = exp2((double)(gamma ? gamma[((int64_t)b * Nv + h) * C + c0 + ht]
+                                 : g[((int64_t)b * T_ + min((int64_t)(c0 + ht + 1) * kChunk, (int64_t)T_) - 1) * Nv + h]));
     // both half-sums at once: lanes reduce within the warp, warps of a half combine in shared memory
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -302,7 +304,7 @@ size_t selector_workspace_bytes(int B, int C) {
 }
 
 cudaError_t launch_selector(const Problem &pb, const float *score, const float *eta, uint8_t *mask,
-                            int32_t *tier_out, void *ws) {
+                            int32_t *tier_out, void *ws, const float *gamma) {
     if (pb.B == 0 || pb.C == 0) return cudaSuccess;
     int npow2 = 1;
     while (npow2 < (pb.C > 2 ? pb.C - 2 : 1)) npow2 <<= 1;
@@ -311,8 +313,8 @@ cudaError_t launch_selector(const Problem &pb, const float *score, const float *
     if (e != cudaSuccess) return e;
     double *gains = (double *)ws;                                    // [B,16,2]
     int32_t *rank = (int32_t *)(gains + (size_t)pb.B * kPairs * 2);  // [B,16,C]
-    e = launch_kernel(pb.pdl, selector_pair_kernel, dim3(kPairs, pb.B), kThreads, smem, pb.stream, score, pb.g, eta,
-                      pb.T, pb.Nv, pb.C, npow2, rank, gains);
+    e = launch_kernel(pb.pdl, selector_pair_kernel, dim3(kPairs, pb.B), kThreads, smem, pb.stream, score, pb.g, gamma,
+                      eta, pb.T, pb.Nv, pb.C, npow2, rank, gains);
     if (e != cudaSuccess) return e;
     return launch_kernel(pb.pdl_ok, selector_tier_kernel, pb.B, 256, 0, pb.stream, pb.C, (const int32_t *)rank,
                          (const double *)gains, mask, tier_out);

@@ -153,6 +153,19 @@ typedef enum { GDN_MODE_DENSE = 0, GDN_MODE_SPARSE = 1, GDN_MODE_ONLINE = 2 } gd
  *                directly instead of the predecessor's compact snapshot
  *                through the group map.  Identical results bit for bit.  bf16,
  *                one-pass scan.
+ *   online_split online selection in two calls, for head pairs sharded over
+ *                ranks (tensor parallelism: the selection couples a sequence's
+ *                16 pairs, Eq. 14).  Both calls use mode GDN_MODE_ONLINE, the
+ *                rank's own pairs (any number) and the same workspace.
+ *                1: the intra step only; writes `score` (required) and keeps
+ *                U and the C-bar blocks in the workspace.  The caller gathers
+ *                every rank's scores and chunk gate tails gamma (g at each
+ *                chunk's last token) and selects with
+ *                gdn_select_events_gamma().  2: the rest of the pipeline
+ *                (compaction, deferred W, scan, output) on the workspace of
+ *                call 1, with the rank's rows of that selection in `mask`.
+ *                The two calls compute what one online prefill computes, bit
+ *                for bit.
  *   reserved     must be zero. */
 typedef struct {
     int32_t tail_window;
@@ -160,7 +173,8 @@ typedef struct {
     int32_t scan_runs;
     int32_t scan_full;
     int32_t states_expanded;
-    int32_t reserved[3];
+    int32_t online_split;
+    int32_t reserved[2];
 } gdn_options;
 
 /* Bytes of workspace the prefill entry points need for `shape`: sparse = 0
@@ -212,6 +226,16 @@ GDN_API gdn_status gdn_select_events_scored(const gdn_shape *shape, const float 
                                     const float *eta, uint8_t *mask_out, int32_t *tier_out,
                                     void *workspace, size_t workspace_bytes, void *stream);
 GDN_API size_t gdn_select_scored_workspace_bytes(const gdn_shape *shape);
+
+/* gdn_select_events_scored with the chunk gate tails given directly: gamma
+ * [B,Nv,C] fp32 (gamma[b,h,c] = g at chunk c's last token) instead of g
+ * [B,T,Nv].  For a selection over head pairs gathered from several ranks
+ * (online_split), where each rank holds only its own heads' gates.  Same
+ * results as gdn_select_events_scored on the same values.  shape gives B, C
+ * (through T) and Nv == 32; workspace as gdn_select_scored_workspace_bytes. */
+GDN_API gdn_status gdn_select_events_gamma(const gdn_shape *shape, const float *score, const float *gamma,
+                                           const float *eta, uint8_t *mask_out, int32_t *tier_out,
+                                           void *workspace, size_t workspace_bytes, void *stream);
 
 /* Synchronises `stream` and reports the status bits of an events struct. */
 GDN_API gdn_status gdn_events_status(const gdn_events *events, void *stream);

@@ -190,7 +190,7 @@ def test_prefill_ex_option_validation(lib):
     assert ex(opt=bnd.GdnOptions(12)) == 6                 # tail window must be 8, 16, 32 or 64
     assert ex(opt=bnd.GdnOptions(16, 2)) == 6              # w_deferred is 0 or 1
     r = bnd.GdnOptions(16, 0)
-    r.reserved[2] = 1
+    r.reserved[1] = 1
     assert ex(opt=r) == 6                                  # reserved fields must be zero
     O = lambda **kw: bnd.GdnOptions(kw.get("tw", 0), kw.get("wd", 0), kw.get("runs", 0), kw.get("full", 0),
                                     kw.get("exp", 0))
@@ -200,6 +200,11 @@ def test_prefill_ex_option_validation(lib):
     assert ex(mode=2, opt=O(full=1)) == 6                  # not with online selection
     assert ex(opt=O(full=2)) == 6 and ex(opt=O(exp=3)) == 6
     assert ex(opt=O(full=1, exp=1)) == 8                   # valid together: stops at the device check here
+    split = lambda v: bnd.GdnOptions(0, 0, 0, 0, 0, v)
+    assert ex(opt=split(1)) == 6                           # two-call online selection: mode online only
+    assert ex(mode=2, opt=split(3)) == 6
+    assert ex(mode=2, opt=split(2), mask=0) == 1           # the second call takes the rank's mask
+    assert ex(mode=2, opt=split(1)) == 1                   # the first call writes the scores (score=NULL here)
     assert ex(mode=7) == 6
     assert ex(mask=0) == 1                                 # sparse mode needs a mask
     assert ex(opt=bnd.GdnOptions(64, 1)) == 8              # valid: stops at the device check here

@@ -172,3 +172,32 @@ def test_online_prefill_ragged_T():
     check_selection(x, res)
     ref = oracle.prefill(x.q, x.k, x.v, x.beta, x.g, mask=res["mask"], solver=oracle.SOLVER_BLOCK_ADJ)
     assert_close(res, ref, "bf16", "online ragged T")
+
+
+@pytest.mark.parametrize("world", [1, 2, 4])
+def test_online_selection_split_over_pair_blocks(world):
+    # online selection in two calls per rank (gated_delta_rule_16_gb300.sharded with the library as
+    # backend), the ranks emulated one after the other on this GPU (no kernel waits for another
+    # rank's): gathered scores and gate tails, one selection, each rank's block finished with its
+    # mask rows.  Equal, bit for bit, to the one-call online prefill of the whole layer.
+    from gated_delta_rule_16_gb300 import sharded
+    x = gdn_synth.make_inputs(2, 23 * 64 + 5, 16, 32, dtype="bf16", seed=45, mask="ones", with_h0=True)
+    t = to_dev(x)
+    eta = torch.from_numpy(np.abs(np.random.default_rng(45).standard_normal((2, 32))).astype(np.float32)).to(dev())
+    o_ref, s_ref, m_ref, tier_ref = gdn.gdn_prefill_sparse_online(t["q"], t["k"], t["v"], t["beta"], t["g"],
+                                                                  h0=t["h0"], eta=eta)
+    full = {"q": t["q"], "k": t["k"], "v": t["v"], "beta": t["beta"], "g": t["g"], "h0": t["h0"], "eta": eta}
+    be = sharded.CudaBackend()
+    xs = [sharded.shard(full, r, world) for r in range(world)]
+    first = [be.scores(xr) for xr in xs]
+    score_all = torch.cat([f[0] for f in first], dim=1)
+    gamma_all = torch.cat([sharded.chunk_gamma(xr["g"]) for xr in xs], dim=1)
+    mask_all, tier_all = be.select(score_all, gamma_all, eta)
+    outs = []
+    for r, xr in enumerate(xs):
+        p0, p1 = sharded.pair_block(r, world, 16)
+        outs.append(be.finish(xr, first[r][1], mask_all[:, p0:p1]))
+    torch.cuda.synchronize()
+    assert torch.equal(mask_all, m_ref) and torch.equal(tier_all, tier_ref)
+    assert torch.equal(torch.cat([o for o, _ in outs], dim=2), o_ref)
+    assert torch.equal(torch.cat([s for _, s in outs], dim=1), s_ref)

@@ -1,9 +1,10 @@
 """Multi-rank host logic of the benchmark on CPU (gloo, world size 2).
 
-The core shards by sequence with no collective on the data path: each rank
-runs its own independent sequence, and only the step time is reduced (max
-over ranks) to form the whole-job throughput.  This runs that reduction and
-the rank -> sequence assignment in two real gloo processes.
+With --shard sequences each rank runs its own independent sequence; with
+--shard pairs (tests/test_sharded.py covers the split itself) the ranks share
+one layer's head pairs.  Either way only the step time is reduced (max over
+ranks) to form the whole-job throughput.  This runs that reduction and the
+rank -> sequence assignment in two real gloo processes.
 """
 import os
 import socket
