@@ -164,7 +164,7 @@ constexpr int kClasses = 4;
 struct ClassStreams {
     bool tried = false, ok = false;
     cudaStream_t s[kClasses - 1];  // classes 0 .. 2 (the last class runs on the caller's stream)
-    cudaEvent_t fork, join[kClasses - 1];
+    cudaEvent_t fork, prefix_done, join[kClasses - 1];
 };
 ClassStreams g_class_streams[64];
 std::mutex g_class_mutex;
@@ -177,7 +177,8 @@ ClassStreams *class_streams() {  // under g_class_mutex; nullptr if they cannot 
         cs.tried = true;
         int least = 0, greatest = 0;
         cudaDeviceGetStreamPriorityRange(&least, &greatest);
-        bool ok = cudaEventCreateWithFlags(&cs.fork, cudaEventDisableTiming) == cudaSuccess;
+        bool ok = cudaEventCreateWithFlags(&cs.fork, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&cs.prefix_done, cudaEventDisableTiming) == cudaSuccess;
         for (int c = 0; ok && c < kClasses - 1; ++c) {
             const int prio = greatest + c < least ? greatest + c : least;  // class 0 first
             ok = cudaStreamCreateWithPriority(&cs.s[c], cudaStreamNonBlocking, prio) == cudaSuccess &&
@@ -325,15 +326,21 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
             stage(3, 1, [&] { return launch_wbuild_tc(pb, ws); });
         } else {
             stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, false, true); });
-            stage(1, 1, [&] { return launch_prefix(pb, ws); });
             if (!intra_split) {
+                stage(1, 1, [&] { return launch_prefix(pb, ws); });
                 stage(2, 1, [&] { return launch_intra_tc(pb, ws, true); });
                 stage(3, 1, [&] { return launch_wbuild_tc(pb, ws); });
             }
         }
         int bound[kClasses + 1];
         const int ncls = class_bounds(pb.R, bound);
+        // the classes' intra steps need only the CSR rows: they fork after the compaction, and the
+        // prefix (P and the group table, for the scans and outputs) runs beside them
         if (e == cudaSuccess) e = cudaEventRecord(cs->fork, pb.stream);
+        if (intra_split) {
+            stage(1, 1, [&] { return launch_prefix(pb, ws); });
+            if (e == cudaSuccess) e = cudaEventRecord(cs->prefix_done, pb.stream);
+        }
         for (int c = 0; c < ncls && e == cudaSuccess; ++c) {
             Problem q = pb;
             q.row_pair = ws.row_pair;
@@ -347,6 +354,7 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
             // classes' kernels need.  (The first kernel of a class also reads the CSR rows.)
             q.pdl = 0;
             if (e == cudaSuccess && intra_split) e = launch_intra_tc(q, ws, false);
+            if (e == cudaSuccess && intra_split && !last) e = cudaStreamWaitEvent(q.stream, cs->prefix_done, 0);
             if (e == cudaSuccess) e = launch_scan_warp(q, ws);
             if (e == cudaSuccess) e = launch_output_tc(q, ws);
             if (counting) g_prof.launches += intra_split ? 3 : 2;
