@@ -7,9 +7,10 @@
 // of a pair are adjacent CTAs (the second read of their K tile comes from L2).
 //   Gram  G = K K^T [128 x 128]        (A = B = the K tile, K-major, by TMA)
 //   A_Delta[t,s] = beta_t G[t,s] 2^(g_t - g_s), s < t in the same chunk; M = I + A_Delta
-//   C = M^-1 (exact) or the block-adjacent approximation (Eq. 7), fp32 on CUDA cores
-//       over compact 16x16 blocks: C_ii = M_ii^-1 (forward substitution),
-//       C_ij = -C_ii sum_{k=j}^{i-1} M_ik C_kj
+//   C = M^-1 (exact) or the block-adjacent approximation (Eq. 7), fp32 over compact
+//       16x16 blocks: C_ii = M_ii^-1 (forward substitution on CUDA cores),
+//       C_ij = -C_ii sum_{k=j}^{i-1} M_ik C_kj (the block-adjacent solver's two products
+//       per block on the warps' tensor cores in three-pass tf32, nearly fp32 accuracy)
 //   U = C diag(beta) V                  (A: C diag(beta) bf16, block-diagonal over the
 //                                        two chunks, K-major; B: V [tok][dv] MN-major by TMA)
 //   s = ||U[48:64,:]||_F (Tail-16 write score)
@@ -164,45 +165,73 @@ __device__ __forceinline__ void offdiag_level(float *F, int tid) {
 }
 
 // Block-adjacent solver's below-diagonal blocks, one warp per block (warps 0..5: chunk w / 3,
-// block column jb = w % 3, row ib = jb + 1): T = M_{ib,jb} C_{jb,jb}, then C_{ib,jb} = -C_{ib,ib} T.
-// Lane (row rr = lane / 2, columns 8 (lane % 2) .. +7); T goes over M's block (each row of it is read
-// only by the two lanes of that row), so the warp needs no block-wide barrier between the products.
-// The sums run over k in the same order as offdiag_level's.
+// block column jb = w % 3, row ib = jb + 1): T = M_{ib,jb} C_{jb,jb}, then C_{ib,jb} = -C_{ib,ib} T,
+// each a 16x16x16 product on the warp's tensor cores (mma m16n8k8 in tf32, fp32 accumulation).
+// Every factor is split into a tf32 head and a tf32 tail (x = hi + lo up to about 2^-22 |x|) and a
+// product takes the three terms lo*hi, hi*lo, hi*hi (the dropped lo*lo is about 2^-22 of it), so it
+// carries nearly fp32 accuracy.  Lane (g = lane / 4,
+// q = lane % 4) holds A[g][q], A[g+8][q], A[g][q+4], A[g+8][q+4] of each 16x8 A slice, B[q][n], B[q+4][n]
+// (n = g) of each 8x8 B slice and D[g][2q], D[g][2q+1], D[g+8][2q], D[g+8][2q+1] of each 16x8 result.
+// T goes over M's block (only this warp reads it) between the two products.
+__device__ __forceinline__ uint32_t tf32_hi(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D[16 x 16] = A[16 x 16] B[16 x 16], both read from solver blocks (row stride BS).
+__device__ __forceinline__ void prod16_3xtf32(const float *A, const float *B, int lane, float (&d)[2][4]) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn) d[nn][0] = d[nn][1] = d[nn][2] = d[nn][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 16; kk += 8) {
+        const float av[4] = {A[g * BS + kk + q], A[(g + 8) * BS + kk + q], A[g * BS + kk + q + 4],
+                             A[(g + 8) * BS + kk + q + 4]};
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ah[e] = tf32_hi(av[e]);
+            al[e] = tf32_hi(av[e] - __uint_as_float(ah[e]));
+        }
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn) {
+            const float b0 = B[(kk + q) * BS + nn * 8 + g], b1 = B[(kk + q + 4) * BS + nn * 8 + g];
+            const uint32_t bh0 = tf32_hi(b0), bh1 = tf32_hi(b1);
+            const uint32_t bl0 = tf32_hi(b0 - __uint_as_float(bh0)), bl1 = tf32_hi(b1 - __uint_as_float(bh1));
+            mma_tf32(d[nn], al, bh0, bh1);
+            mma_tf32(d[nn], ah, bl0, bl1);
+            mma_tf32(d[nn], ah, bh0, bh1);
+        }
+    }
+}
 __device__ __forceinline__ void offdiag_adjacent_warp(float *F, int warp, int lane) {
     if (warp >= 6) return;
     const int cc = warp / 3, jb = warp % 3, ib = jb + 1;
-    const int rr = lane >> 1, c8 = (lane & 1) * 8;
+    const int g = lane >> 2, q = lane & 3;
     float *Mb = blk_m(F, cc, ib, jb);
     const float *Cj = blk_diag(F, cc, jb), *Ci = blk_diag(F, cc, ib);
-    float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0;
+    float d[2][4];
+    prod16_3xtf32(Mb, Cj, lane, d);
+    __syncwarp();  // every lane has read M's block
 #pragma unroll
-    for (int k4 = 0; k4 < kBlk; k4 += 4) {
-        const float4 m = ld4(Mb + rr * BS + k4);
-        const float mv[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            fma4(t0, mv[q], ld4(Cj + (k4 + q) * BS + c8));
-            fma4(t1, mv[q], ld4(Cj + (k4 + q) * BS + c8 + 4));
-        }
+    for (int nn = 0; nn < 2; ++nn) {
+        *reinterpret_cast<float2 *>(Mb + g * BS + nn * 8 + 2 * q) = make_float2(d[nn][0], d[nn][1]);
+        *reinterpret_cast<float2 *>(Mb + (g + 8) * BS + nn * 8 + 2 * q) = make_float2(d[nn][2], d[nn][3]);
     }
-    __syncwarp();  // every lane has read its M row
-    *reinterpret_cast<float4 *>(Mb + rr * BS + c8) = t0;
-    *reinterpret_cast<float4 *>(Mb + rr * BS + c8 + 4) = t1;
     __syncwarp();  // T complete
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    prod16_3xtf32(Ci, Mb, lane, d);
+    float *Cb = blk_c(F, cc, ib, jb);
 #pragma unroll
-    for (int m4 = 0; m4 < kBlk; m4 += 4) {
-        const float4 c = ld4(Ci + rr * BS + m4);
-        const float cv[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            fma4(a0, cv[q], ld4(Mb + (m4 + q) * BS + c8));
-            fma4(a1, cv[q], ld4(Mb + (m4 + q) * BS + c8 + 4));
-        }
+    for (int nn = 0; nn < 2; ++nn) {
+        *reinterpret_cast<float2 *>(Cb + g * BS + nn * 8 + 2 * q) = make_float2(-d[nn][0], -d[nn][1]);
+        *reinterpret_cast<float2 *>(Cb + (g + 8) * BS + nn * 8 + 2 * q) = make_float2(-d[nn][2], -d[nn][3]);
     }
-    float *Cb = blk_c(F, cc, ib, jb) + rr * BS + c8;
-    *reinterpret_cast<float4 *>(Cb) = make_float4(-a0.x, -a0.y, -a0.z, -a0.w);
-    *reinterpret_cast<float4 *>(Cb + 4) = make_float4(-a1.x, -a1.y, -a1.z, -a1.w);
 }
 
 // One row's 32 operand columns (this thread's half of its chunk) as bf16 into the
