@@ -73,12 +73,6 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
-__device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
-    acc.x += a * b.x;
-    acc.y += a * b.y;
-    acc.z += a * b.z;
-    acc.w += a * b.w;
-}
 
 // Solver block addresses inside the fp32 area F (chunk cc, block row ib, block column jb).
 __device__ __forceinline__ int below(int ib, int jb) { return ib * (ib - 1) / 2 + jb; }
@@ -97,76 +91,9 @@ __device__ __forceinline__ int cbar_index(int ib, int jb) {
     return ib == jb ? ib : (jb + 1 == ib ? 3 + ib : (ib == 2 ? 7 : (jb == 1 ? 8 : 9)));
 }
 
-// Exact solver: below-diagonal blocks at distance OFF of both chunks' C (Eq. 7 generalised),
-// once every block closer to the diagonal is known: T = sum_{k=jb}^{ib-1} M_{ib,k} C_{k,jb}
-// is written into C's block, then replaced by C_{ib,jb} = -C_{ib,ib} T.  Task (chunk, block,
-// row, column quad): 4 outputs from 16-byte shared-memory loads.
-template <int OFF>
-__device__ __forceinline__ void offdiag_level(float *F, int tid) {
-    constexpr int NB = 4 - OFF;
-    constexpr int NT = 2 * NB * 64;
-    constexpr int NU = (NT + kThreads - 1) / kThreads;
-    float4 acc[NU];
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int task = tid + u * kThreads;
-        if (task < NT) {
-            const int cc = task / (NB * 64), rem = task % (NB * 64);
-            const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
-            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kb = 0; kb < OFF; ++kb) {
-                const float *Mr = blk_m(F, cc, ib, jb + kb) + rr * BS;
-                const float *Cc = blk_cc(F, cc, jb + kb, jb) + q4;
-#pragma unroll
-                for (int k4 = 0; k4 < kBlk; k4 += 4) {
-                    const float4 m = ld4(Mr + k4);
-                    fma4(t, m.x, ld4(Cc + (k4 + 0) * BS));
-                    fma4(t, m.y, ld4(Cc + (k4 + 1) * BS));
-                    fma4(t, m.z, ld4(Cc + (k4 + 2) * BS));
-                    fma4(t, m.w, ld4(Cc + (k4 + 3) * BS));
-                }
-            }
-            *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) = t;
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int task = tid + u * kThreads;
-        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (task < NT) {
-            const int cc = task / (NB * 64), rem = task % (NB * 64);
-            const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
-            const float *Cr = blk_diag(F, cc, ib) + rr * BS;
-            const float *Tt = blk_c(F, cc, ib, jb) + q4;
-#pragma unroll
-            for (int m4 = 0; m4 < kBlk; m4 += 4) {
-                const float4 c = ld4(Cr + m4);
-                fma4(acc[u], c.x, ld4(Tt + (m4 + 0) * BS));
-                fma4(acc[u], c.y, ld4(Tt + (m4 + 1) * BS));
-                fma4(acc[u], c.z, ld4(Tt + (m4 + 2) * BS));
-                fma4(acc[u], c.w, ld4(Tt + (m4 + 3) * BS));
-            }
-        }
-    }
-    __syncthreads();  // T is in C's block: every reader is done before C replaces it
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int task = tid + u * kThreads;
-        if (task < NT) {
-            const int cc = task / (NB * 64), rem = task % (NB * 64);
-            const int jb = rem >> 6, ib = jb + OFF, rr = (rem >> 2) & 15, q4 = (rem & 3) * 4;
-            *reinterpret_cast<float4 *>(blk_c(F, cc, ib, jb) + rr * BS + q4) =
-                make_float4(-acc[u].x, -acc[u].y, -acc[u].z, -acc[u].w);
-        }
-    }
-    __syncthreads();
-}
-
-// Block-adjacent solver's below-diagonal blocks, one warp per block (warps 0..5: chunk w / 3,
-// block column jb = w % 3, row ib = jb + 1): T = M_{ib,jb} C_{jb,jb}, then C_{ib,jb} = -C_{ib,ib} T,
-// each a 16x16x16 product on the warp's tensor cores (mma m16n8k8 in tf32, fp32 accumulation).
+// Below-diagonal blocks of C, one warp per block: T = sum_{k=jb}^{ib-1} M_{ib,k} C_{k,jb}, then
+// C_{ib,jb} = -C_{ib,ib} T (Eq. 7; the block-adjacent solver keeps ib = jb + 1 only), each a sum of
+// 16x16x16 products on the warp's tensor cores (mma m16n8k8 in tf32, fp32 accumulation).
 // Every factor is split into a tf32 head and a tf32 tail (x = hi + lo up to about 2^-22 |x|) and a
 // product takes the three terms lo*hi, hi*lo, hi*hi (the dropped lo*lo is about 2^-22 of it), so it
 // carries nearly fp32 accuracy.  Lane (g = lane / 4,
@@ -184,11 +111,9 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// D[16 x 16] = A[16 x 16] B[16 x 16], both read from solver blocks (row stride BS).
+// D[16 x 16] += A[16 x 16] B[16 x 16], both read from solver blocks (row stride BS).
 __device__ __forceinline__ void prod16_3xtf32(const float *A, const float *B, int lane, float (&d)[2][4]) {
     const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int nn = 0; nn < 2; ++nn) d[nn][0] = d[nn][1] = d[nn][2] = d[nn][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 16; kk += 8) {
         const float av[4] = {A[g * BS + kk + q], A[(g + 8) * BS + kk + q], A[g * BS + kk + q + 4],
@@ -210,27 +135,33 @@ __device__ __forceinline__ void prod16_3xtf32(const float *A, const float *B, in
         }
     }
 }
-__device__ __forceinline__ void offdiag_adjacent_warp(float *F, int warp, int lane) {
-    if (warp >= 6) return;
-    const int cc = warp / 3, jb = warp % 3, ib = jb + 1;
-    const int g = lane >> 2, q = lane & 3;
-    float *Mb = blk_m(F, cc, ib, jb);
-    const float *Cj = blk_diag(F, cc, jb), *Ci = blk_diag(F, cc, ib);
-    float d[2][4];
-    prod16_3xtf32(Mb, Cj, lane, d);
-    __syncwarp();  // every lane has read M's block
+// The blocks at distance OFF below the diagonal of both chunks (warp w < 2 (4 - OFF): chunk
+// w / (4 - OFF), block column jb = w % (4 - OFF), row ib = jb + OFF); every block closer to the
+// diagonal is known.  T goes to C's block (only this warp reads it) and C replaces it there.
+template <int OFF>
+__device__ __forceinline__ void offdiag_level(float *F, int warp, int lane) {
+    constexpr int NB = 4 - OFF;
+    if (warp < 2 * NB) {
+        const int cc = warp / NB, jb = warp % NB, ib = jb + OFF;
+        const int g = lane >> 2, q = lane & 3;
+        float d[2][4] = {};
 #pragma unroll
-    for (int nn = 0; nn < 2; ++nn) {
-        *reinterpret_cast<float2 *>(Mb + g * BS + nn * 8 + 2 * q) = make_float2(d[nn][0], d[nn][1]);
-        *reinterpret_cast<float2 *>(Mb + (g + 8) * BS + nn * 8 + 2 * q) = make_float2(d[nn][2], d[nn][3]);
-    }
-    __syncwarp();  // T complete
-    prod16_3xtf32(Ci, Mb, lane, d);
-    float *Cb = blk_c(F, cc, ib, jb);
+        for (int kb = 0; kb < OFF; ++kb) prod16_3xtf32(blk_m(F, cc, ib, jb + kb), blk_cc(F, cc, jb + kb, jb), lane, d);
+        float *Cb = blk_c(F, cc, ib, jb);
 #pragma unroll
-    for (int nn = 0; nn < 2; ++nn) {
-        *reinterpret_cast<float2 *>(Cb + g * BS + nn * 8 + 2 * q) = make_float2(-d[nn][0], -d[nn][1]);
-        *reinterpret_cast<float2 *>(Cb + (g + 8) * BS + nn * 8 + 2 * q) = make_float2(-d[nn][2], -d[nn][3]);
+        for (int nn = 0; nn < 2; ++nn) {
+            *reinterpret_cast<float2 *>(Cb + g * BS + nn * 8 + 2 * q) = make_float2(d[nn][0], d[nn][1]);
+            *reinterpret_cast<float2 *>(Cb + (g + 8) * BS + nn * 8 + 2 * q) = make_float2(d[nn][2], d[nn][3]);
+        }
+        __syncwarp();  // T complete
+        float e[2][4] = {};
+        prod16_3xtf32(blk_diag(F, cc, ib), Cb, lane, e);
+        __syncwarp();  // every lane has read T
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn) {
+            *reinterpret_cast<float2 *>(Cb + g * BS + nn * 8 + 2 * q) = make_float2(-e[nn][0], -e[nn][1]);
+            *reinterpret_cast<float2 *>(Cb + (g + 8) * BS + nn * 8 + 2 * q) = make_float2(-e[nn][2], -e[nn][3]);
+        }
     }
 }
 
@@ -388,12 +319,12 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
         for (int i2 = 0; i2 < kBlk; ++i2) Mb[i2 * BS + j] = x[i2];
     }
     __syncthreads();
+    offdiag_level<1>(F, warp, lane);
+    __syncthreads();
     if (exact) {
-        offdiag_level<1>(F, tid);
-        offdiag_level<2>(F, tid);
-        offdiag_level<3>(F, tid);
-    } else {
-        offdiag_adjacent_warp(F, warp, lane);
+        offdiag_level<2>(F, warp, lane);
+        __syncthreads();
+        offdiag_level<3>(F, warp, lane);
         __syncthreads();
     }
     const bool any_event = ev_s[0] >= 0 || ev_s[1] >= 0;
