@@ -43,10 +43,10 @@ FALLBACK_HBM_GBS = 6800.0
 # traffic is then reported as null).
 PROFILED_TRAFFIC = {
     ("qwen35_4b_layer_T32768_sparse29", "select"): 0.065e6,
-    ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.134e6,
-    ("qwen35_4b_layer_T32768_sparse29", "intra"): 627.2e6,
-    ("qwen35_4b_layer_T32768_sparse29", "scan"): 232.7e6,
-    ("qwen35_4b_layer_T32768_sparse29", "output"): 847.7e6,
+    ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.136e6,
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 626.9e6,
+    ("qwen35_4b_layer_T32768_sparse29", "scan"): 230.9e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 847.8e6,
 }
 
 
