@@ -189,9 +189,12 @@ ClassStreams *class_streams() {  // under g_class_mutex; nullptr if they cannot 
     return cs.ok ? &cs : nullptr;
 }
 
-// Class bounds for R rows: returns the number of non-empty classes.
+// Class bounds for R rows (sorted longest first): returns the number of non-empty classes.  Each
+// class's intra step fills the GPU, so the classes' intra steps run one after another; classes of
+// nearly equal size (3/16, 4/16, 4/16 and 5/16 of the rows) start the longest rows' scan after a
+// short intra step and stagger the other classes' scans and outputs behind it.
 int class_bounds(int R, int *bound) {
-    const int cand[kClasses + 1] = {0, (R + 7) / 8, (R + 3) / 4, (R + 1) / 2, R};
+    const int cand[kClasses + 1] = {0, (3 * R + 15) / 16, (7 * R + 15) / 16, (11 * R + 15) / 16, R};
     int n = 0;
     bound[0] = 0;
     for (int c = 1; c <= kClasses; ++c)
