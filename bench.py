@@ -42,11 +42,11 @@ FALLBACK_HBM_GBS = 6800.0
 # one prefill summed per kernel); an entry must be removed whenever its kernel changes (the
 # traffic is then reported as null).
 PROFILED_TRAFFIC = {
-    ("qwen35_4b_layer_T32768_sparse29", "select"): 0.065e6,
-    ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.136e6,
-    ("qwen35_4b_layer_T32768_sparse29", "intra"): 626.9e6,
-    ("qwen35_4b_layer_T32768_sparse29", "scan"): 230.9e6,
-    ("qwen35_4b_layer_T32768_sparse29", "output"): 847.8e6,
+    ("qwen35_4b_layer_T32768_sparse29", "select"): 0.067e6,
+    ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.134e6,
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 626.8e6,
+    ("qwen35_4b_layer_T32768_sparse29", "scan"): 243.3e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 842.3e6,
 }
 
 
