@@ -8,7 +8,7 @@
 //   Gram  G = K K^T [128 x 128]        (A = B = the K tile, K-major, by TMA)
 //   A_Delta[t,s] = beta_t G[t,s] 2^(g_t - g_s), s < t in the same chunk; M = I + A_Delta
 //   C = M^-1 (exact) or the block-adjacent approximation (Eq. 7), fp32 over compact
-//       16x16 blocks: C_ii = M_ii^-1 (forward substitution on CUDA cores),
+//       16x16 blocks: C_ii = M_ii^-1 (8x8 forward substitutions and two 8x8 products on CUDA cores),
 //       C_ij = -C_ii sum_{k=j}^{i-1} M_ik C_kj (the block-adjacent solver's two products
 //       per block on the warps' tensor cores in three-pass tf32, nearly fp32 accuracy)
 //   U = C diag(beta) V                  (A: C diag(beta) bf16, block-diagonal over the
@@ -291,32 +291,68 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
-    // 2. solve.  Diagonal 16x16 blocks by forward substitution, in place: warp w < 4 takes
-    //    blocks 2w and 2w+1 (8 blocks: 2 chunks x 4), one lane per column, the column of
-    //    C_ii in registers and the rows of M_ii broadcast from shared memory:
-    //    C_ii[i][j] = -sum_{s<i} M_ii[i][s] C_ii[s][j]   (C_ii[s][j] = 0 for s < j, 1 for s = j)
+    // 2. solve.  Diagonal 16x16 blocks, in place: warp w < 4 takes blocks 2w and 2w+1 (8 blocks:
+    //    2 chunks x 4), lanes 16 (w' = lane / 16) apart.  Split into 8x8 sub-blocks,
+    //    M_ii = [[A, 0], [B, D]], its inverse is [[A^-1, 0], [-D^-1 B A^-1, D^-1]]:
+    //    (a) A^-1 and D^-1 by forward substitution, one lane per column of a sub-block (rows of the
+    //        sub-block broadcast from shared memory): X[i][j] = -sum_{s<i} M[i][s] X[s][j];
+    //    (b) the lower-left quarter as two 8x8 products, lane (row r, four columns).
     if (warp < 4) {
-        const int blk = 2 * warp + (lane >> 4), j = lane & 15;
-        float *Mb = blk_diag(F, blk >> 2, blk & 3);
-        float x[kBlk];
+        float *Mb = blk_diag(F, (2 * warp + (lane >> 4)) >> 2, (2 * warp + (lane >> 4)) & 3);
+        {   // (a)
+            const int sub = (lane >> 3) & 1, j = lane & 7;
+            float *Sb = Mb + sub * (8 * BS + 8);
+            float x[8];
 #pragma unroll
-        for (int i2 = 0; i2 < kBlk; ++i2) x[i2] = i2 == j ? 1.f : 0.f;
+            for (int i2 = 0; i2 < 8; ++i2) x[i2] = i2 == j ? 1.f : 0.f;
 #pragma unroll
-        for (int i2 = 1; i2 < kBlk; ++i2) {
-            float mr[kBlk];  // row i2 of M_ii, 16-byte loads (broadcast across the half-warp)
+            for (int i2 = 1; i2 < 8; ++i2) {
+                float mr[8];  // row i2 of the sub-block, 16-byte loads (broadcast across its 8 lanes)
 #pragma unroll
-            for (int q4 = 0; q4 < (i2 + 3) / 4; ++q4) {
-                const float4 m4 = ld4(Mb + i2 * BS + 4 * q4);
-                mr[4 * q4] = m4.x; mr[4 * q4 + 1] = m4.y; mr[4 * q4 + 2] = m4.z; mr[4 * q4 + 3] = m4.w;
+                for (int q4 = 0; q4 < (i2 + 3) / 4; ++q4) {
+                    const float4 m4 = ld4(Sb + i2 * BS + 4 * q4);
+                    mr[4 * q4] = m4.x; mr[4 * q4 + 1] = m4.y; mr[4 * q4 + 2] = m4.z; mr[4 * q4 + 3] = m4.w;
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < i2; ++s2) acc += mr[s2] * x[s2];
+                if (i2 > j) x[i2] = -acc;
             }
-            float acc = 0.f;
+            __syncwarp();  // every lane has read its sub-block before the inverse replaces it
 #pragma unroll
-            for (int s2 = 0; s2 < i2; ++s2) acc += mr[s2] * x[s2];
-            if (i2 > j) x[i2] = -acc;
+            for (int i2 = 0; i2 < 8; ++i2) Sb[i2 * BS + j] = x[i2];
+            __syncwarp();
         }
-        __syncwarp();  // every lane has read M_ii before C_ii replaces it
+        {   // (b) T = B A^-1 over B, then -D^-1 T over T
+            const int r = (lane >> 1) & 7, c4 = (lane & 1) * 4;
+            float *Bq = Mb + 8 * BS;           // rows 8..15, columns 0..7
+            const float *XA = Mb, *XD = Mb + 8 * BS + 8;
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            {
+                const float4 b0 = ld4(Bq + r * BS), b1 = ld4(Bq + r * BS + 4);
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-        for (int i2 = 0; i2 < kBlk; ++i2) Mb[i2 * BS + j] = x[i2];
+                for (int k = 0; k < 8; ++k) {
+                    const float4 xa = ld4(XA + k * BS + c4);
+                    t.x += bv[k] * xa.x; t.y += bv[k] * xa.y; t.z += bv[k] * xa.z; t.w += bv[k] * xa.w;
+                }
+            }
+            __syncwarp();  // every lane has read B
+            *reinterpret_cast<float4 *>(Bq + r * BS + c4) = t;
+            __syncwarp();  // T complete
+            float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+            {
+                const float4 d0 = ld4(XD + r * BS), d1 = ld4(XD + r * BS + 4);
+                const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float4 tk = ld4(Bq + k * BS + c4);
+                    l.x += dv[k] * tk.x; l.y += dv[k] * tk.y; l.z += dv[k] * tk.z; l.w += dv[k] * tk.w;
+                }
+            }
+            __syncwarp();  // every lane has read T
+            *reinterpret_cast<float4 *>(Bq + r * BS + c4) = make_float4(-l.x, -l.y, -l.z, -l.w);
+        }
     }
     __syncthreads();
     offdiag_level<1>(F, warp, lane);
