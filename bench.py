@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILED_TRAFFIC = {
     ("qwen35_4b_layer_T32768_sparse29", "select"): 0.067e6,
     ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.134e6,
-    ("qwen35_4b_layer_T32768_sparse29", "intra"): 626.8e6,
-    ("qwen35_4b_layer_T32768_sparse29", "scan"): 243.3e6,
-    ("qwen35_4b_layer_T32768_sparse29", "output"): 842.3e6,
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 626.6e6,
+    ("qwen35_4b_layer_T32768_sparse29", "scan"): 243.4e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 842.2e6,
 }
 
 
