@@ -155,10 +155,10 @@ enum PrefillMode { kDense = 0, kSparse = 1, kOnline = 2 };
 // CSR rows are sorted by event count, longest first, so the scan's critical path is
 // the first rows.  The bf16 prefill splits the rows into classes by CSR index (no
 // event count leaves the device): class c = rows [bound_c, bound_c+1) with bounds
-// 0, R/8, R/4, R/2, R.  Each class runs its intra step (given mask), scan and output
-// on its own stream, the longest class first and at the highest priority, so its
-// scan starts once its own intra step is done while the shorter classes' intra steps,
-// scans and outputs fill the GPU around it.  Streams and events are made once per
+// from class_bounds (classes of 3/16, 4/16, 4/16 and 5/16 of the rows).  Each class
+// runs its intra step (given mask), scan and output on its own stream, the longest
+// class first and at the highest priority, so its scan starts once its own intra step
+// is done while the other classes' intra steps, scans and outputs fill the GPU around it.  Streams and events are made once per
 // device; a mutex keeps one prefill's fork / join sequence together on the host.
 constexpr int kClasses = 4;
 struct ClassStreams {
