@@ -12,8 +12,6 @@
 // Snapshot rule: event e (chunk c, next event of its row at chunk cn, or none)
 // is some group's predecessor iff an even chunk index 2r with c < 2r <= cn
 // exists and 2r <= 2(G-1); such events are numbered densely in event order.
-#include <climits>
-
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -235,12 +233,79 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
 // Word-parallel variant, used when the whole mask fits in shared memory as
 // 32-chunk words (B*P*ceil(C/32) words, 8 KiB of them at B = 8, T = 32K).  Every
 // (sorted row, word) pair is one warp task, so all 32 warps work even when the
-// batch has few rows; event numbers and snapshot slots come from block scans
-// over the per-word counts laid out in sorted-row order, which is CSR order.
+// batch has few rows.  Event numbers and snapshot slots come from one pass of block
+// scans over the per-word counts laid out in sorted-row order, which is CSR order.
+// The kernel is bound by instruction issue on its one SM, so each word is visited
+// three times only: staged, counted inside the scan, and written out.
 constexpr size_t kWordsSmemLimit = 200 * 1024;
 
 __host__ __device__ constexpr size_t words_smem_bytes(int R, int NF) {
-    return sizeof(int) * (2 * (size_t)R + 5 * (size_t)NF + 2);
+    return sizeof(int) * (2 * (size_t)R + 3 * (size_t)NF + 2);
+}
+
+// The events of mask word w (chunks 32w..32w+31) that some group references.  By the
+// snapshot rule an event at chunk c qualifies iff m = (c & ~1) + 2, the first even
+// chunk after c, is at most 2(G-1) and at most the row's next event chunk.  For odd c,
+// m = c + 1 and that holds for every later event; for even c it fails exactly when
+// chunk c + 1, in the same word, holds an event.  So the test needs no other word.
+__device__ __forceinline__ unsigned snap_bits(unsigned bits, int w, int G) {
+    const int top = 2 * (G - 1) - 32 * w - 2;  // the largest allowed (c & ~1) - 32w
+    const unsigned lim = top < 0 ? 0u : top >= 30 ? 0xffffffffu : (2u << ((top & ~1) + 1)) - 1u;
+    return bits & (0xAAAAAAAAu | ~(bits >> 1)) & lim;
+}
+
+__device__ __forceinline__ unsigned warp_incl_scan_u(unsigned x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// Exclusive scans of the words' event counts into evb[0..NF] and of their snapshot
+// counts into refb[0..NF] (entry NF: the totals), word f = j*NW + w being word w of
+// sorted row j.  The two counts (at most 32 each) travel packed in the halves of one
+// unsigned through the warp and block steps of each 1024-word slice, whose sums stay
+// below 2^16, and are unpacked into the running totals.
+__device__ void word_scans(const unsigned *words, const int *order, int NW, int NF, int G, int *evb,
+                           int *refb, unsigned *warp_tot) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int ev_carry = 0, ref_carry = 0;
+    for (int base = 0; base < NF; base += kThreads) {
+        const int f = base + threadIdx.x;
+        unsigned x = 0u;
+        if (f < NF) {
+            const int j = f / NW, w = f - j * NW;
+            const unsigned bits = words[order[j] * NW + w];
+            x = (unsigned)__popc(bits) | ((unsigned)__popc(snap_bits(bits, w, G)) << 16);
+        }
+        const unsigned incl = warp_incl_scan_u(x);
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const unsigned t = warp_tot[lane];
+            const unsigned ti = warp_incl_scan_u(t);
+            warp_tot[lane] = ti - t;  // exclusive warp offsets
+            if (lane == 31) warp_tot[32] = ti;
+        }
+        __syncthreads();
+        const unsigned ex = warp_tot[warp] + incl - x;
+        if (f < NF) {
+            evb[f] = ev_carry + (int)(ex & 0xFFFFu);
+            refb[f] = ref_carry + (int)(ex >> 16);
+        }
+        const unsigned tot = warp_tot[32];
+        ev_carry += (int)(tot & 0xFFFFu);
+        ref_carry += (int)(tot >> 16);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        evb[NF] = ev_carry;
+        refb[NF] = ref_carry;
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -258,16 +323,17 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
     int *evb = order + R;          // [NF+1]  first event number of word f (f = j*NW + w), then E
     int *refb = evb + NF + 1;      // [NF+1]  first snapshot slot of word f, then the slot count
     unsigned *words = reinterpret_cast<unsigned *>(refb + NF + 1);  // [NF] mask bits, physical-row major
-    int *nxt = reinterpret_cast<int *>(words + NF);                 // [NF] first event chunk at or after word w
-    unsigned *refbits = reinterpret_cast<unsigned *>(nxt + NF);     // [NF] referenced events of word f
-    __shared__ int warp_tot[33];
+    __shared__ unsigned warp_tot[33];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const unsigned below = (1u << lane) - 1u;
+    for (int i = threadIdx.x; i < R; i += kThreads) cnt[i] = 0;
     // An online selection writes the mask just before: wait for it.  A caller's mask needs no
     // wait, so the compaction overlaps the kernel before and waits only before it exits.
     if (wait_first) pdl_wait();
     pdl_trigger();
-    // 1. stage the mask: one warp per (row, 256 chunks), eight coalesced loads in flight
+    __syncthreads();
+    // 1. stage the mask and count each row's events: one warp per (row, 256 chunks),
+    //    eight coalesced loads in flight
     const int NB = (NW + 7) >> 3;
     for (int t = warp; t < R * NB; t += kWarps) {
         const int i = t / NB, b = t - i * NB;
@@ -278,67 +344,37 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
             const int c = 256 * b + 32 * q + lane;
             v[q] = c < C && (mr == nullptr || mr[c] != 0);
         }
+        int n = 0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const unsigned bits = __ballot_sync(0xffffffffu, v[q]);
             const int w = 8 * b + q;
+            n += __popc(bits);
             if (lane == 0 && w < NW) words[i * NW + w] = bits;
         }
+        if (lane == 0) atomicAdd(&cnt[i], n);
     }
     __syncthreads();
-    // 2. per physical row: its event count and, per word, the first event chunk at or
-    //    after that word (a suffix minimum, INT_MAX when the rest of the row is empty)
-    for (int i = warp; i < R; i += kWarps) {
-        int n = 0, carry = INT_MAX;
-        for (int w0 = ((NW - 1) >> 5) << 5; w0 >= 0; w0 -= 32) {
-            const int w = w0 + lane;
-            const unsigned bits = w < NW ? words[i * NW + w] : 0u;
-            n += __popc(bits);
-            int x = bits ? 32 * w + __ffs(bits) - 1 : INT_MAX;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_down_sync(0xffffffffu, x, o);
-                if (lane + o < 32) x = min(x, y);
-            }
-            x = min(x, carry);
-            if (w < NW) nxt[i * NW + w] = x;
-            carry = __shfl_sync(0xffffffffu, x, 0);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-        if (lane == 0) cnt[i] = n;
-    }
-    __syncthreads();
-    // 3. rank rows: count descending, id ascending
+    // 2. rank rows: count descending, id ascending
     for (int i = threadIdx.x; i < R; i += kThreads) {
-        int ci = cnt[i], rank = 0;
+        const int ci = cnt[i];
+        int rank = 0;
         for (int j = 0; j < R; ++j) {
-            int cj = cnt[j];
+            const int cj = cnt[j];
             rank += (cj > ci) || (cj == ci && j < i);
         }
         order[rank] = i;
     }
     __syncthreads();
-    // 4. per-word event counts in sorted-row order; their exclusive scan numbers the events
-    for (int f = threadIdx.x; f < NF; f += kThreads) {
-        const int j = f / NW, w = f - j * NW;
-        evb[f] = __popc(words[order[j] * NW + w]);
-    }
-    __syncthreads();
-    block_exclusive_scan(evb, evb, NF, warp_tot);
-    // 5. one warp per (sorted row j, word w): event chunks, run starts, group
-    //    predecessors, and which events some group references (event at
-    //    chunk c, next event of the row at cn or none: referenced iff the smallest even
-    //    chunk index m > c satisfies m <= cn and m <= 2(G-1))
+    // 3. event numbers and snapshot slots of every word
+    word_scans(words, order, NW, NF, G, evb, refb, warp_tot);
+    // 4. one warp per (sorted row j, word w), lane = chunk 32w + lane: event chunks and
+    //    snapshot slots, run starts and group predecessors
     for (int f = warp; f < NF; f += kWarps) {
         const int j = f / NW, w = f - j * NW;
         const int i = order[j];
         const unsigned bits = words[i * NW + w];
-        const int e0 = evb[f], row0 = evb[j * NW];
-        const int c = 32 * w + lane;
-        const bool s = (bits >> lane) & 1u;
-        const int e = e0 + __popc(bits & below);
-        if (s && (int64_t)e < ev_cap) ev_chunk[e] = c;
+        const int e0 = evb[f];
         if (run_first && lane < 2) {  // runs of 16 chunks starting inside this word
             const int rr = 2 * w + lane;
             if (rr < NR) run_first[(int64_t)j * (NR + 1) + rr] = e0 + (lane ? __popc(bits & 0xFFFFu) : 0);
@@ -347,33 +383,17 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
             const int r = 16 * w + lane;
             if (r < G) {
                 const int n_before = e0 + __popc(bits & ((1u << (2 * lane)) - 1u));
-                grp_pred[(int64_t)i * G + r] = n_before > row0 ? n_before - 1 : -1;
+                grp_pred[(int64_t)i * G + r] = n_before > evb[j * NW] ? n_before - 1 : -1;
             }
         }
-        bool ref = false;
-        if (s) {
-            const int m = (c & ~1) + 2;
-            const unsigned later = lane < 31 ? bits >> (lane + 1) : 0u;
-            const int cn = later ? c + __ffs(later) : (w + 1 < NW ? nxt[i * NW + w + 1] : INT_MAX);
-            ref = m <= 2 * (G - 1) && m <= cn;
+        if ((bits >> lane) & 1u) {
+            const int e = e0 + __popc(bits & below);
+            if ((int64_t)e < ev_cap) {
+                const unsigned rb = snap_bits(bits, w, G);
+                ev_chunk[e] = 32 * w + lane;
+                snap_slot[e] = ((rb >> lane) & 1u) ? refb[f] + __popc(rb & below) : -1;
+            }
         }
-        const unsigned rb = __ballot_sync(0xffffffffu, ref);
-        if (lane == 0) {
-            refbits[f] = rb;
-            refb[f] = __popc(rb);
-        }
-    }
-    __syncthreads();
-    block_exclusive_scan(refb, refb, NF, warp_tot);
-    // 6. snapshot slots: referenced events numbered densely in event order
-    for (int f = warp; f < NF; f += kWarps) {
-        const int j = f / NW, w = f - j * NW;
-        const unsigned bits = words[order[j] * NW + w];
-        if (bits == 0u) continue;  // warp-uniform
-        const unsigned rb = refbits[f];
-        const int e = evb[f] + __popc(bits & below);
-        if (((bits >> lane) & 1u) && (int64_t)e < ev_cap)
-            snap_slot[e] = ((rb >> lane) & 1u) ? refb[f] + __popc(rb & below) : -1;
     }
     for (int j = threadIdx.x; j < R; j += kThreads) {
         row_pair[j] = order[j];
