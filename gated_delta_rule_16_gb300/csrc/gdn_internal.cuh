@@ -106,7 +106,7 @@ struct Workspace {
     int32_t *run_first;        // [R, NR+1] first event of each run, per CSR row
     double *P;                 // [B, Nv, C+1] log2 decay prefix (Eq. 19)
     void *grp_info;            // [B, P, G] int4 {snapshot slot, kind, decay head 0, decay head 1}
-    void *U;                   // [B, T, Nv, dv] dtype: U, then U' in place for events
+    void *U;                   // U, then U' in place for events: bf16 head-major [B, Nv, T, dv], fp32 [B, T, Nv, dv]
     float *cbar;               // [B, Nv, C, nblk, 16, 16] compact C-bar blocks (bf16 on the tensor-core path)
     void *W;                   // [ev_cap, 2, 64, d] dtype, W of events (bf16 storage: -W, for the scan's U' product)
     void *snap;                // post-event state snapshots: fp32 [snap_cap, 2, d, dv]; bf16 storage: S^T [snap_cap, 2, dv, d]

@@ -450,8 +450,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tK, const __grid_constant__ 
     __syncthreads();
     // 7. U out (rows past the sequence's end are clipped); W = (C diag(beta 2^g)) K for events
     if (tid == 0 && !abort_s) {
-        tma_store_4d(&tU, 0, h, t0, b, sm + OFF_A);
-        tma_store_4d(&tU, 64, h, t0, b, sm + OFF_A + kSlab);
+        tma_store_4d(&tU, 0, t0, h, b, sm + OFF_A);
+        tma_store_4d(&tU, 64, t0, h, b, sm + OFF_A + kSlab);
         bulk_commit();
         if (any_event) {
             tc_fence_after();
@@ -517,7 +517,7 @@ cudaError_t launch_intra_tc(const Problem &pb, const Workspace &ws, bool write_c
     const uint64_t wrows = (uint64_t)ws.ev_cap * 2 * kChunk;
     if (!make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 128) ||
         !make_tmap_tokens(&tV, pb.v, pb.Nv, pb.T, pb.B, 64, 128) ||
-        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 128) ||
+        !make_tmap_headmajor(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 128) ||
         !make_tmap_bf16_3d(&tW, ws.W, kDim, wrows, 1, kDim * 2, wrows * kDim * 2, 64, 64, 1))
         return cudaErrorInvalidValue;
     IntraParams a;

@@ -223,8 +223,8 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     // 2. K has been read: U' takes its place; QS once its state has landed
     if (tid == 0 && !abort_s) {
         mbar_arrive_expect_tx(&bar_u_ld, 2 * kSlab);
-        tma_load_4d(sm + OFF_K, &tU, 0, h, t0, b, &bar_u_ld);
-        tma_load_4d(sm + OFF_K + kSlab, &tU, 64, h, t0, b, &bar_u_ld);
+        tma_load_4d(sm + OFF_K, &tU, 0, t0, h, b, &bar_u_ld);
+        tma_load_4d(sm + OFF_K + kSlab, &tU, 64, t0, h, b, &bar_u_ld);
         u_issued = true;
         if (kind != 0) {
             if (kind == 1 && !mbar_wait(&bar_s, 0)) {
@@ -316,7 +316,7 @@ cudaError_t launch_output_tc(const Problem &pb, const Workspace &ws) {
     const uint64_t snap_rows = (uint64_t)(ws.snap_cap > 0 ? ws.snap_cap : 1) * 2 * kDim;
     if (!make_tmap_tokens(&tQ, pb.q, pb.Nq, pb.T, pb.B, 64, 128) ||
         !make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 128) ||
-        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 128) ||
+        !make_tmap_headmajor(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 128) ||
         !make_tmap_bf16_3d(&tS, ws.snap, kDim, snap_rows, 1, kDim * 2, snap_rows * kDim * 2, 64, 128, 1) ||
         !make_tmap_tokens(&tO, pb.o, pb.Nv, pb.T, pb.B, 64, 128))
         return cudaErrorInvalidValue;

@@ -205,8 +205,8 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
     auto load_u = [&](int k) {
         const int tok = ev_c[k] * kChunk;
         mbar_arrive_expect_tx(&bar_u, 16384u);
-        tma_load_4d(sm + OFF_U, &tU, 0, h, tok, b, &bar_u);  // rows past the sequence's end read zeros
-        tma_load_4d(sm + OFF_U + 8192, &tU, 64, h, tok, b, &bar_u);
+        tma_load_4d(sm + OFF_U, &tU, 0, tok, h, b, &bar_u);  // rows past the sequence's end read zeros
+        tma_load_4d(sm + OFF_U + 8192, &tU, 64, tok, h, b, &bar_u);
     };
     auto load_k = [&](int k) {
         const int tok = ev_c[k] * kChunk;
@@ -377,8 +377,8 @@ scan_run_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__ 
                              mnmajor_desc(smem_addr(sm + OFF_K), ks, 8192), id2, 1);
                 mma_commit(&bar_mma2);
                 if (mode == kModeFixup) {  // U' of this event back over U (clipped at the sequence's end)
-                    tma_store_4d(&tU, 0, h, c * kChunk, b, sm + OFF_U);
-                    tma_store_4d(&tU, 64, h, c * kChunk, b, sm + OFF_U + 8192);
+                    tma_store_4d(&tU, 0, c * kChunk, h, b, sm + OFF_U);
+                    tma_store_4d(&tU, 64, c * kChunk, h, b, sm + OFF_U + 8192);
                     bulk_commit();
                     if (k + 1 < n_ev) {
                         bulk_wait_read();  // the store has left the U tile
@@ -650,7 +650,7 @@ cudaError_t launch_scan_tc(const Problem &pb, const Workspace &ws, int part) {
     if (!make_tmap_bf16_3d(&tW, ws.W, kDim, (uint64_t)ws.ev_cap * 2 * kChunk, 1, kDim * 2,
                            (uint64_t)ws.ev_cap * 2 * kChunk * kDim * 2, 64, 64, 1, true) ||
         !make_tmap_tokens(&tK, pb.k, pb.Nq, pb.T, pb.B, 64, 64, true) ||
-        !make_tmap_tokens(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 64, true))
+        !make_tmap_headmajor(&tU, ws.U, pb.Nv, pb.T, pb.B, 64, 64, true))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(scan_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRunSmem);
     const int fixup = part == 2;

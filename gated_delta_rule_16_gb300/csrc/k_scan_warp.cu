@@ -58,7 +58,7 @@ struct WarpScanParams {
     const int32_t *row_pair, *row_ptr, *ev_chunk, *snap_slot;
     const double *P;
     const float *g, *h0;
-    __nv_bfloat16 *U;       // [B,T,Nv,128]: U, replaced by U' for events
+    __nv_bfloat16 *U;       // [B,Nv,T,128] (head-major): U, replaced by U' for events
     __nv_bfloat16 *snap;    // [snap_cap,2,128 dv,128 d] post-event states S^T
     float *s_final;
     int32_t *status;
@@ -194,7 +194,7 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
                 tma_load_3d(st + 8192, &tW, 64, wrow, 0, &full[s]);
                 tma_load_4d(st + kTile, &tK, 0, p, c * kChunk, b, &full[s]);  // past the sequence's end: zeros
                 tma_load_4d(st + kTile + 8192, &tK, 64, p, c * kChunk, b, &full[s]);
-                tma_load_4d(st + 2 * kTile, &tU, dv0, h, c * kChunk, b, &full[s]);
+                tma_load_4d(st + 2 * kTile, &tU, dv0, c * kChunk, h, b, &full[s]);
             }
             __syncwarp();
         }
@@ -408,7 +408,7 @@ scan_warp_kernel(const __grid_constant__ CUtensorMap tW, const __grid_constant__
             const int tr = lane >> 1, tok = c * kChunk + t0w + tr;
             const uint4 v = *reinterpret_cast<const uint4 *>(ust_w + tr * 32 + (lane & 1) * 16);
             if (tok < a.T_)  // rows past the sequence's end are not written
-                *reinterpret_cast<uint4 *>(a.U + ((gbase + tok) * a.Nv + h) * kDim + dv0 + (lane & 1) * 8) = v;
+                *reinterpret_cast<uint4 *>(a.U + (((int64_t)b * a.Nv + h) * a.T_ + tok) * kDim + dv0 + (lane & 1) * 8) = v;
             __syncwarp();
         }
         P_end = pe_k;
@@ -489,7 +489,7 @@ cudaError_t launch_scan_warp(const Problem &pb, const Workspace &ws) {
     if (!make_tmap_bf16_3d(&tW, ws.W, kDim, wrows > 0 ? wrows : 1, 1, kDim * 2, (wrows > 0 ? wrows : 1) * kDim * 2,
                            64, 64, 1, true) ||
         !make_tmap_tokens(&tK, pb.k ? pb.k : ws.U, pb.Nq, T, pb.B, 64, 64, true) ||
-        !make_tmap_tokens(&tU, ws.U, pb.Nv, T, pb.B, kSlice, kChunk, false))
+        !make_tmap_headmajor(&tU, ws.U, pb.Nv, T, pb.B, kSlice, kChunk, false))
         return cudaErrorInvalidValue;
     WarpScanParams a;
     a.row_pair = ws.row_pair; a.row_ptr = ws.row_ptr; a.ev_chunk = ws.ev_chunk; a.snap_slot = ws.snap_slot;

@@ -62,6 +62,25 @@ inline bool make_tmap_tokens(CUtensorMap *map, const void *base, uint64_t heads,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Head-major bf16 tensor [B, heads, T, 128] (the workspace's U for bf16 storage) as a 4-D
+// map (128, T, heads, B): a head's token rows are contiguous, so a chunk's tile is one
+// contiguous block.  Coordinates (x, token, head, sequence); a box past a sequence's last
+// token reads zeros and a store there is clipped.
+inline bool make_tmap_headmajor(CUtensorMap *map, const void *base, uint64_t heads, uint64_t T, uint64_t B,
+                                uint32_t box_x, uint32_t box_rows, bool swizzle128 = true) {
+    if (reinterpret_cast<uintptr_t>(base) & 15u) return false;
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    const uint64_t row = 128 * 2;
+    cuuint64_t dims[4] = {128, T, heads, B};
+    cuuint64_t strides[3] = {row, T * row, heads * T * row};
+    cuuint32_t box[4] = {box_x, box_rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A rank-2 fp32 tensor: dims[0] contiguous (elements), rows stride1_bytes apart (a multiple
 // of 16), box {box0, box1}, no swizzle.  Returns false if encoding fails.
 inline bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t stride1_bytes,
