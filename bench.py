@@ -58,12 +58,16 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen35_4b_layer_T32768_sparse29")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="steps of the end-to-end (host-buffer) timing; 0: the same as --steps")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' timings")
     ap.add_argument("--shard", choices=["pairs", "sequences"], default="pairs",
                     help="with several ranks: split the layer's head pairs over the ranks (tensor "
                          "parallelism, strong scaling) or give each rank its own sequence (weak scaling)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.e2e_steps <= 0:
+        args.e2e_steps = args.steps
+    return args
 
 
 def dist_env():
@@ -573,7 +577,8 @@ def run_ours(args):
         "clocks": clk,
         "e2e": {"value": job_throughput(tok, ranks_tokens, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": "gdn_prefill_host (C ABI, host buffers)",
-                "pipelining": "2 streams x 2 workspaces", "serial_ms_per_step": e2e_serial_ms},
+                "pipelining": "2 streams x 2 workspaces", "serial_ms_per_step": e2e_serial_ms,
+                "steps": args.e2e_steps},
         "gpu_launches": n_launch,
         "roofline": {"bound": "hbm", "kernel": "step (the whole hot path: compaction, prefix, intra, scan, output)",
                      "achieved": step_gbs, "peak": peak, "unit": "GB/s", "frac": step_gbs / peak,
