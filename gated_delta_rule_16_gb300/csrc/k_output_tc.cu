@@ -2,24 +2,23 @@
 // Eqs. 22-24) on tcgen05 tensor cores, for bf16 storage.
 //
 // One CTA per (group r, value head h, sequence b): 128 query tokens (chunks
-// c = 2r and c+1) against 128 key tokens; 256 threads, ~100 KB of shared memory
-// and 256 TMEM columns, so two CTAs share an SM.  The two heads of a pair are
-// adjacent CTAs (the second read of their Q and K tiles comes from L2).
+// c = 2r and c+1) against 128 key tokens; 256 threads, ~68 KB of shared memory, 128
+// TMEM columns and at most 80 registers a thread, so three CTAs share an SM and keep
+// enough loads in flight for the kernel's bytes (the two heads of a pair are adjacent
+// CTAs; the second read of their Q and K tiles comes from L2).
 //   QK  = Q K^T                   (A: Q [tok][d] K-major; B: K [tok][d] K-major)
-//   QS  = Q S_c                   (B: snapshot S^T [dv][d] bf16, K-major)
-//   AU  = A U'                    (A: decayed, masked QK in bf16, K-major; B: U' [tok][dv] MN-major)
+//   O   = (f Q) S_c + A U'        (one accumulator: B of the first product the snapshot
+//                                  S^T [dv][d] bf16, K-major; of the second U' [tok][dv] MN-major)
 // where the mask/decay of A is
 //   same chunk, j <= i : 2^(g_i - g_j);   i in c+1, j in c : 2^(g_i + gamma_c - g_j);   else 0
-// and the epilogue forms O_i = (f 2^(g_i + shift_i) QS_i + AU_i) / sqrt(d) with
-// f = 2^(P_c - P_(e+1)) the gap decay of the predecessor snapshot (Eq. 21) and
-// shift_i = gamma_c for tokens of chunk c+1.  Operands arrive by TMA.
-// Shared memory over the CTA's life (three 32 KB tiles):
-//   [0, 32K)    Q (QK and QS) -> the A tile
-//   [32K, 64K)  K (QK) -> U' (loaded once QK is done) -> O staging
-//   [64K, 96K)  the entry state S^T
-// The A values wait in registers (packed bf16) until QS has read Q; QS is issued after
-// they are built, so the snapshot's load does not delay them; AU accumulates into QK's
-// TMEM columns.
+// and row i of Q is scaled, in bf16, by f_i = 2^(P_c - P_(e+1)) 2^(g_i + shift_i): the gap decay
+// of the predecessor snapshot (Eq. 21) times the decay into token i (shift_i = gamma_c for tokens
+// of chunk c+1).  O leaves scaled by 1/sqrt(d).  Operands arrive by TMA.
+// Shared memory over the CTA's life (two 32 KB tiles):
+//   [0, 32K)    Q (QK) -> f Q (QS) -> the A tile
+//   [32K, 64K)  K (QK) -> the entry state S^T -> U' -> O staging
+// The A values wait in registers (packed bf16) from QK until QS has read the scaled Q; the
+// entry state and U' each load once the product before has read that tile.
 #include "gdn_internal.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -31,11 +30,10 @@ using namespace tc;
 
 constexpr int kThreads = 256;  // 8 warps: 2 per TMEM lane quarter, 64 columns each
 constexpr uint32_t kSlab = 16384;          // [128 rows][128 B]
-constexpr uint32_t OFF_Q = 0;              // Q: 2 K-slabs; then the A tile: 2 K-slabs [128 q][64 k]
-constexpr uint32_t OFF_K = 2 * kSlab;      // K: 2 K-slabs; then U': 2 MN-stacks [128 tok][64 dv]; then O
-constexpr uint32_t OFF_S = 4 * kSlab;      // S^T: 2 K-slabs [128 dv][64 d]
-constexpr uint32_t kOutSmem = 1024 + 6 * kSlab;
-constexpr uint32_t TM_QK = 0, TM_QS = 128;  // AU reuses QK's columns
+constexpr uint32_t OFF_Q = 0;              // Q, rows scaled by the state factor for QS; then the A tile
+constexpr uint32_t OFF_K = 2 * kSlab;      // K; then the entry state S^T; then U' [128 tok][64 dv] x 2; then O
+constexpr uint32_t kOutSmem = 1024 + 4 * kSlab;
+constexpr uint32_t TM_O = 0;  // QK, then the output accumulator f Q S + A U' (128 columns)
 
 struct OutParams {
     const float *g, *h0;
@@ -57,7 +55,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tK,
                  const __grid_constant__ CUtensorMap tU, const __grid_constant__ CUtensorMap tS,
                  const __grid_constant__ CUtensorMap tO, OutParams a) {
@@ -71,7 +69,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     __shared__ float cref, gmax_w[4], gmin_w[4];
     __shared__ int fact;  // 1: the mask factorises (the group's log-decay range is moderate)
     __shared__ float fscale;
-    __shared__ int has_s;
+    __shared__ int has_s, s_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; which 64 of 128 columns
@@ -105,19 +103,14 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         tma_load_4d(sm + OFF_K + kSlab, &tK, 64, p, t0, b, &bar_qk_ld);
     }
     if (tid < 128) gs[tid] = a.g[(tok0 + min(tid, nvalid - 1)) * a.Nv + h];  // past the end: a finite g
-    if (warp == 0) tmem_alloc<256>(&tmem_base);
+    if (warp == 0) tmem_alloc<128>(&tmem_base);
     pdl_wait();  // U', the entry-state table and the snapshots come from the kernels before
     if (tid == 0) {  // entry state of the group: one table load (kind 1 snapshot, 2 h0, 0 zero)
         const int4 info = a.grp_info[((int64_t)b * a.P_ + p) * a.G + r];
         const int kind = info.y == 2 && !a.h0 ? 0 : info.y;
         has_s = kind;
         fscale = __int_as_float(hh ? info.w : info.z);
-        if (kind == 1) {
-            const int slot = a.expanded ? (b * a.P_ + p) * a.G + r : info.x;
-            mbar_arrive_expect_tx(&bar_s, 2 * kSlab);
-            tma_load_3d(sm + OFF_S, &tS, 0, (slot * 2 + hh) * kDim, 0, &bar_s);
-            tma_load_3d(sm + OFF_S + kSlab, &tS, 64, (slot * 2 + hh) * kDim, 0, &bar_s);
-        }
+        s_slot = a.expanded ? (b * a.P_ + p) * a.G + r : info.x;
     }
     tc_fence_before();
     __syncthreads();
@@ -140,17 +133,6 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         }
         if (lane == 0) { gmax_w[warp] = mx; gmin_w[warp] = mn; }
     }
-    if (has_s == 2) {  // initial-state path (no predecessor event, h0 given): S^T = h0^T in bf16, K-major slabs
-        const float *src = a.h0 + ((int64_t)b * a.Nv + h) * (kDim * kDim);
-        for (int idx = tid; idx < kDim * 16; idx += kThreads) {  // (dv row, 8-wide d chunk)
-            const int dv = idx & 127, ch = idx >> 7;
-            float v[8];
-#pragma unroll
-            for (int q2 = 0; q2 < 8; ++q2) v[q2] = src[(ch * 8 + q2) * kDim + dv];
-            st_sw128_8(sm + OFF_S + (ch >> 3) * kSlab, dv, (ch & 7) * 8, v);
-        }
-        fence_async_smem();
-    }
     __syncthreads();
     if (tid < 128) {
         const float mx = fmaxf(fmaxf(gmax_w[0], gmax_w[1]), fmaxf(gmax_w[2], gmax_w[3]));
@@ -167,15 +149,15 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     const uint32_t id_km = idesc_bf16(128, 128, false, true);
     const float inv_sqrt_d = rsqrtf((float)kDim);
     const int kind = has_s;
-    bool s_wait_ok = true, u_issued = false;  // thread 0
-    if (tid == 0) {  // QK (QS follows the A values: its state may still be landing)
+    bool s_issued = false, s_wait_ok = true, u_issued = false;  // thread 0
+    if (tid == 0) {  // QK
         if (!mbar_wait(&bar_qk_ld, 0)) {
             abort_s = 1;
             atomicOr(a.status, kStatusTimeout);
         } else {
             tc_fence_after();
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tbase + TM_QK, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                mma_bf16(tbase + TM_O, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
                          kmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id_kk, ks > 0);
             mma_commit(&bar_qk);
         }
@@ -191,16 +173,16 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         const float ef = ex2(Gi - cref);
         const bool fct = fact != 0;
 #pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-            const int j0 = 64 * half + 32 * s2;
-            float qk[32];
-            tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QK + j0), qk);
+        for (int s4 = 0; s4 < 4; ++s4) {
+            const int j0 = 64 * half + 16 * s4;
+            float qk[16];
+            tmem_ld16(tmem_addr(tbase, quarter * 32, TM_O + j0), qk);
             tmem_ld_wait();
-            float w[32];
+            float w[16];
             if (fct) {
                 const float4 *cf = reinterpret_cast<const float4 *>(colf + j0);
 #pragma unroll
-                for (int t4 = 0; t4 < 8; ++t4) {
+                for (int t4 = 0; t4 < 4; ++t4) {
                     const float4 f = cf[t4];
                     const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
@@ -211,21 +193,55 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
                 }
             } else {
 #pragma unroll
-                for (int t = 0; t < 32; ++t)
+                for (int t = 0; t < 16; ++t)
                     w[t] = (j0 + t <= row && !zero_row) ? qk[t] * ex2(Gi - gcum(j0 + t)) : 0.f;
             }
 #pragma unroll
-            for (int t = 0; t < 16; ++t) apk[16 * s2 + t] = pack_bf16(w[2 * t], w[2 * t + 1]);
+            for (int t = 0; t < 8; ++t) apk[8 * s4 + t] = pack_bf16(w[2 * t], w[2 * t + 1]);
         }
     }
     tc_fence_before();
+    __syncthreads();  // QK has read K and every thread has read QK
+    // 2. the entry state takes K's place; the rows of Q are scaled by the state's factor
+    //    f_i = 2^(P_c - P_(e+1)) 2^(g_i + shift_i), so that one accumulator holds f Q S + A U'
+    if (tid == 0 && !abort_s && kind == 1) {
+        mbar_arrive_expect_tx(&bar_s, 2 * kSlab);
+        tma_load_3d(sm + OFF_K, &tS, 0, (s_slot * 2 + hh) * kDim, 0, &bar_s);
+        tma_load_3d(sm + OFF_K + kSlab, &tS, 64, (s_slot * 2 + hh) * kDim, 0, &bar_s);
+        s_issued = true;
+    }
+    if (kind == 2) {  // initial-state path (no predecessor event, h0 given): S^T = h0^T in bf16, K-major slabs
+        const float *src = a.h0 + ((int64_t)b * a.Nv + h) * (kDim * kDim);
+        for (int idx = tid; idx < kDim * 16; idx += kThreads) {  // (dv row, 8-wide d chunk)
+            const int dv = idx & 127, ch = idx >> 7;
+            float v[8];
+#pragma unroll
+            for (int q2 = 0; q2 < 8; ++q2) v[q2] = src[(ch * 8 + q2) * kDim + dv];
+            st_sw128_8(sm + OFF_K + (ch >> 3) * kSlab, dv, (ch & 7) * 8, v);
+        }
+    }
+    if (kind != 0) {  // thread (row, half): the row's 64 columns of Q in slab `half`
+        const float f = fscale * ex2(gs[row] + (row >= 64 ? gs[63] : 0.f));
+        uint8_t *slab = sm + OFF_Q + half * kSlab;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(slab + sw128_offset(row, 8 * c8));
+            const uint4 q = *ptr;
+            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+            uint32_t o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&qw[e]);
+                o4[e] = pack_bf16(__low2float(v) * f, __high2float(v) * f);
+            }
+            *ptr = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
-    // 2. K has been read: U' takes its place; QS once its state has landed
+    // 3. QS = (f Q) S starts the accumulator (no entry state: nothing to add)
     if (tid == 0 && !abort_s) {
-        mbar_arrive_expect_tx(&bar_u_ld, 2 * kSlab);
-        tma_load_4d(sm + OFF_K, &tU, 0, t0, h, b, &bar_u_ld);
-        tma_load_4d(sm + OFF_K + kSlab, &tU, 64, t0, h, b, &bar_u_ld);
-        u_issued = true;
         if (kind != 0) {
             if (kind == 1 && !mbar_wait(&bar_s, 0)) {
                 s_wait_ok = false;
@@ -234,14 +250,20 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
             } else {
                 tc_fence_after();
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(tbase + TM_QS, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
-                             kmajor_desc(smem_addr(sm + OFF_S), ks, kSlab), id_kk, ks > 0);
+                    mma_bf16(tbase + TM_O, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                             kmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id_kk, ks > 0);
             }
         }
         mma_commit(&bar_qs);  // also without QS: arrives at once (QK is done)
     }
-    // 3. once QS has read Q, the A tile goes there
+    // 4. QS has read the scaled Q and the state: U' takes K's place, the A tile Q's
     if (!abort_s && !mbar_wait(&bar_qs, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
+    if (tid == 0 && !abort_s) {
+        mbar_arrive_expect_tx(&bar_u_ld, 2 * kSlab);
+        tma_load_4d(sm + OFF_K, &tU, 0, t0, h, b, &bar_u_ld);
+        tma_load_4d(sm + OFF_K + kSlab, &tU, 64, t0, h, b, &bar_u_ld);
+        u_issued = true;
+    }
     {
         uint8_t *slab = sm + OFF_Q + half * kSlab;
 #pragma unroll
@@ -252,7 +274,7 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    // 4. AU = A U' into QK's columns
+    // 5. AU = A U' added onto QS
     if (tid == 0 && !abort_s) {
         if (!mbar_wait(&bar_u_ld, 0)) {
             abort_s = 1;
@@ -260,30 +282,26 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
         } else {
             tc_fence_after();
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tbase + TM_QK, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
-                         mnmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id_km, ks > 0);
+                mma_bf16(tbase + TM_O, kmajor_desc(smem_addr(sm + OFF_Q), ks, kSlab),
+                         mnmajor_desc(smem_addr(sm + OFF_K), ks, kSlab), id_km, kind != 0 || ks > 0);
             mma_commit(&bar_au);
         }
     }
     __syncthreads();
     if (!abort_s && !mbar_wait(&bar_au, 0)) { abort_s = 1; atomicOr(a.status, kStatusTimeout); }
     tc_fence_after();
-    // 5. epilogue: O rows staged (bf16, 128B-swizzled) over U' (read by now), one TMA store
+    // 6. epilogue: O rows staged (bf16, 128B-swizzled) over U' (read by now), one TMA store
     {
-        const float f = fscale * ex2(gs[row] + (row >= 64 ? gs[63] : 0.f));
-        const bool has = kind != 0;
         uint8_t *stage = sm + OFF_K + half * kSlab;
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
-            float qs[32], au[32];
-            const int col = 64 * half + 32 * s2;
-            tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QK + col), au);
-            if (has) tmem_ld32(tmem_addr(tbase, quarter * 32, TM_QS + col), qs);
+            float o[32];
+            tmem_ld32(tmem_addr(tbase, quarter * 32, TM_O + 64 * half + 32 * s2), o);
             tmem_ld_wait();
 #pragma unroll
-            for (int t = 0; t < 32; ++t) au[t] = ((has ? f * qs[t] : 0.f) + au[t]) * inv_sqrt_d;
+            for (int t = 0; t < 32; ++t) o[t] *= inv_sqrt_d;
 #pragma unroll
-            for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(stage, row, 32 * s2 + 8 * v8, &au[8 * v8]);
+            for (int v8 = 0; v8 < 4; ++v8) st_sw128_8(stage, row, 32 * s2 + 8 * v8, &o[8 * v8]);
         }
     }
     fence_async_smem();
@@ -298,14 +316,14 @@ output_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__
     if (abort_s && tid == 0) {
         // let every copy and MMA issued so far land before the CTA releases its memory
         mbar_wait(&bar_qk_ld, 0);
-        if (kind == 1 && s_wait_ok) mbar_wait(&bar_s, 0);
+        if (s_issued && s_wait_ok) mbar_wait(&bar_s, 0);
         if (u_issued) mbar_wait(&bar_u_ld, 0);
         mma_commit(&bar_drain);
         mbar_wait(&bar_drain, 0);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc<256>(tbase);
+    if (warp == 0) tmem_dealloc<128>(tbase);
 }
 
 }  // namespace
