@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILED_TRAFFIC = {
     ("qwen35_4b_layer_T32768_sparse29", "select"): 0.04e6,
     ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.14e6,
-    ("qwen35_4b_layer_T32768_sparse29", "intra"): 609.2e6,
-    ("qwen35_4b_layer_T32768_sparse29", "scan"): 241.9e6,
-    ("qwen35_4b_layer_T32768_sparse29", "output"): 841.9e6,
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 608.8e6,
+    ("qwen35_4b_layer_T32768_sparse29", "scan"): 244.2e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 837.7e6,
 }
 
 
