@@ -328,7 +328,8 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
             stage(1, 1, [&] { return launch_prefix(pb, ws); });
             stage(3, 1, [&] { return launch_wbuild_tc(pb, ws); });
         } else {
-            stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, false, true); });
+            // with the intra steps per class, only the row order comes before the fork
+            stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, false, true, intra_split ? 1 : 0); });
             if (!intra_split) {
                 stage(1, 1, [&] { return launch_prefix(pb, ws); });
                 stage(2, 1, [&] { return launch_intra_tc(pb, ws, true); });
@@ -337,10 +338,12 @@ gdn_status run_prefill(const gdn_shape *shape, const void *q, const void *k, con
         }
         int bound[kClasses + 1];
         const int ncls = class_bounds(pb.R, bound);
-        // the classes' intra steps need only the CSR rows: they fork after the compaction, and the
-        // prefix (P and the group table, for the scans and outputs) runs beside them
+        // the classes' intra steps need only the row order: they fork after the compaction's first
+        // part, and its second part and the prefix (P and the group table, for the scans and
+        // outputs) run beside them
         if (e == cudaSuccess) e = cudaEventRecord(cs->fork, pb.stream);
-        if (intra_split) {
+        if (intra_split) {  // the rest of the compaction and the prefix, beside the first intra steps
+            stage(0, 1, [&] { return launch_select(pb, ev, ws.snap_cap, nullptr, false, true, 2); });
             stage(1, 1, [&] { return launch_prefix(pb, ws); });
             if (e == cudaSuccess) e = cudaEventRecord(cs->prefix_done, pb.stream);
         }

@@ -134,8 +134,10 @@ gdn_status prefill_sparse_single_stream(const gdn_shape *shape, const void *q, c
 // kRunChunks chunks (entry NR: the row's end); needs kRunChunks = 16 (two runs per mask word).
 // wait_first: the mask comes from the kernel before (else the kernel waits for it only before
 // exiting); or_status: OR the status bits into counts[2] instead of overwriting it.
+// part: 0 everything; 1 the row order only (row_pair); 2 everything but row_pair (after part 1).
+// Masks too large for the word-parallel kernel do everything in part 1 and nothing in part 2.
 cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *run_first,
-                          bool wait_first, bool or_status);
+                          bool wait_first, bool or_status, int part = 0);
 cudaError_t launch_prefix(const Problem &pb, const Workspace &ws);
 cudaError_t launch_intra(const Problem &pb, const Workspace &ws);
 cudaError_t launch_wbuild(const Problem &pb, const Workspace &ws);

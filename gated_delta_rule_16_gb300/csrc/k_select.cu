@@ -84,7 +84,7 @@ select_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
               int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
               int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
               int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
-              int64_t snap_cap, int wait_first, int or_status) {
+              int64_t snap_cap, int wait_first, int or_status, int /*part: always everything*/) {
     extern __shared__ int sm[];
     const int NW = (C + 31) >> 5;   // 32-chunk mask words per row
     int *cnt = sm;               // [R]   events per physical row
@@ -314,7 +314,7 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
                     int32_t *__restrict__ ev_chunk, int32_t *__restrict__ grp_pred,
                     int32_t *__restrict__ snap_slot, int32_t *__restrict__ counts,
                     int32_t *__restrict__ run_first, int NR, int64_t ev_cap,
-                    int64_t snap_cap, int wait_first, int or_status) {
+                    int64_t snap_cap, int wait_first, int or_status, int part) {
     extern __shared__ int sm[];
     const int NW = (C + 31) >> 5;
     const int NF = R * NW;
@@ -366,6 +366,11 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
         order[rank] = i;
     }
     __syncthreads();
+    if (part == 1) {  // the row order alone: the launches that need only it may start
+        for (int j = threadIdx.x; j < R; j += kThreads) row_pair[j] = order[j];
+        if (!wait_first) pdl_wait();
+        return;
+    }
     // 3. event numbers and snapshot slots of every word
     word_scans(words, order, NW, NF, G, evb, refb, warp_tot);
     // 4. one warp per (sorted row j, word w), lane = chunk 32w + lane: event chunks and
@@ -396,7 +401,7 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
         }
     }
     for (int j = threadIdx.x; j < R; j += kThreads) {
-        row_pair[j] = order[j];
+        if (part == 0) row_pair[j] = order[j];
         if (run_first) run_first[(int64_t)j * (NR + 1) + NR] = evb[(j + 1) * NW];
     }
     for (int j = threadIdx.x; j <= R; j += kThreads) row_ptr[j] = evb[j * NW];
@@ -417,10 +422,12 @@ select_words_kernel(const uint8_t *__restrict__ mask, int R, int C, int G,
 }  // namespace
 
 cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_cap, int32_t *run_first,
-                          bool wait_first, bool or_status) {
+                          bool wait_first, bool or_status, int part) {
     const int NW = (pb.C + 31) / 32, NR = (pb.C + kRunChunks - 1) / kRunChunks;
     const size_t fast = words_smem_bytes(pb.R, pb.R * NW);
     const bool use_words = fast <= kWordsSmemLimit;
+    if (!use_words && part == 2) return cudaSuccess;  // part 1 did everything
+    if (!use_words) part = 0;
     auto kernel = use_words ? select_words_kernel : select_kernel;
     const size_t smem = use_words ? fast : sizeof(int) * (6 * (size_t)pb.R + 2 + (size_t)kWarps * NW);
     if (smem > 48 * 1024) {
@@ -429,7 +436,7 @@ cudaError_t launch_select(const Problem &pb, const gdn_events &ev, int64_t snap_
     }
     return launch_kernel(pb.pdl, kernel, 1, kThreads, smem, pb.stream, pb.mask, pb.R, pb.C, pb.G, ev.row_pair,
                          ev.row_ptr, ev.ev_chunk, ev.grp_pred, ev.snap_slot, ev.counts, run_first, NR,
-                         (int64_t)ev.capacity, snap_cap, (int)wait_first, (int)or_status);
+                         (int64_t)ev.capacity, snap_cap, (int)wait_first, (int)or_status, part);
 }
 
 }  // namespace gdn
