@@ -42,11 +42,11 @@ FALLBACK_HBM_GBS = 6800.0
 # one prefill summed per kernel); an entry must be removed whenever its kernel changes (the
 # traffic is then reported as null).
 PROFILED_TRAFFIC = {
-    ("qwen35_4b_layer_T32768_sparse29", "select"): 0.04e6,
+    ("qwen35_4b_layer_T32768_sparse29", "select"): 0.09e6,
     ("qwen35_4b_layer_T32768_sparse29", "prefix"): 0.14e6,
-    ("qwen35_4b_layer_T32768_sparse29", "intra"): 608.8e6,
-    ("qwen35_4b_layer_T32768_sparse29", "scan"): 244.2e6,
-    ("qwen35_4b_layer_T32768_sparse29", "output"): 837.7e6,
+    ("qwen35_4b_layer_T32768_sparse29", "intra"): 609.1e6,
+    ("qwen35_4b_layer_T32768_sparse29", "scan"): 242.0e6,
+    ("qwen35_4b_layer_T32768_sparse29", "output"): 837.1e6,
 }
 
 
