@@ -13,7 +13,7 @@ N_v=32, d=d_v=128, bf16, event-sparse path at 29% retention (Beta(2,5)
 per-pair budgets), block-adjacent solver.  Under torchrun every rank runs its
 own independent sequence (weak scaling, no collective on the data path).
 
---impl reference times the CPU fp64 oracle (the only reference this build has)
+--impl reference times the CPU fp64 oracle (the only reference there is)
 on a bounded sample of the same workload, on the host cores.
 """
 from __future__ import annotations
@@ -536,7 +536,7 @@ def run_ours(args):
     scan_full = timed_variant(gdn, ex_call(solver="block_adj", scan_full=True), x, args.steps, world, dev, stream)
     expanded = timed_variant(gdn, ex_call(solver="block_adj", states_expanded=True), x, args.steps, world, dev,
                              stream)
-    # this build's own dense path on the same layer (every chunk an event, gdn_prefill_dense)
+    # the library's own dense path on the same layer (every chunk an event, gdn_prefill_dense)
     dense = timed_variant(gdn, lambda: gdn.gdn_prefill_dense(
         d_in["q"], d_in["k"], d_in["v"], d_in["beta"], d_in["g"], solver="block_adj", o=o, s_final=s_final,
         workspace=ws, stream=stream), x, args.steps, world, dev, stream)

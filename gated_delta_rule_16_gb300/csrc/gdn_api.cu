@@ -688,7 +688,7 @@ const char *gdn_status_string(gdn_status status) {
         case GDN_ERR_DTYPE: return "unknown dtype or solver";
         case GDN_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
         case GDN_ERR_WORKSPACE: return "workspace smaller than gdn_workspace_bytes()";
-        case GDN_ERR_UNSUPPORTED: return "request not implemented by this build (needs d == dv == 128, ceil(T/64) <= 16384)";
+        case GDN_ERR_UNSUPPORTED: return "request not implemented by this library (needs d == dv == 128, ceil(T/64) <= 16384)";
         case GDN_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
         case GDN_ERR_DEVICE: return "current device is not a compute-capability 10.3 (GB300) GPU";
         case GDN_ERR_CAPACITY: return "device-side event or snapshot capacity exceeded";

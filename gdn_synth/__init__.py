@@ -6,8 +6,8 @@ tensors with the shapes and distributions of the SparseGDN workloads and
 rounds them to the storage dtype.
 
 Workload recipe (SparseGDN reading notes, Sec. 2.1 problem statement and
-Sec. 3.1 setup; distributions are this build's stand-in for the RULER timing
-loads, which are not available):
+Sec. 3.1 setup; these distributions stand in for the RULER timing loads,
+which are not available):
 
 * q, k ~ N(0, 1) per element, then L2-normalised per (token, head);
   v ~ N(0, 1).  Drawn in fp32, stored either as fp32 or rounded

@@ -79,7 +79,7 @@ typedef enum {
     GDN_ERR_DTYPE = 3,       /* unknown dtype or solver enum */
     GDN_ERR_ALIGN = 4,       /* a pointer is not 16-byte (workspace: 256-byte) aligned */
     GDN_ERR_WORKSPACE = 5,   /* workspace smaller than gdn_workspace_bytes() */
-    GDN_ERR_UNSUPPORTED = 6, /* valid request this build does not implement */
+    GDN_ERR_UNSUPPORTED = 6, /* valid request this library does not implement */
     GDN_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
     GDN_ERR_DEVICE = 8,      /* current device is not a compute-capability 10.3 GPU */
     GDN_ERR_CAPACITY = 9,    /* (device-latched) more events or snapshots than capacity */
